@@ -1,0 +1,295 @@
+"""Pins of the oracle to facts outside itself.
+
+Each pin takes a loaded oracle and raises AssertionError when the oracle disagrees with
+what the pages or mathematics fix. None re-types the oracle's own code: decoding uses
+the E2M1 field formula of the OCP MX spec (not a table), routing is checked by a full
+sort, the permutation by its invariants, the FFN by a dense numpy SwiGLU MLP on
+independently decoded weights, and bf16 rounding by a search over neighbouring values.
+test_oracle_pins.py runs them on the real oracle and on builds with planted mistakes.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---- independent decoders --------------------------------------------------------------
+
+def e2m1_from_fields(code: int) -> float:
+    """E2M1 from its bit fields: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0."""
+    sign = (code >> 3) & 1
+    e = (code >> 1) & 3
+    m = code & 1
+    mag = 0.5 * m if e == 0 else 2.0 ** (e - 1) * (1.0 + 0.5 * m)
+    return -mag if sign else mag
+
+
+def ue8m0_value(s: int) -> float:
+    if s == 0:
+        return 0.0
+    if s == 255:
+        return math.inf
+    return math.ldexp(1.0, s - 127)
+
+
+def decode_mxfp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """[R, K/2] codes + [R, K/32] scales -> float64 [R, K]; element 2i is the low nibble."""
+    R = codes.shape[0]
+    K = codes.shape[1] * 2
+    nib = np.stack([codes & 15, codes >> 4], axis=-1).reshape(R, K)
+    vals = np.array([e2m1_from_fields(c) for c in range(16)], np.float64)[nib]
+    sc = np.array([ue8m0_value(s) for s in range(256)], np.float64)[scales]
+    return vals * np.repeat(sc, 32, axis=1)
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def dense_swiglu(x: np.ndarray, gu_codes, gu_scales, d_codes, d_scales) -> np.ndarray:
+    """y = Wd (silu(Wg x) * (Wu x)) for rows of x (float64 [n, H]) with a dense numpy MLP."""
+    Wgu = decode_mxfp4(gu_codes, gu_scales)
+    I = Wgu.shape[0] // 2
+    g = x @ Wgu[:I].T
+    u = x @ Wgu[I:].T
+    h = g / (1.0 + np.exp(-g)) * u
+    return h @ decode_mxfp4(d_codes, d_scales).T
+
+
+def nearest_bf16_bits(v: float) -> int:
+    """Round-to-nearest-even bf16 by bracketing |v| between consecutive bf16 bit patterns."""
+    if v == 0:
+        return 0x8000 if math.copysign(1.0, v) < 0 else 0
+    a = abs(v)
+    lo, hi = 0, 0x7F80                       # search over non-negative finite patterns
+    val = lambda b: float(bf16_to_f64(np.array([b], np.uint16))[0])
+    while hi - lo > 1:                       # invariant: val(lo) <= a < val(hi) (hi may be inf)
+        mid = (lo + hi) // 2
+        if val(mid) <= a:
+            lo = mid
+        else:
+            hi = mid
+    dl, dh = a - val(lo), val(hi) - a
+    if hi == 0x7F80:                         # between max finite and infinity
+        half_ulp_above_max = val(0x7F7F) + (val(0x7F7F) - val(0x7F7E)) / 2
+        b = 0x7F80 if a >= half_ulp_above_max else lo   # the tie goes to the even pattern: inf
+    elif dl < dh or (dl == dh and lo % 2 == 0):
+        b = lo
+    else:
+        b = hi
+    return b | (0x8000 if v < 0 else 0)
+
+
+# ---- small seeded inputs for the pins (not the workload generator: tiny hand sizes) -----
+
+def _rng(tag: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(1234 + tag))
+
+
+def tiny_expert(rng, H, I, lo=118, hi=131):
+    return (rng.integers(0, 256, (2 * I, H // 2), dtype=np.uint8),
+            rng.integers(lo, hi, (2 * I, H // 32), dtype=np.uint8),
+            rng.integers(0, 256, (H, I // 2), dtype=np.uint8),
+            rng.integers(lo, hi, (H, I // 32), dtype=np.uint8))
+
+
+class _Experts:
+    def __init__(self, mats):
+        self.gate_up_codes, self.gate_up_scales, self.down_codes, self.down_scales = [
+            np.ascontiguousarray(np.stack(m)) for m in zip(*mats)]
+
+
+def random_bf16(rng, shape, scale=1.0):
+    from routed_moe_fp4_gb300.synthetic import f32_to_bf16_bits
+    return f32_to_bf16_bits((rng.standard_normal(shape) * scale).astype(np.float32))
+
+
+# ---- the pins ---------------------------------------------------------------------------
+
+def pin_e2m1_table(o):
+    """OCP MX FP4 fields; doubled values are integers; 16 fp32 entries are 64 bytes."""
+    vals = [o.e2m1(c) for c in range(16)]
+    for c, v in enumerate(vals):
+        ref = e2m1_from_fields(c)
+        assert v == ref and math.copysign(1, v) == math.copysign(1, ref), (c, v, ref)
+        assert float(2 * v).is_integer()
+    assert np.array(vals, np.float32).nbytes == 64
+    with open(os.path.join(GOLDEN, "e2m1_table.txt")) as f:
+        stored = [float(l.split()[1]) for l in f if l.strip() and not l.startswith("#")]
+    assert stored == vals, (stored, vals)
+
+
+def pin_e8m0(o):
+    """UE8M0: 2^(s-127) for 1..254, s=0 -> +0, s=255 -> +inf."""
+    for s in range(1, 255):
+        assert o.e8m0(s) == math.ldexp(1.0, s - 127), s
+    z = o.e8m0(0)
+    assert z == 0.0 and math.copysign(1.0, z) > 0
+    assert math.isinf(o.e8m0(255)) and o.e8m0(255) > 0
+
+
+def pin_nibble_order(o):
+    """Element 2i is the low nibble of byte i."""
+    codes = np.array([[0x21, 0xF7] + [0] * 14], np.uint8)       # K = 32: one scale group
+    scales = np.array([[127]], np.uint8)
+    got = [o.mxfp4(codes, scales, 32, 0, k) for k in range(4)]
+    assert got == [0.5, 1.0, 6.0, -6.0], got
+    scales2 = np.array([[125]], np.uint8)
+    assert o.mxfp4(codes, scales2, 32, 0, 1) == 0.25
+
+
+def pin_route_bruteforce(o):
+    """Top-k by a full sort on (-key, index) with many exact ties, bias included."""
+    rng = _rng(1)
+    T, E = 64, 16
+    for k in (1, 3, 8):
+        s = (rng.integers(0, 9, (T, E)) / 8.0).astype(np.float32)
+        b = (rng.integers(-2, 3, E) / 16.0).astype(np.float32)
+        idx, w = o.route(s, b, k)
+        key = s + b                                         # one fp32 addition per element
+        for t in range(T):
+            order = sorted(range(E), key=lambda e: (-float(key[t, e]), e))[:k]
+            assert list(idx[t]) == order, (k, t, list(idx[t]), order)
+    s = rng.random((T, E), dtype=np.float32)
+    idx, w = o.route(s, None, 4)
+    for t in range(T):
+        assert list(idx[t]) == sorted(range(E), key=lambda e: (-float(s[t, e]), e))[:4]
+
+
+def pin_route_weights(o):
+    """Weights sum to 1, equal 1 for k=1, follow the unbiased scores, ignore the bias shift."""
+    rng = _rng(2)
+    T, E = 40, 32
+    s = rng.random((T, E), dtype=np.float32) * 0.9 + 0.05
+    b = (rng.standard_normal(E) * 0.3).astype(np.float32)
+    for k in (1, 2, 8):
+        idx, w = o.route(s, b, k)
+        sums = w.astype(np.float64).sum(1)
+        assert np.all(np.abs(sums - 1.0) <= k * 2.0 ** -23), (k, sums)
+        if k == 1:
+            assert np.all(w == 1.0)
+        sel = np.take_along_axis(s, idx, 1).astype(np.float64)
+        ratio = w.astype(np.float64) / (sel / sel.sum(1, keepdims=True))
+        assert np.all(np.abs(ratio - 1.0) < 1e-6), ratio
+    idx0, w0 = o.route(s, None, 4)
+    idx1, w1 = o.route(s, np.full(E, 0.25, np.float32), 4)
+    assert np.array_equal(idx0, idx1)
+    assert np.array_equal(w0, w1)
+
+
+def pin_permute(o):
+    """Round trip, counts, exclusive offsets, stable token order inside each group."""
+    rng = _rng(3)
+    for (T, E, k) in ((37, 9, 3), (5, 4, 4), (1, 8, 2), (64, 256, 8)):
+        idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        cnt, off, src, inv = o.permute(idx, E, with_shared=True)
+        assert cnt.sum() == T * k + T and cnt[E] == T
+        for e in range(E):
+            assert cnt[e] == int((idx == e).sum())
+        assert off[0] == 0 and np.all(np.diff(off) == cnt)
+        assert len(src) == T * k + T
+        rows = inv.reshape(-1)
+        assert sorted(rows.tolist()) == list(range(T * k))
+        for t in range(T):
+            for j in range(k):
+                r = inv[t, j]
+                assert src[r] == t
+                assert off[idx[t, j]] <= r < off[idx[t, j] + 1]
+        for g in range(E + 1):
+            seg = src[off[g]:off[g + 1]]
+            assert np.all(np.diff(seg) > 0), (g, seg)
+        assert np.array_equal(src[T * k:], np.arange(T))
+
+
+def _dense_case(o, with_shared: bool):
+    rng = _rng(4 + int(with_shared))
+    H, I, I_s, T = 64, 32, 64, 5
+    x = random_bf16(rng, (T, H))
+    ex = _Experts([tiny_expert(rng, H, I)])
+    sh = _Experts([tiny_expert(rng, H, I_s)]) if with_shared else None
+    Wr = np.zeros((1, H), np.float32)
+    r = o.moe_forward(x, Wr, None, 1, ex, sh)
+    xf = bf16_to_f64(x)
+    ref = dense_swiglu(xf, ex.gate_up_codes[0], ex.gate_up_scales[0], ex.down_codes[0], ex.down_scales[0])
+    if with_shared:
+        ref = ref + dense_swiglu(xf, sh.gate_up_codes[0], sh.gate_up_scales[0], sh.down_codes[0],
+                                 sh.down_scales[0])
+    assert np.all(r["idx"] == 0) and np.all(r["w"] == 1.0)
+    err = np.abs(r["out_f64"] - ref).max() / np.abs(ref).max()
+    assert err < 1e-12, err
+
+
+def pin_dense_swiglu(o):
+    """E=1, k=1: the layer is a dense SwiGLU MLP (no scaling factor, clamp or extra terms)."""
+    _dense_case(o, with_shared=False)
+    _dense_case(o, with_shared=True)
+
+
+def pin_dense_gated(o):
+    """Permuted path == all experts on all tokens times the sparse gate matrix, plus shared."""
+    rng = _rng(6)
+    T, H, E, k, I, I_s = 6, 64, 8, 2, 32, 32
+    x = random_bf16(rng, (T, H))
+    Wr = (rng.standard_normal((E, H)) * 0.3).astype(np.float32)
+    b = (rng.standard_normal(E) * 0.1).astype(np.float32)
+    ex = _Experts([tiny_expert(rng, H, I) for _ in range(E)])
+    sh = _Experts([tiny_expert(rng, H, I_s)])
+    r = o.moe_forward(x, Wr, b, k, ex, sh)
+    G = np.zeros((T, E))
+    for t in range(T):
+        for j in range(k):
+            G[t, r["idx"][t, j]] += float(r["w"][t, j])
+    xf = bf16_to_f64(x)
+    ref = dense_swiglu(xf, sh.gate_up_codes[0], sh.gate_up_scales[0], sh.down_codes[0], sh.down_scales[0])
+    for e in range(E):
+        ye = dense_swiglu(xf, ex.gate_up_codes[e], ex.gate_up_scales[e], ex.down_codes[e], ex.down_scales[e])
+        ref = ref + G[:, e:e + 1] * ye
+    err = np.abs(r["out_f64"] - ref).max() / np.sqrt((ref ** 2).mean())
+    assert err < 1e-12, err
+    # the bf16 output is the rounding of the fp64 sum
+    for t in range(T):
+        for m in range(0, H, 7):
+            assert r["out"][t, m] == nearest_bf16_bits(float(r["out_f64"][t, m]))
+
+
+def pin_sigmoid(o):
+    """sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4, symmetry, increasing in the logit."""
+    z = np.array([0.0, math.log(3.0), -math.log(3.0), 2.5, -2.5, 10.0, -10.0, 1e-3, -1e-3])
+    s = o.sigmoid(z).astype(np.float64)
+    assert s[0] == 0.5
+    assert abs(s[1] - 0.75) < 1e-7 and abs(s[2] - 0.25) < 1e-7
+    assert np.all(np.abs(s[1::2] + s[2::2] - 1.0) < 1e-7)
+    zz = np.linspace(-8, 8, 101)
+    ss = o.sigmoid(zz)
+    assert np.all(np.diff(ss.astype(np.float64)) >= 0) and ss[-1] > 0.99
+
+
+def pin_logits(o):
+    """fp64 logits equal a numpy matmul of the decoded bf16 x and fp32 router weights."""
+    rng = _rng(7)
+    T, H, E = 9, 96, 13
+    x = random_bf16(rng, (T, H))
+    Wr = (rng.standard_normal((E, H)) * 0.02).astype(np.float32)
+    z = o.router_logits(x, Wr)
+    ref = bf16_to_f64(x) @ Wr.astype(np.float64).T
+    assert np.abs(z - ref).max() <= 1e-12 * np.abs(ref).max(), np.abs(z - ref).max()
+
+
+def pin_round_bf16(o):
+    """Round to nearest even bf16, checked by bracketing: ties, subnormals, overflow."""
+    cases = [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -8 + 2.0 ** -30, -(2.0 + 2.0 ** -7),
+             3.0e38, 3.4e38, 1e-39, 2.0 ** -133 * 1.5, 2.0 ** -134, 0.0, -0.0, 123.456, -7.77e-3]
+    rng = _rng(8)
+    cases += list(rng.standard_normal(300) * 10.0 ** rng.integers(-6, 6, 300))
+    for v in cases:
+        got = o.round_bf16(float(v))
+        ref = nearest_bf16_bits(float(v))
+        assert got == ref, (v, hex(got), hex(ref))
+
+
+ALL_PINS = [pin_e2m1_table, pin_e8m0, pin_nibble_order, pin_route_bruteforce, pin_route_weights,
+            pin_permute, pin_dense_swiglu, pin_dense_gated, pin_sigmoid, pin_logits, pin_round_bf16]
