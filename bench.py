@@ -1,0 +1,307 @@
+"""Benchmark of the routed MXFP4 MoE layer (one JSON line on stdout, rank 0).
+
+A step is one forward of the whole layer (router, permute, expert FFN, combine) over one batch
+of the workload's seeded synthetic tokens. `value` is whole-job tokens/s with inputs already in
+HBM; `e2e` is the same metric through coli_moe_forward_host with pinned host buffers (the
+host->device copy of x and the device->host copy of out inside the timed region). L2 is flushed
+(a 512 MiB write) before every timed step; each step is timed with CUDA events on the layer's
+stream, and the L2 flush is outside the events.
+
+--impl reference times the plain-C oracle on the host cores on the same workload (the reference
+arm; one oracle forward of a bounded token sample per step).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+Under torchrun every rank runs an independent replica (no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from routed_moe_fp4_gb300 import synthetic as S  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode"
+METRIC = "MoE-layer tokens/s at 1 GB300"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic_bytes(wl, routing: dict) -> dict:
+    """Bytes each stage must move at least once (touched experts measured from cnt)."""
+    E, H, I, I_s, T, k = wl.E, wl.H, wl.I, wl.I_s, wl.T, wl.top_k
+    cnt = routing["cnt"]
+    touched = int((cnt[:E] > 0).sum())
+    shared = 1 if I_s > 0 else 0
+    gu_per = lambda i: 2 * i * (H // 2 + H // 32)        # gate+up codes and scales
+    dn_per = lambda i: H * (i // 2 + i // 32)
+    rows = T * k + T * shared
+    gate_up = touched * gu_per(I) + shared * gu_per(I_s) + rows * H * 2 + rows * max(I, I_s) * 2
+    down = touched * dn_per(I) + shared * dn_per(I_s) + rows * max(I, I_s) * 2 + rows * H * 4
+    router = E * H * 4 + T * H * 2 + T * E * 4
+    return {"touched_experts": touched, "ffn_gate_up": gate_up, "ffn_down": down, "router": router,
+            "layer": gate_up + down + router + T * H * 2}
+
+
+def run_ours(args, wl_name: str) -> dict:
+    import torch
+    import torch.distributed as dist
+    from routed_moe_fp4_gb300 import build, colimoe as cm
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    inputs = S.make_inputs(wl_name, seed=0)
+    wl = inputs.workload
+    stream = torch.cuda.Stream()
+    layer = cm.MoELayer(inputs, stream=stream)
+    x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
+    out = torch.empty_like(x)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    x_host = torch.from_numpy(inputs.x.view(np.int16).copy()).pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+
+    def l2_flush():
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+
+    # warm-up
+    for _ in range(args.warmup):
+        layer.forward(x, out)
+    stream.synchronize()
+    launches_per_step = layer.launches()
+
+    # timed: device-resident inputs
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        l2_flush()
+        starts[i].record(stream)
+        layer.forward(x, out)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # stage breakdown (profiled forwards, outside the timed region)
+    layer.set_profiling(True)
+    stage_runs = []
+    for _ in range(max(3, min(args.steps, 10))):
+        l2_flush()
+        layer.forward(x, out)
+        stage_runs.append(layer.stage_times())
+    layer.set_profiling(False)
+    stages = {k: statistics.median([r[k] for r in stage_runs]) for k in stage_runs[0]}
+
+    # end to end: host buffers through coli_moe_forward_host
+    for _ in range(2):
+        layer.forward_host(x_host, out_host)
+    e2e_ms = []
+    for _ in range(args.steps):
+        l2_flush()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        layer.forward_host(x_host, out_host)
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_step = sum(e2e_ms) / len(e2e_ms)
+
+    routing = layer.routing(wl.T)
+    ab = algorithmic_bytes(wl, routing)
+    hbm_gbs, bf16_tf, peak_kind = _peaks()
+    dom = max(("ffn_gate_up", "ffn_down"), key=lambda k: stages[k])
+    achieved = ab[dom] / (stages[dom] * 1e-3) / 1e9
+    tokens = wl.T * ws
+    result = {
+        "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)xfp16, fp32 accumulate",
+        "data": "synthetic (seeded SplitMix64; MXFP4 experts, bf16 activations)",
+        "config": {"workload": f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E}, top_k={wl.top_k}, I={wl.I}, "
+                               f"I_s={wl.I_s}, MXFP4 E2M1 + UE8M0/32", "tokens_per_gpu": wl.T,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "flushed (512 MiB write) before every timed step"},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
+                     "frac": achieved / hbm_gbs, "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": ab[dom],
+                     "kernel_ms": stages[dom]},
+        "layer_roofline": {"bytes": ab["layer"], "ms": ms_per_step,
+                           "achieved_gbs": ab["layer"] / (ms_per_step * 1e-3) / 1e9,
+                           "frac": ab["layer"] / (ms_per_step * 1e-3) / 1e9 / hbm_gbs},
+        "stages_ms": stages, "touched_experts": ab["touched_experts"],
+        "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_step,
+                "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clock_info,
+    }
+    layer.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def oracle_sample(wl_name: str, budget_s: float):
+    """Times the oracle's full forward on the workload's tokens, repeated up to `budget_s`."""
+    from oracle.oracle import Oracle
+    inputs = S.make_inputs(wl_name, seed=0)
+    wl = inputs.workload
+    o = Oracle()
+    n_tok, runs = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        o.moe_forward(inputs.x, inputs.router_w, inputs.router_b, wl.top_k, inputs.experts, inputs.shared)
+        n_tok += wl.T
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": n_tok / el, "unit": "tokens/s", "cores": o.threads(), "kind": "oracle",
+            "sample": f"{runs} full oracle forward(s) of the {wl.name} workload ({wl.T} tokens each), "
+                      f"{el:.1f} s"}
+
+
+def run_reference(args, wl_name: str):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    from oracle.oracle import Oracle
+    inputs = S.make_inputs(wl_name, seed=0)
+    wl = inputs.workload
+    o = Oracle()
+    fwd = lambda: o.moe_forward(inputs.x, inputs.router_w, inputs.router_b, wl.top_k, inputs.experts,
+                                inputs.shared)
+    for _ in range(args.warmup):
+        fwd()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fwd()
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    v = wl.T / (ms * 1e-3)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E}, top_k={wl.top_k}, I={wl.I}, "
+                                   f"I_s={wl.I_s}, MXFP4 E2M1 + UE8M0/32"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": o.threads(), "kind": "oracle",
+                             "sample": f"{args.steps} timed full oracle forwards of {wl.T} tokens"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        res = run_reference(args, args.workload)
+    else:
+        res = run_ours(args, args.workload)
+        if res is not None:
+            res["cpu_baseline"] = oracle_sample(args.workload, args.cpu_budget)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * colimoe.h -- C ABI of the GB300 routed MXFP4 mixture-of-experts layer (libcolimoe.so).
+ *
+ * One routed MoE layer of a DeepSeek-V4-style decoder on one NVIDIA GB300 (sm_103a):
+ *   A1 router   fp32 logits x.Wr^T, s = sigmoid(logit), key = fp32(s + b), top-k keys
+ *               (ties -> lower expert index, descending order), w_j = s_j / sum_j s_j in fp32
+ *               ("the CUDA tier wired into the DeepSeek V4 engine", What it is: route on device)
+ *   A2 permute  per-expert histogram, exclusive scan, stable scatter of (token, slot) pairs
+ *               into expert-grouped rows, inverse map (same list: expert-grouped GEMM rows)
+ *   A3 gate/up  h = silu(Wg x) * (Wu x) per expert on its rows, MXFP4 weights
+ *   A4 down     y = Wd h
+ *               ("DeepSeek V4 Flash CPU inference with NVMe expert streaming": FP4 E2M1 experts
+ *               with UE8M0 group-32 scales; the dual gate+up matvec; hidden 4096 x moe_inter 2048)
+ *   A5 combine  out = y_shared + sum_j w_j y_j, rounded to bf16
+ *               ("the CUDA tier wired into the DeepSeek V4 engine": fused routed+shared MoE)
+ *
+ * Style follows "DeepSeek V4: the CUDA kernels, as a tier rather than an engine": a header that
+ * needs only <stdint.h>; the caller calls in and the library never calls out; the device is
+ * checked up front. There is no CPU fallback: every failure is an error code.
+ *
+ * Conventions
+ *  - Return codes: COLI_OK (0) or a negative COLI_ERR_*. Nothing throws across the ABI.
+ *    After an error, coli_moe_last_error() describes it.
+ *  - Pointers marked "device" must point to GB300 device memory (cudaMalloc or equivalent);
+ *    "host" pointers to host memory. The caller owns every pointer it passes; the library owns
+ *    only the handle and its workspace.
+ *  - A handle is bound to one device and one CUDA stream (given at create). coli_moe_forward
+ *    enqueues all its work on that stream and returns without synchronising; it allocates
+ *    nothing. Forwards on one handle must not overlap on the device (they share the workspace).
+ *
+ * Weight format (MXFP4, OCP Microscaling v1.0 FP4 E2M1 elements, UE8M0 scale per 32 elements):
+ *  - A matrix of R rows and K columns is stored K-major: codes [R][K/2] bytes, element k of a row
+ *    in byte k/2, low nibble for even k and high nibble for odd k; scales [R][K/32] bytes, byte
+ *    s giving the fp32 whose bit pattern is s << 23 (2^(s-127); s=0 -> +0, s=255 -> +inf, the
+ *    edges the pages' MXFP4 decode reproduces).
+ *  - Element value = E2M1(code) * UE8M0(scale of its group of 32 along K).
+ */
+#ifndef COLIMOE_H
+#define COLIMOE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define COLI_API __attribute__((visibility("default")))
+#else
+#define COLI_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    COLI_OK = 0,
+    COLI_ERR_INVALID_ARG = -1,      /* a NULL or out-of-range argument; nothing was enqueued */
+    COLI_ERR_UNSUPPORTED_ARCH = -2, /* the current device is not an sm_103 GB300 */
+    COLI_ERR_OUT_OF_MEMORY = -3,    /* workspace allocation failed at create */
+    COLI_ERR_CUDA = -4,             /* a CUDA runtime/driver call or kernel launch failed */
+};
+
+/* FFN path selection for coli_moe_set_ffn_path. */
+enum {
+    COLI_FFN_AUTO = 0,   /* tensor-core grouped GEMM when tokens per touched expert are many */
+    COLI_FFN_GEMV = 1,   /* weight-streaming GEMV kernels (small token counts) */
+    COLI_FFN_GEMM = 2,   /* tcgen05 grouped GEMM kernels */
+};
+
+typedef struct coli_moe coli_moe_t;
+
+/* One set of MXFP4 experts (device pointers, caller-owned). With E experts of hidden H and
+ * intermediate I:
+ *   gate_up_codes  [E][2I][H/2]   rows 0..I-1 are the gate matrix, rows I..2I-1 the up matrix
+ *   gate_up_scales [E][2I][H/32]
+ *   down_codes     [E][H][I/2]
+ *   down_scales    [E][H][I/32]
+ * The shared expert uses the same struct with E = 1 and I = shared_inter.
+ * Every pointer must be 16-byte aligned. */
+typedef struct {
+    const uint8_t *gate_up_codes;
+    const uint8_t *gate_up_scales;
+    const uint8_t *down_codes;
+    const uint8_t *down_scales;
+} coli_mxfp4_experts;
+
+typedef struct {
+    int32_t num_experts;   /* E, 1..1024 */
+    int32_t hidden;        /* H, a multiple of 128 */
+    int32_t inter;         /* I, a multiple of 128 */
+    int32_t shared_inter;  /* I_s, a multiple of 128, or 0 for a layer without shared expert */
+    int32_t max_tokens;    /* largest T a forward will be given, >= 1 */
+    int32_t max_top_k;     /* largest top_k a forward will be given, 1..min(E, 32) */
+} coli_moe_config;
+
+/* Creates a handle on the current CUDA device, bound to `cuda_stream` (a cudaStream_t; NULL =
+ * the legacy default stream). Checks that the device is sm_103 and allocates the workspace for
+ * (max_tokens, max_top_k). On success *out receives the handle; on failure *out is set to NULL
+ * and the error text is available from coli_moe_last_error(NULL). */
+COLI_API int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **out);
+
+/* One forward pass of the layer (A1..A5), enqueued on the handle's stream.
+ *   x_bf16         device, bf16 [T][H] row-major, 16-byte aligned
+ *   T              tokens, 0..max_tokens (0: nothing is enqueued, returns COLI_OK)
+ *   router_w       device, fp32 [E][H], 16-byte aligned
+ *   router_bias    device, fp32 [E], or NULL for a zero bias
+ *   packed_experts the E routed experts (device pointers), I = cfg.inter
+ *   shared_expert  the shared expert (E = 1, I = cfg.shared_inter), or NULL for none; must be
+ *                  NULL when cfg.shared_inter == 0
+ *   top_k          1..cfg.max_top_k
+ *   out_bf16       device, bf16 [T][H], 16-byte aligned; may not alias x_bf16
+ * Errors: COLI_ERR_INVALID_ARG for bad arguments (nothing enqueued), COLI_ERR_CUDA when a launch
+ * fails. Device-side execution errors surface on the stream as usual in CUDA. */
+COLI_API int coli_moe_forward(coli_moe_t *h, const void *x_bf16, int32_t T,
+                     const float *router_w, const float *router_bias,
+                     const coli_mxfp4_experts *packed_experts,
+                     const coli_mxfp4_experts *shared_expert,
+                     int32_t top_k, void *out_bf16);
+
+/* The same forward with x and out in HOST memory: copies x to the device, runs the forward and
+ * copies the result back, then synchronises the handle's stream before returning. Pinned host
+ * buffers give asynchronous copies. Weights and router arguments are device pointers as above.
+ * Uses a per-handle device staging buffer sized at create. */
+COLI_API int coli_moe_forward_host(coli_moe_t *h, const void *x_bf16_host, int32_t T,
+                          const float *router_w, const float *router_bias,
+                          const coli_mxfp4_experts *packed_experts,
+                          const coli_mxfp4_experts *shared_expert,
+                          int32_t top_k, void *out_bf16_host);
+
+/* Releases the handle and its workspace (synchronises its stream first). NULL is a no-op. */
+COLI_API void coli_moe_destroy(coli_moe_t *h);
+
+/* Text of the last error on this handle (or of the last failed create when h is NULL). The
+ * string stays valid until the next call on the same handle. Never returns NULL. */
+COLI_API const char *coli_moe_last_error(const coli_moe_t *h);
+
+/* Forces the FFN path (COLI_FFN_AUTO / _GEMV / _GEMM). Returns COLI_ERR_INVALID_ARG for an
+ * unknown value. Both paths compute the same result within rounding. */
+COLI_API int coli_moe_set_ffn_path(coli_moe_t *h, int32_t path);
+
+/* Routing of the last forward, copied to HOST buffers (synchronises the stream). Any field may
+ * be NULL to skip it. Sizes use that forward's T, k and the handle's E:
+ *   scores    fp32  [T][E]   sigmoid scores s
+ *   idx       int32 [T][k]   chosen experts, descending key
+ *   weights   fp32  [T][k]   renormalised weights
+ *   cnt       int32 [E+1]    rows per group; group E is the shared expert (T rows, or 0)
+ *   off       int32 [E+2]    exclusive prefix of cnt
+ *   src_token int32 [T*k+T]  token of each expert-grouped row (shared rows are 0..T-1)
+ *   inv_row   int32 [T][k]   row of (token, slot)                                             */
+typedef struct {
+    float *scores;
+    int32_t *idx;
+    float *weights;
+    int32_t *cnt;
+    int32_t *off;
+    int32_t *src_token;
+    int32_t *inv_row;
+} coli_moe_routing;
+
+COLI_API int coli_moe_debug_routing(coli_moe_t *h, coli_moe_routing *dst);
+
+/* Kernel launches the last forward enqueued (for launch accounting). */
+COLI_API int32_t coli_moe_last_launch_count(const coli_moe_t *h);
+
+/* Stage timing. With profiling enabled (enable != 0) every forward records CUDA events on the
+ * handle's stream between its stages; coli_moe_stage_times then synchronises the stream and
+ * writes the last forward's stage durations in milliseconds to ms[0..COLI_STAGES-1]:
+ * router, permute, FFN gate/up, FFN down, combine. Returns COLI_ERR_INVALID_ARG when profiling
+ * is off or no forward has run since it was enabled. */
+#define COLI_STAGES 5
+COLI_API int coli_moe_set_profiling(coli_moe_t *h, int32_t enable);
+COLI_API int coli_moe_stage_times(coli_moe_t *h, float *ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COLIMOE_H */

@@ -1,0 +1,248 @@
+"""Python binding of libcolimoe.so: the C ABI of include/colimoe.h under the same names.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels. torch
+provides device memory and streams. There is no CPU fallback: if the library is missing or the
+device is not a GB300, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libcolimoe.so")
+
+COLI_OK = 0
+COLI_ERR_INVALID_ARG = -1
+COLI_ERR_UNSUPPORTED_ARCH = -2
+COLI_ERR_OUT_OF_MEMORY = -3
+COLI_ERR_CUDA = -4
+COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM = 0, 1, 2
+
+EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "coli_moe_destroy",
+            "coli_moe_last_error", "coli_moe_set_ffn_path", "coli_moe_debug_routing",
+            "coli_moe_last_launch_count", "coli_moe_set_profiling", "coli_moe_stage_times")
+COLI_STAGES = 5
+STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
+
+
+class coli_moe_config(C.Structure):
+    _fields_ = [("num_experts", C.c_int32), ("hidden", C.c_int32), ("inter", C.c_int32),
+                ("shared_inter", C.c_int32), ("max_tokens", C.c_int32), ("max_top_k", C.c_int32)]
+
+
+class coli_mxfp4_experts(C.Structure):
+    _fields_ = [("gate_up_codes", C.c_void_p), ("gate_up_scales", C.c_void_p),
+                ("down_codes", C.c_void_p), ("down_scales", C.c_void_p)]
+
+
+class coli_moe_routing(C.Structure):
+    _fields_ = [("scores", C.c_void_p), ("idx", C.c_void_p), ("weights", C.c_void_p), ("cnt", C.c_void_p),
+                ("off", C.c_void_p), ("src_token", C.c_void_p), ("inv_row", C.c_void_p)]
+
+
+class ColiError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"colimoe error {code}: {msg}")
+        self.code = code
+
+
+_lib: Optional[C.CDLL] = None
+
+
+def load(path: str = LIB_PATH) -> C.CDLL:
+    """Loads the library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m routed_moe_fp4_gb300.build` "
+                           "(nvcc, sm_103a); there is no fallback implementation")
+    lib = C.CDLL(path)
+    vp = C.c_void_p
+    lib.coli_moe_create.argtypes = [C.POINTER(coli_moe_config), vp, C.POINTER(vp)]
+    lib.coli_moe_create.restype = C.c_int
+    fwd_args = [vp, vp, C.c_int32, vp, vp, C.POINTER(coli_mxfp4_experts), C.POINTER(coli_mxfp4_experts),
+                C.c_int32, vp]
+    lib.coli_moe_forward.argtypes = fwd_args
+    lib.coli_moe_forward.restype = C.c_int
+    lib.coli_moe_forward_host.argtypes = fwd_args
+    lib.coli_moe_forward_host.restype = C.c_int
+    lib.coli_moe_destroy.argtypes = [vp]
+    lib.coli_moe_destroy.restype = None
+    lib.coli_moe_last_error.argtypes = [vp]
+    lib.coli_moe_last_error.restype = C.c_char_p
+    lib.coli_moe_set_ffn_path.argtypes = [vp, C.c_int32]
+    lib.coli_moe_set_ffn_path.restype = C.c_int
+    lib.coli_moe_debug_routing.argtypes = [vp, C.POINTER(coli_moe_routing)]
+    lib.coli_moe_debug_routing.restype = C.c_int
+    lib.coli_moe_last_launch_count.argtypes = [vp]
+    lib.coli_moe_last_launch_count.restype = C.c_int32
+    lib.coli_moe_set_profiling.argtypes = [vp, C.c_int32]
+    lib.coli_moe_set_profiling.restype = C.c_int
+    lib.coli_moe_stage_times.argtypes = [vp, C.POINTER(C.c_float)]
+    lib.coli_moe_stage_times.restype = C.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    """Device/host address of a torch tensor, numpy array or int (None stays None)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    if hasattr(t, "ctypes"):
+        return t.ctypes.data
+    raise TypeError(f"cannot take the address of {type(t)}")
+
+
+def _check(h, rc: int) -> int:
+    if rc != COLI_OK:
+        raise ColiError(rc, coli_moe_last_error(h))
+    return rc
+
+
+# ---- the ABI under its own names --------------------------------------------------------
+
+def coli_moe_last_error(h=None) -> str:
+    return load().coli_moe_last_error(h).decode()
+
+
+def coli_moe_create(cfg: coli_moe_config, cuda_stream=None) -> C.c_void_p:
+    """cuda_stream: a torch.cuda.Stream, a raw cudaStream_t int, or None (default stream)."""
+    lib = load()
+    st = getattr(cuda_stream, "cuda_stream", cuda_stream)
+    out = C.c_void_p()
+    rc = lib.coli_moe_create(C.byref(cfg), st, C.byref(out))
+    _check(None, rc)
+    return out
+
+
+def coli_moe_forward(h, x_bf16, T: int, router_w, router_bias, packed_experts: coli_mxfp4_experts,
+                     shared_expert: Optional[coli_mxfp4_experts], top_k: int, out_bf16) -> int:
+    rc = load().coli_moe_forward(h, _ptr(x_bf16), T, _ptr(router_w), _ptr(router_bias), C.byref(packed_experts),
+                                 C.byref(shared_expert) if shared_expert is not None else None, top_k,
+                                 _ptr(out_bf16))
+    return _check(h, rc)
+
+
+def coli_moe_forward_host(h, x_bf16_host, T: int, router_w, router_bias, packed_experts: coli_mxfp4_experts,
+                          shared_expert: Optional[coli_mxfp4_experts], top_k: int, out_bf16_host) -> int:
+    rc = load().coli_moe_forward_host(h, _ptr(x_bf16_host), T, _ptr(router_w), _ptr(router_bias),
+                                      C.byref(packed_experts),
+                                      C.byref(shared_expert) if shared_expert is not None else None, top_k,
+                                      _ptr(out_bf16_host))
+    return _check(h, rc)
+
+
+def coli_moe_destroy(h) -> None:
+    load().coli_moe_destroy(h)
+
+
+def coli_moe_set_ffn_path(h, path: int) -> int:
+    return _check(h, load().coli_moe_set_ffn_path(h, path))
+
+
+def coli_moe_debug_routing(h, dst: coli_moe_routing) -> int:
+    return _check(h, load().coli_moe_debug_routing(h, C.byref(dst)))
+
+
+def coli_moe_last_launch_count(h) -> int:
+    return load().coli_moe_last_launch_count(h)
+
+
+def coli_moe_set_profiling(h, enable: bool) -> int:
+    return _check(h, load().coli_moe_set_profiling(h, int(bool(enable))))
+
+
+def coli_moe_stage_times(h) -> dict:
+    """Stage durations (ms) of the last profiled forward, by stage name."""
+    buf = (C.c_float * COLI_STAGES)()
+    _check(h, load().coli_moe_stage_times(h, buf))
+    return dict(zip(STAGE_NAMES, [float(v) for v in buf]))
+
+
+# ---- convenience: device-resident inputs of a workload -----------------------------------
+
+class DeviceExperts:
+    """MXFP4 expert arrays copied to the device, with the struct the ABI takes."""
+
+    def __init__(self, host, device="cuda"):
+        import torch
+        self.tensors = [torch.from_numpy(a).to(device) for a in
+                        (host.gate_up_codes, host.gate_up_scales, host.down_codes, host.down_scales)]
+        self.struct = coli_mxfp4_experts(*[t.data_ptr() for t in self.tensors])
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() for t in self.tensors)
+
+
+class MoELayer:
+    """A handle plus device copies of one workload's weights (router, experts, shared)."""
+
+    def __init__(self, inputs, max_tokens: Optional[int] = None, stream=None, device="cuda"):
+        import torch
+        wl = inputs.workload
+        self.wl = wl
+        self.top_k = wl.top_k
+        self.router_w = torch.from_numpy(inputs.router_w).to(device)
+        self.router_b = None if inputs.router_b is None else torch.from_numpy(inputs.router_b).to(device)
+        self.experts = DeviceExperts(inputs.experts, device)
+        self.shared = DeviceExperts(inputs.shared, device) if inputs.shared is not None else None
+        cfg = coli_moe_config(wl.E, wl.H, wl.I, wl.I_s if inputs.shared is not None else 0,
+                              max_tokens or max(wl.T, 1), wl.top_k)
+        self.stream = stream
+        self.h = coli_moe_create(cfg, stream)
+
+    def forward(self, x, out, T: Optional[int] = None) -> None:
+        T = x.shape[0] if T is None else T
+        coli_moe_forward(self.h, x, T, self.router_w, self.router_b, self.experts.struct,
+                         self.shared.struct if self.shared is not None else None, self.top_k, out)
+
+    def forward_host(self, x_host, out_host, T: Optional[int] = None) -> None:
+        T = x_host.shape[0] if T is None else T
+        coli_moe_forward_host(self.h, x_host, T, self.router_w, self.router_b, self.experts.struct,
+                              self.shared.struct if self.shared is not None else None, self.top_k, out_host)
+
+    def set_ffn_path(self, path: int) -> None:
+        coli_moe_set_ffn_path(self.h, path)
+
+    def routing(self, T: int):
+        """Routing of the last forward as numpy arrays."""
+        import numpy as np
+        wl = self.wl
+        k, E = self.top_k, wl.E
+        rows = T * k + (T if self.shared is not None else 0)
+        r = dict(scores=np.zeros((T, E), np.float32), idx=np.zeros((T, k), np.int32),
+                 weights=np.zeros((T, k), np.float32), cnt=np.zeros(E + 1, np.int32),
+                 off=np.zeros(E + 2, np.int32), src_token=np.zeros(rows, np.int32),
+                 inv_row=np.zeros((T, k), np.int32))
+        dst = coli_moe_routing(*[r[n].ctypes.data for n in
+                                 ("scores", "idx", "weights", "cnt", "off", "src_token", "inv_row")])
+        coli_moe_debug_routing(self.h, dst)
+        return r
+
+    def set_profiling(self, enable: bool) -> None:
+        coli_moe_set_profiling(self.h, enable)
+
+    def stage_times(self) -> dict:
+        return coli_moe_stage_times(self.h)
+
+    def launches(self) -> int:
+        return coli_moe_last_launch_count(self.h)
+
+    def close(self) -> None:
+        if self.h:
+            coli_moe_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

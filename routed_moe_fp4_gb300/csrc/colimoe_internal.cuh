@@ -1,0 +1,73 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "colimoe.h"
+
+namespace colimoe {
+
+// One expert set in the packed MXFP4 layout (see colimoe.h).
+struct ExpertSet {
+    const uint8_t *gu_codes;    // [E][2I][H/2]
+    const uint8_t *gu_scales;   // [E][2I][H/32]
+    const uint8_t *d_codes;     // [E][H][I/2]
+    const uint8_t *d_scales;    // [E][H][I/32]
+};
+
+// Device workspace, sized at create for (max_tokens, max_top_k).
+struct Workspace {
+    float *scores = nullptr;        // [Tm][E]
+    int32_t *idx = nullptr;         // [Tm][km]
+    float *w = nullptr;             // [Tm][km]
+    int32_t *inv_row = nullptr;     // [Tm][km]
+    int32_t *src_token = nullptr;   // [Tm*km + Tm]
+    int32_t *cnt = nullptr;         // [E+1]
+    int32_t *off = nullptr;         // [E+2]
+    int32_t *touched = nullptr;     // [E+1] non-empty groups, ascending
+    int32_t *n_touched = nullptr;   // [1]
+    __nv_bfloat16 *xp = nullptr;    // [Tm*km + Tm][H] expert-grouped activation rows
+    __nv_bfloat16 *h = nullptr;     // [Tm*km + Tm][I_max] SwiGLU output rows
+    float *y = nullptr;             // [Tm*km + Tm][H] expert output rows
+    __nv_bfloat16 *x_stage = nullptr;    // [Tm][H] forward_host input staging
+    __nv_bfloat16 *out_stage = nullptr;  // [Tm][H] forward_host output staging
+    void *tile_sched = nullptr;     // grouped-GEMM tile schedule (see gemm_tc.cu)
+    size_t tile_sched_bytes = 0;
+};
+
+// Arguments of the expert FFN stage: groups 0..E-1 are the routed experts, group E the
+// shared expert. Group g owns rows [off[g], off[g] + cnt[g]) of xp / h / y.
+struct FfnArgs {
+    ExpertSet routed;
+    ExpertSet shared;
+    int E, H, I, I_s, I_max;
+    int rows;                       // T*k + (shared ? T : 0), known on the host
+    const int32_t *cnt;
+    const int32_t *off;
+    const int32_t *touched;
+    const int32_t *n_touched;
+    const __nv_bfloat16 *xp;
+    __nv_bfloat16 *h;
+    float *y;
+};
+
+// Launchers. Each returns the number of kernels it enqueued, or -1 on a launch error
+// (the CUDA error is then available from cudaGetLastError()).
+int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
+                  int E, int top_k, float *scores, int32_t *idx, float *w, cudaStream_t st);
+int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
+                   int H, Workspace &ws, cudaStream_t st);
+// `mid` (may be null): an event recorded between the gate/up and the down kernels.
+int launch_ffn_gemv(const FfnArgs &a, int num_sms, cudaEvent_t mid, cudaStream_t st);
+int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T, int H, int top_k,
+                   bool with_shared, __nv_bfloat16 *out, cudaStream_t st);
+
+// Grouped tcgen05 GEMM path (gemm_tc.cu).
+size_t gemm_sched_bytes(int E, int max_rows);
+bool gemm_available();
+int launch_ffn_gemm(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
+
+}  // namespace colimoe

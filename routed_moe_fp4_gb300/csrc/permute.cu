@@ -1,0 +1,149 @@
+// A2 permute: per-expert histogram, exclusive scan, deterministic scatter into expert-grouped
+// rows and the inverse map ("the CUDA tier wired into the DeepSeek V4 engine", What it is:
+// expert-grouped GEMM rows).
+//
+// The row of (token t, slot j) with e = idx[t][j] is off[e] + #{t' < t : e in idx[t']}: a stable
+// grouping by (expert, token), computed without atomics on positions, so it is the same on every
+// run. Group E is the shared expert with rows off[E] + t for every token t. The activation rows
+// are gathered into that order (xp) for the expert FFN.
+#include "colimoe_internal.cuh"
+
+namespace colimoe {
+namespace {
+
+__global__ void permute_count(const int32_t *__restrict__ idx, int n, int32_t *__restrict__ cnt) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        atomicAdd(&cnt[idx[i]], 1);
+}
+
+// Exclusive block scan of one value per thread (blockDim.x == 1024). Returns the exclusive
+// prefix; *total receives the block sum.
+__device__ int block_exclusive_scan(int v, int *smem_warp, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) smem_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = smem_warp[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        smem_warp[lane] = wi - w;          // exclusive prefix of warp sums
+        if (lane == 31) smem_warp[32] = wi;
+    }
+    __syncthreads();
+    const int res = smem_warp[warp] + incl - v;
+    *total = smem_warp[32];
+    __syncthreads();
+    return res;
+}
+
+// One block of 1024 threads; groups g = 0..E (E <= 1024 + shared handled as the last entry).
+__global__ void __launch_bounds__(1024)
+permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__restrict__ touched,
+             int32_t *__restrict__ n_touched, int E, int shared_rows) {
+    __shared__ int smem[33];
+    const int G = E + 1;
+    if (threadIdx.x == 0) cnt[E] = shared_rows;
+    __syncthreads();
+    int base = 0, tbase = 0;
+    for (int g0 = 0; g0 < G; g0 += 1024) {
+        const int g = g0 + threadIdx.x;
+        const int c = g < G ? cnt[g] : 0;
+        int tot, ttot;
+        const int ex = block_exclusive_scan(c, smem, &tot);
+        const int tex = block_exclusive_scan(c > 0 ? 1 : 0, smem, &ttot);
+        if (g < G) {
+            off[g] = base + ex;
+            if (c > 0) touched[tbase + tex] = g;
+        }
+        base += tot;
+        tbase += ttot;
+    }
+    if (threadIdx.x == 0) {
+        off[G] = base;
+        *n_touched = tbase;
+    }
+}
+
+// Block e scans the tokens in order and places the (t, j) pairs routed to expert e.
+// Block E writes the shared expert's identity rows.
+__global__ void __launch_bounds__(256)
+permute_scatter(const int32_t *__restrict__ idx, int T, int E, int top_k, const int32_t *__restrict__ cnt,
+                const int32_t *__restrict__ off, int32_t *__restrict__ src_token, int32_t *__restrict__ inv_row) {
+    const int e = blockIdx.x;
+    if (e == E) {
+        const int base = off[E];
+        for (int t = threadIdx.x; t < cnt[E]; t += blockDim.x) src_token[base + t] = t;
+        return;
+    }
+    if (cnt[e] == 0) return;
+    __shared__ int warp_tot[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int running = off[e];
+    for (int t0 = 0; t0 < T; t0 += 256) {
+        const int t = t0 + threadIdx.x;
+        int slot = -1;
+        if (t < T) {
+            for (int j = 0; j < top_k; ++j)
+                if (idx[(size_t)t * top_k + j] == e) slot = j;
+        }
+        const unsigned ballot = __ballot_sync(0xffffffffu, slot >= 0);
+        const int in_warp = __popc(ballot & ((1u << lane) - 1u));
+        if (lane == 0) warp_tot[warp] = __popc(ballot);
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            before += (w < warp) ? warp_tot[w] : 0;
+            total += warp_tot[w];
+        }
+        if (slot >= 0) {
+            const int row = running + before + in_warp;
+            src_token[row] = t;
+            inv_row[(size_t)t * top_k + slot] = row;
+        }
+        running += total;
+        __syncthreads();
+    }
+}
+
+// xp[row] = x[src_token[row]] for every row, 16 bytes per thread step.
+__global__ void __launch_bounds__(256)
+permute_gather(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
+               __nv_bfloat16 *__restrict__ xp) {
+    const int vec_per_row = H / 8;
+    const size_t total = (size_t)rows * vec_per_row;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int row = (int)(i / vec_per_row), v = (int)(i % vec_per_row);
+        const int t = src_token[row];
+        reinterpret_cast<uint4 *>(xp + (size_t)row * H)[v] =
+            __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * H) + v);
+    }
+}
+
+}  // namespace
+
+int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
+                   int H, Workspace &ws, cudaStream_t st) {
+    const int n = T * top_k;
+    const int rows = n + (with_shared ? T : 0);
+    if (cudaMemsetAsync(ws.cnt, 0, sizeof(int32_t) * (E + 1), st) != cudaSuccess) return -1;
+    permute_count<<<(n + 255) / 256, 256, 0, st>>>(idx, n, ws.cnt);
+    permute_scan<<<1, 1024, 0, st>>>(ws.cnt, ws.off, ws.touched, ws.n_touched, E, with_shared ? T : 0);
+    permute_scatter<<<E + 1, 256, 0, st>>>(idx, T, E, top_k, ws.cnt, ws.off, ws.src_token, ws.inv_row);
+    const size_t vecs = (size_t)rows * (H / 8);
+    const int blocks = (int)((vecs + 255) / 256 < 65536 ? (vecs + 255) / 256 : 65536);
+    permute_gather<<<blocks, 256, 0, st>>>(x, H, ws.src_token, rows, ws.xp);
+    return cudaPeekAtLastError() == cudaSuccess ? 4 : -1;
+}
+
+}  // namespace colimoe

@@ -1,0 +1,230 @@
+// A1 router: fp32 logits, sigmoid scores, bias-adjusted top-k with warp shuffles, renormalised
+// weights ("the CUDA tier wired into the DeepSeek V4 engine", What it is: route on device).
+//
+// logits[t][e] = sum_h x[t][h] * Wr[e][h] in fp32 (x is bf16, exact in fp32); s = 1/(1+exp(-z)).
+// key = fp32(s + b); the top_k largest keys in descending order, bit-identical keys going to
+// the lower expert index; w_j = s_j / S, S the fp32 sum of the chosen s in slot order, one
+// IEEE division each. Built without fast-math: every add, divide and expf is the IEEE/accurate one.
+#include "colimoe_internal.cuh"
+
+#include <float.h>
+
+namespace colimoe {
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ float sigmoidf_ieee(float z) {
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+}
+
+// Small T: one warp per expert, lanes across H, up to 8 tokens per block row.
+constexpr int kSmallWarps = 4;
+constexpr int kSmallTok = 8;
+
+__global__ void __launch_bounds__(kSmallWarps * 32)
+router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const float *__restrict__ wr,
+                    int E, float *__restrict__ scores) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kSmallWarps + warp;
+    const int t0 = blockIdx.y * kSmallTok;
+    if (e >= E) return;
+    const int nt = min(kSmallTok, T - t0);
+    float acc[kSmallTok];
+#pragma unroll
+    for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
+    const float4 *wrow = reinterpret_cast<const float4 *>(wr + (size_t)e * H);
+    for (int c = lane; c < H / 4; c += 32) {
+        const float4 wv = __ldg(wrow + c);
+#pragma unroll
+        for (int t = 0; t < kSmallTok; ++t) {
+            if (t < nt) {
+                const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(x + (size_t)(t0 + t) * H) + c);
+                float a = acc[t];
+                a = fmaf(bf16_lo(xv.x), wv.x, a);
+                a = fmaf(bf16_hi(xv.x), wv.y, a);
+                a = fmaf(bf16_lo(xv.y), wv.z, a);
+                a = fmaf(bf16_hi(xv.y), wv.w, a);
+                acc[t] = a;
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kSmallTok; ++t) {
+        float a = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (lane == 0 && t < nt) scores[(size_t)(t0 + t) * E + e] = sigmoidf_ieee(a);
+    }
+}
+
+// Large T: a 64 tokens x 64 experts tile per block, 4 x 4 outputs per thread, K chunks of 32.
+constexpr int kTileT = 64, kTileE = 64, kTileK = 32;
+
+__global__ void __launch_bounds__(256)
+router_logits_tiled(const __nv_bfloat16 *__restrict__ x, int T, int H, const float *__restrict__ wr,
+                    int E, float *__restrict__ scores) {
+    __shared__ float xs[kTileK][kTileT + 4];
+    __shared__ float ws[kTileK][kTileE + 4];
+    const int tid = threadIdx.x;
+    const int tt = blockIdx.x * kTileT, ee = blockIdx.y * kTileE;
+    const int ty = tid / 16, tx = tid % 16;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+
+    const int lr = tid / 4, lk = (tid % 4) * 8;   // loader: row (token / expert), 8 k values
+    for (int k0 = 0; k0 < H; k0 += kTileK) {
+        {   // x tile: 64 tokens x 32 k as bf16 -> fp32, transposed
+            const int t = tt + lr;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (t < T) v = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * H + k0 + lk));
+            xs[lk + 0][lr] = bf16_lo(v.x); xs[lk + 1][lr] = bf16_hi(v.x);
+            xs[lk + 2][lr] = bf16_lo(v.y); xs[lk + 3][lr] = bf16_hi(v.y);
+            xs[lk + 4][lr] = bf16_lo(v.z); xs[lk + 5][lr] = bf16_hi(v.z);
+            xs[lk + 6][lr] = bf16_lo(v.w); xs[lk + 7][lr] = bf16_hi(v.w);
+        }
+        {   // router tile: 64 experts x 32 k, transposed
+            const int e = ee + lr;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            if (e < E) {
+                const float4 *p = reinterpret_cast<const float4 *>(wr + (size_t)e * H + k0 + lk);
+                a = __ldg(p);
+                b = __ldg(p + 1);
+            }
+            ws[lk + 0][lr] = a.x; ws[lk + 1][lr] = a.y; ws[lk + 2][lr] = a.z; ws[lk + 3][lr] = a.w;
+            ws[lk + 4][lr] = b.x; ws[lk + 5][lr] = b.y; ws[lk + 6][lr] = b.z; ws[lk + 7][lr] = b.w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < kTileK; ++k) {
+            const float4 av = *reinterpret_cast<const float4 *>(&xs[k][ty * 4]);
+            const float4 bv = *reinterpret_cast<const float4 *>(&ws[k][tx * 4]);
+            const float a[4] = {av.x, av.y, av.z, av.w};
+            const float b[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = tt + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int e = ee + tx * 4 + j;
+            if (e < E) scores[(size_t)t * E + e] = sigmoidf_ieee(acc[i][j]);
+        }
+    }
+}
+
+// Top-k: one warp per token; lane l holds experts l, l+32, ...; k rounds of a warp arg-max on
+// (key descending, expert ascending).
+template <int NPL>
+__global__ void __launch_bounds__(256)
+router_topk(const float *__restrict__ scores, const float *__restrict__ bias, int T, int E, int top_k,
+            int32_t *__restrict__ idx, float *__restrict__ w) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= T) return;
+    float key[NPL], sc[NPL];
+    uint32_t taken = 0;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+            sc[i] = scores[(size_t)t * E + e];
+            key[i] = __fadd_rn(sc[i], bias ? bias[e] : 0.0f);
+        } else {
+            sc[i] = 0.f;
+            key[i] = -INFINITY;
+            taken |= 1u << i;          // padding slots are never chosen
+        }
+    }
+    float s_sel[32];
+    int e_sel[32];
+    for (int j = 0; j < top_k; ++j) {
+        float bk = -INFINITY, bs = 0.f;
+        int be = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            const int e = lane + 32 * i;
+            const bool free_ = !((taken >> i) & 1u);
+            if (free_ && (key[i] > bk || (key[i] == bk && e < be))) {
+                bk = key[i];
+                be = e;
+                bs = sc[i];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+            if (ok > bk || (ok == bk && oe < be)) {
+                bk = ok;
+                be = oe;
+                bs = os;
+            }
+        }
+        if (be == INT_MAX) {           // only NaN keys left: take the lowest free expert
+            int cand = INT_MAX;
+            float cs = 0.f;
+#pragma unroll
+            for (int i = NPL - 1; i >= 0; --i)
+                if (!((taken >> i) & 1u)) { cand = lane + 32 * i; cs = sc[i]; }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const int oc = __shfl_xor_sync(0xffffffffu, cand, o);
+                const float os = __shfl_xor_sync(0xffffffffu, cs, o);
+                if (oc < cand) { cand = oc; cs = os; }
+            }
+            be = cand;
+            bs = cs;
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        s_sel[j] = bs;
+        e_sel[j] = be;
+    }
+    if (lane == 0) {
+        float S = 0.0f;
+        for (int j = 0; j < top_k; ++j) S = __fadd_rn(S, s_sel[j]);
+        for (int j = 0; j < top_k; ++j) {
+            idx[(size_t)t * top_k + j] = e_sel[j];
+            w[(size_t)t * top_k + j] = __fdiv_rn(s_sel[j], S);
+        }
+    }
+}
+
+}  // namespace
+
+int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
+                  int E, int top_k, float *scores, int32_t *idx, float *w, cudaStream_t st) {
+    int n = 0;
+    if (T < 64) {
+        dim3 grid((E + kSmallWarps - 1) / kSmallWarps, (T + kSmallTok - 1) / kSmallTok);
+        router_logits_small<<<grid, kSmallWarps * 32, 0, st>>>(x, T, H, router_w, E, scores);
+    } else {
+        dim3 grid((T + kTileT - 1) / kTileT, (E + kTileE - 1) / kTileE);
+        router_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, router_w, E, scores);
+    }
+    ++n;
+    const int npl = (E + 31) / 32;
+    const dim3 grid((T + 7) / 8);
+    if (npl <= 1)       router_topk<1><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
+    else if (npl <= 2)  router_topk<2><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
+    else if (npl <= 4)  router_topk<4><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
+    else if (npl <= 8)  router_topk<8><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
+    else if (npl <= 16) router_topk<16><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
+    else                router_topk<32><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
+    ++n;
+    return cudaPeekAtLastError() == cudaSuccess ? n : -1;
+}
+
+}  // namespace colimoe

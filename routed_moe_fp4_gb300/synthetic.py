@@ -211,11 +211,12 @@ def make_experts(seed: int, tag: str, E: int, H: int, I: int, threads: Optional[
     return out
 
 
-def make_inputs(name: str, seed: int = 0, T: Optional[int] = None, with_experts: bool = True,
+def make_inputs(name, seed: int = 0, T: Optional[int] = None, with_experts: bool = True,
                 unbiased: bool = False) -> MoEInputs:
-    """All inputs of a named workload. `T` overrides the token count (rows keep their streams).
-    `unbiased` returns no router bias (used when the stored bias is being fitted)."""
-    wl = WORKLOADS[name]
+    """All inputs of a workload (a name in WORKLOADS or a Workload). `T` overrides the token count
+    (rows keep their streams). `unbiased` returns no router bias (used when the stored bias is
+    being fitted)."""
+    wl = WORKLOADS[name] if isinstance(name, str) else name
     if T is not None:
         wl = dataclasses.replace(wl, T=T)
     cal = calibration()
@@ -242,6 +243,7 @@ def make_inputs(name: str, seed: int = 0, T: Optional[int] = None, with_experts:
     if with_experts:
         experts = make_experts(seed, wl.name + "/experts", wl.E, wl.H, wl.I)
         shared = make_experts(seed, wl.name + "/shared", 1, wl.H, wl.I_s) if wl.I_s > 0 else None
+
     else:
         experts = shared = None
     return MoEInputs(wl, x, router_w, router_b, experts, shared)

@@ -1,0 +1,118 @@
+"""GPU-vs-oracle parity protocol (used by the -m gpu tests and the smoke check).
+
+Routing is compared given identical fp32 scores: the GPU's scores must be within 1e-5 of the
+oracle's fp64 sigmoid of fp64 logits; the oracle's key/top-k/renormalisation and permutation run
+on the GPU's scores and must match the GPU's idx, w, cnt, off, src_token and inv_row bit for bit;
+the oracle's expert FFN and combine then use those indices and weights, and the GPU output must
+satisfy max|err| <= 2e-2 * RMS(oracle output). Tokens whose fp64-score routing differs from the
+GPU's must sit within 1e-5 of a key tie at the k / k+1 boundary.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+
+SCORE_TOL = 1e-5
+OUT_TOL = 2e-2          # max |err| <= OUT_TOL * RMS(oracle output)
+TIE_TOL = 1e-5
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclasses.dataclass
+class ParityReport:
+    T: int
+    tokens_checked: int
+    max_score_err: float
+    routing_bit_exact: bool
+    own_routing_diffs: int
+    max_err: float
+    rms_ref: float
+    rel_err: float
+    launches: int
+
+    @property
+    def ok(self) -> bool:
+        return (self.max_score_err <= SCORE_TOL and self.routing_bit_exact and self.rel_err <= OUT_TOL)
+
+
+def run_gpu(inputs, path: int = 0, T: Optional[int] = None, repeats: int = 1, layer=None):
+    """Runs the library on `inputs`; returns (out bf16 bits [T, H], routing dict, launches)."""
+    import torch
+    from routed_moe_fp4_gb300 import colimoe as cm
+    T = inputs.x.shape[0] if T is None else T
+    own = layer is None
+    if own:
+        layer = cm.MoELayer(inputs, max_tokens=max(T, 1))
+    layer.set_ffn_path(path)
+    x = torch.from_numpy(inputs.x[:T].view(np.int16)).cuda()
+    outs = []
+    for _ in range(repeats):
+        out = torch.empty((T, inputs.workload.H), dtype=torch.int16, device="cuda")
+        layer.forward(x, out, T)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy().view(np.uint16))
+    routing = layer.routing(T)
+    launches = layer.launches()
+    if own:
+        layer.close()
+    return outs, routing, launches
+
+
+def check(oracle, inputs, out_bits: np.ndarray, routing: dict, tokens: Optional[Sequence[int]] = None,
+          launches: int = 0) -> ParityReport:
+    wl = inputs.workload
+    T = out_bits.shape[0]
+    k = wl.top_k
+    s_gpu = routing["scores"]
+    # (ii) bit-exact routing and permutation from the GPU's scores
+    idx_o, w_o = oracle.route(s_gpu, inputs.router_b, k)
+    cnt_o, off_o, src_o, inv_o = oracle.permute(idx_o, wl.E, with_shared=inputs.shared is not None)
+    exact = (np.array_equal(idx_o, routing["idx"]) and np.array_equal(w_o.view(np.uint32),
+                                                                       routing["weights"].view(np.uint32))
+             and np.array_equal(cnt_o, routing["cnt"]) and np.array_equal(off_o, routing["off"])
+             and np.array_equal(src_o, routing["src_token"]) and np.array_equal(inv_o, routing["inv_row"]))
+    if tokens is None:
+        tokens = list(range(T))
+    tokens = np.asarray(sorted(set(int(t) for t in tokens)), np.int32)
+    # (i) scores against fp64 sigmoid of fp64 logits, on the checked tokens
+    s_ref = oracle.scores(np.ascontiguousarray(inputs.x[tokens]), inputs.router_w)
+    max_score_err = float(np.abs(s_ref.astype(np.float64) - s_gpu[tokens].astype(np.float64)).max())
+    # (iv) the oracle's own routing: differences only at near-ties
+    idx_own, _ = oracle.route(s_ref, inputs.router_b, k)
+    diffs = 0
+    for n, t in enumerate(tokens):
+        if set(idx_own[n].tolist()) != set(routing["idx"][t].tolist()):
+            key = s_ref[n].astype(np.float64) + (0 if inputs.router_b is None else inputs.router_b)
+            srt = np.sort(key)[::-1]
+            assert srt[k - 1] - srt[k] < TIE_TOL, f"token {t}: own routing differs away from a tie"
+            diffs += 1
+    # (iii) output: oracle FFN + combine with the GPU's (== oracle's) indices and weights
+    ref_bits, ref64 = oracle.tokens_output(inputs.x, routing["idx"], routing["weights"], inputs.experts,
+                                           inputs.shared, tokens)
+    got = bf16_bits_to_f32(out_bits[tokens]).astype(np.float64)
+    ref = bf16_bits_to_f32(ref_bits).astype(np.float64)
+    err = float(np.abs(got - ref).max())
+    rms = float(np.sqrt((ref64 ** 2).mean()))
+    return ParityReport(T, len(tokens), max_score_err, bool(exact), diffs, err, rms,
+                        err / rms if rms > 0 else err, launches)
+
+
+def sample_tokens(routing: dict, T: int, n: int, seed: int = 0) -> list:
+    """A seeded token sample that includes tokens routed to the heaviest and lightest touched experts."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    idx = routing["idx"]
+    cnt = routing["cnt"][:-1]
+    touched = np.where(cnt > 0)[0]
+    picks = set()
+    if len(touched):
+        heavy, light = touched[np.argmax(cnt[touched])], touched[np.argmin(cnt[touched])]
+        for e in (heavy, light):
+            picks.add(int(np.where((idx == e).any(1))[0][0]))
+    picks.update(int(t) for t in rng.choice(T, size=min(n, T), replace=False))
+    picks.update({0, T - 1})
+    return sorted(picks)

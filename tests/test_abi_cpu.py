@@ -1,0 +1,74 @@
+"""The C-ABI library loads and exports every symbol the header declares; host-side argument
+checks that need no GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from routed_moe_fp4_gb300 import build, colimoe
+    build.build()
+    return colimoe.load()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "colimoe.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"COLI_API[^;(]*?\b(coli_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    assert {"coli_moe_create", "coli_moe_forward", "coli_moe_destroy"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from routed_moe_fp4_gb300 import colimoe
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(colimoe.EXPORTED)
+
+
+def test_create_rejects_bad_config(lib):
+    from routed_moe_fp4_gb300 import colimoe as cm
+    bad = [
+        cm.coli_moe_config(0, 256, 128, 128, 4, 2),       # E = 0
+        cm.coli_moe_config(8, 200, 128, 128, 4, 2),       # H not a multiple of 128
+        cm.coli_moe_config(8, 256, 96, 128, 4, 2),        # I not a multiple of 128
+        cm.coli_moe_config(8, 256, 128, 100, 4, 2),       # I_s not a multiple of 128
+        cm.coli_moe_config(8, 256, 128, 128, 0, 2),       # max_tokens = 0
+        cm.coli_moe_config(8, 256, 128, 128, 4, 9),       # max_top_k > E
+        cm.coli_moe_config(64, 256, 128, 128, 4, 33),     # max_top_k > 32
+    ]
+    for cfg in bad:
+        out = C.c_void_p(1)
+        rc = lib.coli_moe_create(C.byref(cfg), None, C.byref(out))
+        assert rc == cm.COLI_ERR_INVALID_ARG
+        assert out.value is None
+        assert "invalid config" in cm.coli_moe_last_error(None)
+
+
+def test_null_arguments(lib):
+    from routed_moe_fp4_gb300 import colimoe as cm
+    assert lib.coli_moe_create(None, None, None) == cm.COLI_ERR_INVALID_ARG
+    lib.coli_moe_destroy(None)                       # no-op
+    assert lib.coli_moe_set_ffn_path(None, 0) == cm.COLI_ERR_INVALID_ARG
+    assert lib.coli_moe_forward(None, None, 0, None, None, None, None, 1, None) == cm.COLI_ERR_INVALID_ARG
+    assert lib.coli_moe_last_launch_count(None) == 0
+    assert isinstance(cm.coli_moe_last_error(None), str)
+
+
+def test_create_without_gpu_is_an_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this host has a GPU")
+    from routed_moe_fp4_gb300 import colimoe as cm
+    cfg = cm.coli_moe_config(8, 256, 128, 128, 4, 2)
+    out = C.c_void_p()
+    rc = lib.coli_moe_create(C.byref(cfg), None, C.byref(out))
+    assert rc == cm.COLI_ERR_UNSUPPORTED_ARCH and out.value is None

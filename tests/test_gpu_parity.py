@@ -1,0 +1,152 @@
+"""CUDA path vs the oracle (needs a GB300). Every case goes through the C ABI."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from routed_moe_fp4_gb300 import synthetic as S
+from tests import parity as P
+
+pytestmark = pytest.mark.gpu
+
+GEMV, GEMM, AUTO = 1, 2, 0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from routed_moe_fp4_gb300 import build, colimoe
+    build.build()
+    colimoe.load()
+
+
+def _assert_ok(rep):
+    assert rep.routing_bit_exact, "routing/permutation differ from the oracle on identical scores"
+    assert rep.max_score_err <= P.SCORE_TOL, rep
+    assert rep.rel_err <= P.OUT_TOL, rep
+
+
+def _run(oracle, inputs, path, n_tokens=None, repeats=1):
+    outs, routing, launches = P.run_gpu(inputs, path=path, repeats=repeats)
+    T = inputs.x.shape[0]
+    tokens = None if n_tokens is None or n_tokens >= T else P.sample_tokens(routing, T, n_tokens)
+    rep = P.check(oracle, inputs, outs[0], routing, tokens, launches)
+    return rep, outs, routing
+
+
+@pytest.mark.parametrize("path", [GEMV, AUTO])
+def test_tiny_all_tokens(oracle, path):
+    inputs = S.make_inputs("tiny")
+    rep, outs, _ = _run(oracle, inputs, path)
+    _assert_ok(rep)
+    assert rep.launches > 0
+
+
+def test_tiny_matches_oracle_forward_exactly_routed(oracle):
+    """The full oracle forward (its own scores) agrees with the GPU on routing for the tiny case."""
+    inputs = S.make_inputs("tiny")
+    outs, routing, _ = P.run_gpu(inputs)
+    ref = oracle.moe_forward(inputs.x, inputs.router_w, inputs.router_b, 2, inputs.experts, inputs.shared)
+    assert np.array_equal(ref["idx"], routing["idx"])
+    got = P.bf16_bits_to_f32(outs[0]).astype(np.float64)
+    want = P.bf16_bits_to_f32(ref["out"]).astype(np.float64)
+    assert np.abs(got - want).max() <= P.OUT_TOL * np.sqrt((ref["out_f64"] ** 2).mean())
+
+
+def test_decode_all_tokens(oracle):
+    inputs = S.make_inputs("decode")
+    rep, _, _ = _run(oracle, inputs, AUTO)
+    _assert_ok(rep)
+    assert rep.own_routing_diffs == 0      # the margin workload has no near-ties
+
+
+@pytest.mark.parametrize("T", list(S.SWEEP_T))
+def test_sweep(oracle, T):
+    inputs = S.make_inputs(f"sweep_T{T}")
+    rep, _, _ = _run(oracle, inputs, AUTO, n_tokens=6)
+    _assert_ok(rep)
+
+
+def test_prefill_sampled(oracle):
+    inputs = S.make_inputs("prefill")
+    rep, _, _ = _run(oracle, inputs, AUTO, n_tokens=12)
+    _assert_ok(rep)
+
+
+def test_skewed_sampled(oracle):
+    inputs = S.make_inputs("skewed")
+    rep, _, routing = _run(oracle, inputs, AUTO, n_tokens=8)
+    _assert_ok(rep)
+    assert routing["cnt"][:-1].max() > 3000      # the Zipf head expert
+
+
+def test_repeatable_bitwise(oracle):
+    """Two forwards on the same inputs give bit-identical outputs (fixed-order reductions)."""
+    inputs = S.make_inputs("sweep_T16")
+    outs, _, _ = P.run_gpu(inputs, repeats=2)
+    assert np.array_equal(outs[0], outs[1])
+
+
+def _custom(name, **kw):
+    base = dataclasses.replace(S.WORKLOADS["tiny"], name=name)
+    return dataclasses.replace(base, **kw)
+
+
+@pytest.mark.parametrize("wl", [
+    _custom("edge_k1", top_k=1),
+    _custom("edge_E1", E=1, top_k=1),
+    _custom("edge_noshared", I_s=0),
+    _custom("edge_shared_wider", I_s=256),
+    _custom("edge_ragged", T=37, H=384, E=16, top_k=3),
+    _custom("edge_T1", T=1),
+    _custom("edge_many_experts", T=9, E=300, top_k=8, H=256),
+], ids=lambda w: w.name)
+def test_edge_cases(oracle, wl):
+    inputs = S.make_inputs(wl)
+    rep, _, _ = _run(oracle, inputs, AUTO)
+    _assert_ok(rep)
+
+
+def test_zero_tokens_is_noop():
+    import torch
+    from routed_moe_fp4_gb300 import colimoe as cm
+    inputs = S.make_inputs("tiny")
+    layer = cm.MoELayer(inputs)
+    x = torch.zeros((1, 256), dtype=torch.int16, device="cuda")
+    out = torch.full((1, 256), 7, dtype=torch.int16, device="cuda")
+    layer.forward(x, out, T=0)
+    torch.cuda.synchronize()
+    assert int(out[0, 0]) == 7 and layer.launches() == 0
+    layer.close()
+
+
+def test_bad_arguments_rejected():
+    import torch
+    from routed_moe_fp4_gb300 import colimoe as cm
+    inputs = S.make_inputs("tiny")
+    layer = cm.MoELayer(inputs)
+    x = torch.zeros((4, 256), dtype=torch.int16, device="cuda")
+    out = torch.zeros_like(x)
+    with pytest.raises(cm.ColiError) as e:
+        cm.coli_moe_forward(layer.h, x, 5, layer.router_w, None, layer.experts.struct, None, 2, out)
+    assert e.value.code == cm.COLI_ERR_INVALID_ARG and "max_tokens" in str(e.value)
+    with pytest.raises(cm.ColiError):
+        cm.coli_moe_forward(layer.h, x, 4, layer.router_w, None, layer.experts.struct, None, 3, out)
+    with pytest.raises(cm.ColiError):
+        cm.coli_moe_forward(layer.h, x, 4, layer.router_w, None, layer.experts.struct, None, 2, x)
+    layer.close()
+
+
+def test_forward_host_matches_device(oracle):
+    import torch
+    from routed_moe_fp4_gb300 import colimoe as cm
+    inputs = S.make_inputs("sweep_T4")
+    outs, _, _ = P.run_gpu(inputs)
+    layer = cm.MoELayer(inputs)
+    x_host = torch.from_numpy(inputs.x.view(np.int16)).pin_memory()
+    out_host = torch.zeros_like(x_host).pin_memory()
+    layer.forward_host(x_host, out_host)
+    assert np.array_equal(out_host.numpy().view(np.uint16), outs[0])
+    layer.close()
