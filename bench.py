@@ -291,13 +291,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--skip-cpu", action="store_true", help="no cpu_baseline (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         res = run_reference(args, args.workload)
     else:
         res = run_ours(args, args.workload)
-        if res is not None:
+        if res is not None and not args.skip_cpu:
             res["cpu_baseline"] = oracle_sample(args.workload, args.cpu_budget)
     if res is not None:
         print(json.dumps(res), flush=True)

@@ -4,8 +4,11 @@ Routing is compared given identical fp32 scores: the GPU's scores must be within
 oracle's fp64 sigmoid of fp64 logits; the oracle's key/top-k/renormalisation and permutation run
 on the GPU's scores and must match the GPU's idx, w, cnt, off, src_token and inv_row bit for bit;
 the oracle's expert FFN and combine then use those indices and weights, and the GPU output must
-satisfy max|err| <= 2e-2 * RMS(oracle output). Tokens whose fp64-score routing differs from the
-GPU's must sit within 1e-5 of a key tie at the k / k+1 boundary.
+satisfy |out - ref| <= 2e-2 * RMS(ref) + ulp_bf16(ref)/2 for every output, ref being the oracle's
+unrounded fp64 value: the bar bounds the computation's error, and the half ulp is the rounding
+that the bf16 output format forces on any implementation (a single rounding flip at an output of
+4x RMS is already 1 bf16 ulp > 2e-2 * RMS). Tokens whose fp64-score routing differs from the GPU's
+must sit within 1e-5 of a key tie at the k / k+1 boundary.
 """
 from __future__ import annotations
 
@@ -15,8 +18,16 @@ from typing import Optional, Sequence
 import numpy as np
 
 SCORE_TOL = 1e-5
-OUT_TOL = 2e-2          # max |err| <= OUT_TOL * RMS(oracle output)
+OUT_TOL = 2e-2          # max(|out - ref| - ulp_bf16(ref)/2) <= OUT_TOL * RMS(ref)
 TIE_TOL = 1e-5
+
+
+def half_ulp_bf16(v: np.ndarray) -> np.ndarray:
+    """Half the bf16 spacing at |v|: the rounding error any bf16 output of v may carry."""
+    a = np.abs(np.asarray(v, np.float64))
+    _, e = np.frexp(a)                      # a = m * 2^e, m in [0.5, 1)
+    ulp = np.ldexp(1.0, np.maximum(e - 8, -133))
+    return 0.5 * ulp
 
 
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
@@ -34,6 +45,7 @@ class ParityReport:
     rms_ref: float
     rel_err: float
     launches: int
+    rel_err_bf16: float = 0.0   # max |out - round_bf16(ref)| / RMS, for information
 
     @property
     def ok(self) -> bool:
@@ -96,10 +108,12 @@ def check(oracle, inputs, out_bits: np.ndarray, routing: dict, tokens: Optional[
                                            inputs.shared, tokens)
     got = bf16_bits_to_f32(out_bits[tokens]).astype(np.float64)
     ref = bf16_bits_to_f32(ref_bits).astype(np.float64)
-    err = float(np.abs(got - ref).max())
+    excess = np.abs(got - ref64) - half_ulp_bf16(ref64)
+    err = float(max(excess.max(), 0.0))
     rms = float(np.sqrt((ref64 ** 2).mean()))
+    err_bf16 = float(np.abs(got - ref).max())
     return ParityReport(T, len(tokens), max_score_err, bool(exact), diffs, err, rms,
-                        err / rms if rms > 0 else err, launches)
+                        err / rms if rms > 0 else err, launches, err_bf16 / rms if rms > 0 else err_bf16)
 
 
 def sample_tokens(routing: dict, T: int, n: int, seed: int = 0) -> list:
