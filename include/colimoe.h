@@ -160,6 +160,13 @@ COLI_API int coli_moe_debug_routing(coli_moe_t *h, coli_moe_routing *dst);
 /* Kernel launches the last forward enqueued (for launch accounting). */
 COLI_API int32_t coli_moe_last_launch_count(const coli_moe_t *h);
 
+/* Device error word. Kernels that wait on barriers bound every wait (about two seconds); a wait
+ * that runs out makes the kernel stop, record a code here (1: waiting for a weight stage,
+ * 2: waiting for a free stage, 3: waiting for an MMA, 4: waiting for an accumulator) and return,
+ * leaving that forward's output incomplete. Synchronises the stream, writes the code (0 = no
+ * error) to *code and clears it. */
+COLI_API int coli_moe_device_error(coli_moe_t *h, int32_t *code);
+
 /* Stage timing. With profiling enabled (enable != 0) every forward records CUDA events on the
  * handle's stream between its stages; coli_moe_stage_times then synchronises the stream and
  * writes the last forward's stage durations in milliseconds to ms[0..COLI_STAGES-1]:

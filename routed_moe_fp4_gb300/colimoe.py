@@ -22,7 +22,8 @@ COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM = 0, 1, 2
 
 EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "coli_moe_destroy",
             "coli_moe_last_error", "coli_moe_set_ffn_path", "coli_moe_debug_routing",
-            "coli_moe_last_launch_count", "coli_moe_set_profiling", "coli_moe_stage_times")
+            "coli_moe_last_launch_count", "coli_moe_set_profiling", "coli_moe_stage_times",
+            "coli_moe_device_error")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
 
@@ -83,6 +84,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_moe_set_profiling.restype = C.c_int
     lib.coli_moe_stage_times.argtypes = [vp, C.POINTER(C.c_float)]
     lib.coli_moe_stage_times.restype = C.c_int
+    lib.coli_moe_device_error.argtypes = [vp, C.POINTER(C.c_int32)]
+    lib.coli_moe_device_error.restype = C.c_int
     _lib = lib
     return lib
 
@@ -159,6 +162,13 @@ def coli_moe_set_profiling(h, enable: bool) -> int:
     return _check(h, load().coli_moe_set_profiling(h, int(bool(enable))))
 
 
+def coli_moe_device_error(h) -> int:
+    """Device error code of the forwards since the last call (0 = none); clears it."""
+    code = C.c_int32()
+    _check(h, load().coli_moe_device_error(h, C.byref(code)))
+    return code.value
+
+
 def coli_moe_stage_times(h) -> dict:
     """Stage durations (ms) of the last profiled forward, by stage name."""
     buf = (C.c_float * COLI_STAGES)()
@@ -232,6 +242,9 @@ class MoELayer:
 
     def stage_times(self) -> dict:
         return coli_moe_stage_times(self.h)
+
+    def device_error(self) -> int:
+        return coli_moe_device_error(self.h)
 
     def launches(self) -> int:
         return coli_moe_last_launch_count(self.h)

@@ -44,8 +44,9 @@ void set_err(coli_moe_t *h, const char *fmt, ...) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_ws(Workspace &ws) {
-    void *ptrs[] = {ws.scores, ws.idx, ws.w, ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched,
-                    ws.n_touched, ws.xp, ws.h, ws.y, ws.x_stage, ws.out_stage, ws.tile_sched};
+    void *ptrs[] = {ws.scores, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt,     ws.off,       ws.touched,
+                    ws.n_touched, ws.xp, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
+                    ws.out_stage, ws.tile_sched};
     for (void *p : ptrs)
         if (p) cudaFree(p);
     ws = Workspace();
@@ -122,6 +123,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     const bool with_shared = shared != nullptr;
     Workspace &ws = h->ws;
     int launches = 0, n;
+    const bool gemm = use_gemm(h, T, top_k);
     const bool prof = h->profiling;
     h->stage_valid = false;
     if (prof) cudaEventRecord(h->ev[0], st);
@@ -131,7 +133,8 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     if (n < 0) goto launch_fail;
     launches += n;
     if (prof) cudaEventRecord(h->ev[1], st);
-    n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, ws, st);
+    n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, gemm, ws,
+                       st);
     if (n < 0) goto launch_fail;
     launches += n;
     if (prof) cudaEventRecord(h->ev[2], st);
@@ -144,16 +147,25 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         a.I = c.inter;
         a.I_s = c.shared_inter;
         a.I_max = h->I_max;
+        a.T = T;
+        a.top_k = top_k;
         a.rows = T * top_k + (with_shared ? T : 0);
         a.cnt = ws.cnt;
         a.off = ws.off;
         a.touched = ws.touched;
         a.n_touched = ws.n_touched;
+        a.src_token = ws.src_token;
+        a.x = static_cast<const __nv_bfloat16 *>(x_bf16);
         a.xp = ws.xp;
+        a.xh = ws.xh;
+        a.xinv = ws.xinv;
         a.h = ws.h;
+        a.hh = ws.hh;
+        a.hinv = ws.hinv;
         a.y = ws.y;
+        a.err = ws.err;
         cudaEvent_t mid = prof ? h->ev[3] : nullptr;
-        if (use_gemm(h, T, top_k)) {
+        if (gemm) {
             n = launch_ffn_gemm(a, h->num_sms, ws.tile_sched, mid, st);
             if (n == -2) {
                 set_err(h, "tensor-core grouped GEMM path is not available for this configuration");
@@ -242,7 +254,10 @@ int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **
               alloc(&ws.inv_row, Tm * km) && alloc(&ws.src_token, rows) && alloc(&ws.cnt, E + 1) &&
               alloc(&ws.off, E + 2) && alloc(&ws.touched, E + 1) && alloc(&ws.n_touched, 4) &&
               alloc(&ws.xp, rows * H) && alloc(&ws.h, rows * (size_t)h->I_max) && alloc(&ws.y, rows * H) &&
-              alloc(&ws.x_stage, Tm * H) && alloc(&ws.out_stage, Tm * H);
+              alloc(&ws.xh, Tm * H) && alloc(&ws.xinv, Tm) && alloc(&ws.hh, rows * (size_t)h->I_max) &&
+              alloc(&ws.hinv, rows) && alloc(&ws.err, 4) && alloc(&ws.x_stage, Tm * H) &&
+              alloc(&ws.out_stage, Tm * H);
+    if (ok) ok = cudaMemset(ws.err, 0, sizeof(int)) == cudaSuccess;
     if (ok) {
         ws.tile_sched_bytes = gemm_sched_bytes((int)E, (int)rows);
         ok = cudaMalloc(&ws.tile_sched, ws.tile_sched_bytes + 256) == cudaSuccess;
@@ -342,6 +357,17 @@ int coli_moe_debug_routing(coli_moe_t *h, coli_moe_routing *dst) {
 }
 
 int32_t coli_moe_last_launch_count(const coli_moe_t *h) { return h ? h->last_launches : 0; }
+
+int coli_moe_device_error(coli_moe_t *h, int32_t *code) {
+    if (!h || !code) return COLI_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess ||
+        cudaMemcpy(code, h->ws.err, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(h->ws.err, 0, sizeof(int32_t)) != cudaSuccess) {
+        set_err(h, "stream error: %s", cudaGetErrorString(cudaGetLastError()));
+        return COLI_ERR_CUDA;
+    }
+    return COLI_OK;
+}
 
 int coli_moe_set_profiling(coli_moe_t *h, int32_t enable) {
     if (!h) return COLI_ERR_INVALID_ARG;

@@ -32,6 +32,11 @@ struct Workspace {
     __nv_bfloat16 *xp = nullptr;    // [Tm*km + Tm][H] expert-grouped activation rows
     __nv_bfloat16 *h = nullptr;     // [Tm*km + Tm][I_max] SwiGLU output rows
     float *y = nullptr;             // [Tm*km + Tm][H] expert output rows
+    __half *xh = nullptr;           // [Tm][H] tokens as scaled fp16, permuted unit layout (GEMV path)
+    float *xinv = nullptr;          // [Tm] inverse scales of xh
+    __half *hh = nullptr;           // [Tm*km + Tm][I_max] h rows as scaled fp16 (GEMV path)
+    float *hinv = nullptr;          // [Tm*km + Tm]
+    int *err = nullptr;             // device error word (0 = none), see sm103_ptx.cuh
     __nv_bfloat16 *x_stage = nullptr;    // [Tm][H] forward_host input staging
     __nv_bfloat16 *out_stage = nullptr;  // [Tm][H] forward_host output staging
     void *tile_sched = nullptr;     // grouped-GEMM tile schedule (see gemm_tc.cu)
@@ -44,22 +49,31 @@ struct FfnArgs {
     ExpertSet routed;
     ExpertSet shared;
     int E, H, I, I_s, I_max;
+    int T, top_k;
     int rows;                       // T*k + (shared ? T : 0), known on the host
     const int32_t *cnt;
     const int32_t *off;
     const int32_t *touched;
     const int32_t *n_touched;
-    const __nv_bfloat16 *xp;
-    __nv_bfloat16 *h;
-    float *y;
+    const int32_t *src_token;
+    const __nv_bfloat16 *x;         // [T][H] input tokens
+    const __nv_bfloat16 *xp;        // [rows][H] expert-grouped activation rows (GEMM path)
+    __half *xh;                     // GEMV path: scaled fp16 tokens and inverse scales
+    float *xinv;
+    __nv_bfloat16 *h;               // [rows][I_max]
+    __half *hh;                     // GEMV path: scaled fp16 h rows and inverse scales
+    float *hinv;
+    float *y;                       // [rows][H]
+    int *err;
 };
 
 // Launchers. Each returns the number of kernels it enqueued, or -1 on a launch error
 // (the CUDA error is then available from cudaGetLastError()).
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
                   int E, int top_k, float *scores, int32_t *idx, float *w, cudaStream_t st);
+// `gather`: also copy the activation rows into expert-grouped order (ws.xp).
 int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, Workspace &ws, cudaStream_t st);
+                   int H, bool gather, Workspace &ws, cudaStream_t st);
 // `mid` (may be null): an event recorded between the gate/up and the down kernels.
 int launch_ffn_gemv(const FfnArgs &a, int num_sms, cudaEvent_t mid, cudaStream_t st);
 int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T, int H, int top_k,

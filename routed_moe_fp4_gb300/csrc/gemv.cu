@@ -5,26 +5,35 @@
 //          matvec; FP4 E2M1 experts with UE8M0 group-32 scales)
 // down:    y[row][m] = sum_i Wd[m][i] h[row][i]
 //
-// Work is a flat list of (touched group, block of weight rows) items; each block walks a
-// contiguous range of it, so every block streams the same number of weight bytes. A warp owns
-// four weight rows; lane l reads the 16-byte code chunks l, l+32, ... of each row (one chunk =
-// one 32-element scale group), so a warp reads 512 contiguous bytes per row per step.
+// Structure: one persistent block per SM walks a contiguous range of a flat list of (touched
+// group, block of weight rows) items, so every block streams about the same number of weight
+// bytes. A producer warp streams each item's code and scale rows (contiguous in the packed
+// layout) into a ring of shared-memory stages with 1-D bulk TMA copies; eight consumer warps
+// take a stage when its mbarrier completes, compute, and release it. Every wait is bounded.
 //
-// Arithmetic: each activation row is staged in shared memory as fp16 after multiplying it by a
-// power of two that puts its largest magnitude in [2^8, 2^9) (exact; undone at the end). E2M1
-// codes become exact fp16 pairs (cvt.rn.f16x2.e2m1x2); the products of one 32-element group
-// are accumulated with HFMA2 (16 terms per half, |sum| < 6 * 2^9 * 16 < 65504), then converted
-// to fp32, scaled by the group's UE8M0 factor (fp32 bits s << 23) and summed in fp32.
+// Arithmetic: activation rows are pre-scaled by a power of two that puts their largest magnitude
+// in [2^8, 2^9) and stored as fp16 (exact for bf16 inputs; undone at the end). E2M1 codes become
+// exact fp16 pairs (cvt.rn.f16x2.e2m1x2); the products of one 32-element group are summed with
+// HFMA2 (16 terms per half, |sum| < 6 * 2^9 * 16 < 65504), converted to fp32, scaled by the
+// group's UE8M0 factor (fp32 bits s << 23) and summed in fp32.
+//
+// Activation layout (fp16 rows, K elements, NC = K/32): 16-byte unit (q, c), holding elements
+// 32c + 8q .. 32c + 8q + 7, sits at unit index q * NC + c, so lane c of a warp reads unit
+// q * NC + c for q = 0..3 and each load instruction covers 512 contiguous bytes.
 #include "colimoe_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace colimoe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kTB = 2;                    // tokens per staged chunk
-constexpr int kGateUpI = 2 * kWarps;      // i-values per gate/up item (2 per warp)
-constexpr int kDownM = 4 * kWarps;        // output rows per down item (4 per warp)
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kIB = kConsumerWarps;            // i-values per gate/up item (one per consumer warp)
+constexpr int kMB = 4 * kConsumerWarps;        // output rows per down item (four per consumer warp)
+constexpr int kTB = 4;                         // tokens per pass over a resident stage
+constexpr uint32_t kSmemBudget = 200 * 1024;
+
+enum Mode { kGateUp = 0, kDown = 1 };
 
 __device__ __forceinline__ void e2m1x8_to_h2(uint32_t w, uint32_t (&o)[4]) {
     asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
@@ -40,19 +49,11 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
 }
 
 __device__ __forceinline__ float h2_sum(uint32_t v) {
-    const __half2 h = *reinterpret_cast<const __half2 *>(&v);
-    const float2 f = __half22float2(h);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v));
     return f.x + f.y;
 }
 
 __device__ __forceinline__ float ue8m0(uint32_t s) { return __uint_as_float(s << 23); }
-
-__device__ __forceinline__ uint4 ld_stream(const uint8_t *p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -60,100 +61,57 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Stages rows [0, n) of `src` (bf16, K used columns, row stride `ld` elements) into xs as fp16,
-// layout [kTB][4][K/32] of 16-byte units: unit (q, c) of token t holds elements 32c + 8q ..
-// 32c + 8q + 7. Missing rows are zero. inv[t] receives the power of two that undoes the staging
-// scale.
-__device__ void stage_rows(const __nv_bfloat16 *__restrict__ src, int n, int K, int ld, uint4 *xs, float *inv) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NC = K / 32;
-    if (warp < kTB) {
-        const int t = warp;
-        uint4 *dst = xs + (size_t)t * 4 * NC;
-        if (t >= n) {
-            for (int v = lane; v < K / 8; v += 32) dst[(v & 3) * NC + (v >> 2)] = make_uint4(0, 0, 0, 0);
-            if (lane == 0) inv[t] = 0.f;
-            return;
-        }
-        const uint4 *row = reinterpret_cast<const uint4 *>(src + (size_t)t * ld);
-        uint32_t mx = 0;   // max |bf16| bit pattern (monotone for non-negative floats)
-        for (int v = lane; v < K / 8; v += 32) {
-            const uint4 q = row[v];
-            const uint32_t a[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                mx = max(mx, a[i] & 0x7FFFu);
-                mx = max(mx, (a[i] >> 16) & 0x7FFFu);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        // exponent of the largest magnitude; scale = 2^(8 - e) clamped to the normal fp32 range
-        const int e = (int)((mx >> 7) & 0xFF) - 127;
-        int se = 8 - e;
-        se = max(-126, min(126, se));
-        const float scale = (mx == 0 || mx >= 0x7F80u) ? 1.0f : __uint_as_float((uint32_t)(se + 127) << 23);
-        if (lane == 0) inv[t] = (mx == 0 || mx >= 0x7F80u) ? 1.0f : __uint_as_float((uint32_t)(127 - se) << 23);
-        for (int v = lane; v < K / 8; v += 32) {
-            const uint4 q = row[v];
-            const uint32_t a[4] = {q.x, q.y, q.z, q.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = __uint_as_float(a[i] << 16) * scale;
-                const float hi = __uint_as_float(a[i] & 0xFFFF0000u) * scale;
-                const __half2 hv = __floats2half2_rn(lo, hi);
-                o[i] = *reinterpret_cast<const uint32_t *>(&hv);
-            }
-            dst[(v & 3) * NC + (v >> 2)] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-    }
+struct ItemInfo {
+    int g, blk, Ig;
+    bool valid;
+    const ExpertSet *es;
+    size_t ge;
+};
+
+template <int MODE>
+__device__ __forceinline__ ItemInfo decode_item(const FfnArgs &a, long it, int ipg) {
+    ItemInfo r;
+    r.g = a.touched[it / ipg];
+    r.blk = (int)(it % ipg);
+    const bool sh = r.g == a.E;
+    r.Ig = sh ? a.I_s : a.I;
+    r.es = sh ? &a.shared : &a.routed;
+    r.ge = sh ? 0 : (size_t)r.g;
+    r.valid = MODE == kGateUp ? r.blk * kIB < r.Ig : true;
+    return r;
 }
 
-// Dot products of four weight rows with NT staged tokens. rowp[r] points at the code bytes of
-// row r, sclp[r] at its scale bytes. Returns warp-reduced sums in acc (valid on every lane).
-template <int NT>
-__device__ __forceinline__ void rows4_dot(const uint8_t *const (&rowp)[4], const uint8_t *const (&sclp)[4],
-                                          int NC, const uint4 *xs, float (&acc)[4][NT]) {
+// Dot products of R weight rows (codes/scales in shared memory) with NT activation rows (global,
+// permuted fp16 layout). Returns warp-reduced sums (valid on every lane).
+template <int R, int NT>
+__device__ __forceinline__ void dot_rows(const uint8_t *const (&codes)[R], const uint8_t *const (&scales)[R], int NC,
+                                         const uint4 *const (&xrow)[NT], float (&acc)[R][NT]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[r][t] = 0.f;
-    int c = lane;
-    uint4 cur[4];
-    uint32_t csc[4];
-    if (c < NC) {
+    for (int c = lane; c < NC; c += 32) {
+        uint4 cw[R];
+        float sc[R];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            cur[r] = ld_stream(rowp[r] + (size_t)c * 16);
-            csc[r] = __ldg(sclp[r] + c);
+        for (int r = 0; r < R; ++r) {
+            cw[r] = *reinterpret_cast<const uint4 *>(codes[r] + (size_t)c * 16);
+            sc[r] = ue8m0(scales[r][c]);
         }
-    }
-    for (; c < NC; c += 32) {
-        uint4 nxt[4];
-        uint32_t nsc[4];
-        const bool more = c + 32 < NC;
-        if (more) {
+        uint32_t hacc[R][NT];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                nxt[r] = ld_stream(rowp[r] + (size_t)(c + 32) * 16);
-                nsc[r] = __ldg(sclp[r] + c + 32);
-            }
-        }
-        uint32_t hacc[4][NT];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < R; ++r)
 #pragma unroll
             for (int t = 0; t < NT; ++t) hacc[r][t] = 0u;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint4 xv[NT];
 #pragma unroll
-            for (int t = 0; t < NT; ++t) xv[t] = xs[(size_t)t * 4 * NC + q * NC + c];
+            for (int t = 0; t < NT; ++t) xv[t] = __ldg(xrow[t] + q * NC + c);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const uint32_t word = q == 0 ? cur[r].x : q == 1 ? cur[r].y : q == 2 ? cur[r].z : cur[r].w;
+            for (int r = 0; r < R; ++r) {
+                const uint32_t word = q == 0 ? cw[r].x : q == 1 ? cw[r].y : q == 2 ? cw[r].z : cw[r].w;
                 uint32_t v[4];
                 e2m1x8_to_h2(word, v);
 #pragma unroll
@@ -166,161 +124,244 @@ __device__ __forceinline__ void rows4_dot(const uint8_t *const (&rowp)[4], const
             }
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const float s = ue8m0(csc[r]);
+        for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int t = 0; t < NT; ++t) acc[r][t] = fmaf(s, h2_sum(hacc[r][t]), acc[r][t]);
-        }
-        if (more) {
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                cur[r] = nxt[r];
-                csc[r] = nsc[r];
-            }
-        }
+            for (int t = 0; t < NT; ++t) acc[r][t] = fmaf(sc[r], h2_sum(hacc[r][t]), acc[r][t]);
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int t = 0; t < NT; ++t) acc[r][t] = warp_sum(acc[r][t]);
 }
 
 template <int NT>
-__device__ __forceinline__ void gateup_item(const FfnArgs &a, const uint8_t *gu_c, const uint8_t *gu_s, int Ig,
-                                            int i, int out_row0, const uint4 *xs, const float *inv) {
-    const int lane = threadIdx.x & 31;
-    const int H = a.H;
-    const uint8_t *rowp[4] = {gu_c + (size_t)i * (H / 2), gu_c + (size_t)(i + 1) * (H / 2),
-                              gu_c + (size_t)(Ig + i) * (H / 2), gu_c + (size_t)(Ig + i + 1) * (H / 2)};
-    const uint8_t *sclp[4] = {gu_s + (size_t)i * (H / 32), gu_s + (size_t)(i + 1) * (H / 32),
-                              gu_s + (size_t)(Ig + i) * (H / 32), gu_s + (size_t)(Ig + i + 1) * (H / 32)};
-    float acc[4][NT];
-    rows4_dot<NT>(rowp, sclp, H / 32, xs, acc);
+__device__ __forceinline__ void gateup_compute(const FfnArgs &a, const uint8_t *stage, const ItemInfo &itm, int r0,
+                                               int n0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.H, NC = H / 32;
+    const uint8_t *codes[2] = {stage + (size_t)warp * (H / 2), stage + (size_t)(kIB + warp) * (H / 2)};
+    const uint8_t *sbase = stage + (size_t)2 * kIB * (H / 2);
+    const uint8_t *scales[2] = {sbase + (size_t)warp * NC, sbase + (size_t)(kIB + warp) * NC};
+    const uint4 *xrow[NT];
+    int tok[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-#pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-            if (lane == t * 2 + ii) {
-                const float g = acc[ii][t] * inv[t];
-                const float u = acc[2 + ii][t] * inv[t];
-                const float hval = __fdiv_rn(g, 1.0f + expf(-g)) * u;
-                a.h[(size_t)(out_row0 + t) * a.I_max + i + ii] = __float2bfloat16_rn(hval);
-            }
-        }
+        tok[t] = a.src_token[r0 + n0 + t];
+        xrow[t] = reinterpret_cast<const uint4 *>(a.xh + (size_t)tok[t] * H);
     }
-}
-
-__global__ void __launch_bounds__(kThreads, 2)
-gemv_gateup(FfnArgs a, int items_per_group) {
-    extern __shared__ uint4 smem[];
-    uint4 *xs = smem;
-    float *inv = reinterpret_cast<float *>(smem + (size_t)kTB * 4 * (a.H / 32));
-    const long total = (long)(*a.n_touched) * items_per_group;
-    const long beg = total * blockIdx.x / gridDim.x;
-    const long end = total * (blockIdx.x + 1) / gridDim.x;
-    const int warp = threadIdx.x >> 5;
-    int staged_g = -1, staged_n0 = -1;
-    for (long it = beg; it < end; ++it) {
-        const int g = a.touched[it / items_per_group];
-        const int i0 = (int)(it % items_per_group) * kGateUpI;
-        const bool sh = g == a.E;
-        const int Ig = sh ? a.I_s : a.I;
-        if (i0 >= Ig) continue;
-        const ExpertSet &es = sh ? a.shared : a.routed;
-        const size_t ge = sh ? 0 : (size_t)g;
-        const uint8_t *gu_c = es.gu_codes + ge * 2 * Ig * (a.H / 2);
-        const uint8_t *gu_s = es.gu_scales + ge * 2 * Ig * (a.H / 32);
-        const int r0 = a.off[g], n = a.cnt[g];
-        for (int n0 = 0; n0 < n; n0 += kTB) {
-            if (g != staged_g || n0 != staged_n0) {
-                __syncthreads();
-                stage_rows(a.xp + (size_t)(r0 + n0) * a.H, min(kTB, n - n0), a.H, a.H, xs, inv);
-                __syncthreads();
-                staged_g = g;
-                staged_n0 = n0;
-            }
-            const int nt = min(kTB, n - n0);
-            const int i = i0 + warp * 2;
-            if (nt == 1) gateup_item<1>(a, gu_c, gu_s, Ig, i, r0 + n0, xs, inv);
-            else gateup_item<2>(a, gu_c, gu_s, Ig, i, r0 + n0, xs, inv);
+    float acc[2][NT];
+    dot_rows<2, NT>(codes, scales, NC, xrow, acc);
+    const int i = itm.blk * kIB + warp;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        if (lane == t) {
+            const float inv = a.xinv[tok[t]];
+            const float g = acc[0][t] * inv, u = acc[1][t] * inv;
+            const float hval = __fdiv_rn(g, 1.0f + expf(-g)) * u;
+            a.h[(size_t)(r0 + n0 + t) * a.I_max + i] = __float2bfloat16_rn(hval);
         }
     }
 }
 
 template <int NT>
-__device__ __forceinline__ void down_item(const FfnArgs &a, const uint8_t *d_c, const uint8_t *d_s, int Ig,
-                                          int m, int out_row0, const uint4 *xs, const float *inv) {
-    const int lane = threadIdx.x & 31;
-    const uint8_t *rowp[4], *sclp[4];
+__device__ __forceinline__ void down_compute(const FfnArgs &a, const uint8_t *stage, const ItemInfo &itm, int r0,
+                                             int n0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Ig = itm.Ig, NC = Ig / 32;
+    const uint8_t *codes[4], *scales[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        rowp[r] = d_c + (size_t)(m + r) * (Ig / 2);
-        sclp[r] = d_s + (size_t)(m + r) * (Ig / 32);
+        codes[r] = stage + (size_t)(4 * warp + r) * (Ig / 2);
+        scales[r] = stage + (size_t)kMB * (Ig / 2) + (size_t)(4 * warp + r) * NC;
     }
+    const uint4 *xrow[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) xrow[t] = reinterpret_cast<const uint4 *>(a.hh + (size_t)(r0 + n0 + t) * a.I_max);
     float acc[4][NT];
-    rows4_dot<NT>(rowp, sclp, Ig / 32, xs, acc);
+    dot_rows<4, NT>(codes, scales, NC, xrow, acc);
+    const int m = itm.blk * kMB + 4 * warp;
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            if (lane == t * 4 + r) a.y[(size_t)(out_row0 + t) * a.H + m + r] = acc[r][t] * inv[t];
+            if (lane == t * 4 + r) a.y[(size_t)(r0 + n0 + t) * a.H + m + r] = acc[r][t] * a.hinv[r0 + n0 + t];
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-gemv_down(FfnArgs a, int items_per_group) {
-    extern __shared__ uint4 smem[];
-    uint4 *xs = smem;
-    float *inv = reinterpret_cast<float *>(smem + (size_t)kTB * 4 * (a.I_max / 32));
-    const long total = (long)(*a.n_touched) * items_per_group;
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+gemv_tma(FfnArgs a, int ipg, int nst, uint32_t stage_stride) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)nst * stage_stride);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * nst);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < nst; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&bars[s]), 1);                       // full: producer
+            ptx::mbar_init(ptx::smem_addr(&bars[nst + s]), kConsumerWarps);    // empty: consumers
+        }
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    const long total = (long)(*a.n_touched) * ipg;
     const long beg = total * blockIdx.x / gridDim.x;
     const long end = total * (blockIdx.x + 1) / gridDim.x;
-    const int warp = threadIdx.x >> 5;
-    int staged_g = -1, staged_n0 = -1;
-    for (long it = beg; it < end; ++it) {
-        const int g = a.touched[it / items_per_group];
-        const int m0 = (int)(it % items_per_group) * kDownM;
-        const bool sh = g == a.E;
-        const int Ig = sh ? a.I_s : a.I;
-        const ExpertSet &es = sh ? a.shared : a.routed;
-        const size_t ge = sh ? 0 : (size_t)g;
-        const uint8_t *d_c = es.d_codes + ge * (size_t)a.H * (Ig / 2);
-        const uint8_t *d_s = es.d_scales + ge * (size_t)a.H * (Ig / 32);
-        const int r0 = a.off[g], n = a.cnt[g];
-        for (int n0 = 0; n0 < n; n0 += kTB) {
-            if (g != staged_g || n0 != staged_n0) {
-                __syncthreads();
-                // h rows have stride I_max; stage the first Ig columns of each
-                stage_rows(a.h + (size_t)(r0 + n0) * a.I_max, min(kTB, n - n0), Ig, a.I_max, xs, inv);
-                __syncthreads();
-                staged_g = g;
-                staged_n0 = n0;
+    const int H = a.H;
+    int issued = 0;
+
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {   // producer
+            const uint64_t pol = ptx::policy_evict_first();
+            for (long it = beg; it < end; ++it) {
+                const ItemInfo itm = decode_item<MODE>(a, it, ipg);
+                if (!itm.valid) continue;
+                const int slot = issued % nst;
+                const uint32_t ph = (uint32_t)(issued / nst) & 1u;
+                if (!ptx::mbar_wait(ptx::smem_addr(&bars[nst + slot]), ph ^ 1u, a.err, ptx::kErrWaitEmpty, abort_flag))
+                    break;
+                const uint32_t full = ptx::smem_addr(&bars[slot]);
+                const uint32_t dst = ptx::smem_addr(smem + (size_t)slot * stage_stride);
+                if (MODE == kGateUp) {
+                    const int Ig = itm.Ig, i0 = itm.blk * kIB;
+                    const uint8_t *gc = itm.es->gu_codes + itm.ge * 2 * Ig * (size_t)(H / 2);
+                    const uint8_t *gs = itm.es->gu_scales + itm.ge * 2 * Ig * (size_t)(H / 32);
+                    const uint32_t cb = kIB * (H / 2), sb = kIB * (H / 32);
+                    ptx::mbar_arrive_expect_tx(full, 2 * (cb + sb));
+                    ptx::bulk_g2s_hint(dst, gc + (size_t)i0 * (H / 2), cb, full, pol);
+                    ptx::bulk_g2s_hint(dst + cb, gc + (size_t)(Ig + i0) * (H / 2), cb, full, pol);
+                    ptx::bulk_g2s_hint(dst + 2 * cb, gs + (size_t)i0 * (H / 32), sb, full, pol);
+                    ptx::bulk_g2s_hint(dst + 2 * cb + sb, gs + (size_t)(Ig + i0) * (H / 32), sb, full, pol);
+                } else {
+                    const int Ig = itm.Ig, m0 = itm.blk * kMB;
+                    const uint8_t *dc = itm.es->d_codes + itm.ge * (size_t)H * (Ig / 2);
+                    const uint8_t *ds = itm.es->d_scales + itm.ge * (size_t)H * (Ig / 32);
+                    const uint32_t cb = kMB * (Ig / 2), sb = kMB * (Ig / 32);
+                    ptx::mbar_arrive_expect_tx(full, cb + sb);
+                    ptx::bulk_g2s_hint(dst, dc + (size_t)m0 * (Ig / 2), cb, full, pol);
+                    ptx::bulk_g2s_hint(dst + cb, ds + (size_t)m0 * (Ig / 32), sb, full, pol);
+                }
+                ++issued;
             }
-            const int nt = min(kTB, n - n0);
-            const int m = m0 + warp * 4;
-            if (nt == 1) down_item<1>(a, d_c, d_s, Ig, m, r0 + n0, xs, inv);
-            else down_item<2>(a, d_c, d_s, Ig, m, r0 + n0, xs, inv);
+        }
+    } else {   // consumers
+        int used = 0;
+        for (long it = beg; it < end; ++it) {
+            const ItemInfo itm = decode_item<MODE>(a, it, ipg);
+            if (!itm.valid) continue;
+            const int slot = used % nst;
+            const uint32_t ph = (uint32_t)(used / nst) & 1u;
+            if (!ptx::mbar_wait(ptx::smem_addr(&bars[slot]), ph, a.err, ptx::kErrWaitFull, abort_flag)) break;
+            const uint8_t *stage = smem + (size_t)slot * stage_stride;
+            const int r0 = a.off[itm.g], n = a.cnt[itm.g];
+            for (int n0 = 0; n0 < n; n0 += kTB) {
+                const int nt = min(kTB, n - n0);
+                if (MODE == kGateUp) {
+                    if (nt == 1) gateup_compute<1>(a, stage, itm, r0, n0);
+                    else if (nt == 2) gateup_compute<2>(a, stage, itm, r0, n0);
+                    else if (nt == 3) gateup_compute<3>(a, stage, itm, r0, n0);
+                    else gateup_compute<4>(a, stage, itm, r0, n0);
+                } else {
+                    if (nt == 1) down_compute<1>(a, stage, itm, r0, n0);
+                    else if (nt == 2) down_compute<2>(a, stage, itm, r0, n0);
+                    else if (nt == 3) down_compute<3>(a, stage, itm, r0, n0);
+                    else down_compute<4>(a, stage, itm, r0, n0);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&bars[nst + slot]));
+            ++used;
         }
     }
+    __syncthreads();
+    // After an abort the producer waits (bounded) for the copies it issued, so no TMA write
+    // lands in shared memory after the block has exited.
+    if (*abort_flag && warp == kConsumerWarps && lane == 0) {
+        for (int j = issued > nst ? issued - nst : 0; j < issued; ++j)
+            ptx::mbar_wait(ptx::smem_addr(&bars[j % nst]), (uint32_t)(j / nst) & 1u, nullptr, 0, nullptr);
+    }
+}
+
+// Rows of bf16 -> fp16 scaled by a power of two (largest magnitude in [2^8, 2^9)), written in the
+// permuted unit layout; inv[row] receives the inverse scale. One warp per row. Rows >= split use
+// K2 columns, the others K1.
+__global__ void __launch_bounds__(256)
+prep_rows_f16(const __nv_bfloat16 *__restrict__ src, int src_ld, int nrows, int K1, int split, int K2,
+              __half *__restrict__ dst, int dst_ld, float *__restrict__ inv) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= nrows) return;
+    const int K = row >= split ? K2 : K1;
+    const int NC = K / 32;
+    const uint4 *in = reinterpret_cast<const uint4 *>(src + (size_t)row * src_ld);
+    uint4 *out = reinterpret_cast<uint4 *>(dst + (size_t)row * dst_ld);
+    uint32_t mx = 0;
+    for (int v = lane; v < K / 8; v += 32) {
+        const uint4 q = in[v];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const bool plain = mx == 0 || mx >= 0x7F80u;   // all zero, or inf/nan present: no scaling
+    int se = 8 - ((int)((mx >> 7) & 0xFF) - 127);
+    se = max(-126, min(126, se));
+    const float scale = plain ? 1.0f : __uint_as_float((uint32_t)(se + 127) << 23);
+    if (lane == 0) inv[row] = plain ? 1.0f : __uint_as_float((uint32_t)(127 - se) << 23);
+    for (int v = lane; v < K / 8; v += 32) {
+        const uint4 q = in[v];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 hv = __floats2half2_rn(__uint_as_float(w[i] << 16) * scale,
+                                                 __uint_as_float(w[i] & 0xFFFF0000u) * scale);
+            o[i] = *reinterpret_cast<const uint32_t *>(&hv);
+        }
+        out[(v & 3) * NC + (v >> 2)] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+template <int MODE>
+uint32_t stage_bytes(const FfnArgs &a) {
+    const int Imax = a.I_max;
+    const uint32_t b = MODE == kGateUp ? 2u * kIB * (uint32_t)(a.H / 2 + a.H / 32)
+                                       : (uint32_t)kMB * (uint32_t)(Imax / 2 + Imax / 32);
+    return (b + 127u) & ~127u;
+}
+
+template <int MODE>
+int launch_mode(const FfnArgs &a, int num_sms, cudaStream_t st) {
+    const uint32_t stride = stage_bytes<MODE>(a);
+    int nst = (int)(kSmemBudget / stride);
+    nst = nst > 8 ? 8 : nst;
+    if (nst < 2) return -2;
+    const size_t smem = (size_t)nst * stride + 2 * nst * sizeof(uint64_t) + 16;
+    if (cudaFuncSetAttribute(gemv_tma<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return -1;
+    const int ipg = MODE == kGateUp ? (a.I_max + kIB - 1) / kIB : a.H / kMB;
+    gemv_tma<MODE><<<num_sms, kThreads, smem, st>>>(a, ipg, nst, stride);
+    return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
 }  // namespace
 
 int launch_ffn_gemv(const FfnArgs &a, int num_sms, cudaEvent_t mid, cudaStream_t st) {
-    const int blocks = 2 * num_sms;
-    const size_t smem_gu = (size_t)kTB * 4 * (a.H / 32) * sizeof(uint4) + kTB * sizeof(float);
-    const size_t smem_dn = (size_t)kTB * 4 * (a.I_max / 32) * sizeof(uint4) + kTB * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(gemv_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-        cudaFuncSetAttribute(gemv_down, cudaFuncAttributeMaxDynamicSharedMemorySize, 100 * 1024);
-        attr_set = true;
-    }
-    const int gu_items = (max(a.I, a.I_s) + kGateUpI - 1) / kGateUpI;
-    gemv_gateup<<<blocks, kThreads, smem_gu, st>>>(a, gu_items);
+    int n = 0, r;
+    // tokens -> scaled fp16 (gate/up activations)
+    prep_rows_f16<<<(a.T + 7) / 8, 256, 0, st>>>(a.x, a.H, a.T, a.H, a.T, a.H, a.xh, a.H, a.xinv);
+    ++n;
+    if ((r = launch_mode<kGateUp>(a, num_sms, st)) < 0) return r;
+    n += r;
     if (mid) cudaEventRecord(mid, st);
-    const int dn_items = a.H / kDownM;
-    gemv_down<<<blocks, kThreads, smem_dn, st>>>(a, dn_items);
-    return cudaPeekAtLastError() == cudaSuccess ? 2 : -1;
+    // h rows -> scaled fp16 (down activations); shared rows (from T*k on) have I_s columns
+    prep_rows_f16<<<(a.rows + 7) / 8, 256, 0, st>>>(a.h, a.I_max, a.rows, a.I, a.T * a.top_k, a.I_s, a.hh, a.I_max,
+                                                    a.hinv);
+    ++n;
+    if ((r = launch_mode<kDown>(a, num_sms, st)) < 0) return r;
+    n += r;
+    return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }
 
 }  // namespace colimoe

@@ -133,13 +133,14 @@ permute_gather(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__rest
 }  // namespace
 
 int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, Workspace &ws, cudaStream_t st) {
+                   int H, bool gather, Workspace &ws, cudaStream_t st) {
     const int n = T * top_k;
     const int rows = n + (with_shared ? T : 0);
     if (cudaMemsetAsync(ws.cnt, 0, sizeof(int32_t) * (E + 1), st) != cudaSuccess) return -1;
     permute_count<<<(n + 255) / 256, 256, 0, st>>>(idx, n, ws.cnt);
     permute_scan<<<1, 1024, 0, st>>>(ws.cnt, ws.off, ws.touched, ws.n_touched, E, with_shared ? T : 0);
     permute_scatter<<<E + 1, 256, 0, st>>>(idx, T, E, top_k, ws.cnt, ws.off, ws.src_token, ws.inv_row);
+    if (!gather) return cudaPeekAtLastError() == cudaSuccess ? 3 : -1;
     const size_t vecs = (size_t)rows * (H / 8);
     const int blocks = (int)((vecs + 255) / 256 < 65536 ? (vecs + 255) / 256 : 65536);
     permute_gather<<<blocks, 256, 0, st>>>(x, H, ws.src_token, rows, ws.xp);

@@ -19,34 +19,50 @@ __device__ __forceinline__ float sigmoidf_ieee(float z) {
     return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
 }
 
-// Small T: one warp per expert, lanes across H, up to 8 tokens per block row.
-constexpr int kSmallWarps = 4;
+// Small T: two experts per block, two warps per expert (each half of H), up to 8 tokens per
+// block row. Lanes read the router row as float4; four loads are issued before they are used so
+// every warp keeps several HBM requests in flight.
 constexpr int kSmallTok = 8;
 
-__global__ void __launch_bounds__(kSmallWarps * 32)
+__global__ void __launch_bounds__(128)
 router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const float *__restrict__ wr,
                     int E, float *__restrict__ scores) {
+    __shared__ float part[2][kSmallTok];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kSmallWarps + warp;
+    const int e = blockIdx.x * 2 + (warp >> 1), half = warp & 1;
     const int t0 = blockIdx.y * kSmallTok;
-    if (e >= E) return;
     const int nt = min(kSmallTok, T - t0);
     float acc[kSmallTok];
 #pragma unroll
     for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
-    const float4 *wrow = reinterpret_cast<const float4 *>(wr + (size_t)e * H);
-    for (int c = lane; c < H / 4; c += 32) {
-        const float4 wv = __ldg(wrow + c);
+    if (e < E) {
+        const int nv = H / 8;                            // float4 per half row
+        const float4 *wrow = reinterpret_cast<const float4 *>(wr + (size_t)e * H) + half * nv;
+        const uint2 *xbase = reinterpret_cast<const uint2 *>(x + (size_t)t0 * H) + half * nv;
+        for (int c0 = lane; c0 < nv; c0 += 128) {
+            float4 wv[4];
 #pragma unroll
-        for (int t = 0; t < kSmallTok; ++t) {
-            if (t < nt) {
-                const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(x + (size_t)(t0 + t) * H) + c);
-                float a = acc[t];
-                a = fmaf(bf16_lo(xv.x), wv.x, a);
-                a = fmaf(bf16_hi(xv.x), wv.y, a);
-                a = fmaf(bf16_lo(xv.y), wv.z, a);
-                a = fmaf(bf16_hi(xv.y), wv.w, a);
-                acc[t] = a;
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + 32 * u;
+                wv[u] = c < nv ? __ldg(wrow + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int t = 0; t < kSmallTok; ++t) {
+                if (t < nt) {
+                    float a = acc[t];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = c0 + 32 * u;
+                        if (c < nv) {
+                            const uint2 xv = __ldg(xbase + (size_t)t * (H / 4) + c);
+                            a = fmaf(bf16_lo(xv.x), wv[u].x, a);
+                            a = fmaf(bf16_hi(xv.x), wv[u].y, a);
+                            a = fmaf(bf16_lo(xv.y), wv[u].z, a);
+                            a = fmaf(bf16_hi(xv.y), wv[u].w, a);
+                        }
+                    }
+                    acc[t] = a;
+                }
             }
         }
     }
@@ -55,7 +71,19 @@ router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
         float a = acc[t];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (lane == 0 && t < nt) scores[(size_t)(t0 + t) * E + e] = sigmoidf_ieee(a);
+        acc[t] = a;
+    }
+    if (half == 1 && lane == 0) {
+#pragma unroll
+        for (int t = 0; t < kSmallTok; ++t) part[warp >> 1][t] = acc[t];
+    }
+    __syncthreads();
+    if (half == 0 && lane < nt && e < E) {
+        float a = 0.f;
+#pragma unroll
+        for (int t = 0; t < kSmallTok; ++t)
+            if (t == lane) a = acc[t] + part[warp >> 1][t];
+        scores[(size_t)(t0 + lane) * E + e] = sigmoidf_ieee(a);
     }
 }
 
@@ -208,8 +236,8 @@ int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, c
                   int E, int top_k, float *scores, int32_t *idx, float *w, cudaStream_t st) {
     int n = 0;
     if (T < 64) {
-        dim3 grid((E + kSmallWarps - 1) / kSmallWarps, (T + kSmallTok - 1) / kSmallTok);
-        router_logits_small<<<grid, kSmallWarps * 32, 0, st>>>(x, T, H, router_w, E, scores);
+        dim3 grid((E + 1) / 2, (T + kSmallTok - 1) / kSmallTok);
+        router_logits_small<<<grid, 128, 0, st>>>(x, T, H, router_w, E, scores);
     } else {
         dim3 grid((T + kTileT - 1) / kTileT, (E + kTileE - 1) / kTileE);
         router_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, router_w, E, scores);

@@ -70,6 +70,7 @@ def run_gpu(inputs, path: int = 0, T: Optional[int] = None, repeats: int = 1, la
         outs.append(out.cpu().numpy().view(np.uint16))
     routing = layer.routing(T)
     launches = layer.launches()
+    assert layer.device_error() == 0, "a kernel wait ran out (device error word set)"
     if own:
         layer.close()
     return outs, routing, launches
