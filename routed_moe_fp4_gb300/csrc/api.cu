@@ -44,7 +44,7 @@ void set_err(coli_moe_t *h, const char *fmt, ...) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_ws(Workspace &ws) {
-    void *ptrs[] = {ws.scores, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt,     ws.off,       ws.touched,
+    void *ptrs[] = {ws.scores, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
                     ws.n_touched, ws.xp, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
                     ws.out_stage, ws.tile_sched};
     for (void *p : ptrs)
@@ -133,8 +133,8 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     if (n < 0) goto launch_fail;
     launches += n;
     if (prof) cudaEventRecord(h->ev[1], st);
-    n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, gemm, ws,
-                       st);
+    n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, gemm,
+                       kGemvCostTokens, ws, st);
     if (n < 0) goto launch_fail;
     launches += n;
     if (prof) cudaEventRecord(h->ev[2], st);
@@ -154,6 +154,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         a.off = ws.off;
         a.touched = ws.touched;
         a.n_touched = ws.n_touched;
+        a.touched_cost = ws.touched_cost;
         a.src_token = ws.src_token;
         a.x = static_cast<const __nv_bfloat16 *>(x_bf16);
         a.xp = ws.xp;
@@ -252,7 +253,7 @@ int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **
     Workspace &ws = h->ws;
     bool ok = alloc(&ws.scores, Tm * E) && alloc(&ws.idx, Tm * km) && alloc(&ws.w, Tm * km) &&
               alloc(&ws.inv_row, Tm * km) && alloc(&ws.src_token, rows) && alloc(&ws.cnt, E + 1) &&
-              alloc(&ws.off, E + 2) && alloc(&ws.touched, E + 1) && alloc(&ws.n_touched, 4) &&
+              alloc(&ws.off, E + 2) && alloc(&ws.touched, E + 1) && alloc(&ws.touched_cost, E + 2) && alloc(&ws.n_touched, 4) &&
               alloc(&ws.xp, rows * H) && alloc(&ws.h, rows * (size_t)h->I_max) && alloc(&ws.y, rows * H) &&
               alloc(&ws.xh, Tm * H) && alloc(&ws.xinv, Tm) && alloc(&ws.hh, rows * (size_t)h->I_max) &&
               alloc(&ws.hinv, rows) && alloc(&ws.err, 4) && alloc(&ws.x_stage, Tm * H) &&

@@ -28,6 +28,7 @@ struct Workspace {
     int32_t *cnt = nullptr;         // [E+1]
     int32_t *off = nullptr;         // [E+2]
     int32_t *touched = nullptr;     // [E+1] non-empty groups, ascending
+    int32_t *touched_cost = nullptr;  // [E+2] exclusive prefix of per-group work cost
     int32_t *n_touched = nullptr;   // [1]
     __nv_bfloat16 *xp = nullptr;    // [Tm*km + Tm][H] expert-grouped activation rows
     __nv_bfloat16 *h = nullptr;     // [Tm*km + Tm][I_max] SwiGLU output rows
@@ -55,6 +56,7 @@ struct FfnArgs {
     const int32_t *off;
     const int32_t *touched;
     const int32_t *n_touched;
+    const int32_t *touched_cost;    // [n_touched + 1] exclusive prefix of per-group cost
     const int32_t *src_token;
     const __nv_bfloat16 *x;         // [T][H] input tokens
     const __nv_bfloat16 *xp;        // [rows][H] expert-grouped activation rows (GEMM path)
@@ -71,9 +73,12 @@ struct FfnArgs {
 // (the CUDA error is then available from cudaGetLastError()).
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
                   int E, int top_k, float *scores, int32_t *idx, float *w, cudaStream_t st);
-// `gather`: also copy the activation rows into expert-grouped order (ws.xp).
+// `gather`: also copy the activation rows into expert-grouped order (ws.xp). `cost_tokens`: rows
+// per unit of work cost in ws.touched_cost (see permute_scan).
 int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, bool gather, Workspace &ws, cudaStream_t st);
+                   int H, bool gather, int cost_tokens, Workspace &ws, cudaStream_t st);
+// Rows per cost unit the GEMV kernels assume.
+constexpr int kGemvCostTokens = 4;
 // `mid` (may be null): an event recorded between the gate/up and the down kernels.
 int launch_ffn_gemv(const FfnArgs &a, int num_sms, cudaEvent_t mid, cudaStream_t st);
 int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T, int H, int top_k,

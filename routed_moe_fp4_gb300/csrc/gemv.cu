@@ -14,8 +14,10 @@
 // Arithmetic: activation rows are pre-scaled by a power of two that puts their largest magnitude
 // in [2^8, 2^9) and stored as fp16 (exact for bf16 inputs; undone at the end). E2M1 codes become
 // exact fp16 pairs (cvt.rn.f16x2.e2m1x2); the products of one 32-element group are summed with
-// HFMA2 (16 terms per half, |sum| < 6 * 2^9 * 16 < 65504), converted to fp32, scaled by the
-// group's UE8M0 factor (fp32 bits s << 23) and summed in fp32.
+// HFMA2 in two chains (8 terms per half each, |sum| < 6 * 2^9 * 8 < 65504), converted to fp32,
+// scaled by the group's UE8M0 factor (fp32 bits s << 23) and summed in fp32. Blocks split the
+// items by cost (one unit per weight pass plus one per 4-token pass over the stage), so a group
+// with many rows, such as the shared expert, does not leave a long tail on a few blocks.
 //
 // Activation layout (fp16 rows, K elements, NC = K/32): 16-byte unit (q, c), holding elements
 // 32c + 8q .. 32c + 8q + 7, sits at unit index q * NC + c, so lane c of a warp reads unit
@@ -30,7 +32,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kIB = kConsumerWarps;            // i-values per gate/up item (one per consumer warp)
 constexpr int kMB = 4 * kConsumerWarps;        // output rows per down item (four per consumer warp)
-constexpr int kTB = 4;                         // tokens per pass over a resident stage
+constexpr int kTB = kGemvCostTokens;           // tokens per pass over a resident stage
 constexpr uint32_t kSmemBudget = 200 * 1024;
 
 enum Mode { kGateUp = 0, kDown = 1 };
@@ -99,11 +101,11 @@ __device__ __forceinline__ void dot_rows(const uint8_t *const (&codes)[R], const
             cw[r] = *reinterpret_cast<const uint4 *>(codes[r] + (size_t)c * 16);
             sc[r] = ue8m0(scales[r][c]);
         }
-        uint32_t hacc[R][NT];
+        uint32_t hacc[R][NT], hacc2[R][NT];   // two chains per (row, token) for ILP
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int t = 0; t < NT; ++t) hacc[r][t] = 0u;
+            for (int t = 0; t < NT; ++t) hacc[r][t] = hacc2[r][t] = 0u;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint4 xv[NT];
@@ -117,16 +119,17 @@ __device__ __forceinline__ void dot_rows(const uint8_t *const (&codes)[R], const
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     hacc[r][t] = hfma2_u32(v[0], xv[t].x, hacc[r][t]);
-                    hacc[r][t] = hfma2_u32(v[1], xv[t].y, hacc[r][t]);
+                    hacc2[r][t] = hfma2_u32(v[1], xv[t].y, hacc2[r][t]);
                     hacc[r][t] = hfma2_u32(v[2], xv[t].z, hacc[r][t]);
-                    hacc[r][t] = hfma2_u32(v[3], xv[t].w, hacc[r][t]);
+                    hacc2[r][t] = hfma2_u32(v[3], xv[t].w, hacc2[r][t]);
                 }
             }
         }
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int t = 0; t < NT; ++t) acc[r][t] = fmaf(sc[r], h2_sum(hacc[r][t]), acc[r][t]);
+            for (int t = 0; t < NT; ++t)
+                acc[r][t] = fmaf(sc[r], h2_sum(hacc[r][t]) + h2_sum(hacc2[r][t]), acc[r][t]);
     }
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -187,6 +190,29 @@ __device__ __forceinline__ void down_compute(const FfnArgs &a, const uint8_t *st
             if (lane == t * 4 + r) a.y[(size_t)(r0 + n0 + t) * a.H + m + r] = acc[r][t] * a.hinv[r0 + n0 + t];
 }
 
+// First flat item index (group-major, ipg items per group) whose cost start is >= target, where
+// item (u, b) of touched group u starts at ipg * P[u] + b * (P[u+1] - P[u]) cost units.
+// Executed by one full warp; the result is valid on every lane.
+__device__ long item_at_cost(const int32_t *__restrict__ P, int nt, int ipg, long target) {
+    const int lane = threadIdx.x & 31;
+    if (nt <= 0) return 0;
+    int lo = 0, hi = nt;                 // find the last u in [0, nt) with ipg * P[u] <= target
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) / 32;
+        const int u = lo + lane * step;
+        const bool ok = u < hi && (long)ipg * P[u] <= target;
+        const unsigned b = __ballot_sync(0xffffffffu, ok);
+        const int last = 31 - __clz(b);  // lane 0 always qualifies (P[lo] <= target holds)
+        lo = lo + last * step;
+        hi = min(hi, lo + step);
+    }
+    const long c0 = (long)ipg * P[lo];
+    const int per = P[lo + 1] - P[lo];
+    long b = (target - c0 + per - 1) / per;
+    if (b >= ipg) return (long)(lo + 1) * ipg;
+    return (long)lo * ipg + b;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_tma(FfnArgs a, int ipg, int nst, uint32_t stage_stride) {
@@ -194,6 +220,7 @@ gemv_tma(FfnArgs a, int ipg, int nst, uint32_t stage_stride) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)nst * stage_stride);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * nst);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    long *range = reinterpret_cast<long *>(bars + 2 * nst + 1);
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             ptx::mbar_init(ptx::smem_addr(&bars[s]), 1);                       // full: producer
@@ -202,11 +229,18 @@ gemv_tma(FfnArgs a, int ipg, int nst, uint32_t stage_stride) {
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
+    if (warp == 0) {   // this block's share of the total cost, as a range of flat items
+        const int nt = *a.n_touched;
+        const long total = (long)ipg * a.touched_cost[nt];
+        const long b0 = item_at_cost(a.touched_cost, nt, ipg, total * blockIdx.x / gridDim.x);
+        const long b1 = item_at_cost(a.touched_cost, nt, ipg, total * (blockIdx.x + 1) / gridDim.x);
+        if (lane == 0) {
+            range[0] = b0;
+            range[1] = b1;
+        }
+    }
     __syncthreads();
-
-    const long total = (long)(*a.n_touched) * ipg;
-    const long beg = total * blockIdx.x / gridDim.x;
-    const long end = total * (blockIdx.x + 1) / gridDim.x;
+    const long beg = range[0], end = range[1];
     const int H = a.H;
     int issued = 0;
 
@@ -337,7 +371,7 @@ int launch_mode(const FfnArgs &a, int num_sms, cudaStream_t st) {
     int nst = (int)(kSmemBudget / stride);
     nst = nst > 8 ? 8 : nst;
     if (nst < 2) return -2;
-    const size_t smem = (size_t)nst * stride + 2 * nst * sizeof(uint64_t) + 16;
+    const size_t smem = (size_t)nst * stride + (2 * nst + 4) * sizeof(uint64_t);
     if (cudaFuncSetAttribute(gemv_tma<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return -1;
     const int ipg = MODE == kGateUp ? (a.I_max + kIB - 1) / kIB : a.H / kMB;

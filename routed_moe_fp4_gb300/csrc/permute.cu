@@ -47,30 +47,41 @@ __device__ int block_exclusive_scan(int v, int *smem_warp, int *total) {
 }
 
 // One block of 1024 threads; groups g = 0..E (E <= 1024 + shared handled as the last entry).
+// Also lists the non-empty groups in ascending order (touched) with an exclusive prefix of their
+// work cost, 1 + ceil(rows / cost_tokens) per weight pass (touched_cost[n_touched] = total), which
+// the expert-FFN kernels use to split work evenly across blocks.
 __global__ void __launch_bounds__(1024)
 permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__restrict__ touched,
-             int32_t *__restrict__ n_touched, int E, int shared_rows) {
+             int32_t *__restrict__ touched_cost, int32_t *__restrict__ n_touched, int E, int shared_rows,
+             int cost_tokens) {
     __shared__ int smem[33];
     const int G = E + 1;
     if (threadIdx.x == 0) cnt[E] = shared_rows;
     __syncthreads();
-    int base = 0, tbase = 0;
+    int base = 0, tbase = 0, cbase = 0;
     for (int g0 = 0; g0 < G; g0 += 1024) {
         const int g = g0 + threadIdx.x;
         const int c = g < G ? cnt[g] : 0;
-        int tot, ttot;
+        const int cost = c > 0 ? 1 + (c + cost_tokens - 1) / cost_tokens : 0;
+        int tot, ttot, ctot;
         const int ex = block_exclusive_scan(c, smem, &tot);
         const int tex = block_exclusive_scan(c > 0 ? 1 : 0, smem, &ttot);
+        const int cex = block_exclusive_scan(cost, smem, &ctot);
         if (g < G) {
             off[g] = base + ex;
-            if (c > 0) touched[tbase + tex] = g;
+            if (c > 0) {
+                touched[tbase + tex] = g;
+                touched_cost[tbase + tex] = cbase + cex;
+            }
         }
         base += tot;
         tbase += ttot;
+        cbase += ctot;
     }
     if (threadIdx.x == 0) {
         off[G] = base;
         *n_touched = tbase;
+        touched_cost[tbase] = cbase;
     }
 }
 
@@ -133,12 +144,13 @@ permute_gather(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__rest
 }  // namespace
 
 int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, bool gather, Workspace &ws, cudaStream_t st) {
+                   int H, bool gather, int cost_tokens, Workspace &ws, cudaStream_t st) {
     const int n = T * top_k;
     const int rows = n + (with_shared ? T : 0);
     if (cudaMemsetAsync(ws.cnt, 0, sizeof(int32_t) * (E + 1), st) != cudaSuccess) return -1;
     permute_count<<<(n + 255) / 256, 256, 0, st>>>(idx, n, ws.cnt);
-    permute_scan<<<1, 1024, 0, st>>>(ws.cnt, ws.off, ws.touched, ws.n_touched, E, with_shared ? T : 0);
+    permute_scan<<<1, 1024, 0, st>>>(ws.cnt, ws.off, ws.touched, ws.touched_cost, ws.n_touched, E,
+                                     with_shared ? T : 0, cost_tokens);
     permute_scatter<<<E + 1, 256, 0, st>>>(idx, T, E, top_k, ws.cnt, ws.off, ws.src_token, ws.inv_row);
     if (!gather) return cudaPeekAtLastError() == cudaSuccess ? 3 : -1;
     const size_t vecs = (size_t)rows * (H / 8);
