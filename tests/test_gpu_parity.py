@@ -112,6 +112,38 @@ def test_edge_cases(oracle, wl):
     _assert_ok(rep)
 
 
+@pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T16", "sweep_T128"])
+def test_gemm_path(oracle, name):
+    """The tcgen05 grouped-GEMM path, forced, against the oracle."""
+    inputs = S.make_inputs(name)
+    rep, _, _ = _run(oracle, inputs, GEMM, n_tokens=8)
+    _assert_ok(rep)
+
+
+@pytest.mark.parametrize("wl", [
+    _custom("gemm_ragged", T=37, H=384, E=16, top_k=3),
+    _custom("gemm_shared_wider", I_s=256),
+    _custom("gemm_noshared", I_s=0),
+    _custom("gemm_many_rows", T=300, E=4, top_k=2),
+], ids=lambda w: w.name)
+def test_gemm_edge_cases(oracle, wl):
+    inputs = S.make_inputs(wl)
+    rep, _, _ = _run(oracle, inputs, GEMM)
+    _assert_ok(rep)
+
+
+def test_gemm_matches_gemv(oracle):
+    """Both FFN paths agree with each other within the parity bar on the same routing."""
+    inputs = S.make_inputs("sweep_T64")
+    o1, r1, _ = P.run_gpu(inputs, path=GEMV)
+    o2, r2, _ = P.run_gpu(inputs, path=GEMM)
+    assert np.array_equal(r1["idx"], r2["idx"])
+    a = P.bf16_bits_to_f32(o1[0]).astype(np.float64)
+    b = P.bf16_bits_to_f32(o2[0]).astype(np.float64)
+    rms = np.sqrt((a ** 2).mean())
+    assert np.abs(a - b).max() <= 2 * P.OUT_TOL * rms
+
+
 def test_zero_tokens_is_noop():
     import torch
     from routed_moe_fp4_gb300 import colimoe as cm
