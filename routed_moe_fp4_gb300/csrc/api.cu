@@ -44,7 +44,7 @@ void set_err(coli_moe_t *h, const char *fmt, ...) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_ws(Workspace &ws) {
-    void *ptrs[] = {ws.scores, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
+    void *ptrs[] = {ws.scores, ws.logit_part, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
                     ws.n_touched, ws.xp, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
                     ws.out_stage, ws.tile_sched};
     for (void *p : ptrs)
@@ -129,7 +129,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     if (prof) cudaEventRecord(h->ev[0], st);
 
     n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
-                      ws.scores, ws.idx, ws.w, st);
+                      ws.scores, ws.idx, ws.w, ws.logit_part, ws.logit_part_floats, h->num_sms, st);
     if (n < 0) goto launch_fail;
     launches += n;
     if (prof) cudaEventRecord(h->ev[1], st);
@@ -251,7 +251,8 @@ int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **
     const size_t Tm = c.max_tokens, km = c.max_top_k, E = c.num_experts, H = c.hidden;
     const size_t rows = Tm * km + Tm;
     Workspace &ws = h->ws;
-    bool ok = alloc(&ws.scores, Tm * E) && alloc(&ws.idx, Tm * km) && alloc(&ws.w, Tm * km) &&
+    ws.logit_part_floats = 4 * (Tm > 1024 ? Tm : 1024) * E;
+    bool ok = alloc(&ws.scores, Tm * E) && alloc(&ws.logit_part, ws.logit_part_floats) && alloc(&ws.idx, Tm * km) && alloc(&ws.w, Tm * km) &&
               alloc(&ws.inv_row, Tm * km) && alloc(&ws.src_token, rows) && alloc(&ws.cnt, E + 1) &&
               alloc(&ws.off, E + 2) && alloc(&ws.touched, E + 1) && alloc(&ws.touched_cost, E + 2) && alloc(&ws.n_touched, 4) &&
               alloc(&ws.xp, rows * H) && alloc(&ws.h, rows * (size_t)h->I_max) && alloc(&ws.y, rows * H) &&

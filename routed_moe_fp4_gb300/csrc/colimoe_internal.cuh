@@ -21,6 +21,8 @@ struct ExpertSet {
 // Device workspace, sized at create for (max_tokens, max_top_k).
 struct Workspace {
     float *scores = nullptr;        // [Tm][E]
+    float *logit_part = nullptr;    // [logit_part_floats] split-K partial router logits
+    size_t logit_part_floats = 0;
     int32_t *idx = nullptr;         // [Tm][km]
     float *w = nullptr;             // [Tm][km]
     int32_t *inv_row = nullptr;     // [Tm][km]
@@ -71,8 +73,10 @@ struct FfnArgs {
 
 // Launchers. Each returns the number of kernels it enqueued, or -1 on a launch error
 // (the CUDA error is then available from cudaGetLastError()).
+// `partial` ([partial_floats] fp32) holds split-K partial logits for larger T.
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
-                  int E, int top_k, float *scores, int32_t *idx, float *w, cudaStream_t st);
+                  int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
+                  int num_sms, cudaStream_t st);
 // `gather`: also copy the activation rows into expert-grouped order (ws.xp). `cost_tokens`: rows
 // per unit of work cost in ws.touched_cost (see permute_scan).
 int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,

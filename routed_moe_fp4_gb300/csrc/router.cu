@@ -9,6 +9,8 @@
 
 #include <float.h>
 
+#include <algorithm>
+
 namespace colimoe {
 namespace {
 
@@ -90,13 +92,18 @@ router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
 // Large T: a 64 tokens x 64 experts tile per block, 4 x 4 outputs per thread, K chunks of 32.
 constexpr int kTileT = 64, kTileE = 64, kTileK = 32;
 
+// gridDim.z splits H into slices of `hs` columns: with one split the block writes sigmoid(logit)
+// to `out` ([T][E]); with several it writes its partial logits to out + z * T * E and
+// router_split_reduce sums them in split order (deterministic) and applies the sigmoid.
 __global__ void __launch_bounds__(256)
 router_logits_tiled(const __nv_bfloat16 *__restrict__ x, int T, int H, const float *__restrict__ wr,
-                    int E, float *__restrict__ scores) {
+                    int E, int hs, float *__restrict__ out) {
     __shared__ float xs[kTileK][kTileT + 4];
     __shared__ float ws[kTileK][kTileE + 4];
     const int tid = threadIdx.x;
     const int tt = blockIdx.x * kTileT, ee = blockIdx.y * kTileE;
+    const int kb = blockIdx.z * hs, ke = min(H, kb + hs);
+    const bool split = gridDim.z > 1;
     const int ty = tid / 16, tx = tid % 16;
     float acc[4][4];
 #pragma unroll
@@ -105,7 +112,7 @@ router_logits_tiled(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 
     const int lr = tid / 4, lk = (tid % 4) * 8;   // loader: row (token / expert), 8 k values
-    for (int k0 = 0; k0 < H; k0 += kTileK) {
+    for (int k0 = kb; k0 < ke; k0 += kTileK) {
         {   // x tile: 64 tokens x 32 k as bf16 -> fp32, transposed
             const int t = tt + lr;
             uint4 v = make_uint4(0, 0, 0, 0);
@@ -140,6 +147,7 @@ router_logits_tiled(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
         }
         __syncthreads();
     }
+    float *dst = out + (split ? (size_t)blockIdx.z * T * E : 0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int t = tt + ty * 4 + i;
@@ -147,8 +155,17 @@ router_logits_tiled(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int e = ee + tx * 4 + j;
-            if (e < E) scores[(size_t)t * E + e] = sigmoidf_ieee(acc[i][j]);
+            if (e < E) dst[(size_t)t * E + e] = split ? acc[i][j] : sigmoidf_ieee(acc[i][j]);
         }
+    }
+}
+
+__global__ void __launch_bounds__(256)
+router_split_reduce(const float *__restrict__ part, int n, int splits, float *__restrict__ scores) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        float a = part[i];
+        for (int z = 1; z < splits; ++z) a += part[(size_t)z * n + i];
+        scores[i] = sigmoidf_ieee(a);
     }
 }
 
@@ -233,16 +250,31 @@ router_topk(const float *__restrict__ scores, const float *__restrict__ bias, in
 }  // namespace
 
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
-                  int E, int top_k, float *scores, int32_t *idx, float *w, cudaStream_t st) {
+                  int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
+                  int num_sms, cudaStream_t st) {
     int n = 0;
     if (T < 64) {
         dim3 grid((E + 1) / 2, (T + kSmallTok - 1) / kSmallTok);
         router_logits_small<<<grid, 128, 0, st>>>(x, T, H, router_w, E, scores);
+        ++n;
     } else {
-        dim3 grid((T + kTileT - 1) / kTileT, (E + kTileE - 1) / kTileE);
-        router_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, router_w, E, scores);
+        const int tiles = ((T + kTileT - 1) / kTileT) * ((E + kTileE - 1) / kTileE);
+        int splits = (2 * num_sms + tiles - 1) / tiles;          // aim for two blocks per SM
+        splits = std::min(splits, std::max(1, H / (8 * kTileK)));  // at least 8 K chunks per split
+        while (splits > 1 && (size_t)splits * T * E > partial_floats) --splits;
+        const int chunks = H / kTileK;
+        const int hs = ((chunks + splits - 1) / splits) * kTileK;
+        splits = (H + hs - 1) / hs;
+        dim3 grid((T + kTileT - 1) / kTileT, (E + kTileE - 1) / kTileE, splits);
+        router_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, router_w, E, hs, splits > 1 ? partial : scores);
+        ++n;
+        if (splits > 1) {
+            const int cnt = T * E;
+            router_split_reduce<<<std::min((cnt + 255) / 256, 4 * num_sms), 256, 0, st>>>(partial, cnt, splits,
+                                                                                          scores);
+            ++n;
+        }
     }
-    ++n;
     const int npl = (E + 31) / 32;
     const dim3 grid((T + 7) / 8);
     if (npl <= 1)       router_topk<1><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
