@@ -60,9 +60,13 @@ enum {
 
 /* FFN path selection for coli_moe_set_ffn_path. */
 enum {
-    COLI_FFN_AUTO = 0,   /* tensor-core grouped GEMM when tokens per touched expert are many */
-    COLI_FFN_GEMV = 1,   /* weight-streaming GEMV kernels (small token counts) */
-    COLI_FFN_GEMM = 2,   /* tcgen05 grouped GEMM kernels */
+    COLI_FFN_AUTO = 0,      /* the block-scaled GEMM when its conditions hold, else GEMV / bf16 GEMM */
+    COLI_FFN_GEMV = 1,      /* weight-streaming GEMV kernels on the CUDA cores */
+    COLI_FFN_GEMM = 2,      /* block-scaled tcgen05 GEMM: E2M1 weights straight from HBM to the tensor
+                               cores (kind::mxf8f6f4), activations as exact E4M3 terms; needs 32-byte
+                               aligned code pointers. Follows the hardware's UE8M0 decoding, which
+                               differs from the format above only for scale bytes 0 and 255. */
+    COLI_FFN_GEMM_BF16 = 3, /* tcgen05 GEMM with the weights dequantised to bf16 in shared memory */
 };
 
 typedef struct coli_moe coli_moe_t;

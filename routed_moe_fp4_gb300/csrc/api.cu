@@ -44,7 +44,7 @@ void set_err(coli_moe_t *h, const char *fmt, ...) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_ws(Workspace &ws) {
-    void *ptrs[] = {ws.scores, ws.logit_part, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
+    void *ptrs[] = {ws.xq, ws.xqs, ws.hq, ws.hqs, ws.scores, ws.logit_part, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
                     ws.n_touched, ws.xp, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
                     ws.out_stage, ws.tile_sched};
     for (void *p : ptrs)
@@ -74,14 +74,28 @@ ExpertSet to_set(const coli_mxfp4_experts *e) {
     return s;
 }
 
-// Tokens per touched expert above which the tensor-core grouped GEMM beats weight streaming.
-bool use_gemm(const coli_moe_t *h, int T, int top_k) {
-    if (h->ffn_path == COLI_FFN_GEMV) return false;
-    if (h->ffn_path == COLI_FFN_GEMM) return true;
-    if (!gemm_available()) return false;
+enum FfnKind { kFfnGemv, kFfnMx, kFfnBf16 };
+
+bool mx_pointers_ok(const coli_mxfp4_experts *r, const coli_mxfp4_experts *s) {
+    auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
+    return al(r->gate_up_codes) && al(r->down_codes) && (!s || (al(s->gate_up_codes) && al(s->down_codes)));
+}
+
+// The FFN kernels a forward uses: the block-scaled GEMM whenever it can run (weights go to the
+// tensor cores without passing through the ALU, at every token count); otherwise the bf16 GEMM
+// when tokens per touched expert are many, the GEMV when they are few.
+FfnKind pick_ffn(const coli_moe_t *h, int T, int top_k, const coli_mxfp4_experts *r, const coli_mxfp4_experts *s) {
+    switch (h->ffn_path) {
+        case COLI_FFN_GEMV: return kFfnGemv;
+        case COLI_FFN_GEMM: return kFfnMx;
+        case COLI_FFN_GEMM_BF16: return kFfnBf16;
+        default: break;
+    }
+    if (mx_available() && mx_pointers_ok(r, s)) return kFfnMx;
+    if (!gemm_available()) return kFfnGemv;
     const double E = h->cfg.num_experts;
     const double touched = E * (1.0 - pow(1.0 - (double)top_k / E, (double)T));
-    return (double)T * top_k / (touched > 0 ? touched : 1.0) > 3.0;
+    return (double)T * top_k / (touched > 0 ? touched : 1.0) > 3.0 ? kFfnBf16 : kFfnGemv;
 }
 
 int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router_w, const float *router_bias,
@@ -123,7 +137,8 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     const bool with_shared = shared != nullptr;
     Workspace &ws = h->ws;
     int launches = 0, n;
-    const bool gemm = use_gemm(h, T, top_k);
+    const FfnKind ffn = pick_ffn(h, T, top_k, packed, shared);
+    const bool gemm = ffn == kFfnBf16;
     const bool prof = h->profiling;
     h->stage_valid = false;
     if (prof) cudaEventRecord(h->ev[0], st);
@@ -164,9 +179,20 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         a.hh = ws.hh;
         a.hinv = ws.hinv;
         a.y = ws.y;
+        a.xq = ws.xq;
+        a.xqs = ws.xqs;
+        a.hq = ws.hq;
+        a.hqs = ws.hqs;
         a.err = ws.err;
         cudaEvent_t mid = prof ? h->ev[3] : nullptr;
-        if (gemm) {
+        if (ffn == kFfnMx) {
+            n = launch_ffn_mx(a, h->num_sms, ws.tile_sched, mid, st);
+            if (n == -2) {
+                set_err(h, "block-scaled GEMM path unavailable (needs 32-byte aligned code pointers and a "
+                           "tensor-map encoder)");
+                return COLI_ERR_INVALID_ARG;
+            }
+        } else if (gemm) {
             n = launch_ffn_gemm(a, h->num_sms, ws.tile_sched, mid, st);
             if (n == -2) {
                 set_err(h, "tensor-core grouped GEMM path is not available for this configuration");
@@ -259,9 +285,14 @@ int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **
               alloc(&ws.xh, Tm * H) && alloc(&ws.xinv, Tm) && alloc(&ws.hh, rows * (size_t)h->I_max) &&
               alloc(&ws.hinv, rows) && alloc(&ws.err, 4) && alloc(&ws.x_stage, Tm * H) &&
               alloc(&ws.out_stage, Tm * H);
+    if (ok)
+        ok = alloc(&ws.xq, 2 * rows * H) && alloc(&ws.xqs, 2 * rows * (H / 32)) &&
+             alloc(&ws.hq, 3 * rows * (size_t)h->I_max) && alloc(&ws.hqs, 3 * rows * (size_t)(h->I_max / 32));
     if (ok) ok = cudaMemset(ws.err, 0, sizeof(int)) == cudaSuccess;
     if (ok) {
         ws.tile_sched_bytes = gemm_sched_bytes((int)E, (int)rows);
+        const size_t mx_bytes = mx_sched_ints((int)E, (int)rows) * sizeof(int32_t);
+        if (mx_bytes > ws.tile_sched_bytes) ws.tile_sched_bytes = mx_bytes;
         ok = cudaMalloc(&ws.tile_sched, ws.tile_sched_bytes + 256) == cudaSuccess;
     }
     if (!ok) {
@@ -323,7 +354,7 @@ void coli_moe_destroy(coli_moe_t *h) {
 const char *coli_moe_last_error(const coli_moe_t *h) { return h ? h->err : g_create_err; }
 
 int coli_moe_set_ffn_path(coli_moe_t *h, int32_t path) {
-    if (!h || path < COLI_FFN_AUTO || path > COLI_FFN_GEMM) {
+    if (!h || path < COLI_FFN_AUTO || path > COLI_FFN_GEMM_BF16) {
         if (h) set_err(h, "unknown FFN path %d", path);
         return COLI_ERR_INVALID_ARG;
     }

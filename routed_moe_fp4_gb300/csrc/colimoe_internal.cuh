@@ -35,6 +35,10 @@ struct Workspace {
     __nv_bfloat16 *xp = nullptr;    // [Tm*km + Tm][H] expert-grouped activation rows
     __nv_bfloat16 *h = nullptr;     // [Tm*km + Tm][I_max] SwiGLU output rows
     float *y = nullptr;             // [Tm*km + Tm][H] expert output rows
+    uint8_t *xq = nullptr;          // [2][rows][H] E4M3 terms of the activation rows (block-scaled path)
+    uint8_t *xqs = nullptr;         // [2][rows][H/32] their UE8M0 scales
+    uint8_t *hq = nullptr;          // [3][rows][I_max] E4M3 terms of h
+    uint8_t *hqs = nullptr;         // [3][rows][I_max/32]
     __half *xh = nullptr;           // [Tm][H] tokens as scaled fp16, permuted unit layout (GEMV path)
     float *xinv = nullptr;          // [Tm] inverse scales of xh
     __half *hh = nullptr;           // [Tm*km + Tm][I_max] h rows as scaled fp16 (GEMV path)
@@ -68,6 +72,7 @@ struct FfnArgs {
     __half *hh;                     // GEMV path: scaled fp16 h rows and inverse scales
     float *hinv;
     float *y;                       // [rows][H]
+    uint8_t *xq, *xqs, *hq, *hqs;   // block-scaled path: E4M3 activation terms and scales
     int *err;
 };
 
@@ -88,7 +93,13 @@ int launch_ffn_gemv(const FfnArgs &a, int num_sms, cudaEvent_t mid, cudaStream_t
 int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T, int H, int top_k,
                    bool with_shared, __nv_bfloat16 *out, cudaStream_t st);
 
-// Grouped tcgen05 GEMM path (gemm_tc.cu).
+// Block-scaled MXFP4 tcgen05 GEMM path (gemm_mx.cu): native E2M1 weights x E4M3 activation terms.
+bool mx_available();
+size_t mx_sched_ints(int E, int max_rows);
+bool mx_supported(const FfnArgs &a);
+int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
+
+// Grouped tcgen05 GEMM path with weights dequantised to bf16 in shared memory (gemm_tc.cu).
 size_t gemm_sched_bytes(int E, int max_rows);
 bool gemm_available();
 int launch_ffn_gemm(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);

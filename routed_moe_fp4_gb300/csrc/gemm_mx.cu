@@ -1,0 +1,557 @@
+// A3/A4 on the tensor cores with native MXFP4 weights: block-scaled tcgen05.mma
+// (kind::mxf8f6f4, E2M1 weights x E4M3 activations, UE8M0 scales per 32 elements, fp32 accumulate).
+// ("DeepSeek V4 Flash CPU inference with NVMe expert streaming": FP4 E2M1 experts with UE8M0
+// group-32 scales; the gate/up pair and the down projection. "the CUDA tier wired into the
+// DeepSeek V4 engine": expert-grouped GEMM rows.)
+//
+// The weights never pass through the ALU: TMA copies the packed E2M1 codes into shared memory in
+// the unpacked 16-value/16-byte form the MMA reads (tensor-map type 16U4_ALIGN16B, 128-byte
+// swizzle), and the UE8M0 scale bytes go to TMEM, where the MMA applies them per 32-element block.
+//
+// Activations are split into E4M3 terms that the MMA multiplies exactly, each term with its own
+// UE8M0 scale per 32 elements:
+//   x (bf16, 8 significant bits): two terms reproduce it (the residual of a 4-bit rounding of an
+//     8-bit value fits in 4 bits), up to elements 2^14 below their block maximum;
+//   h (fp32, from the gate/up epilogue): three terms, relative error about 2^-12.
+// The term results are separate accumulators in TMEM that the epilogue adds.
+//
+// Swap-AB tiles: 128 weight rows (M) x up to 64 tokens of one group (N). One persistent block per
+// SM; warp roles:
+//   warp 0     TMA producer (weight codes, activation terms) into a 4-stage ring, 128 K per stage
+//   warp 1     TMEM owner and MMA issuer
+//   warps 2-5  scale loaders: the stage's UE8M0 bytes -> TMEM (tcgen05.st), layout: lane l,
+//              column c holds the four K-block scales of row l + 32c (replicated per lane quarter)
+//   warps 6-9  epilogue: gate/up -> SwiGLU -> three E4M3 terms of h (scales from warp-wide block
+//              maxima: a warp holds the 32 consecutive i-values of one scale block); down -> y
+// Every barrier wait is bounded (sm103_ptx.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp8.h>
+
+#include "colimoe_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace colimoe {
+namespace {
+
+constexpr int BM = 128, BN = 64, BK = 128;
+constexpr int NS = 4;
+constexpr int kThreads = 320;
+constexpr uint32_t kASmem = BM * BK;           // 16 KB: one unpacked E2M1 tile
+constexpr uint32_t kATx = BM * BK / 2;         // 8 KB of packed codes per tile
+constexpr uint32_t kBSmem = BN * BK;           // 8 KB: one E4M3 activation term tile
+// stage: A0 | A1 | B0 | B1 | B2
+constexpr uint32_t kOffA0 = 0, kOffA1 = kASmem, kOffB = 2 * kASmem;
+constexpr uint32_t kStageBytes = 2 * kASmem + 3 * kBSmem;   // 57344
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 16 per stage
+constexpr int kXTerms = 2, kHTerms = 3;
+
+enum Mode { kGateUp = 0, kDown = 1 };
+
+struct MxParams {
+    int E, H, I, I_s, I_max, rows;
+    int mode, m_tiles, nterms;
+    const int32_t *cnt, *off, *touched, *n_touched, *ntile_prefix, *ntile_owner;
+    const uint8_t *w_scales_routed, *w_scales_shared;   // UE8M0 bytes of the weight rows
+    const uint8_t *act_scales;                          // [nterms][rows][K/32]
+    int act_ld;                                         // K of the activation terms (H or I_max)
+    // gate/up epilogue outputs: h terms and their scales
+    uint8_t *hq;                                        // [3][rows][I_max]
+    uint8_t *hs;                                        // [3][rows][I_max/32]
+    float *y;                                           // down epilogue output [rows][H]
+    int *err;
+};
+
+struct TileInfo {
+    int g, mt, row0, n_valid, Ig, nk;
+    bool valid, shared;
+    size_t ge;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const MxParams &p, int t) {
+    TileInfo ti;
+    ti.mt = t % p.m_tiles;
+    const int r = t / p.m_tiles;
+    const int u = p.ntile_owner[r];
+    ti.g = p.touched[u];
+    const int nt = r - p.ntile_prefix[u];
+    ti.shared = ti.g == p.E;
+    ti.Ig = ti.shared ? p.I_s : p.I;
+    ti.ge = ti.shared ? 0 : (size_t)ti.g;
+    ti.row0 = p.off[ti.g] + nt * BN;
+    ti.n_valid = min(BN, p.cnt[ti.g] - nt * BN);
+    ti.valid = p.mode == kGateUp ? ti.mt * BM < ti.Ig : true;
+    ti.nk = (p.mode == kGateUp ? p.H : ti.Ig) / BK;
+    return ti;
+}
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Block-scaled instruction descriptor: A E2M1 (5), B E4M3 (0), UE8M0 scales, M x N, scale-factor
+// byte ids for A and B (the K block of the 32-wide MMA within the 128-wide stage).
+__device__ __forceinline__ uint32_t idesc_mx(int N, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(BM >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mx(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x2(uint32_t taddr, uint32_t a, uint32_t b) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// One E4M3 term of a warp-wide block of 32 values (one per lane): scale byte s with
+// |v| / 2^(s-127) < 256, the E4M3 code of v / 2^(s-127) (round to nearest even), and the
+// residual v - code * 2^(s-127) (exact in fp32).
+__device__ __forceinline__ uint8_t e4m3_term(float v, float &resid, uint32_t &sbyte) {
+    const float amax = warp_max(fabsf(v));
+    const uint32_t ef = (__float_as_uint(amax) >> 23) & 0xFF;
+    uint32_t s = (amax > 0.f && ef < 255) ? (ef > 8 ? ef - 7 : 1) : 127;
+    s = min(s, 253u);
+    const float scale = __uint_as_float(s << 23);            // 2^(s-127)
+    const float inv = __uint_as_float((254u - s) << 23);     // 2^(127-s)
+    uint16_t q2;
+    asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, %1, %1;\n mov.b16 %0, t;\n}\n" : "=h"(q2) : "f"(v * inv));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q2));
+    const float back = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+    resid = v - back * scale;
+    sbyte = s;
+    return (uint8_t)(q2 & 0xFF);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
+        const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
+        const __grid_constant__ CUtensorMap tm_b2, const MxParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
+    // barriers: tma_full[NS], sf_full[NS], empty[NS], acc_full, acc_empty, drain
+    uint64_t *tma_full = bar, *sf_full = bar + NS, *empty = bar + 2 * NS, *acc_full = bar + 3 * NS,
+             *acc_empty = bar + 3 * NS + 1, *drain = bar + 3 * NS + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * NS + 3);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool gu = p.mode == kGateUp;
+    const int n_a = gu ? 2 : 1;
+    const int nterms = p.nterms;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&tma_full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sf_full[s]), 128);
+            ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(acc_full), 1);
+        ptx::mbar_init(ptx::smem_addr(acc_empty), 4);
+        ptx::mbar_init(ptx::smem_addr(drain), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total_tiles = p.m_tiles * p.ntile_prefix[*p.n_touched];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tm_a_routed);
+            ptx::prefetch_tmap(&tm_b0);
+            const uint64_t pol = ptx::policy_evict_first();
+            const CUtensorMap *tb[3] = {&tm_b0, &tm_b1, &tm_b2};
+            const uint32_t tx = n_a * kATx + nterms * kBSmem;
+            uint32_t it = 0;
+            for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+                const TileInfo ti = decode_tile(p, t);
+                if (!ti.valid) continue;
+                const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
+                const int rpe = gu ? 2 * ti.Ig : p.H;
+                const int arow = (int)ti.ge * rpe + ti.mt * BM;
+                for (int k = 0; k < ti.nk; ++k, ++it) {
+                    const int s = it % NS;
+                    if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
+                                        abort_flag))
+                        break;
+                    const uint32_t fb = ptx::smem_addr(&tma_full[s]);
+                    const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
+                    ptx::mbar_arrive_expect_tx(fb, tx);
+                    ptx::tma_load_2d_hint(st + kOffA0, ta, k * BK, arow, fb, pol);
+                    if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, k * BK, arow + ti.Ig, fb, pol);
+                    for (int tt = 0; tt < nterms; ++tt)
+                        ptx::tma_load_2d(st + kOffB + tt * kBSmem, tb[tt], k * BK, ti.row0, fb);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, tcount = 0;
+            for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+                const TileInfo ti = decode_tile(p, t);
+                if (!ti.valid) continue;
+                if (!ptx::mbar_wait(ptx::smem_addr(acc_empty), (tcount & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
+                                    abort_flag))
+                    break;
+                ++tcount;
+                ptx::tc_fence_after();
+                const int n_mma = (ti.n_valid + 15) & ~15;
+                bool ok = true;
+                for (int k = 0; k < ti.nk; ++k, ++it) {
+                    const int s = it % NS;
+                    const uint32_t ph = (it / NS) & 1u;
+                    if (!ptx::mbar_wait(ptx::smem_addr(&tma_full[s]), ph, p.err, ptx::kErrWaitFull, abort_flag) ||
+                        !ptx::mbar_wait(ptx::smem_addr(&sf_full[s]), ph, p.err, ptx::kErrWaitFull, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_addr(smem + s * kStageBytes);
+                    const uint32_t sf = tmem + kSfCol0 + s * 16;
+#pragma unroll
+                    for (int kb = 0; kb < BK / 32; ++kb) {
+                        const uint32_t idesc = idesc_mx(n_mma, kb);
+                        for (int a = 0; a < n_a; ++a) {
+                            const uint64_t ad = sw128_desc(sa + (a ? kOffA1 : kOffA0) + kb * 32);
+                            for (int tt = 0; tt < nterms; ++tt) {
+                                const uint32_t d = tmem + (uint32_t)((a * nterms + tt) * BN);
+                                mma_mx(d, ad, sw128_desc(sa + kOffB + tt * kBSmem + kb * 32), idesc, sf + 4 * a,
+                                       sf + 8 + 2 * tt, (k > 0 || kb > 0) ? 1u : 0u);
+                            }
+                        }
+                    }
+                    ptx::mma_commit(ptx::smem_addr(&empty[s]));
+                }
+                if (!ok) break;
+                ptx::mma_commit(ptx::smem_addr(acc_full));
+            }
+            ptx::mma_commit(ptx::smem_addr(drain));
+            ptx::mbar_wait(ptx::smem_addr(drain), 0, nullptr, 0, nullptr);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------------ scale loaders
+        const int quad = warp & 3;                       // the TMEM lane quarter this warp writes
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+            const TileInfo ti = decode_tile(p, t);
+            if (!ti.valid) continue;
+            const int K = gu ? p.H : ti.Ig;
+            const int kb_row = K / 32;                   // scale bytes per weight row
+            const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
+            const int rpe = gu ? 2 * ti.Ig : p.H;
+            const size_t arow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM;
+            const int kba = p.act_ld / 32;               // scale bytes per activation row
+            bool ok = true;
+            for (int k = 0; k < ti.nk; ++k, ++it) {
+                uint32_t wa[2][4], wb[3][2];
+#pragma unroll
+                for (int a = 0; a < 2; ++a)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const size_t row = arow + (a ? ti.Ig : 0) + lane + 32 * c;
+                        wa[a][c] = (a < n_a) ? __ldg(reinterpret_cast<const uint32_t *>(ws + row * kb_row) + k)
+                                             : 0x7F7F7F7Fu;
+                    }
+#pragma unroll
+                for (int tt = 0; tt < 3; ++tt)
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const int row = ti.row0 + lane + 32 * c;
+                        wb[tt][c] = (tt < nterms && row < p.rows)
+                                        ? __ldg(reinterpret_cast<const uint32_t *>(
+                                                    p.act_scales + ((size_t)tt * p.rows + row) * kba) + k)
+                                        : 0x7F7F7F7Fu;
+                    }
+                const int s = it % NS;
+                if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
+                                    abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t col = lane_base + kSfCol0 + s * 16;
+                tmem_st_x4(col, wa[0][0], wa[0][1], wa[0][2], wa[0][3]);
+                tmem_st_x4(col + 4, wa[1][0], wa[1][1], wa[1][2], wa[1][3]);
+                tmem_st_x2(col + 8, wb[0][0], wb[0][1]);
+                tmem_st_x2(col + 10, wb[1][0], wb[1][1]);
+                tmem_st_x2(col + 12, wb[2][0], wb[2][1]);
+                tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
+            }
+            if (!ok) break;
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int quad = warp & 3;
+        const int m = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        uint32_t tcount = 0;
+        for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+            const TileInfo ti = decode_tile(p, t);
+            if (!ti.valid) continue;
+            if (!ptx::mbar_wait(ptx::smem_addr(acc_full), tcount & 1u, p.err, ptx::kErrWaitAccum, abort_flag)) break;
+            ++tcount;
+            ptx::tc_fence_after();
+            const int mrow = ti.mt * BM + m;
+            for (int c0 = 0; c0 < ti.n_valid; c0 += 16) {
+                if (gu) {
+                    uint32_t gh[16], gl[16], uh[16], ul[16];
+                    ptx::tmem_ld16(lane_base + 0 * BN + c0, gh);
+                    ptx::tmem_ld16(lane_base + 1 * BN + c0, gl);
+                    ptx::tmem_ld16(lane_base + 2 * BN + c0, uh);
+                    ptx::tmem_ld16(lane_base + 3 * BN + c0, ul);
+                    ptx::tmem_ld_wait();
+                    for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j) {
+                        const float g = __uint_as_float(gh[j]) + __uint_as_float(gl[j]);
+                        const float u = __uint_as_float(uh[j]) + __uint_as_float(ul[j]);
+                        float v = __fdiv_rn(g, 1.0f + expf(-g)) * u;
+                        const size_t row = (size_t)ti.row0 + c0 + j;
+#pragma unroll
+                        for (int tt = 0; tt < kHTerms; ++tt) {
+                            uint32_t sb;
+                            float r;
+                            const uint8_t q = e4m3_term(v, r, sb);
+                            p.hq[((size_t)tt * p.rows + row) * p.I_max + mrow] = q;
+                            if (lane == 0) p.hs[((size_t)tt * p.rows + row) * (p.I_max / 32) + mrow / 32] = (uint8_t)sb;
+                            v = r;
+                        }
+                    }
+                } else {
+                    uint32_t d[3][16];
+                    ptx::tmem_ld16(lane_base + 0 * BN + c0, d[0]);
+                    ptx::tmem_ld16(lane_base + 1 * BN + c0, d[1]);
+                    ptx::tmem_ld16(lane_base + 2 * BN + c0, d[2]);
+                    ptx::tmem_ld_wait();
+                    for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j) {
+                        float acc = __uint_as_float(d[0][j]);
+                        for (int tt = 1; tt < nterms; ++tt) acc += __uint_as_float(d[tt][j]);
+                        p.y[((size_t)ti.row0 + c0 + j) * p.H + mrow] = acc;
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(acc_empty));
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// x rows (expert-grouped, via src_token) -> two E4M3 terms with UE8M0 scales per 32 elements.
+// One warp per row; a warp handles one 32-element block per step (lane = element).
+__global__ void __launch_bounds__(256)
+quant_x_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
+             uint8_t *__restrict__ xq, uint8_t *__restrict__ xs) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const __nv_bfloat16 *src = x + (size_t)src_token[row] * H;
+    for (int b = 0; b < H / 32; ++b) {
+        float v = __bfloat162float(src[b * 32 + lane]);
+#pragma unroll
+        for (int tt = 0; tt < kXTerms; ++tt) {
+            uint32_t sb;
+            float r;
+            const uint8_t q = e4m3_term(v, r, sb);
+            xq[((size_t)tt * rows + row) * H + b * 32 + lane] = q;
+            if (lane == 0) xs[((size_t)tt * rows + row) * (H / 32) + b] = (uint8_t)sb;
+            v = r;
+        }
+    }
+}
+
+// n-tile bookkeeping (BN rows per tile): prefix[u] over touched groups, owner[r] = group of tile r.
+__global__ void __launch_bounds__(1024)
+mx_ntiles(const int32_t *__restrict__ cnt, const int32_t *__restrict__ touched, const int32_t *__restrict__ n_touched,
+          int32_t *__restrict__ prefix, int32_t *__restrict__ owner) {
+    __shared__ int part[1024];
+    const int nt = *n_touched;
+    int carry = 0;
+    for (int u0 = 0; u0 < nt; u0 += 1024) {
+        const int u = u0 + threadIdx.x;
+        const int c = u < nt ? (cnt[touched[u]] + BN - 1) / BN : 0;
+        part[threadIdx.x] = c;
+        __syncthreads();
+        for (int o = 1; o < 1024; o <<= 1) {
+            const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+            __syncthreads();
+            part[threadIdx.x] += v;
+            __syncthreads();
+        }
+        const int excl = carry + part[threadIdx.x] - c;
+        if (u < nt) {
+            prefix[u] = excl;
+            for (int r = 0; r < c; ++r) owner[excl + r] = u;
+        }
+        carry += part[1023];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) prefix[nt] = carry;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Packed E2M1 rows of K elements: unpacked into 16-values-per-16-bytes smem, 128 x 128 boxes.
+bool map_codes(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows) {
+    auto enc = encoder();
+    if (!enc || (reinterpret_cast<uintptr_t>(base) & 31)) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K / 2};
+    const cuuint32_t box[2] = {BK, BM};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// E4M3 activation rows (bytes): 128 x 64 boxes with the 128-byte swizzle.
+bool map_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K};
+    const cuuint32_t box[2] = {BK, BN};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool mx_available() { return encoder() != nullptr; }
+
+size_t mx_sched_ints(int E, int max_rows) { return (size_t)E + 2 + (size_t)max_rows / BN + E + 2; }
+
+bool mx_supported(const FfnArgs &a) {
+    auto al = [](const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
+    return mx_available() && al(a.routed.gu_codes) && al(a.routed.d_codes) && al(a.shared.gu_codes) &&
+           al(a.shared.d_codes);
+}
+
+int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
+    if (!mx_supported(a)) return -2;
+    int32_t *prefix = static_cast<int32_t *>(sched);
+    int32_t *owner = prefix + a.E + 2;
+    int n = 0;
+    quant_x_rows<<<(a.rows + 7) / 8, 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
+    mx_ntiles<<<1, 1024, 0, st>>>(a.cnt, a.touched, a.n_touched, prefix, owner);
+    n += 2;
+
+    const size_t smem = NS * kStageBytes + 1024 + 256;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(gemm_mx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        attr = true;
+    }
+    MxParams p{};
+    p.E = a.E;
+    p.H = a.H;
+    p.I = a.I;
+    p.I_s = a.I_s;
+    p.I_max = a.I_max;
+    p.rows = a.rows;
+    p.cnt = a.cnt;
+    p.off = a.off;
+    p.touched = a.touched;
+    p.n_touched = a.n_touched;
+    p.ntile_prefix = prefix;
+    p.ntile_owner = owner;
+    p.hq = a.hq;
+    p.hs = a.hqs;
+    p.y = a.y;
+    p.err = a.err;
+
+    CUtensorMap tar, tas, tb0, tb1, tb2;
+    // gate/up: A = gate/up code rows, B = two terms of x
+    p.mode = kGateUp;
+    p.m_tiles = (a.I_max + BM - 1) / BM;
+    p.nterms = kXTerms;
+    p.w_scales_routed = a.routed.gu_scales;
+    p.w_scales_shared = a.shared.gu_scales;
+    p.act_scales = a.xqs;
+    p.act_ld = a.H;
+    bool ok = map_codes(&tar, a.routed.gu_codes, a.H, (uint64_t)a.E * 2 * a.I) &&
+              map_act(&tb0, a.xq, a.H, a.rows) && map_act(&tb1, a.xq + (size_t)a.rows * a.H, a.H, a.rows);
+    tb2 = tb1;
+    if (a.shared.gu_codes) ok = ok && map_codes(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s);
+    else tas = tar;
+    if (!ok) return -2;
+    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb0, tb1, tb2, p);
+    ++n;
+    if (mid) cudaEventRecord(mid, st);
+
+    // down: A = down code rows, B = three terms of h
+    p.mode = kDown;
+    p.m_tiles = a.H / BM;
+    p.nterms = kHTerms;
+    p.w_scales_routed = a.routed.d_scales;
+    p.w_scales_shared = a.shared.d_scales;
+    p.act_scales = a.hqs;
+    p.act_ld = a.I_max;
+    ok = map_codes(&tar, a.routed.d_codes, a.I, (uint64_t)a.E * a.H) &&
+         map_act(&tb0, a.hq, a.I_max, a.rows) && map_act(&tb1, a.hq + (size_t)a.rows * a.I_max, a.I_max, a.rows) &&
+         map_act(&tb2, a.hq + 2 * (size_t)a.rows * a.I_max, a.I_max, a.rows);
+    if (a.shared.d_codes) ok = ok && map_codes(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H);
+    else tas = tar;
+    if (!ok) return -2;
+    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb0, tb1, tb2, p);
+    ++n;
+    return cudaPeekAtLastError() == cudaSuccess ? n : -1;
+}
+
+}  // namespace colimoe

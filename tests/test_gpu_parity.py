@@ -9,7 +9,7 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-GEMV, GEMM, AUTO = 1, 2, 0
+GEMV, GEMM, AUTO, BF16 = 1, 2, 0, 3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -112,11 +112,12 @@ def test_edge_cases(oracle, wl):
     _assert_ok(rep)
 
 
+@pytest.mark.parametrize("path", [GEMM, BF16, GEMV], ids=["mx", "bf16", "gemv"])
 @pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T16", "sweep_T128"])
-def test_gemm_path(oracle, name):
-    """The tcgen05 grouped-GEMM path, forced, against the oracle."""
+def test_ffn_paths(oracle, name, path):
+    """Each FFN path, forced, against the oracle."""
     inputs = S.make_inputs(name)
-    rep, _, _ = _run(oracle, inputs, GEMM, n_tokens=8)
+    rep, _, _ = _run(oracle, inputs, path, n_tokens=8)
     _assert_ok(rep)
 
 
@@ -126,17 +127,19 @@ def test_gemm_path(oracle, name):
     _custom("gemm_noshared", I_s=0),
     _custom("gemm_many_rows", T=300, E=4, top_k=2),
 ], ids=lambda w: w.name)
-def test_gemm_edge_cases(oracle, wl):
+@pytest.mark.parametrize("path", [GEMM, BF16], ids=["mx", "bf16"])
+def test_gemm_edge_cases(oracle, wl, path):
     inputs = S.make_inputs(wl)
-    rep, _, _ = _run(oracle, inputs, GEMM)
+    rep, _, _ = _run(oracle, inputs, path)
     _assert_ok(rep)
 
 
-def test_gemm_matches_gemv(oracle):
-    """Both FFN paths agree with each other within the parity bar on the same routing."""
+@pytest.mark.parametrize("path", [GEMM, BF16], ids=["mx", "bf16"])
+def test_gemm_matches_gemv(oracle, path):
+    """The FFN paths agree with each other within the parity bar on the same routing."""
     inputs = S.make_inputs("sweep_T64")
     o1, r1, _ = P.run_gpu(inputs, path=GEMV)
-    o2, r2, _ = P.run_gpu(inputs, path=GEMM)
+    o2, r2, _ = P.run_gpu(inputs, path=path)
     assert np.array_equal(r1["idx"], r2["idx"])
     a = P.bf16_bits_to_f32(o1[0]).astype(np.float64)
     b = P.bf16_bits_to_f32(o2[0]).astype(np.float64)
