@@ -13,14 +13,17 @@
 //   x (bf16, 8 significant bits): two terms reproduce it (the residual of a 4-bit rounding of an
 //     8-bit value fits in 4 bits), up to elements 2^14 below their block maximum;
 //   h (fp32, from the gate/up epilogue): three terms, relative error about 2^-12.
-// The term results are separate accumulators in TMEM that the epilogue adds.
+// All terms of one weight matrix accumulate into the same TMEM accumulator (the MMA applies each
+// term's scales per 32-element block), so the sum over terms costs nothing.
 //
 // Swap-AB tiles: 128 weight rows (M) x up to 64 tokens of one group (N). One persistent block per
 // SM; warp roles:
-//   warp 0     TMA producer (weight codes, activation terms) into a 4-stage ring, 128 K per stage
-//   warp 1     TMEM owner and MMA issuer
+//   warp 0     TMA producer (weight codes, activation terms) into a 4-stage ring, 128 K per stage;
+//              tiles with at most 16 tokens load a 16-row activation box
+//   warp 1     TMEM owner and MMA issuer; accumulators double buffered (2 x 128 columns)
 //   warps 2-5  scale loaders: the stage's UE8M0 bytes -> TMEM (tcgen05.st), layout: lane l,
-//              column c holds the four K-block scales of row l + 32c (replicated per lane quarter)
+//              column c holds the four K-block scales of row l + 32c (replicated per lane quarter);
+//              the words of the next four stages are loaded ahead into registers
 //   warps 6-9  epilogue: gate/up -> SwiGLU -> three E4M3 terms of h (scales from warp-wide block
 //              maxima: a warp holds the 32 consecutive i-values of one scale block); down -> y
 // Every barrier wait is bounded (sm103_ptx.cuh).
@@ -44,7 +47,10 @@ constexpr uint32_t kBSmem = BN * BK;           // 8 KB: one E4M3 activation term
 constexpr uint32_t kOffA0 = 0, kOffA1 = kASmem, kOffB = 2 * kASmem;
 constexpr uint32_t kStageBytes = 2 * kASmem + 3 * kBSmem;   // 57344
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 128;             // per accumulator buffer: up to two matrices x BN
 constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 16 per stage
+constexpr int kSmallBN = 16;                   // activation box rows for tiles with few tokens
+constexpr int kPrefetch = 4;                   // scale-word lookahead (stages)
 constexpr int kXTerms = 2, kHTerms = 3;
 
 enum Mode { kGateUp = 0, kDown = 1 };
@@ -152,14 +158,15 @@ __device__ __forceinline__ uint8_t e4m3_term(float v, float &resid, uint32_t &sb
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
         const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
-        const __grid_constant__ CUtensorMap tm_b2, const MxParams p) {
+        const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_s0,
+        const __grid_constant__ CUtensorMap tm_s1, const __grid_constant__ CUtensorMap tm_s2, const MxParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
-    // barriers: tma_full[NS], sf_full[NS], empty[NS], acc_full, acc_empty, drain
+    // barriers: tma_full[NS], sf_full[NS], empty[NS], acc_full[2], acc_empty[2], drain
     uint64_t *tma_full = bar, *sf_full = bar + NS, *empty = bar + 2 * NS, *acc_full = bar + 3 * NS,
-             *acc_empty = bar + 3 * NS + 1, *drain = bar + 3 * NS + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * NS + 3);
+             *acc_empty = bar + 3 * NS + 2, *drain = bar + 3 * NS + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * NS + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,8 +179,10 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
             ptx::mbar_init(ptx::smem_addr(&sf_full[s]), 128);
             ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
         }
-        ptx::mbar_init(ptx::smem_addr(acc_full), 1);
-        ptx::mbar_init(ptx::smem_addr(acc_empty), 4);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_addr(&acc_full[b]), 1);
+            ptx::mbar_init(ptx::smem_addr(&acc_empty[b]), 4);
+        }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -195,11 +204,13 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
             ptx::prefetch_tmap(&tm_b0);
             const uint64_t pol = ptx::policy_evict_first();
             const CUtensorMap *tb[3] = {&tm_b0, &tm_b1, &tm_b2};
-            const uint32_t tx = n_a * kATx + nterms * kBSmem;
+            const CUtensorMap *tsm[3] = {&tm_s0, &tm_s1, &tm_s2};
             uint32_t it = 0;
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
                 const TileInfo ti = decode_tile(p, t);
                 if (!ti.valid) continue;
+                const bool small = ti.n_valid <= kSmallBN;
+                const uint32_t tx = n_a * kATx + nterms * (small ? kSmallBN * BK : kBSmem);
                 const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
                 const int rpe = gu ? 2 * ti.Ig : p.H;
                 const int arow = (int)ti.ge * rpe + ti.mt * BM;
@@ -214,7 +225,7 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                     ptx::tma_load_2d_hint(st + kOffA0, ta, k * BK, arow, fb, pol);
                     if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, k * BK, arow + ti.Ig, fb, pol);
                     for (int tt = 0; tt < nterms; ++tt)
-                        ptx::tma_load_2d(st + kOffB + tt * kBSmem, tb[tt], k * BK, ti.row0, fb);
+                        ptx::tma_load_2d(st + kOffB + tt * kBSmem, small ? tsm[tt] : tb[tt], k * BK, ti.row0, fb);
                 }
             }
         }
@@ -225,7 +236,8 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
                 const TileInfo ti = decode_tile(p, t);
                 if (!ti.valid) continue;
-                if (!ptx::mbar_wait(ptx::smem_addr(acc_empty), (tcount & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
+                const uint32_t buf = tcount & 1u, use = tcount >> 1;
+                if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[buf]), (use & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
                                     abort_flag))
                     break;
                 ++tcount;
@@ -248,17 +260,16 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                         const uint32_t idesc = idesc_mx(n_mma, kb);
                         for (int a = 0; a < n_a; ++a) {
                             const uint64_t ad = sw128_desc(sa + (a ? kOffA1 : kOffA0) + kb * 32);
-                            for (int tt = 0; tt < nterms; ++tt) {
-                                const uint32_t d = tmem + (uint32_t)((a * nterms + tt) * BN);
+                            const uint32_t d = tmem + buf * kAccCols + (uint32_t)(a * BN);
+                            for (int tt = 0; tt < nterms; ++tt)
                                 mma_mx(d, ad, sw128_desc(sa + kOffB + tt * kBSmem + kb * 32), idesc, sf + 4 * a,
-                                       sf + 8 + 2 * tt, (k > 0 || kb > 0) ? 1u : 0u);
-                            }
+                                       sf + 8 + 2 * tt, (k > 0 || kb > 0 || tt > 0) ? 1u : 0u);
                         }
                     }
                     ptx::mma_commit(ptx::smem_addr(&empty[s]));
                 }
                 if (!ok) break;
-                ptx::mma_commit(ptx::smem_addr(acc_full));
+                ptx::mma_commit(ptx::smem_addr(&acc_full[buf]));
             }
             ptx::mma_commit(ptx::smem_addr(drain));
             ptx::mbar_wait(ptx::smem_addr(drain), 0, nullptr, 0, nullptr);
@@ -267,8 +278,10 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
         // ------------------------------------------------------------------ scale loaders
         const int quad = warp & 3;                       // the TMEM lane quarter this warp writes
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const int kba = p.act_ld / 32;                   // scale bytes per activation row
         uint32_t it = 0;
-        for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok && !*abort_flag; t += gridDim.x) {
             const TileInfo ti = decode_tile(p, t);
             if (!ti.valid) continue;
             const int K = gu ? p.H : ti.Ig;
@@ -276,46 +289,65 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
             const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
             const int rpe = gu ? 2 * ti.Ig : p.H;
             const size_t arow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM;
-            const int kba = p.act_ld / 32;               // scale bytes per activation row
-            bool ok = true;
-            for (int k = 0; k < ti.nk; ++k, ++it) {
-                uint32_t wa[2][4], wb[3][2];
+            // this lane's rows: weight rows arow + lane + 32c (+ Ig for up), activation rows row0 + lane + 32c
+            const uint32_t *wp[2][4];
+            const uint32_t *bp[3][2];
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    wp[a][c] = (a < n_a) ? reinterpret_cast<const uint32_t *>(
+                                               ws + (arow + (a ? ti.Ig : 0) + lane + 32 * c) * kb_row)
+                                         : nullptr;
+#pragma unroll
+            for (int tt = 0; tt < 3; ++tt)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int row = ti.row0 + lane + 32 * c;
+                    bp[tt][c] = (tt < nterms && row < p.rows)
+                                    ? reinterpret_cast<const uint32_t *>(p.act_scales +
+                                                                         ((size_t)tt * p.rows + row) * kba)
+                                    : nullptr;
+                }
+            uint32_t wa[kPrefetch][8], wb[kPrefetch][6];
+            auto load = [&](int k, uint32_t(&a8)[8], uint32_t(&b6)[6]) {
 #pragma unroll
                 for (int a = 0; a < 2; ++a)
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const size_t row = arow + (a ? ti.Ig : 0) + lane + 32 * c;
-                        wa[a][c] = (a < n_a) ? __ldg(reinterpret_cast<const uint32_t *>(ws + row * kb_row) + k)
-                                             : 0x7F7F7F7Fu;
-                    }
+                    for (int c = 0; c < 4; ++c) a8[a * 4 + c] = wp[a][c] ? __ldg(wp[a][c] + k) : 0x7F7F7F7Fu;
 #pragma unroll
                 for (int tt = 0; tt < 3; ++tt)
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int row = ti.row0 + lane + 32 * c;
-                        wb[tt][c] = (tt < nterms && row < p.rows)
-                                        ? __ldg(reinterpret_cast<const uint32_t *>(
-                                                    p.act_scales + ((size_t)tt * p.rows + row) * kba) + k)
-                                        : 0x7F7F7F7Fu;
+                    for (int c = 0; c < 2; ++c) b6[tt * 2 + c] = bp[tt][c] ? __ldg(bp[tt][c] + k) : 0x7F7F7F7Fu;
+            };
+#pragma unroll
+            for (int j = 0; j < kPrefetch; ++j)
+                if (j < ti.nk) load(j, wa[j], wb[j]);
+            for (int k0 = 0; k0 < ti.nk && ok; k0 += kPrefetch) {
+#pragma unroll
+                for (int j = 0; j < kPrefetch; ++j) {
+                    const int k = k0 + j;
+                    if (k >= ti.nk) break;
+                    const int s = it % NS;
+                    if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
+                                        abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                const int s = it % NS;
-                if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
-                                    abort_flag)) {
-                    ok = false;
-                    break;
+                    ptx::tc_fence_after();
+                    const uint32_t col = lane_base + kSfCol0 + s * 16;
+                    tmem_st_x4(col, wa[j][0], wa[j][1], wa[j][2], wa[j][3]);
+                    tmem_st_x4(col + 4, wa[j][4], wa[j][5], wa[j][6], wa[j][7]);
+                    tmem_st_x2(col + 8, wb[j][0], wb[j][1]);
+                    tmem_st_x2(col + 10, wb[j][2], wb[j][3]);
+                    tmem_st_x2(col + 12, wb[j][4], wb[j][5]);
+                    tmem_st_wait();
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
+                    ++it;
+                    if (k + kPrefetch < ti.nk) load(k + kPrefetch, wa[j], wb[j]);
                 }
-                ptx::tc_fence_after();
-                const uint32_t col = lane_base + kSfCol0 + s * 16;
-                tmem_st_x4(col, wa[0][0], wa[0][1], wa[0][2], wa[0][3]);
-                tmem_st_x4(col + 4, wa[1][0], wa[1][1], wa[1][2], wa[1][3]);
-                tmem_st_x2(col + 8, wb[0][0], wb[0][1]);
-                tmem_st_x2(col + 10, wb[1][0], wb[1][1]);
-                tmem_st_x2(col + 12, wb[2][0], wb[2][1]);
-                tmem_st_wait();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
             }
-            if (!ok) break;
         }
     } else {
         // ------------------------------------------------------------------ epilogue
@@ -326,21 +358,22 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
         for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
             const TileInfo ti = decode_tile(p, t);
             if (!ti.valid) continue;
-            if (!ptx::mbar_wait(ptx::smem_addr(acc_full), tcount & 1u, p.err, ptx::kErrWaitAccum, abort_flag)) break;
+            const uint32_t buf = tcount & 1u, use = tcount >> 1;
+            if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[buf]), use & 1u, p.err, ptx::kErrWaitAccum, abort_flag))
+                break;
             ++tcount;
             ptx::tc_fence_after();
             const int mrow = ti.mt * BM + m;
+            const uint32_t acc = lane_base + buf * kAccCols;
             for (int c0 = 0; c0 < ti.n_valid; c0 += 16) {
                 if (gu) {
-                    uint32_t gh[16], gl[16], uh[16], ul[16];
-                    ptx::tmem_ld16(lane_base + 0 * BN + c0, gh);
-                    ptx::tmem_ld16(lane_base + 1 * BN + c0, gl);
-                    ptx::tmem_ld16(lane_base + 2 * BN + c0, uh);
-                    ptx::tmem_ld16(lane_base + 3 * BN + c0, ul);
+                    uint32_t gr[16], ur[16];
+                    ptx::tmem_ld16(acc + c0, gr);
+                    ptx::tmem_ld16(acc + BN + c0, ur);
                     ptx::tmem_ld_wait();
                     for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j) {
-                        const float g = __uint_as_float(gh[j]) + __uint_as_float(gl[j]);
-                        const float u = __uint_as_float(uh[j]) + __uint_as_float(ul[j]);
+                        const float g = __uint_as_float(gr[j]);
+                        const float u = __uint_as_float(ur[j]);
                         float v = __fdiv_rn(g, 1.0f + expf(-g)) * u;
                         const size_t row = (size_t)ti.row0 + c0 + j;
 #pragma unroll
@@ -354,21 +387,16 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                         }
                     }
                 } else {
-                    uint32_t d[3][16];
-                    ptx::tmem_ld16(lane_base + 0 * BN + c0, d[0]);
-                    ptx::tmem_ld16(lane_base + 1 * BN + c0, d[1]);
-                    ptx::tmem_ld16(lane_base + 2 * BN + c0, d[2]);
+                    uint32_t d[16];
+                    ptx::tmem_ld16(acc + c0, d);
                     ptx::tmem_ld_wait();
-                    for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j) {
-                        float acc = __uint_as_float(d[0][j]);
-                        for (int tt = 1; tt < nterms; ++tt) acc += __uint_as_float(d[tt][j]);
-                        p.y[((size_t)ti.row0 + c0 + j) * p.H + mrow] = acc;
-                    }
+                    for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j)
+                        p.y[((size_t)ti.row0 + c0 + j) * p.H + mrow] = __uint_as_float(d[j]);
                 }
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(acc_empty));
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&acc_empty[buf]));
         }
     }
 
@@ -457,13 +485,13 @@ bool map_codes(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// E4M3 activation rows (bytes): 128 x 64 boxes with the 128-byte swizzle.
-bool map_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows) {
+// E4M3 activation rows (bytes): 128 x box_rows boxes with the 128-byte swizzle.
+bool map_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows = BN) {
     auto enc = encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {K, rows};
     const cuuint64_t strides[1] = {K};
-    const cuuint32_t box[2] = {BK, BN};
+    const cuuint32_t box[2] = {BK, box_rows};
     const cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -516,7 +544,7 @@ int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, c
     p.y = a.y;
     p.err = a.err;
 
-    CUtensorMap tar, tas, tb0, tb1, tb2;
+    CUtensorMap tar, tas, tb0, tb1, tb2, ts0, ts1, ts2;
     // gate/up: A = gate/up code rows, B = two terms of x
     p.mode = kGateUp;
     p.m_tiles = (a.I_max + BM - 1) / BM;
@@ -526,12 +554,15 @@ int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, c
     p.act_scales = a.xqs;
     p.act_ld = a.H;
     bool ok = map_codes(&tar, a.routed.gu_codes, a.H, (uint64_t)a.E * 2 * a.I) &&
-              map_act(&tb0, a.xq, a.H, a.rows) && map_act(&tb1, a.xq + (size_t)a.rows * a.H, a.H, a.rows);
+              map_act(&tb0, a.xq, a.H, a.rows) && map_act(&tb1, a.xq + (size_t)a.rows * a.H, a.H, a.rows) &&
+              map_act(&ts0, a.xq, a.H, a.rows, kSmallBN) &&
+              map_act(&ts1, a.xq + (size_t)a.rows * a.H, a.H, a.rows, kSmallBN);
     tb2 = tb1;
+    ts2 = ts1;
     if (a.shared.gu_codes) ok = ok && map_codes(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s);
     else tas = tar;
     if (!ok) return -2;
-    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb0, tb1, tb2, p);
+    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb0, tb1, tb2, ts0, ts1, ts2, p);
     ++n;
     if (mid) cudaEventRecord(mid, st);
 
@@ -543,13 +574,15 @@ int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, c
     p.w_scales_shared = a.shared.d_scales;
     p.act_scales = a.hqs;
     p.act_ld = a.I_max;
-    ok = map_codes(&tar, a.routed.d_codes, a.I, (uint64_t)a.E * a.H) &&
-         map_act(&tb0, a.hq, a.I_max, a.rows) && map_act(&tb1, a.hq + (size_t)a.rows * a.I_max, a.I_max, a.rows) &&
-         map_act(&tb2, a.hq + 2 * (size_t)a.rows * a.I_max, a.I_max, a.rows);
+    const uint8_t *h1 = a.hq + (size_t)a.rows * a.I_max, *h2 = a.hq + 2 * (size_t)a.rows * a.I_max;
+    ok = map_codes(&tar, a.routed.d_codes, a.I, (uint64_t)a.E * a.H) && map_act(&tb0, a.hq, a.I_max, a.rows) &&
+         map_act(&tb1, h1, a.I_max, a.rows) && map_act(&tb2, h2, a.I_max, a.rows) &&
+         map_act(&ts0, a.hq, a.I_max, a.rows, kSmallBN) && map_act(&ts1, h1, a.I_max, a.rows, kSmallBN) &&
+         map_act(&ts2, h2, a.I_max, a.rows, kSmallBN);
     if (a.shared.d_codes) ok = ok && map_codes(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H);
     else tas = tar;
     if (!ok) return -2;
-    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb0, tb1, tb2, p);
+    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb0, tb1, tb2, ts0, ts1, ts2, p);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }
