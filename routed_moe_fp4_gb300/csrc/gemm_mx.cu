@@ -21,9 +21,10 @@
 //   warp 0     TMA producer (weight codes, activation terms) into a 4-stage ring, 128 K per stage;
 //              tiles with at most 16 tokens load a 16-row activation box
 //   warp 1     TMEM owner and MMA issuer; accumulators double buffered (2 x 128 columns)
-//   warps 2-5  scale loaders: the stage's UE8M0 bytes -> TMEM (tcgen05.st), layout: lane l,
-//              column c holds the four K-block scales of row l + 32c (replicated per lane quarter);
-//              the words of the next four stages are loaded ahead into registers
+//   warps 2-5  scale loaders: the stage's UE8M0 bytes -> TMEM (tcgen05.st). The MMA reads weight
+//              row 32q + i from lane 32q + i, column q, and activation row n from lane 32q + n%32,
+//              column n/32, in each lane quarter q; warp q loads its 32 weight rows' bytes with
+//              16-byte loads that cover four stages, one group ahead
 //   warps 6-9  epilogue: gate/up -> SwiGLU -> three E4M3 terms of h (scales from warp-wide block
 //              maxima: a warp holds the 32 consecutive i-values of one scale block); down -> y
 // Every barrier wait is bounded (sm103_ptx.cuh).
@@ -50,7 +51,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 128;             // per accumulator buffer: up to two matrices x BN
 constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 16 per stage
 constexpr int kSmallBN = 16;                   // activation box rows for tiles with few tokens
-constexpr int kPrefetch = 4;                   // scale-word lookahead (stages)
 constexpr int kXTerms = 2, kHTerms = 3;
 
 enum Mode { kGateUp = 0, kDown = 1 };
@@ -121,6 +121,10 @@ __device__ __forceinline__ void tmem_st_x4(uint32_t taddr, uint32_t a, uint32_t 
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t a) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_x2(uint32_t taddr, uint32_t a, uint32_t b) {
@@ -276,7 +280,11 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------------ scale loaders
-        const int quad = warp & 3;                       // the TMEM lane quarter this warp writes
+        // TMEM scale layout the MMA reads (M = 128): weight row 32q + i takes its four K-block
+        // bytes from lane 32q + i, column base + q; activation row n takes them from lane
+        // 32q + n % 32, column base + n / 32, in every lane quarter q. Warp `quad` writes quarter
+        // quad: its own 32 weight rows and a copy of the activation rows.
+        const int quad = warp & 3;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         const int kba = p.act_ld / 32;                   // scale bytes per activation row
         uint32_t it = 0;
@@ -288,46 +296,81 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
             const int kb_row = K / 32;                   // scale bytes per weight row
             const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
             const int rpe = gu ? 2 * ti.Ig : p.H;
-            const size_t arow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM;
-            // this lane's rows: weight rows arow + lane + 32c (+ Ig for up), activation rows row0 + lane + 32c
-            const uint32_t *wp[2][4];
-            const uint32_t *bp[3][2];
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    wp[a][c] = (a < n_a) ? reinterpret_cast<const uint32_t *>(
-                                               ws + (arow + (a ? ti.Ig : 0) + lane + 32 * c) * kb_row)
-                                         : nullptr;
+            const size_t wrow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM + quad * 32 + lane;
+            const uint8_t *wp[2] = {ws + wrow * kb_row, n_a > 1 ? ws + (wrow + ti.Ig) * kb_row : nullptr};
+            const uint8_t *bp[3][2];
 #pragma unroll
             for (int tt = 0; tt < 3; ++tt)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const int row = ti.row0 + lane + 32 * c;
-                    bp[tt][c] = (tt < nterms && row < p.rows)
-                                    ? reinterpret_cast<const uint32_t *>(p.act_scales +
-                                                                         ((size_t)tt * p.rows + row) * kba)
+                    bp[tt][c] = (tt < nterms && row < p.rows && lane + 32 * c < ti.n_valid + 15)
+                                    ? p.act_scales + ((size_t)tt * p.rows + row) * kba
                                     : nullptr;
                 }
-            uint32_t wa[kPrefetch][8], wb[kPrefetch][6];
-            auto load = [&](int k, uint32_t(&a8)[8], uint32_t(&b6)[6]) {
-#pragma unroll
-                for (int a = 0; a < 2; ++a)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) a8[a * 4 + c] = wp[a][c] ? __ldg(wp[a][c] + k) : 0x7F7F7F7Fu;
-#pragma unroll
-                for (int tt = 0; tt < 3; ++tt)
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) b6[tt * 2 + c] = bp[tt][c] ? __ldg(bp[tt][c] + k) : 0x7F7F7F7Fu;
+            // one 16-byte load covers four stages when the rows' scale bytes allow it
+            const bool vec = (kb_row % 16 == 0) && (kba % 16 == 0) && (ti.nk % 4 == 0);
+            auto put = [&](int s, uint32_t a0, uint32_t a1, const uint32_t (&b)[6]) {
+                const uint32_t col = lane_base + kSfCol0 + s * 16;
+                tmem_st_x1(col + quad, a0);
+                if (n_a > 1) tmem_st_x1(col + 4 + quad, a1);
+                tmem_st_x2(col + 8, b[0], b[1]);
+                if (nterms > 1) tmem_st_x2(col + 10, b[2], b[3]);
+                if (nterms > 2) tmem_st_x2(col + 12, b[4], b[5]);
+                tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
             };
+            auto ld16 = [](const uint8_t *q, int g) {
+                return q ? __ldg(reinterpret_cast<const uint4 *>(q) + g) : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu,
+                                                                                  0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            };
+            auto ld4 = [](const uint8_t *q, int k) {
+                return q ? __ldg(reinterpret_cast<const uint32_t *>(q) + k) : 0x7F7F7F7Fu;
+            };
+            if (vec) {
+                uint4 ca[2], cb[6];
+                ca[0] = ld16(wp[0], 0);
+                ca[1] = ld16(wp[1], 0);
 #pragma unroll
-            for (int j = 0; j < kPrefetch; ++j)
-                if (j < ti.nk) load(j, wa[j], wb[j]);
-            for (int k0 = 0; k0 < ti.nk && ok; k0 += kPrefetch) {
+                for (int i = 0; i < 6; ++i) cb[i] = ld16(bp[i / 2][i % 2], 0);
+                for (int g = 0; g < ti.nk / 4 && ok; ++g) {
+                    uint4 na[2], nb[6];
+                    const bool more = g + 1 < ti.nk / 4;
+                    if (more) {
+                        na[0] = ld16(wp[0], g + 1);
+                        na[1] = ld16(wp[1], g + 1);
 #pragma unroll
-                for (int j = 0; j < kPrefetch; ++j) {
-                    const int k = k0 + j;
-                    if (k >= ti.nk) break;
+                        for (int i = 0; i < 6; ++i) nb[i] = ld16(bp[i / 2][i % 2], g + 1);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int s = it % NS;
+                        if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err,
+                                            ptx::kErrWaitEmpty, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        auto pick = [j](const uint4 &v) { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; };
+                        const uint32_t b[6] = {pick(cb[0]), pick(cb[1]), pick(cb[2]), pick(cb[3]), pick(cb[4]),
+                                               pick(cb[5])};
+                        put(s, pick(ca[0]), pick(ca[1]), b);
+                        ++it;
+                    }
+                    if (more) {
+                        ca[0] = na[0];
+                        ca[1] = na[1];
+#pragma unroll
+                        for (int i = 0; i < 6; ++i) cb[i] = nb[i];
+                    }
+                }
+            } else {
+                for (int k = 0; k < ti.nk && ok; ++k) {
+                    const uint32_t a0 = ld4(wp[0], k), a1 = ld4(wp[1], k);
+                    uint32_t b[6];
+#pragma unroll
+                    for (int i = 0; i < 6; ++i) b[i] = ld4(bp[i / 2][i % 2], k);
                     const int s = it % NS;
                     if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
                                         abort_flag)) {
@@ -335,17 +378,8 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t col = lane_base + kSfCol0 + s * 16;
-                    tmem_st_x4(col, wa[j][0], wa[j][1], wa[j][2], wa[j][3]);
-                    tmem_st_x4(col + 4, wa[j][4], wa[j][5], wa[j][6], wa[j][7]);
-                    tmem_st_x2(col + 8, wb[j][0], wb[j][1]);
-                    tmem_st_x2(col + 10, wb[j][2], wb[j][3]);
-                    tmem_st_x2(col + 12, wb[j][4], wb[j][5]);
-                    tmem_st_wait();
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
+                    put(s, a0, a1, b);
                     ++it;
-                    if (k + kPrefetch < ti.nk) load(k + kPrefetch, wa[j], wb[j]);
                 }
             }
         }
