@@ -13,14 +13,16 @@
 //   x (bf16, 8 significant bits): two terms reproduce it (the residual of a 4-bit rounding of an
 //     8-bit value fits in 4 bits), up to elements 2^14 below their block maximum;
 //   h (fp32, from the gate/up epilogue): three terms, relative error about 2^-12.
-// All terms of one weight matrix accumulate into the same TMEM accumulator (the MMA applies each
-// term's scales per 32-element block), so the sum over terms costs nothing.
+// The terms are stacked along N (term t at activation rows [t * bh, (t + 1) * bh) of the tile), so
+// one MMA per weight matrix and 32-wide K block covers all of them; the epilogue adds the term
+// columns. Block-scaled MMAs carry a large fixed cost each, which makes their count per stage the
+// quantity to minimise.
 //
-// Swap-AB tiles: 128 weight rows (M) x up to 64 tokens of one group (N). One persistent block per
-// SM; warp roles:
+// Swap-AB tiles: 128 weight rows (M) x up to 32 (gate/up) or 64 (down) tokens of one group (N).
+// One persistent block per SM; warp roles:
 //   warp 0     TMA producer (weight codes, activation terms) into a 4-stage ring, 128 K per stage;
-//              tiles with at most 16 tokens load a 16-row activation box
-//   warp 1     TMEM owner and MMA issuer; accumulators double buffered (2 x 128 columns)
+//              the activation box is 16, 32 or 64 rows high, the smallest that holds the tile
+//   warp 1     TMEM owner and MMA issuer; accumulators double buffered (2 x 192 columns)
 //   warps 2-5  scale loaders: the stage's UE8M0 bytes -> TMEM (tcgen05.st). The MMA reads weight
 //              row 32q + i from lane 32q + i, column q, and activation row n from lane 32q + n%32,
 //              column n/32, in each lane quarter q; warp q loads its 32 weight rows' bytes with
@@ -38,26 +40,27 @@
 namespace colimoe {
 namespace {
 
-constexpr int BM = 128, BN = 64, BK = 128;
+constexpr int BM = 128, BK = 128;
+constexpr int kBnGateUp = 32, kBnDown = 64;    // tokens per tile
 constexpr int NS = 4;
 constexpr int kThreads = 320;
 constexpr uint32_t kASmem = BM * BK;           // 16 KB: one unpacked E2M1 tile
 constexpr uint32_t kATx = BM * BK / 2;         // 8 KB of packed codes per tile
-constexpr uint32_t kBSmem = BN * BK;           // 8 KB: one E4M3 activation term tile
-// stage: A0 | A1 | B0 | B1 | B2
+constexpr uint32_t kBSmemMax = 3 * 64 * BK;    // activation terms stacked along N: up to 192 rows
+// stage: A0 | A1 | B (terms stacked: term t at rows [t * bh, (t + 1) * bh))
 constexpr uint32_t kOffA0 = 0, kOffA1 = kASmem, kOffB = 2 * kASmem;
-constexpr uint32_t kStageBytes = 2 * kASmem + 3 * kBSmem;   // 57344
+constexpr uint32_t kStageBytes = 2 * kASmem + kBSmemMax;   // 57344
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = 128;             // per accumulator buffer: up to two matrices x BN
-constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 16 per stage
-constexpr int kSmallBN = 16;                   // activation box rows for tiles with few tokens
+constexpr uint32_t kAccCols = 192;             // per accumulator buffer: matrices x terms x box rows
+constexpr uint32_t kSfCol0 = 384;              // scale-factor columns: 16 per stage
+constexpr int kBoxRows[3] = {16, 32, 64};      // activation box heights (16-row steps of the tile)
 constexpr int kXTerms = 2, kHTerms = 3;
 
 enum Mode { kGateUp = 0, kDown = 1 };
 
 struct MxParams {
     int E, H, I, I_s, I_max, rows;
-    int mode, m_tiles, nterms;
+    int mode, m_tiles, nterms, bn;
     const int32_t *cnt, *off, *touched, *n_touched, *ntile_prefix, *ntile_owner;
     const uint8_t *w_scales_routed, *w_scales_shared;   // UE8M0 bytes of the weight rows
     const uint8_t *act_scales;                          // [nterms][rows][K/32]
@@ -71,6 +74,7 @@ struct MxParams {
 
 struct TileInfo {
     int g, mt, row0, n_valid, Ig, nk;
+    int box, bh;            // activation box map index and height (rows per term)
     bool valid, shared;
     size_t ge;
 };
@@ -85,10 +89,12 @@ __device__ __forceinline__ TileInfo decode_tile(const MxParams &p, int t) {
     ti.shared = ti.g == p.E;
     ti.Ig = ti.shared ? p.I_s : p.I;
     ti.ge = ti.shared ? 0 : (size_t)ti.g;
-    ti.row0 = p.off[ti.g] + nt * BN;
-    ti.n_valid = min(BN, p.cnt[ti.g] - nt * BN);
+    ti.row0 = p.off[ti.g] + nt * p.bn;
+    ti.n_valid = min(p.bn, p.cnt[ti.g] - nt * p.bn);
     ti.valid = p.mode == kGateUp ? ti.mt * BM < ti.Ig : true;
     ti.nk = (p.mode == kGateUp ? p.H : ti.Ig) / BK;
+    ti.box = ti.n_valid <= 16 ? 0 : ti.n_valid <= 32 ? 1 : 2;
+    ti.bh = 16 << ti.box;
     return ti;
 }
 
@@ -159,11 +165,14 @@ __device__ __forceinline__ uint8_t e4m3_term(float v, float &resid, uint32_t &sb
     return (uint8_t)(q2 & 0xFF);
 }
 
+// Activation term maps: [term][box height index].
+struct BMaps {
+    CUtensorMap m[3][3];
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
-        const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
-        const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_s0,
-        const __grid_constant__ CUtensorMap tm_s1, const __grid_constant__ CUtensorMap tm_s2, const MxParams p) {
+        const __grid_constant__ BMaps tm_b, const MxParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
@@ -205,16 +214,12 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             ptx::prefetch_tmap(&tm_a_routed);
-            ptx::prefetch_tmap(&tm_b0);
             const uint64_t pol = ptx::policy_evict_first();
-            const CUtensorMap *tb[3] = {&tm_b0, &tm_b1, &tm_b2};
-            const CUtensorMap *tsm[3] = {&tm_s0, &tm_s1, &tm_s2};
             uint32_t it = 0;
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
                 const TileInfo ti = decode_tile(p, t);
                 if (!ti.valid) continue;
-                const bool small = ti.n_valid <= kSmallBN;
-                const uint32_t tx = n_a * kATx + nterms * (small ? kSmallBN * BK : kBSmem);
+                const uint32_t tx = n_a * kATx + nterms * ti.bh * BK;
                 const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
                 const int rpe = gu ? 2 * ti.Ig : p.H;
                 const int arow = (int)ti.ge * rpe + ti.mt * BM;
@@ -229,7 +234,7 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                     ptx::tma_load_2d_hint(st + kOffA0, ta, k * BK, arow, fb, pol);
                     if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, k * BK, arow + ti.Ig, fb, pol);
                     for (int tt = 0; tt < nterms; ++tt)
-                        ptx::tma_load_2d(st + kOffB + tt * kBSmem, small ? tsm[tt] : tb[tt], k * BK, ti.row0, fb);
+                        ptx::tma_load_2d(st + kOffB + tt * ti.bh * BK, &tm_b.m[tt][ti.box], k * BK, ti.row0, fb);
                 }
             }
         }
@@ -246,7 +251,7 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                     break;
                 ++tcount;
                 ptx::tc_fence_after();
-                const int n_mma = (ti.n_valid + 15) & ~15;
+                const int n_mma = nterms * ti.bh;       // terms stacked along N
                 bool ok = true;
                 for (int k = 0; k < ti.nk; ++k, ++it) {
                     const int s = it % NS;
@@ -262,12 +267,11 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
 #pragma unroll
                     for (int kb = 0; kb < BK / 32; ++kb) {
                         const uint32_t idesc = idesc_mx(n_mma, kb);
+                        const uint64_t bd = sw128_desc(sa + kOffB + kb * 32);
                         for (int a = 0; a < n_a; ++a) {
                             const uint64_t ad = sw128_desc(sa + (a ? kOffA1 : kOffA0) + kb * 32);
-                            const uint32_t d = tmem + buf * kAccCols + (uint32_t)(a * BN);
-                            for (int tt = 0; tt < nterms; ++tt)
-                                mma_mx(d, ad, sw128_desc(sa + kOffB + tt * kBSmem + kb * 32), idesc, sf + 4 * a,
-                                       sf + 8 + 2 * tt, (k > 0 || kb > 0 || tt > 0) ? 1u : 0u);
+                            const uint32_t d = tmem + buf * kAccCols + (uint32_t)(a * n_mma);
+                            mma_mx(d, ad, bd, idesc, sf + 4 * a, sf + 8, (k > 0 || kb > 0) ? 1u : 0u);
                         }
                     }
                     ptx::mma_commit(ptx::smem_addr(&empty[s]));
@@ -298,16 +302,16 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
             const int rpe = gu ? 2 * ti.Ig : p.H;
             const size_t wrow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM + quad * 32 + lane;
             const uint8_t *wp[2] = {ws + wrow * kb_row, n_a > 1 ? ws + (wrow + ti.Ig) * kb_row : nullptr};
-            const uint8_t *bp[3][2];
+            // activation row n = lane + 32c of the stacked B tile: term n / bh, token n % bh
+            const int nb_rows = nterms * ti.bh, nb_cols = (nb_rows + 31) / 32;
+            const uint8_t *bp[6];
 #pragma unroll
-            for (int tt = 0; tt < 3; ++tt)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int row = ti.row0 + lane + 32 * c;
-                    bp[tt][c] = (tt < nterms && row < p.rows && lane + 32 * c < ti.n_valid + 15)
-                                    ? p.act_scales + ((size_t)tt * p.rows + row) * kba
-                                    : nullptr;
-                }
+            for (int c = 0; c < 6; ++c) {
+                const int n = lane + 32 * c;
+                const int tt = n / ti.bh, j = n % ti.bh;
+                bp[c] = (n < nb_rows && j < ti.n_valid) ? p.act_scales + ((size_t)tt * p.rows + ti.row0 + j) * kba
+                                                        : nullptr;
+            }
             // one 16-byte load covers four stages when the rows' scale bytes allow it
             const bool vec = (kb_row % 16 == 0) && (kba % 16 == 0) && (ti.nk % 4 == 0);
             auto put = [&](int s, uint32_t a0, uint32_t a1, const uint32_t (&b)[6]) {
@@ -315,8 +319,8 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                 tmem_st_x1(col + quad, a0);
                 if (n_a > 1) tmem_st_x1(col + 4 + quad, a1);
                 tmem_st_x2(col + 8, b[0], b[1]);
-                if (nterms > 1) tmem_st_x2(col + 10, b[2], b[3]);
-                if (nterms > 2) tmem_st_x2(col + 12, b[4], b[5]);
+                if (nb_cols > 2) tmem_st_x2(col + 10, b[2], b[3]);
+                if (nb_cols > 4) tmem_st_x2(col + 12, b[4], b[5]);
                 tmem_st_wait();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
@@ -333,7 +337,7 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                 ca[0] = ld16(wp[0], 0);
                 ca[1] = ld16(wp[1], 0);
 #pragma unroll
-                for (int i = 0; i < 6; ++i) cb[i] = ld16(bp[i / 2][i % 2], 0);
+                for (int i = 0; i < 6; ++i) cb[i] = ld16(bp[i], 0);
                 for (int g = 0; g < ti.nk / 4 && ok; ++g) {
                     uint4 na[2], nb[6];
                     const bool more = g + 1 < ti.nk / 4;
@@ -341,7 +345,7 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                         na[0] = ld16(wp[0], g + 1);
                         na[1] = ld16(wp[1], g + 1);
 #pragma unroll
-                        for (int i = 0; i < 6; ++i) nb[i] = ld16(bp[i / 2][i % 2], g + 1);
+                        for (int i = 0; i < 6; ++i) nb[i] = ld16(bp[i], g + 1);
                     }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -370,7 +374,7 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                     const uint32_t a0 = ld4(wp[0], k), a1 = ld4(wp[1], k);
                     uint32_t b[6];
 #pragma unroll
-                    for (int i = 0; i < 6; ++i) b[i] = ld4(bp[i / 2][i % 2], k);
+                    for (int i = 0; i < 6; ++i) b[i] = ld4(bp[i], k);
                     const int s = it % NS;
                     if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
                                         abort_flag)) {
@@ -399,15 +403,18 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
             ptx::tc_fence_after();
             const int mrow = ti.mt * BM + m;
             const uint32_t acc = lane_base + buf * kAccCols;
+            const int ncols = nterms * ti.bh;           // accumulator columns per matrix
             for (int c0 = 0; c0 < ti.n_valid; c0 += 16) {
                 if (gu) {
-                    uint32_t gr[16], ur[16];
-                    ptx::tmem_ld16(acc + c0, gr);
-                    ptx::tmem_ld16(acc + BN + c0, ur);
+                    uint32_t g0[16], g1[16], u0[16], u1[16];
+                    ptx::tmem_ld16(acc + c0, g0);
+                    ptx::tmem_ld16(acc + ti.bh + c0, g1);
+                    ptx::tmem_ld16(acc + ncols + c0, u0);
+                    ptx::tmem_ld16(acc + ncols + ti.bh + c0, u1);
                     ptx::tmem_ld_wait();
                     for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j) {
-                        const float g = __uint_as_float(gr[j]);
-                        const float u = __uint_as_float(ur[j]);
+                        const float g = __uint_as_float(g0[j]) + __uint_as_float(g1[j]);
+                        const float u = __uint_as_float(u0[j]) + __uint_as_float(u1[j]);
                         float v = __fdiv_rn(g, 1.0f + expf(-g)) * u;
                         const size_t row = (size_t)ti.row0 + c0 + j;
 #pragma unroll
@@ -421,11 +428,14 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
                         }
                     }
                 } else {
-                    uint32_t d[16];
-                    ptx::tmem_ld16(acc + c0, d);
+                    uint32_t d0[16], d1[16], d2[16];
+                    ptx::tmem_ld16(acc + c0, d0);
+                    ptx::tmem_ld16(acc + ti.bh + c0, d1);
+                    ptx::tmem_ld16(acc + 2 * ti.bh + c0, d2);
                     ptx::tmem_ld_wait();
                     for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j)
-                        p.y[((size_t)ti.row0 + c0 + j) * p.H + mrow] = __uint_as_float(d[j]);
+                        p.y[((size_t)ti.row0 + c0 + j) * p.H + mrow] =
+                            (__uint_as_float(d0[j]) + __uint_as_float(d1[j])) + __uint_as_float(d2[j]);
                 }
             }
             ptx::tc_fence_before();
@@ -465,16 +475,16 @@ quant_x_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restri
     }
 }
 
-// n-tile bookkeeping (BN rows per tile): prefix[u] over touched groups, owner[r] = group of tile r.
+// n-tile bookkeeping (bn rows per tile): prefix[u] over touched groups, owner[r] = group of tile r.
 __global__ void __launch_bounds__(1024)
 mx_ntiles(const int32_t *__restrict__ cnt, const int32_t *__restrict__ touched, const int32_t *__restrict__ n_touched,
-          int32_t *__restrict__ prefix, int32_t *__restrict__ owner) {
+          int bn, int32_t *__restrict__ prefix, int32_t *__restrict__ owner) {
     __shared__ int part[1024];
     const int nt = *n_touched;
     int carry = 0;
     for (int u0 = 0; u0 < nt; u0 += 1024) {
         const int u = u0 + threadIdx.x;
-        const int c = u < nt ? (cnt[touched[u]] + BN - 1) / BN : 0;
+        const int c = u < nt ? (cnt[touched[u]] + bn - 1) / bn : 0;
         part[threadIdx.x] = c;
         __syncthreads();
         for (int o = 1; o < 1024; o <<= 1) {
@@ -520,7 +530,7 @@ bool map_codes(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows) {
 }
 
 // E4M3 activation rows (bytes): 128 x box_rows boxes with the 128-byte swizzle.
-bool map_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows = BN) {
+bool map_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows) {
     auto enc = encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {K, rows};
@@ -536,7 +546,9 @@ bool map_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32
 
 bool mx_available() { return encoder() != nullptr; }
 
-size_t mx_sched_ints(int E, int max_rows) { return (size_t)E + 2 + (size_t)max_rows / BN + E + 2; }
+size_t mx_sched_ints(int E, int max_rows) {
+    return 2 * ((size_t)E + 2) + (size_t)max_rows / kBnGateUp + (size_t)max_rows / kBnDown + 2 * ((size_t)E + 2);
+}
 
 bool mx_supported(const FfnArgs &a) {
     auto al = [](const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
@@ -544,14 +556,24 @@ bool mx_supported(const FfnArgs &a) {
            al(a.shared.d_codes);
 }
 
+// The three box heights of one activation term.
+bool map_term(CUtensorMap (&m)[3], const void *base, uint64_t K, uint64_t rows) {
+    for (int b = 0; b < 3; ++b)
+        if (!map_act(&m[b], base, K, rows, kBoxRows[b])) return false;
+    return true;
+}
+
 int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
     if (!mx_supported(a)) return -2;
-    int32_t *prefix = static_cast<int32_t *>(sched);
-    int32_t *owner = prefix + a.E + 2;
+    int32_t *prefix_gu = static_cast<int32_t *>(sched);
+    int32_t *owner_gu = prefix_gu + a.E + 2;
+    int32_t *prefix_dn = owner_gu + a.rows / kBnGateUp + a.E + 2;
+    int32_t *owner_dn = prefix_dn + a.E + 2;
     int n = 0;
     quant_x_rows<<<(a.rows + 7) / 8, 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
-    mx_ntiles<<<1, 1024, 0, st>>>(a.cnt, a.touched, a.n_touched, prefix, owner);
-    n += 2;
+    mx_ntiles<<<1, 1024, 0, st>>>(a.cnt, a.touched, a.n_touched, kBnGateUp, prefix_gu, owner_gu);
+    mx_ntiles<<<1, 1024, 0, st>>>(a.cnt, a.touched, a.n_touched, kBnDown, prefix_dn, owner_dn);
+    n += 3;
 
     const size_t smem = NS * kStageBytes + 1024 + 256;
     static bool attr = false;
@@ -571,16 +593,18 @@ int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, c
     p.off = a.off;
     p.touched = a.touched;
     p.n_touched = a.n_touched;
-    p.ntile_prefix = prefix;
-    p.ntile_owner = owner;
     p.hq = a.hq;
     p.hs = a.hqs;
     p.y = a.y;
     p.err = a.err;
 
-    CUtensorMap tar, tas, tb0, tb1, tb2, ts0, ts1, ts2;
+    CUtensorMap tar, tas;
+    BMaps tb;
     // gate/up: A = gate/up code rows, B = two terms of x
     p.mode = kGateUp;
+    p.bn = kBnGateUp;
+    p.ntile_prefix = prefix_gu;
+    p.ntile_owner = owner_gu;
     p.m_tiles = (a.I_max + BM - 1) / BM;
     p.nterms = kXTerms;
     p.w_scales_routed = a.routed.gu_scales;
@@ -588,35 +612,33 @@ int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, c
     p.act_scales = a.xqs;
     p.act_ld = a.H;
     bool ok = map_codes(&tar, a.routed.gu_codes, a.H, (uint64_t)a.E * 2 * a.I) &&
-              map_act(&tb0, a.xq, a.H, a.rows) && map_act(&tb1, a.xq + (size_t)a.rows * a.H, a.H, a.rows) &&
-              map_act(&ts0, a.xq, a.H, a.rows, kSmallBN) &&
-              map_act(&ts1, a.xq + (size_t)a.rows * a.H, a.H, a.rows, kSmallBN);
-    tb2 = tb1;
-    ts2 = ts1;
+              map_term(tb.m[0], a.xq, a.H, a.rows) && map_term(tb.m[1], a.xq + (size_t)a.rows * a.H, a.H, a.rows);
+    for (int b = 0; b < 3; ++b) tb.m[2][b] = tb.m[1][b];
     if (a.shared.gu_codes) ok = ok && map_codes(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s);
     else tas = tar;
     if (!ok) return -2;
-    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb0, tb1, tb2, ts0, ts1, ts2, p);
+    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb, p);
     ++n;
     if (mid) cudaEventRecord(mid, st);
 
     // down: A = down code rows, B = three terms of h
     p.mode = kDown;
+    p.bn = kBnDown;
+    p.ntile_prefix = prefix_dn;
+    p.ntile_owner = owner_dn;
     p.m_tiles = a.H / BM;
     p.nterms = kHTerms;
     p.w_scales_routed = a.routed.d_scales;
     p.w_scales_shared = a.shared.d_scales;
     p.act_scales = a.hqs;
     p.act_ld = a.I_max;
-    const uint8_t *h1 = a.hq + (size_t)a.rows * a.I_max, *h2 = a.hq + 2 * (size_t)a.rows * a.I_max;
-    ok = map_codes(&tar, a.routed.d_codes, a.I, (uint64_t)a.E * a.H) && map_act(&tb0, a.hq, a.I_max, a.rows) &&
-         map_act(&tb1, h1, a.I_max, a.rows) && map_act(&tb2, h2, a.I_max, a.rows) &&
-         map_act(&ts0, a.hq, a.I_max, a.rows, kSmallBN) && map_act(&ts1, h1, a.I_max, a.rows, kSmallBN) &&
-         map_act(&ts2, h2, a.I_max, a.rows, kSmallBN);
+    ok = map_codes(&tar, a.routed.d_codes, a.I, (uint64_t)a.E * a.H);
+    for (int t = 0; t < kHTerms && ok; ++t)
+        ok = map_term(tb.m[t], a.hq + (size_t)t * a.rows * a.I_max, a.I_max, a.rows);
     if (a.shared.d_codes) ok = ok && map_codes(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H);
     else tas = tar;
     if (!ok) return -2;
-    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb0, tb1, tb2, ts0, ts1, ts2, p);
+    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb, p);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }
