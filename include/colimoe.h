@@ -180,6 +180,32 @@ COLI_API int coli_moe_device_error(coli_moe_t *h, int32_t *code);
 COLI_API int coli_moe_set_profiling(coli_moe_t *h, int32_t enable);
 COLI_API int coli_moe_stage_times(coli_moe_t *h, float *ms);
 
+/* Routing with no device allocation. Runs the router of coli_moe_forward (A1: scores, bias-
+ * adjusted top-k, renormalised weights) on the given stream and writes idx_out [T][top_k] (int32)
+ * and weights_out [T][top_k] (fp32), device pointers owned by the caller, identical to the idx and
+ * weights coli_moe_forward computes for the same inputs. The pages have no counterpart to this call.
+ *
+ * Who it is for: callers that cannot let a library allocate device memory while they route -- code
+ * running while a CUDA graph is being captured, runtimes whose own pool owns all device memory,
+ * loops where a first-call allocation is not acceptable. It calls no cudaMalloc, cudaFree or other
+ * allocating routine. Its scratch (scores and split-K partial logits) is a fixed 5 MiB array inside
+ * the library image, present on every device that loads the library until the process exits.
+ *
+ * Limits and behaviour:
+ *  - T * E <= 262144 (for example 1024 tokens with 256 experts); larger sizes are rejected with
+ *    COLI_ERR_INVALID_ARG and a message from coli_moe_last_error(NULL). Also 1 <= E <= 1024, H a
+ *    positive multiple of 128, 1 <= top_k <= min(E, 32); T = 0 returns COLI_OK at once.
+ *  - The first call on a device, with that device current, looks up the array's device address
+ *    (cudaGetSymbolAddress) and the device's properties; make that first call before any stream
+ *    capture begins. Later calls only enqueue kernels.
+ *  - Every call shares the one array: calls whose kernels overlap on the GPU (different streams,
+ *    or different host threads on one device) race and may corrupt each other's results. Nothing
+ *    in the array needs to start at zero: each call overwrites all the scratch it reads.
+ *  - x_bf16 [T][H] bf16, router_w [E][H] fp32 (both 16-byte aligned), router_bias [E] or NULL. */
+COLI_API int coli_moe_route_static(const void *x_bf16, int32_t T, int32_t H, const float *router_w,
+                                   const float *router_bias, int32_t E, int32_t top_k, int32_t *idx_out,
+                                   float *weights_out, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

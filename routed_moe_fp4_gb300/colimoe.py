@@ -23,7 +23,7 @@ COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM, COLI_FFN_GEMM_BF16 = 0, 1, 2, 3
 EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "coli_moe_destroy",
             "coli_moe_last_error", "coli_moe_set_ffn_path", "coli_moe_debug_routing",
             "coli_moe_last_launch_count", "coli_moe_set_profiling", "coli_moe_stage_times",
-            "coli_moe_device_error")
+            "coli_moe_device_error", "coli_moe_route_static")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
 
@@ -86,6 +86,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_moe_stage_times.restype = C.c_int
     lib.coli_moe_device_error.argtypes = [vp, C.POINTER(C.c_int32)]
     lib.coli_moe_device_error.restype = C.c_int
+    lib.coli_moe_route_static.argtypes = [vp, C.c_int32, C.c_int32, vp, vp, C.c_int32, C.c_int32, vp, vp, vp]
+    lib.coli_moe_route_static.restype = C.c_int
     _lib = lib
     return lib
 
@@ -174,6 +176,15 @@ def coli_moe_stage_times(h) -> dict:
     buf = (C.c_float * COLI_STAGES)()
     _check(h, load().coli_moe_stage_times(h, buf))
     return dict(zip(STAGE_NAMES, [float(v) for v in buf]))
+
+
+def coli_moe_route_static(x_bf16, T: int, H: int, router_w, router_bias, E: int, top_k: int, idx_out,
+                          weights_out, cuda_stream=None) -> int:
+    """Routing into caller buffers with no device allocation (see include/colimoe.h)."""
+    st = getattr(cuda_stream, "cuda_stream", cuda_stream)
+    rc = load().coli_moe_route_static(_ptr(x_bf16), T, H, _ptr(router_w), _ptr(router_bias), E, top_k,
+                                      _ptr(idx_out), _ptr(weights_out), st)
+    return _check(None, rc)
 
 
 # ---- convenience: device-resident inputs of a workload -----------------------------------

@@ -227,6 +227,13 @@ launch_fail : {
 
 }  // namespace
 
+void colimoe::set_create_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_create_err, sizeof g_create_err, fmt, ap);
+    va_end(ap);
+}
+
 extern "C" {
 
 int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **out) {

@@ -76,6 +76,9 @@ struct FfnArgs {
     int *err;
 };
 
+// Records the text coli_moe_last_error(NULL) returns (printf-style).
+void set_create_error(const char *fmt, ...);
+
 // Launchers. Each returns the number of kernels it enqueued, or -1 on a launch error
 // (the CUDA error is then available from cudaGetLastError()).
 // `partial` ([partial_floats] fp32) holds split-K partial logits for larger T.
