@@ -149,7 +149,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     launches += n;
     if (prof) cudaEventRecord(h->ev[1], st);
     n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, gemm,
-                       kGemvCostTokens, ws, st);
+                       kGemvCostTokens, ffn == kFfnMx, ws, st);
     if (n < 0) goto launch_fail;
     launches += n;
     if (prof) cudaEventRecord(h->ev[2], st);

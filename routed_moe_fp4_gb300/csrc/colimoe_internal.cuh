@@ -86,11 +86,30 @@ int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, c
                   int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
                   int num_sms, cudaStream_t st);
 // `gather`: also copy the activation rows into expert-grouped order (ws.xp). `cost_tokens`: rows
-// per unit of work cost in ws.touched_cost (see permute_scan).
+// per unit of work cost in ws.touched_cost (see permute_scan). `ntiles`: also write the
+// block-scaled GEMM's n-tile layout (NtileLayout) into ws.tile_sched.
 int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, bool gather, int cost_tokens, Workspace &ws, cudaStream_t st);
+                   int H, bool gather, int cost_tokens, bool ntiles, Workspace &ws, cudaStream_t st);
 // Rows per cost unit the GEMV kernels assume.
 constexpr int kGemvCostTokens = 4;
+
+// Token tiles of the block-scaled GEMM (gate/up, down). The permute scan writes, per tile size, an
+// exclusive prefix of ceil(cnt / size) over the touched groups and the owning group of each tile.
+constexpr int kNtileSmall = 32, kNtileLarge = 64;
+struct NtileLayout {
+    int32_t *prefix_small, *owner_small, *prefix_large, *owner_large;
+};
+__host__ __device__ inline size_t ntile_layout_ints(int E, int rows) {
+    return 2 * ((size_t)E + 2) + (size_t)rows / kNtileSmall + (size_t)rows / kNtileLarge + 2 * ((size_t)E + 2);
+}
+__host__ __device__ inline NtileLayout ntile_layout(void *base, int E, int rows) {
+    NtileLayout l;
+    l.prefix_small = static_cast<int32_t *>(base);
+    l.owner_small = l.prefix_small + E + 2;
+    l.prefix_large = l.owner_small + rows / kNtileSmall + E + 2;
+    l.owner_large = l.prefix_large + E + 2;
+    return l;
+}
 // `mid` (may be null): an event recorded between the gate/up and the down kernels.
 int launch_ffn_gemv(const FfnArgs &a, int num_sms, cudaEvent_t mid, cudaStream_t st);
 int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T, int H, int top_k,

@@ -41,7 +41,7 @@ namespace colimoe {
 namespace {
 
 constexpr int BM = 128, BK = 128;
-constexpr int kBnGateUp = 32, kBnDown = 64;    // tokens per tile
+constexpr int kBnGateUp = kNtileSmall, kBnDown = kNtileLarge;   // tokens per tile
 constexpr int NS = 4;
 constexpr int kThreads = 320;
 constexpr uint32_t kASmem = BM * BK;           // 16 KB: one unpacked E2M1 tile
@@ -452,56 +452,60 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
     }
 }
 
+// UE8M0 byte s for a block maximum: |v| / 2^(s-127) < 256 (same rule as e4m3_term).
+__device__ __forceinline__ uint32_t block_scale_byte(float amax) {
+    const uint32_t ef = (__float_as_uint(amax) >> 23) & 0xFF;
+    const uint32_t s = (amax > 0.f && ef < 255) ? (ef > 8 ? ef - 7 : 1) : 127;
+    return min(s, 253u);
+}
+
 // x rows (expert-grouped, via src_token) -> two E4M3 terms with UE8M0 scales per 32 elements.
-// One warp per row; a warp handles one 32-element block per step (lane = element).
+// One thread per (row, 32-element block): it reads the block's 64 bytes, finds its maximum, and
+// writes 32 code bytes per term and one scale byte per term; a warp covers 2 KB of one row.
 __global__ void __launch_bounds__(256)
 quant_x_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
              uint8_t *__restrict__ xq, uint8_t *__restrict__ xs) {
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const __nv_bfloat16 *src = x + (size_t)src_token[row] * H;
-    for (int b = 0; b < H / 32; ++b) {
-        float v = __bfloat162float(src[b * 32 + lane]);
+    const int nb = H / 32;
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long)rows * nb) return;
+    const int row = (int)(i / nb), b = (int)(i % nb);
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)src_token[row] * H + b * 32);
+    float v[32];
 #pragma unroll
-        for (int tt = 0; tt < kXTerms; ++tt) {
-            uint32_t sb;
-            float r;
-            const uint8_t q = e4m3_term(v, r, sb);
-            xq[((size_t)tt * rows + row) * H + b * 32 + lane] = q;
-            if (lane == 0) xs[((size_t)tt * rows + row) * (H / 32) + b] = (uint8_t)sb;
-            v = r;
+    for (int q = 0; q < 4; ++q) {
+        const uint4 u = __ldg(src + q);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[q * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+            v[q * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
         }
     }
-}
-
-// n-tile bookkeeping (bn rows per tile): prefix[u] over touched groups, owner[r] = group of tile r.
-__global__ void __launch_bounds__(1024)
-mx_ntiles(const int32_t *__restrict__ cnt, const int32_t *__restrict__ touched, const int32_t *__restrict__ n_touched,
-          int bn, int32_t *__restrict__ prefix, int32_t *__restrict__ owner) {
-    __shared__ int part[1024];
-    const int nt = *n_touched;
-    int carry = 0;
-    for (int u0 = 0; u0 < nt; u0 += 1024) {
-        const int u = u0 + threadIdx.x;
-        const int c = u < nt ? (cnt[touched[u]] + bn - 1) / bn : 0;
-        part[threadIdx.x] = c;
-        __syncthreads();
-        for (int o = 1; o < 1024; o <<= 1) {
-            const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
-            __syncthreads();
-            part[threadIdx.x] += v;
-            __syncthreads();
+#pragma unroll
+    for (int tt = 0; tt < kXTerms; ++tt) {
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        const uint32_t sb = block_scale_byte(amax);
+        const float scale = __uint_as_float(sb << 23), inv = __uint_as_float((254u - sb) << 23);
+        uint32_t packed[8];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            uint16_t q2;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(q2) : "f"(v[e + 1] * inv), "f"(v[e] * inv));
+            uint32_t h2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(q2));
+            const float2 back = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+            v[e] -= back.x * scale;                // residuals for the next term (exact)
+            v[e + 1] -= back.y * scale;
+            if (e % 4 == 0) packed[e / 4] = q2;
+            else packed[e / 4] |= (uint32_t)q2 << 16;
         }
-        const int excl = carry + part[threadIdx.x] - c;
-        if (u < nt) {
-            prefix[u] = excl;
-            for (int r = 0; r < c; ++r) owner[excl + r] = u;
-        }
-        carry += part[1023];
-        __syncthreads();
+        uint4 *dst = reinterpret_cast<uint4 *>(xq + ((size_t)tt * rows + row) * H + b * 32);
+        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        xs[((size_t)tt * rows + row) * nb + b] = (uint8_t)sb;
     }
-    if (threadIdx.x == 0) prefix[nt] = carry;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -546,9 +550,7 @@ bool map_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32
 
 bool mx_available() { return encoder() != nullptr; }
 
-size_t mx_sched_ints(int E, int max_rows) {
-    return 2 * ((size_t)E + 2) + (size_t)max_rows / kBnGateUp + (size_t)max_rows / kBnDown + 2 * ((size_t)E + 2);
-}
+size_t mx_sched_ints(int E, int max_rows) { return ntile_layout_ints(E, max_rows); }
 
 bool mx_supported(const FfnArgs &a) {
     auto al = [](const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
@@ -565,15 +567,14 @@ bool map_term(CUtensorMap (&m)[3], const void *base, uint64_t K, uint64_t rows) 
 
 int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
     if (!mx_supported(a)) return -2;
-    int32_t *prefix_gu = static_cast<int32_t *>(sched);
-    int32_t *owner_gu = prefix_gu + a.E + 2;
-    int32_t *prefix_dn = owner_gu + a.rows / kBnGateUp + a.E + 2;
-    int32_t *owner_dn = prefix_dn + a.E + 2;
+    // n-tile prefixes and owners were written by the permute scan (NtileLayout)
+    const NtileLayout nl = ntile_layout(sched, a.E, a.rows);
+    int32_t *prefix_gu = nl.prefix_small, *owner_gu = nl.owner_small;
+    int32_t *prefix_dn = nl.prefix_large, *owner_dn = nl.owner_large;
     int n = 0;
-    quant_x_rows<<<(a.rows + 7) / 8, 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
-    mx_ntiles<<<1, 1024, 0, st>>>(a.cnt, a.touched, a.n_touched, kBnGateUp, prefix_gu, owner_gu);
-    mx_ntiles<<<1, 1024, 0, st>>>(a.cnt, a.touched, a.n_touched, kBnDown, prefix_dn, owner_dn);
-    n += 3;
+    const long qthreads = (long)a.rows * (a.H / 32);
+    quant_x_rows<<<(unsigned)((qthreads + 255) / 256), 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
+    n += 1;
 
     const size_t smem = NS * kStageBytes + 1024 + 256;
     static bool attr = false;

@@ -21,50 +21,49 @@ __device__ __forceinline__ float sigmoidf_ieee(float z) {
     return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
 }
 
-// Small T: two experts per block, two warps per expert (each half of H), up to 8 tokens per
-// block row. Lanes read the router row as float4; four loads are issued before they are used so
-// every warp keeps several HBM requests in flight.
+// Small T: one expert per block, its router row split over eight warps, up to 8 tokens per block
+// row. Lanes read the row as float4, four loads issued before use; the eight warp partials are
+// added in warp order (deterministic).
 constexpr int kSmallTok = 8;
+constexpr int kSmallWarps = 8;
 
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kSmallWarps * 32)
 router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const float *__restrict__ wr,
                     int E, float *__restrict__ scores) {
-    __shared__ float part[2][kSmallTok];
+    __shared__ float part[kSmallWarps][kSmallTok];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 2 + (warp >> 1), half = warp & 1;
+    const int e = blockIdx.x;
     const int t0 = blockIdx.y * kSmallTok;
     const int nt = min(kSmallTok, T - t0);
     float acc[kSmallTok];
 #pragma unroll
     for (int t = 0; t < kSmallTok; ++t) acc[t] = 0.f;
-    if (e < E) {
-        const int nv = H / 8;                            // float4 per half row
-        const float4 *wrow = reinterpret_cast<const float4 *>(wr + (size_t)e * H) + half * nv;
-        const uint2 *xbase = reinterpret_cast<const uint2 *>(x + (size_t)t0 * H) + half * nv;
-        for (int c0 = lane; c0 < nv; c0 += 128) {
-            float4 wv[4];
+    const int nv = H / (4 * kSmallWarps);                    // float4 per warp slice
+    const float4 *wrow = reinterpret_cast<const float4 *>(wr + (size_t)e * H) + warp * nv;
+    const uint2 *xbase = reinterpret_cast<const uint2 *>(x + (size_t)t0 * H) + warp * nv;
+    for (int c0 = lane; c0 < nv; c0 += 128) {
+        float4 wv[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + 32 * u;
-                wv[u] = c < nv ? __ldg(wrow + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + 32 * u;
+            wv[u] = c < nv ? __ldg(wrow + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-            for (int t = 0; t < kSmallTok; ++t) {
-                if (t < nt) {
-                    float a = acc[t];
+        for (int t = 0; t < kSmallTok; ++t) {
+            if (t < nt) {
+                float a = acc[t];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int c = c0 + 32 * u;
-                        if (c < nv) {
-                            const uint2 xv = __ldg(xbase + (size_t)t * (H / 4) + c);
-                            a = fmaf(bf16_lo(xv.x), wv[u].x, a);
-                            a = fmaf(bf16_hi(xv.x), wv[u].y, a);
-                            a = fmaf(bf16_lo(xv.y), wv[u].z, a);
-                            a = fmaf(bf16_hi(xv.y), wv[u].w, a);
-                        }
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + 32 * u;
+                    if (c < nv) {
+                        const uint2 xv = __ldg(xbase + (size_t)t * (H / 4) + c);
+                        a = fmaf(bf16_lo(xv.x), wv[u].x, a);
+                        a = fmaf(bf16_hi(xv.x), wv[u].y, a);
+                        a = fmaf(bf16_lo(xv.y), wv[u].z, a);
+                        a = fmaf(bf16_hi(xv.y), wv[u].w, a);
                     }
-                    acc[t] = a;
                 }
+                acc[t] = a;
             }
         }
     }
@@ -73,18 +72,13 @@ router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
         float a = acc[t];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        acc[t] = a;
-    }
-    if (half == 1 && lane == 0) {
-#pragma unroll
-        for (int t = 0; t < kSmallTok; ++t) part[warp >> 1][t] = acc[t];
+        if (lane == 0) part[warp][t] = a;
     }
     __syncthreads();
-    if (half == 0 && lane < nt && e < E) {
-        float a = 0.f;
+    if (warp == 0 && lane < nt) {
+        float a = part[0][lane];
 #pragma unroll
-        for (int t = 0; t < kSmallTok; ++t)
-            if (t == lane) a = acc[t] + part[warp >> 1][t];
+        for (int w = 1; w < kSmallWarps; ++w) a += part[w][lane];
         scores[(size_t)(t0 + lane) * E + e] = sigmoidf_ieee(a);
     }
 }
@@ -254,8 +248,8 @@ int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, c
                   int num_sms, cudaStream_t st) {
     int n = 0;
     if (T < 64) {
-        dim3 grid((E + 1) / 2, (T + kSmallTok - 1) / kSmallTok);
-        router_logits_small<<<grid, 128, 0, st>>>(x, T, H, router_w, E, scores);
+        dim3 grid(E, (T + kSmallTok - 1) / kSmallTok);
+        router_logits_small<<<grid, kSmallWarps * 32, 0, st>>>(x, T, H, router_w, E, scores);
         ++n;
     } else {
         const int tiles = ((T + kTileT - 1) / kTileT) * ((E + kTileE - 1) / kTileE);
