@@ -109,19 +109,56 @@ def _dist():
 
 
 def algorithmic_bytes(wl, routing: dict) -> dict:
-    """Bytes each stage must move at least once (touched experts measured from cnt)."""
+    """Bytes each stage of the block-scaled path must move at least once (touched experts from cnt).
+
+    gate/up: the touched experts' gate and up codes + scales, the two E4M3 terms of the activation
+             rows (+ scales) read, the three E4M3 terms of h (+ scales) written;
+    down:    the down codes + scales, the h terms read, y (fp32) written;
+    layer:   weights of the touched experts + router weights + x read + out written (the minimum
+             any implementation moves)."""
     E, H, I, I_s, T, k = wl.E, wl.H, wl.I, wl.I_s, wl.T, wl.top_k
     cnt = routing["cnt"]
     touched = int((cnt[:E] > 0).sum())
     shared = 1 if I_s > 0 else 0
+    Imax = max(I, I_s)
     gu_per = lambda i: 2 * i * (H // 2 + H // 32)        # gate+up codes and scales
     dn_per = lambda i: H * (i // 2 + i // 32)
     rows = T * k + T * shared
-    gate_up = touched * gu_per(I) + shared * gu_per(I_s) + rows * H * 2 + rows * max(I, I_s) * 2
-    down = touched * dn_per(I) + shared * dn_per(I_s) + rows * max(I, I_s) * 2 + rows * H * 4
+    x_terms = 2 * rows * (H + H // 32)
+    h_terms = 3 * rows * (Imax + Imax // 32)
+    weights = touched * (gu_per(I) + dn_per(I)) + shared * (gu_per(I_s) + dn_per(I_s))
+    gate_up = touched * gu_per(I) + shared * gu_per(I_s) + x_terms + h_terms
+    down = touched * dn_per(I) + shared * dn_per(I_s) + h_terms + rows * H * 4
     router = E * H * 4 + T * H * 2 + T * E * 4
     return {"touched_experts": touched, "ffn_gate_up": gate_up, "ffn_down": down, "router": router,
-            "layer": gate_up + down + router + T * H * 2}
+            "layer": weights + E * H * 4 + 2 * T * H * 2}
+
+
+def profiled_traffic(kernel_file: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary (profiles/<name>.json), or None when the
+    kernel's source has changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"gemm_mx_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        prof = json.load(f)
+    with open(os.path.join(ROOT, "routed_moe_fp4_gb300", "csrc", kernel_file), "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    if prof.get("source_sha256") != sha:
+        return None
+    return prof["gate_up"]["dram_read_bytes"] + prof["gate_up"]["dram_write_bytes"]
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest value over all ranks (the timed region ends when the slowest rank ends)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def run_ours(args, wl_name: str) -> dict:
@@ -172,11 +209,7 @@ def run_ours(args, wl_name: str) -> dict:
     if ws > 1:
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), device="cuda")
     ms_per_step = total_ms / args.steps
 
     # stage breakdown (profiled forwards, outside the timed region)
@@ -204,20 +237,21 @@ def run_ours(args, wl_name: str) -> dict:
     routing = layer.routing(wl.T)
     ab = algorithmic_bytes(wl, routing)
     hbm_gbs, bf16_tf, peak_kind = _peaks()
-    dom = max(("ffn_gate_up", "ffn_down"), key=lambda k: stages[k])
+    dom = "ffn_gate_up"            # the largest kernel: gemm_mx, gate/up launch
     achieved = ab[dom] / (stages[dom] * 1e-3) / 1e9
+    traffic = profiled_traffic("gemm_mx.cu", wl.name)
     tokens = wl.T * ws
     result = {
         "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)xfp16, fp32 accumulate",
+        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 e2m1 x e4m3 activation terms, fp32 accumulate",
         "data": "synthetic (seeded SplitMix64; MXFP4 experts, bf16 activations)",
         "config": {"workload": f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E}, top_k={wl.top_k}, I={wl.I}, "
                                f"I_s={wl.I_s}, MXFP4 E2M1 + UE8M0/32", "tokens_per_gpu": wl.T,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed (512 MiB write) before every timed step"},
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                     "frac": achieved / hbm_gbs, "traffic": None,
+        "roofline": {"kernel": "gemm_mx (gate/up launch)", "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
+                     "unit": "GB/s", "frac": achieved / hbm_gbs, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": ab[dom],
                      "kernel_ms": stages[dom]},
         "layer_roofline": {"bytes": ab["layer"], "ms": ms_per_step,

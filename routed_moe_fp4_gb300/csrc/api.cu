@@ -152,7 +152,6 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
                        kGemvCostTokens, ffn == kFfnMx, ws, st);
     if (n < 0) goto launch_fail;
     launches += n;
-    if (prof) cudaEventRecord(h->ev[2], st);
     {
         FfnArgs a{};
         a.routed = to_set(packed);
@@ -184,6 +183,12 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         a.hq = ws.hq;
         a.hqs = ws.hqs;
         a.err = ws.err;
+        if (ffn == kFfnMx) {     // the activation terms belong to the permute stage
+            n = launch_quant_x(a, st);
+            if (n < 0) goto launch_fail;
+            launches += n;
+        }
+        if (prof) cudaEventRecord(h->ev[2], st);
         cudaEvent_t mid = prof ? h->ev[3] : nullptr;
         if (ffn == kFfnMx) {
             n = launch_ffn_mx(a, h->num_sms, ws.tile_sched, mid, st);

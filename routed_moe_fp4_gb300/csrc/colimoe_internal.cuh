@@ -120,6 +120,8 @@ bool mx_available();
 size_t mx_sched_ints(int E, int max_rows);
 bool mx_supported(const FfnArgs &a);
 int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
+// Expert-grouped activation rows -> two E4M3 terms + UE8M0 scales (ws.xq / ws.xqs).
+int launch_quant_x(const FfnArgs &a, cudaStream_t st);
 
 // Grouped tcgen05 GEMM path with weights dequantised to bf16 in shared memory (gemm_tc.cu).
 size_t gemm_sched_bytes(int E, int max_rows);

@@ -550,6 +550,12 @@ bool map_act(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32
 
 bool mx_available() { return encoder() != nullptr; }
 
+int launch_quant_x(const FfnArgs &a, cudaStream_t st) {
+    const long qthreads = (long)a.rows * (a.H / 32);
+    quant_x_rows<<<(unsigned)((qthreads + 255) / 256), 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
+    return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+}
+
 size_t mx_sched_ints(int E, int max_rows) { return ntile_layout_ints(E, max_rows); }
 
 bool mx_supported(const FfnArgs &a) {
@@ -572,9 +578,6 @@ int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, c
     int32_t *prefix_gu = nl.prefix_small, *owner_gu = nl.owner_small;
     int32_t *prefix_dn = nl.prefix_large, *owner_dn = nl.owner_large;
     int n = 0;
-    const long qthreads = (long)a.rows * (a.H / 32);
-    quant_x_rows<<<(unsigned)((qthreads + 255) / 256), 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
-    n += 1;
 
     const size_t smem = NS * kStageBytes + 1024 + 256;
     static bool attr = false;
