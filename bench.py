@@ -108,11 +108,23 @@ def _dist():
     return ws, rank, local
 
 
-def algorithmic_bytes(wl, routing: dict) -> dict:
-    """Bytes each stage of the block-scaled path must move at least once (touched experts from cnt).
+# FFN paths: ABI value, kernel (source file stem), activation terms of x and of h as
+# (count, bytes per element), and the arithmetic the path computes in.
+FFN_PATHS = {
+    "auto": (0, None, None, None, None),
+    "gemv": (1, "gemv", None, None, "mxfp4 e2m1 weights dequantised to fp16, fp16 x fp16 FMA, fp32 sums"),
+    "mx": (2, "gemm_mx", (2, 1.0), (3, 1.0), "mxfp4 e2m1 x e4m3 activation terms, fp32 accumulate"),
+    "bf16": (3, "gemm_tc", None, None, "mxfp4 e2m1 dequantised to bf16, bf16 tensor cores, fp32 accumulate"),
+    "mxf4": (4, "gemm_mx4", (4, 0.5), (4, 0.5), "mxfp4 e2m1 x e2m1 activation terms, fp32 accumulate"),
+}
+PATH_BY_ABI = {v[0]: k for k, v in FFN_PATHS.items()}
 
-    gate/up: the touched experts' gate and up codes + scales, the two E4M3 terms of the activation
-             rows (+ scales) read, the three E4M3 terms of h (+ scales) written;
+
+def algorithmic_bytes(wl, routing: dict, path: str = "mxf4") -> dict:
+    """Bytes each stage of a block-scaled path must move at least once (touched experts from cnt).
+
+    gate/up: the touched experts' gate and up codes + scales, the activation terms of x (+ scales)
+             read, the terms of h (+ scales) written;
     down:    the down codes + scales, the h terms read, y (fp32) written;
     layer:   weights of the touched experts + router weights + x read + out written (the minimum
              any implementation moves)."""
@@ -124,8 +136,9 @@ def algorithmic_bytes(wl, routing: dict) -> dict:
     gu_per = lambda i: 2 * i * (H // 2 + H // 32)        # gate+up codes and scales
     dn_per = lambda i: H * (i // 2 + i // 32)
     rows = T * k + T * shared
-    x_terms = 2 * rows * (H + H // 32)
-    h_terms = 3 * rows * (Imax + Imax // 32)
+    (nx, bx), (nh, bh) = FFN_PATHS[path][2] or (2, 1.0), FFN_PATHS[path][3] or (3, 1.0)
+    x_terms = int(nx * rows * (H * bx + H // 32))
+    h_terms = int(nh * rows * (Imax * bh + Imax // 32))
     weights = touched * (gu_per(I) + dn_per(I)) + shared * (gu_per(I_s) + dn_per(I_s))
     gate_up = touched * gu_per(I) + shared * gu_per(I_s) + x_terms + h_terms
     down = touched * dn_per(I) + shared * dn_per(I_s) + h_terms + rows * H * 4
@@ -134,16 +147,16 @@ def algorithmic_bytes(wl, routing: dict) -> dict:
             "layer": weights + E * H * 4 + 2 * T * H * 2}
 
 
-def profiled_traffic(kernel_file: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary (profiles/<name>.json), or None when the
-    kernel's source has changed since the counters were taken."""
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per gate/up launch from a committed ncu summary (profiles/<kernel>_<workload>.json),
+    or None when the kernel's source has changed since the counters were taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"gemm_mx_{workload}.json")
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         prof = json.load(f)
-    with open(os.path.join(ROOT, "routed_moe_fp4_gb300", "csrc", kernel_file), "rb") as f:
+    with open(os.path.join(ROOT, "routed_moe_fp4_gb300", "csrc", kernel + ".cu"), "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()
     if prof.get("source_sha256") != sha:
         return None
@@ -175,6 +188,8 @@ def run_ours(args, wl_name: str) -> dict:
     wl = inputs.workload
     stream = torch.cuda.Stream()
     layer = cm.MoELayer(inputs, stream=stream)
+    if args.ffn_path != "auto":
+        layer.set_ffn_path(FFN_PATHS[args.ffn_path][0])
     x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
     out = torch.empty_like(x)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -190,6 +205,8 @@ def run_ours(args, wl_name: str) -> dict:
         layer.forward(x, out)
     stream.synchronize()
     launches_per_step = layer.launches()
+    path = PATH_BY_ABI[layer.ffn_path()]
+    kernel = FFN_PATHS[path][1]
 
     # timed: device-resident inputs
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -235,22 +252,22 @@ def run_ours(args, wl_name: str) -> dict:
     e2e_step = sum(e2e_ms) / len(e2e_ms)
 
     routing = layer.routing(wl.T)
-    ab = algorithmic_bytes(wl, routing)
+    ab = algorithmic_bytes(wl, routing, path)
     hbm_gbs, bf16_tf, peak_kind = _peaks()
-    dom = "ffn_gate_up"            # the largest kernel: gemm_mx, gate/up launch
+    dom = "ffn_gate_up"            # the largest kernel: the FFN GEMM's gate/up launch
     achieved = ab[dom] / (stages[dom] * 1e-3) / 1e9
-    traffic = profiled_traffic("gemm_mx.cu", wl.name)
+    traffic = profiled_traffic(kernel, wl.name)
     tokens = wl.T * ws
     result = {
         "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4 e2m1 x e4m3 activation terms, fp32 accumulate",
+        "scaling": "weak", "vs_baseline": None, "dtype": FFN_PATHS[path][4],
         "data": "synthetic (seeded SplitMix64; MXFP4 experts, bf16 activations)",
         "config": {"workload": f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E}, top_k={wl.top_k}, I={wl.I}, "
                                f"I_s={wl.I_s}, MXFP4 E2M1 + UE8M0/32", "tokens_per_gpu": wl.T,
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "ffn_path": path, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed (512 MiB write) before every timed step"},
-        "roofline": {"kernel": "gemm_mx (gate/up launch)", "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
+        "roofline": {"kernel": f"{kernel} (gate/up launch)", "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
                      "unit": "GB/s", "frac": achieved / hbm_gbs, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": ab[dom],
                      "kernel_ms": stages[dom]},
@@ -326,6 +343,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--skip-cpu", action="store_true", help="no cpu_baseline (profiling runs)")
+    ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
+                    help="force an FFN path (default: the library's own choice)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":

@@ -60,13 +60,18 @@ enum {
 
 /* FFN path selection for coli_moe_set_ffn_path. */
 enum {
-    COLI_FFN_AUTO = 0,      /* the block-scaled GEMM when its conditions hold, else GEMV / bf16 GEMM */
+    COLI_FFN_AUTO = 0,      /* COLI_FFN_GEMM_MXF4 when a tensor-map encoder is available, else the
+                               other block-scaled GEMM, else GEMV / bf16 GEMM */
     COLI_FFN_GEMV = 1,      /* weight-streaming GEMV kernels on the CUDA cores */
     COLI_FFN_GEMM = 2,      /* block-scaled tcgen05 GEMM: E2M1 weights straight from HBM to the tensor
                                cores (kind::mxf8f6f4), activations as exact E4M3 terms; needs 32-byte
                                aligned code pointers. Follows the hardware's UE8M0 decoding, which
                                differs from the format above only for scale bytes 0 and 255. */
     COLI_FFN_GEMM_BF16 = 3, /* tcgen05 GEMM with the weights dequantised to bf16 in shared memory */
+    COLI_FFN_GEMM_MXF4 = 4, /* block-scaled tcgen05 GEMM with FP4 on both sides (kind::mxf4, 64 K per
+                               instruction): E2M1 weights from HBM as stored, activations as four
+                               E2M1 terms with UE8M0 scales per 32 elements (about 2e-4 relative
+                               error on x and h). Same UE8M0 decoding note as COLI_FFN_GEMM. */
 };
 
 typedef struct coli_moe coli_moe_t;
@@ -136,8 +141,8 @@ COLI_API void coli_moe_destroy(coli_moe_t *h);
  * string stays valid until the next call on the same handle. Never returns NULL. */
 COLI_API const char *coli_moe_last_error(const coli_moe_t *h);
 
-/* Forces the FFN path (COLI_FFN_AUTO / _GEMV / _GEMM). Returns COLI_ERR_INVALID_ARG for an
- * unknown value. Both paths compute the same result within rounding. */
+/* Forces the FFN path (COLI_FFN_AUTO / _GEMV / _GEMM / _GEMM_BF16 / _GEMM_MXF4). Returns
+ * COLI_ERR_INVALID_ARG for an unknown value. All paths compute the same result within rounding. */
 COLI_API int coli_moe_set_ffn_path(coli_moe_t *h, int32_t path);
 
 /* Routing of the last forward, copied to HOST buffers (synchronises the stream). Any field may
@@ -163,6 +168,10 @@ COLI_API int coli_moe_debug_routing(coli_moe_t *h, coli_moe_routing *dst);
 
 /* Kernel launches the last forward enqueued (for launch accounting). */
 COLI_API int32_t coli_moe_last_launch_count(const coli_moe_t *h);
+
+/* FFN path (COLI_FFN_GEMV / _GEMM / _GEMM_BF16 / _GEMM_MXF4) the last forward ran; COLI_FFN_AUTO
+ * before the first forward, after a forward with T = 0, or for a NULL handle. */
+COLI_API int32_t coli_moe_last_ffn_path(const coli_moe_t *h);
 
 /* Device error word. Kernels that wait on barriers bound every wait (about two seconds); a wait
  * that runs out makes the kernel stop, record a code here (1: waiting for a weight stage,

@@ -18,11 +18,11 @@ COLI_ERR_INVALID_ARG = -1
 COLI_ERR_UNSUPPORTED_ARCH = -2
 COLI_ERR_OUT_OF_MEMORY = -3
 COLI_ERR_CUDA = -4
-COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM, COLI_FFN_GEMM_BF16 = 0, 1, 2, 3
+COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM, COLI_FFN_GEMM_BF16, COLI_FFN_GEMM_MXF4 = 0, 1, 2, 3, 4
 
 EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "coli_moe_destroy",
             "coli_moe_last_error", "coli_moe_set_ffn_path", "coli_moe_debug_routing",
-            "coli_moe_last_launch_count", "coli_moe_set_profiling", "coli_moe_stage_times",
+            "coli_moe_last_launch_count", "coli_moe_last_ffn_path", "coli_moe_set_profiling", "coli_moe_stage_times",
             "coli_moe_device_error", "coli_moe_route_static")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
@@ -80,6 +80,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_moe_debug_routing.restype = C.c_int
     lib.coli_moe_last_launch_count.argtypes = [vp]
     lib.coli_moe_last_launch_count.restype = C.c_int32
+    lib.coli_moe_last_ffn_path.argtypes = [vp]
+    lib.coli_moe_last_ffn_path.restype = C.c_int32
     lib.coli_moe_set_profiling.argtypes = [vp, C.c_int32]
     lib.coli_moe_set_profiling.restype = C.c_int
     lib.coli_moe_stage_times.argtypes = [vp, C.POINTER(C.c_float)]
@@ -158,6 +160,10 @@ def coli_moe_debug_routing(h, dst: coli_moe_routing) -> int:
 
 def coli_moe_last_launch_count(h) -> int:
     return load().coli_moe_last_launch_count(h)
+
+
+def coli_moe_last_ffn_path(h) -> int:
+    return load().coli_moe_last_ffn_path(h)
 
 
 def coli_moe_set_profiling(h, enable: bool) -> int:
@@ -259,6 +265,10 @@ class MoELayer:
 
     def launches(self) -> int:
         return coli_moe_last_launch_count(self.h)
+
+    def ffn_path(self) -> int:
+        """The FFN path the last forward ran (COLI_FFN_*)."""
+        return coli_moe_last_ffn_path(self.h)
 
     def close(self) -> None:
         if self.h:

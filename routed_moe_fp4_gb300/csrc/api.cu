@@ -23,6 +23,7 @@ struct coli_moe {
     int last_T = 0, last_k = 0;
     bool last_shared = false;
     int32_t last_launches = 0;
+    int32_t last_path = COLI_FFN_AUTO;
     bool profiling = false;
     bool stage_valid = false;
     cudaEvent_t ev[COLI_STAGES + 1] = {};
@@ -74,23 +75,26 @@ ExpertSet to_set(const coli_mxfp4_experts *e) {
     return s;
 }
 
-enum FfnKind { kFfnGemv, kFfnMx, kFfnBf16 };
+enum FfnKind { kFfnGemv, kFfnMx, kFfnBf16, kFfnMx4 };
 
 bool mx_pointers_ok(const coli_mxfp4_experts *r, const coli_mxfp4_experts *s) {
     auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
     return al(r->gate_up_codes) && al(r->down_codes) && (!s || (al(s->gate_up_codes) && al(s->down_codes)));
 }
 
-// The FFN kernels a forward uses: the block-scaled GEMM whenever it can run (weights go to the
-// tensor cores without passing through the ALU, at every token count); otherwise the bf16 GEMM
-// when tokens per touched expert are many, the GEMV when they are few.
+// The FFN kernels a forward uses: the FP4 x FP4 block-scaled GEMM whenever it can run (weights go
+// to the tensor cores as stored, 64 K per instruction, at every token count); then the E2M1 x E4M3
+// block-scaled GEMM; otherwise the bf16 GEMM when tokens per touched expert are many, the GEMV
+// when they are few.
 FfnKind pick_ffn(const coli_moe_t *h, int T, int top_k, const coli_mxfp4_experts *r, const coli_mxfp4_experts *s) {
     switch (h->ffn_path) {
         case COLI_FFN_GEMV: return kFfnGemv;
         case COLI_FFN_GEMM: return kFfnMx;
         case COLI_FFN_GEMM_BF16: return kFfnBf16;
+        case COLI_FFN_GEMM_MXF4: return kFfnMx4;
         default: break;
     }
+    if (mx4_available()) return kFfnMx4;
     if (mx_available() && mx_pointers_ok(r, s)) return kFfnMx;
     if (!gemm_available()) return kFfnGemv;
     const double E = h->cfg.num_experts;
@@ -104,6 +108,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     const coli_moe_config &c = h->cfg;
     if (T == 0) {
         h->last_launches = 0;
+        h->last_path = COLI_FFN_AUTO;
         return COLI_OK;
     }
     if (T < 0 || T > c.max_tokens) {
@@ -149,7 +154,8 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     launches += n;
     if (prof) cudaEventRecord(h->ev[1], st);
     n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, gemm,
-                       kGemvCostTokens, ffn == kFfnMx, ws, st);
+                       kGemvCostTokens,
+                       ffn == kFfnMx ? kNtileMx : ffn == kFfnMx4 ? kNtileMx4 : 0, ws, st);
     if (n < 0) goto launch_fail;
     launches += n;
     {
@@ -183,14 +189,20 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         a.hq = ws.hq;
         a.hqs = ws.hqs;
         a.err = ws.err;
-        if (ffn == kFfnMx) {     // the activation terms belong to the permute stage
-            n = launch_quant_x(a, st);
+        if (ffn == kFfnMx || ffn == kFfnMx4) {   // the activation terms belong to the permute stage
+            n = ffn == kFfnMx ? launch_quant_x(a, st) : launch_quant_x4(a, st);
             if (n < 0) goto launch_fail;
             launches += n;
         }
         if (prof) cudaEventRecord(h->ev[2], st);
         cudaEvent_t mid = prof ? h->ev[3] : nullptr;
-        if (ffn == kFfnMx) {
+        if (ffn == kFfnMx4) {
+            n = launch_ffn_mx4(a, h->num_sms, ws.tile_sched, mid, st);
+            if (n == -2) {
+                set_err(h, "FP4 block-scaled GEMM path unavailable (needs a tensor-map encoder)");
+                return COLI_ERR_INVALID_ARG;
+            }
+        } else if (ffn == kFfnMx) {
             n = launch_ffn_mx(a, h->num_sms, ws.tile_sched, mid, st);
             if (n == -2) {
                 set_err(h, "block-scaled GEMM path unavailable (needs 32-byte aligned code pointers and a "
@@ -221,6 +233,8 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     h->last_k = top_k;
     h->last_shared = with_shared;
     h->last_launches = launches;
+    h->last_path = ffn == kFfnGemv ? COLI_FFN_GEMV : ffn == kFfnMx ? COLI_FFN_GEMM
+                 : ffn == kFfnBf16 ? COLI_FFN_GEMM_BF16 : COLI_FFN_GEMM_MXF4;
     return COLI_OK;
 
 launch_fail : {
@@ -298,12 +312,12 @@ int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **
               alloc(&ws.hinv, rows) && alloc(&ws.err, 4) && alloc(&ws.x_stage, Tm * H) &&
               alloc(&ws.out_stage, Tm * H);
     if (ok)
-        ok = alloc(&ws.xq, 2 * rows * H) && alloc(&ws.xqs, 2 * rows * (H / 32)) &&
-             alloc(&ws.hq, 3 * rows * (size_t)h->I_max) && alloc(&ws.hqs, 3 * rows * (size_t)(h->I_max / 32));
+        ok = alloc(&ws.xq, 2 * rows * H) && alloc(&ws.xqs, 4 * rows * (H / 32)) &&
+             alloc(&ws.hq, 3 * rows * (size_t)h->I_max) && alloc(&ws.hqs, 4 * rows * (size_t)(h->I_max / 32));
     if (ok) ok = cudaMemset(ws.err, 0, sizeof(int)) == cudaSuccess;
     if (ok) {
         ws.tile_sched_bytes = gemm_sched_bytes((int)E, (int)rows);
-        const size_t mx_bytes = mx_sched_ints((int)E, (int)rows) * sizeof(int32_t);
+        const size_t mx_bytes = ntile_layout_ints((int)E, (int)rows) * sizeof(int32_t);
         if (mx_bytes > ws.tile_sched_bytes) ws.tile_sched_bytes = mx_bytes;
         ok = cudaMalloc(&ws.tile_sched, ws.tile_sched_bytes + 256) == cudaSuccess;
     }
@@ -366,7 +380,7 @@ void coli_moe_destroy(coli_moe_t *h) {
 const char *coli_moe_last_error(const coli_moe_t *h) { return h ? h->err : g_create_err; }
 
 int coli_moe_set_ffn_path(coli_moe_t *h, int32_t path) {
-    if (!h || path < COLI_FFN_AUTO || path > COLI_FFN_GEMM_BF16) {
+    if (!h || path < COLI_FFN_AUTO || path > COLI_FFN_GEMM_MXF4) {
         if (h) set_err(h, "unknown FFN path %d", path);
         return COLI_ERR_INVALID_ARG;
     }
@@ -402,6 +416,8 @@ int coli_moe_debug_routing(coli_moe_t *h, coli_moe_routing *dst) {
 }
 
 int32_t coli_moe_last_launch_count(const coli_moe_t *h) { return h ? h->last_launches : 0; }
+
+int32_t coli_moe_last_ffn_path(const coli_moe_t *h) { return h ? h->last_path : COLI_FFN_AUTO; }
 
 int coli_moe_device_error(coli_moe_t *h, int32_t *code) {
     if (!h || !code) return COLI_ERR_INVALID_ARG;

@@ -35,10 +35,13 @@ struct Workspace {
     __nv_bfloat16 *xp = nullptr;    // [Tm*km + Tm][H] expert-grouped activation rows
     __nv_bfloat16 *h = nullptr;     // [Tm*km + Tm][I_max] SwiGLU output rows
     float *y = nullptr;             // [Tm*km + Tm][H] expert output rows
-    uint8_t *xq = nullptr;          // [2][rows][H] E4M3 terms of the activation rows (block-scaled path)
-    uint8_t *xqs = nullptr;         // [2][rows][H/32] their UE8M0 scales
-    uint8_t *hq = nullptr;          // [3][rows][I_max] E4M3 terms of h
-    uint8_t *hqs = nullptr;         // [3][rows][I_max/32]
+    // Activation terms of the block-scaled paths: two E4M3 terms of x ([2][rows][H]) or four packed
+    // E2M1 terms ([4][rows][H/2]); three E4M3 terms of h ([3][rows][I_max]) or four packed E2M1
+    // terms ([4][rows][I_max/2]); UE8M0 scales per 32 elements, [terms][rows][K/32].
+    uint8_t *xq = nullptr;          // 2 * rows * H bytes
+    uint8_t *xqs = nullptr;         // 4 * rows * H/32
+    uint8_t *hq = nullptr;          // 3 * rows * I_max
+    uint8_t *hqs = nullptr;         // 4 * rows * I_max/32
     __half *xh = nullptr;           // [Tm][H] tokens as scaled fp16, permuted unit layout (GEMV path)
     float *xinv = nullptr;          // [Tm] inverse scales of xh
     __half *hh = nullptr;           // [Tm*km + Tm][I_max] h rows as scaled fp16 (GEMV path)
@@ -72,7 +75,7 @@ struct FfnArgs {
     __half *hh;                     // GEMV path: scaled fp16 h rows and inverse scales
     float *hinv;
     float *y;                       // [rows][H]
-    uint8_t *xq, *xqs, *hq, *hqs;   // block-scaled path: E4M3 activation terms and scales
+    uint8_t *xq, *xqs, *hq, *hqs;   // block-scaled paths: activation terms and scales
     int *err;
 };
 
@@ -86,27 +89,32 @@ int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, c
                   int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
                   int num_sms, cudaStream_t st);
 // `gather`: also copy the activation rows into expert-grouped order (ws.xp). `cost_tokens`: rows
-// per unit of work cost in ws.touched_cost (see permute_scan). `ntiles`: also write the
-// block-scaled GEMM's n-tile layout (NtileLayout) into ws.tile_sched.
+// per unit of work cost in ws.touched_cost (see permute_scan). `ntile`: when non-zero, also write
+// the block-scaled GEMM's n-tile layout (NtileLayout, tiles of `ntile` and 2 * `ntile` rows) into
+// ws.tile_sched.
 int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, bool gather, int cost_tokens, bool ntiles, Workspace &ws, cudaStream_t st);
+                   int H, bool gather, int cost_tokens, int ntile, Workspace &ws, cudaStream_t st);
 // Rows per cost unit the GEMV kernels assume.
 constexpr int kGemvCostTokens = 4;
 
-// Token tiles of the block-scaled GEMM (gate/up, down). The permute scan writes, per tile size, an
-// exclusive prefix of ceil(cnt / size) over the touched groups and the owning group of each tile.
-constexpr int kNtileSmall = 32, kNtileLarge = 64;
+// Token tiles of the block-scaled GEMMs: gate/up tiles of n rows, down tiles of 2n rows.
+constexpr int kNtileMx = 32;    // E2M1 weights x E4M3 activation terms (gemm_mx.cu)
+constexpr int kNtileMx4 = 16;   // E2M1 weights x E2M1 activation terms (gemm_mx4.cu)
+constexpr int kNtileMin = 16;   // the layout below is sized for tiles of at least this many rows
+// The permute scan writes, per tile size, an exclusive prefix of ceil(cnt / size) over the touched
+// groups and the owning group of each tile. A tile size s >= kNtileMin gives at most
+// rows / s + E + 1 tiles.
 struct NtileLayout {
     int32_t *prefix_small, *owner_small, *prefix_large, *owner_large;
 };
 __host__ __device__ inline size_t ntile_layout_ints(int E, int rows) {
-    return 2 * ((size_t)E + 2) + (size_t)rows / kNtileSmall + (size_t)rows / kNtileLarge + 2 * ((size_t)E + 2);
+    return 2 * ((size_t)E + 2) + 2 * ((size_t)rows / kNtileMin + (size_t)E + 2);
 }
 __host__ __device__ inline NtileLayout ntile_layout(void *base, int E, int rows) {
     NtileLayout l;
     l.prefix_small = static_cast<int32_t *>(base);
     l.owner_small = l.prefix_small + E + 2;
-    l.prefix_large = l.owner_small + rows / kNtileSmall + E + 2;
+    l.prefix_large = l.owner_small + rows / kNtileMin + E + 2;
     l.owner_large = l.prefix_large + E + 2;
     return l;
 }
@@ -117,11 +125,18 @@ int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T
 
 // Block-scaled MXFP4 tcgen05 GEMM path (gemm_mx.cu): native E2M1 weights x E4M3 activation terms.
 bool mx_available();
-size_t mx_sched_ints(int E, int max_rows);
 bool mx_supported(const FfnArgs &a);
 int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
 // Expert-grouped activation rows -> two E4M3 terms + UE8M0 scales (ws.xq / ws.xqs).
 int launch_quant_x(const FfnArgs &a, cudaStream_t st);
+
+// Block-scaled tcgen05 GEMM path with FP4 on both sides (gemm_mx4.cu): E2M1 weights x four E2M1
+// activation terms.
+bool mx4_available();
+bool mx4_supported(const FfnArgs &a);
+int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
+// Expert-grouped activation rows -> four packed E2M1 terms + UE8M0 scales (ws.xq / ws.xqs).
+int launch_quant_x4(const FfnArgs &a, cudaStream_t st);
 
 // Grouped tcgen05 GEMM path with weights dequantised to bf16 in shared memory (gemm_tc.cu).
 size_t gemm_sched_bytes(int E, int max_rows);

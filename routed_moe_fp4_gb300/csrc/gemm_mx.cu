@@ -41,7 +41,7 @@ namespace colimoe {
 namespace {
 
 constexpr int BM = 128, BK = 128;
-constexpr int kBnGateUp = kNtileSmall, kBnDown = kNtileLarge;   // tokens per tile
+constexpr int kBnGateUp = kNtileMx, kBnDown = 2 * kNtileMx;   // tokens per tile
 constexpr int NS = 4;
 constexpr int kThreads = 320;
 constexpr uint32_t kASmem = BM * BK;           // 16 KB: one unpacked E2M1 tile
@@ -556,7 +556,6 @@ int launch_quant_x(const FfnArgs &a, cudaStream_t st) {
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
-size_t mx_sched_ints(int E, int max_rows) { return ntile_layout_ints(E, max_rows); }
 
 bool mx_supported(const FfnArgs &a) {
     auto al = [](const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 31) == 0; };

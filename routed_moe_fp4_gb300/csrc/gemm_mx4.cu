@@ -1,0 +1,545 @@
+// A3/A4 on the tensor cores with FP4 on both sides: block-scaled tcgen05.mma kind::mxf4
+// (E2M1 x E2M1, UE8M0 scale per 32 elements, fp32 accumulate, 64 K per instruction).
+// ("DeepSeek V4 Flash CPU inference with NVMe expert streaming": FP4 E2M1 experts with UE8M0
+// group-32 scales; the gate/up pair and the down projection. "the CUDA tier wired into the
+// DeepSeek V4 engine": expert-grouped GEMM rows.)
+//
+// The weight codes go from HBM to the tensor cores as they are stored: a plain byte TMA with the
+// 128-byte swizzle puts 256 packed E2M1 values of each weight row in one 128-byte shared-memory row
+// (K = 256 per stage, 128 contiguous bytes read per row), and kind::mxf4 reads them packed. The
+// UE8M0 scale bytes go to TMEM. Each MMA instruction covers 64 K, twice what the E2M1 x E4M3 kind
+// covers, and block-scaled MMAs cost a roughly fixed time per instruction, so this path moves
+// twice the weight bytes per instruction.
+//
+// Activations become four E2M1 terms, each with its own UE8M0 scale per 32 elements (the residual
+// of one term is the input of the next): about 2e-4 relative error for Gaussian data, and exact
+// for values with few significant bits. x terms come from quant_x4_rows; h terms are made in the
+// gate/up epilogue, where a warp holds the 32 consecutive i-values of one scale block. The terms
+// are stacked along N (term t at activation rows [t * bh, (t + 1) * bh)); the epilogue adds them.
+//
+// Tiles: 128 weight rows (M) x 16 (gate/up) or up to 32 (down) tokens of one group. One persistent
+// block per SM; warp roles as in the E4M3 path: TMA producer (warp 0), TMEM owner and MMA issuer
+// (warp 1), scale loaders (warps 2-5; weight row 32q + i reads its scales from lane 32q + i,
+// column (word) * 4 + q; activation row n from lane 32q + n % 32, column n / 32 of its word, in
+// every lane quarter q; the words of one stage sit 4 columns apart), epilogue (warps 6-9). Four stages, double-buffered accumulators, bounded
+// waits. A K that is not a multiple of 256 ends with a half stage.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "colimoe_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace colimoe {
+namespace {
+
+constexpr int BM = 128, BK = 256, MK = 64;     // weight rows, K per stage, K per MMA
+constexpr int kBnGateUp = kNtileMx4, kBnDown = 2 * kNtileMx4;   // tokens per tile
+constexpr int kTerms = 4;                      // E2M1 terms per activation
+constexpr int NS = 4;
+constexpr int kThreads = 320;
+constexpr uint32_t kASmem = BM * BK / 2;       // 16 KB: 128 rows x 256 packed codes
+constexpr uint32_t kBSmemMax = kTerms * 32 * (BK / 2);   // 16 KB: up to 4 terms x 32 rows
+constexpr uint32_t kOffA0 = 0, kOffA1 = kASmem, kOffB = 2 * kASmem;
+constexpr uint32_t kStageBytes = 2 * kASmem + kBSmemMax;   // 49152
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = 128;             // per accumulator buffer
+constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 32 per stage
+constexpr uint32_t kSfStage = 32;
+
+enum Mode { kGateUp = 0, kDown = 1 };
+
+struct Mx4Params {
+    int E, H, I, I_s, I_max, rows;
+    int mode, m_tiles, bn;
+    const int32_t *cnt, *off, *touched, *n_touched, *ntile_prefix, *ntile_owner;
+    const uint8_t *w_scales_routed, *w_scales_shared;
+    const uint8_t *act_scales;          // [kTerms][rows][K/32]
+    int act_ld;                         // K of the activation terms (H or I_max)
+    uint8_t *hq;                        // [kTerms][rows][I_max/2] packed E2M1 terms of h
+    uint8_t *hs;                        // [kTerms][rows][I_max/32]
+    float *y;
+    int *err;
+};
+
+struct TileInfo {
+    int g, mt, row0, n_valid, Ig, K, nk, box, bh;
+    bool valid, shared;
+    size_t ge;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t) {
+    TileInfo ti;
+    ti.mt = t % p.m_tiles;
+    const int r = t / p.m_tiles;
+    const int u = p.ntile_owner[r];
+    ti.g = p.touched[u];
+    const int nt = r - p.ntile_prefix[u];
+    ti.shared = ti.g == p.E;
+    ti.Ig = ti.shared ? p.I_s : p.I;
+    ti.ge = ti.shared ? 0 : (size_t)ti.g;
+    ti.row0 = p.off[ti.g] + nt * p.bn;
+    ti.n_valid = min(p.bn, p.cnt[ti.g] - nt * p.bn);
+    ti.valid = p.mode == kGateUp ? ti.mt * BM < ti.Ig : true;
+    ti.K = p.mode == kGateUp ? p.H : ti.Ig;
+    ti.nk = (ti.K + BK - 1) / BK;
+    ti.box = ti.n_valid <= 16 ? 0 : 1;
+    ti.bh = 16 << ti.box;
+    return ti;
+}
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Block-scaled descriptor, kind::mxf4: A and B E2M1 (1), UE8M0, M x N; sf_id 0 or 2 selects the
+// scale byte pair of the 64-wide MMA within a 128-wide scale word.
+__device__ __forceinline__ uint32_t idesc_mx4(int N, int sf_id) {
+    return ((uint32_t)sf_id << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(BM >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
+__device__ __forceinline__ void mma_mx4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t a) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// UE8M0 byte for an E2M1 term of a block with maximum amax: |v| / 2^(s-127) < 4.
+__device__ __forceinline__ uint32_t e2m1_scale_byte(float amax) {
+    const uint32_t ef = (__float_as_uint(amax) >> 23) & 0xFF;
+    const uint32_t s = (amax > 0.f && ef < 255) ? (ef > 2 ? ef - 1 : 1) : 127;
+    return min(s, 253u);
+}
+
+// Two values -> one byte of E2M1 codes (lo in bits 0-3) and their decoded values.
+__device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi, float &blo, float &bhi) {
+    uint32_t b;
+    asm("{\n .reg .b8 q;\n cvt.rn.satfinite.e2m1x2.f32 q, %1, %2;\n cvt.u32.u8 %0, q;\n}\n"
+        : "=r"(b) : "f"(hi), "f"(lo));
+    uint32_t h2;
+    asm("{\n .reg .b8 q;\n cvt.u8.u32 q, %1;\n cvt.rn.f16x2.e2m1x2 %0, q;\n}\n" : "=r"(h2) : "r"(b));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+    blo = f.x;
+    bhi = f.y;
+    return b;
+}
+
+struct BMaps4 {
+    CUtensorMap m[kTerms][2];   // [term][box height 16 / 32]
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
+         const __grid_constant__ BMaps4 tm_b, const Mx4Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
+    uint64_t *tma_full = bar, *sf_full = bar + NS, *empty = bar + 2 * NS, *acc_full = bar + 3 * NS,
+             *acc_empty = bar + 3 * NS + 2, *drain = bar + 3 * NS + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 3 * NS + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool gu = p.mode == kGateUp;
+    const int n_a = gu ? 2 : 1;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&tma_full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sf_full[s]), 128);
+            ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_addr(&acc_full[b]), 1);
+            ptx::mbar_init(ptx::smem_addr(&acc_empty[b]), 4);
+        }
+        ptx::mbar_init(ptx::smem_addr(drain), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total_tiles = p.m_tiles * p.ntile_prefix[*p.n_touched];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tm_a_routed);
+            const uint64_t pol = ptx::policy_evict_first();
+            uint32_t it = 0;
+            for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+                const TileInfo ti = decode_tile(p, t);
+                if (!ti.valid) continue;
+                const uint32_t tx = n_a * kASmem + kTerms * ti.bh * (BK / 2);
+                const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
+                const int rpe = gu ? 2 * ti.Ig : p.H;
+                const int arow = (int)ti.ge * rpe + ti.mt * BM;
+                for (int k = 0; k < ti.nk; ++k, ++it) {
+                    const int s = it % NS;
+                    if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
+                                        abort_flag))
+                        break;
+                    const uint32_t fb = ptx::smem_addr(&tma_full[s]);
+                    const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
+                    ptx::mbar_arrive_expect_tx(fb, tx);
+                    ptx::tma_load_2d_hint(st + kOffA0, ta, k * (BK / 2), arow, fb, pol);
+                    if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, k * (BK / 2), arow + ti.Ig, fb, pol);
+                    for (int tt = 0; tt < kTerms; ++tt)
+                        ptx::tma_load_2d(st + kOffB + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box], k * (BK / 2),
+                                         ti.row0, fb);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, tcount = 0;
+            for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+                const TileInfo ti = decode_tile(p, t);
+                if (!ti.valid) continue;
+                const uint32_t buf = tcount & 1u, use = tcount >> 1;
+                if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[buf]), (use & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
+                                    abort_flag))
+                    break;
+                ++tcount;
+                ptx::tc_fence_after();
+                const int n_mma = kTerms * ti.bh;
+                bool ok = true;
+                for (int k = 0; k < ti.nk; ++k, ++it) {
+                    const int s = it % NS;
+                    const uint32_t ph = (it / NS) & 1u;
+                    if (!ptx::mbar_wait(ptx::smem_addr(&tma_full[s]), ph, p.err, ptx::kErrWaitFull, abort_flag) ||
+                        !ptx::mbar_wait(ptx::smem_addr(&sf_full[s]), ph, p.err, ptx::kErrWaitFull, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t sa = ptx::smem_addr(smem + s * kStageBytes);
+                    const uint32_t sf = tmem + kSfCol0 + s * kSfStage;
+                    const int ksteps = min(BK, ti.K - k * BK) / MK;   // 4, or 2 in a final half stage
+                    for (int j = 0; j < ksteps; ++j) {
+                        const uint32_t idesc = idesc_mx4(n_mma, 2 * (j & 1));
+                        const uint64_t bd = sw128_desc(sa + kOffB + j * 32);
+                        for (int a = 0; a < n_a; ++a) {
+                            const uint64_t ad = sw128_desc(sa + (a ? kOffA1 : kOffA0) + j * 32);
+                            const uint32_t d = tmem + buf * kAccCols + (uint32_t)(a * n_mma);
+                            mma_mx4(d, ad, bd, idesc, sf + 8 * a + 4 * (j >> 1), sf + 16 + 4 * (j >> 1),
+                                    (k > 0 || j > 0) ? 1u : 0u);
+                        }
+                    }
+                    ptx::mma_commit(ptx::smem_addr(&empty[s]));
+                }
+                if (!ok) break;
+                ptx::mma_commit(ptx::smem_addr(&acc_full[buf]));
+            }
+            ptx::mma_commit(ptx::smem_addr(drain));
+            ptx::mbar_wait(ptx::smem_addr(drain), 0, nullptr, 0, nullptr);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------------ scale loaders
+        const int quad = warp & 3;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        const int kba = p.act_ld / 32;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok && !*abort_flag; t += gridDim.x) {
+            const TileInfo ti = decode_tile(p, t);
+            if (!ti.valid) continue;
+            const int kb_row = ti.K / 32;
+            const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
+            const int rpe = gu ? 2 * ti.Ig : p.H;
+            const size_t wrow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM + quad * 32 + lane;
+            const uint8_t *wp[2] = {ws + wrow * kb_row, n_a > 1 ? ws + (wrow + ti.Ig) * kb_row : nullptr};
+            const int n_mma = kTerms * ti.bh, nbc = (n_mma + 31) / 32;
+            const uint8_t *bp[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int n = lane + 32 * c;
+                const int tt = n / ti.bh, j = n % ti.bh;
+                bp[c] = (c < nbc && j < ti.n_valid) ? p.act_scales + ((size_t)tt * p.rows + ti.row0 + j) * kba
+                                                    : nullptr;
+            }
+            for (int k = 0; k < ti.nk && ok; ++k) {
+                // this stage's 8 scale bytes per row (4 in a final half stage)
+                const bool half = (ti.K - k * BK) < BK;
+                auto ld = [&](const uint8_t *q, int w) -> uint32_t {
+                    return (q && !(half && w == 1)) ? __ldg(reinterpret_cast<const uint32_t *>(q) + 2 * k + w)
+                                                    : 0x7F7F7F7Fu;
+                };
+                uint32_t a0[2] = {ld(wp[0], 0), ld(wp[0], 1)};
+                uint32_t a1[2] = {ld(wp[1], 0), ld(wp[1], 1)};
+                uint32_t b[4][2];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    b[c][0] = ld(bp[c], 0);
+                    b[c][1] = ld(bp[c], 1);
+                }
+                const int s = it % NS;
+                if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
+                                    abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t col = lane_base + kSfCol0 + s * kSfStage;
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    tmem_st_x1(col + 4 * w + quad, a0[w]);
+                    if (n_a > 1) tmem_st_x1(col + 8 + 4 * w + quad, a1[w]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (c < nbc) tmem_st_x1(col + 16 + 4 * w + c, b[c][w]);
+                }
+                tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
+                ++it;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int quad = warp & 3;
+        const int m = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        uint32_t tcount = 0;
+        for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
+            const TileInfo ti = decode_tile(p, t);
+            if (!ti.valid) continue;
+            const uint32_t buf = tcount & 1u, use = tcount >> 1;
+            if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[buf]), use & 1u, p.err, ptx::kErrWaitAccum, abort_flag))
+                break;
+            ++tcount;
+            ptx::tc_fence_after();
+            const int mrow = ti.mt * BM + m;
+            const uint32_t acc = lane_base + buf * kAccCols;
+            const int ncols = kTerms * ti.bh;
+            for (int c0 = 0; c0 < ti.n_valid; c0 += 16) {
+                float v0[16], v1[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v0[j] = v1[j] = 0.f;
+#pragma unroll
+                for (int tt = 0; tt < kTerms; ++tt) {   // add the term columns
+                    uint32_t r[16];
+                    ptx::tmem_ld16(acc + tt * ti.bh + c0, r);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v0[j] += __uint_as_float(r[j]);
+                    if (gu) {
+                        ptx::tmem_ld16(acc + ncols + tt * ti.bh + c0, r);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v1[j] += __uint_as_float(r[j]);
+                    }
+                }
+                for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j) {
+                    const size_t row = (size_t)ti.row0 + c0 + j;
+                    if (!gu) {
+                        p.y[row * p.H + mrow] = v0[j];
+                        continue;
+                    }
+                    float v = __fdiv_rn(v0[j], 1.0f + expf(-v0[j])) * v1[j];
+#pragma unroll
+                    for (int tt = 0; tt < kTerms; ++tt) {
+                        const uint32_t sb = e2m1_scale_byte(warp_max(fabsf(v)));
+                        const float scale = __uint_as_float(sb << 23), inv = __uint_as_float((254u - sb) << 23);
+                        float back, unused;
+                        const uint32_t code = e2m1_pair(v * inv, 0.f, back, unused) & 0xF;
+                        v -= back * scale;
+                        const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+                        if ((lane & 1) == 0)
+                            p.hq[((size_t)tt * p.rows + row) * (p.I_max / 2) + mrow / 2] = (uint8_t)(code | (hi << 4));
+                        if (lane == 0) p.hs[((size_t)tt * p.rows + row) * (p.I_max / 32) + mrow / 32] = (uint8_t)sb;
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&acc_empty[buf]));
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Expert-grouped x rows -> four E2M1 terms (packed, two codes per byte) with UE8M0 scales per 32
+// elements. One thread per (row, 32-element block).
+__global__ void __launch_bounds__(256)
+quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
+              uint8_t *__restrict__ xq, uint8_t *__restrict__ xs) {
+    const int nb = H / 32;
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long)rows * nb) return;
+    const int row = (int)(i / nb), b = (int)(i % nb);
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)src_token[row] * H + b * 32);
+    float v[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 u = __ldg(src + q);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[q * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+            v[q * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+#pragma unroll
+    for (int tt = 0; tt < kTerms; ++tt) {
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        const uint32_t sb = e2m1_scale_byte(amax);
+        const float scale = __uint_as_float(sb << 23), inv = __uint_as_float((254u - sb) << 23);
+        uint32_t packed[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            float blo, bhi;
+            const uint32_t byte = e2m1_pair(v[e] * inv, v[e + 1] * inv, blo, bhi);
+            v[e] -= blo * scale;
+            v[e + 1] -= bhi * scale;
+            packed[e / 8] |= byte << (8 * ((e / 2) % 4));
+        }
+        *reinterpret_cast<uint4 *>(xq + ((size_t)tt * rows + row) * (H / 2) + b * 16) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        xs[((size_t)tt * rows + row) * nb + b] = (uint8_t)sb;
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Rows of packed 4-bit codes (K/2 bytes each), 128-byte x box_rows boxes with the 128-byte swizzle.
+bool map_packed(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+    auto enc = encoder();
+    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+    const cuuint64_t dims[2] = {K / 2, rows};
+    const cuuint64_t strides[1] = {K / 2};
+    const cuuint32_t box[2] = {BK / 2, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map_terms(BMaps4 &b, const uint8_t *base, uint64_t K, uint64_t rows) {
+    for (int t = 0; t < kTerms; ++t)
+        for (int h = 0; h < 2; ++h)
+            if (!map_packed(&b.m[t][h], base + (size_t)t * rows * (K / 2), K, rows, 16u << h)) return false;
+    return true;
+}
+
+}  // namespace
+
+bool mx4_available() { return encoder() != nullptr; }
+
+bool mx4_supported(const FfnArgs &a) { return encoder() != nullptr && a.H % 128 == 0; }
+
+int launch_quant_x4(const FfnArgs &a, cudaStream_t st) {
+    const long threads = (long)a.rows * (a.H / 32);
+    quant_x4_rows<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
+    return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+}
+
+int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
+    if (!mx4_supported(a)) return -2;
+    const NtileLayout nl = ntile_layout(sched, a.E, a.rows);
+    const size_t smem = NS * kStageBytes + 1024 + 256;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(gemm_mx4, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return -1;
+        attr = true;
+    }
+    Mx4Params p{};
+    p.E = a.E;
+    p.H = a.H;
+    p.I = a.I;
+    p.I_s = a.I_s;
+    p.I_max = a.I_max;
+    p.rows = a.rows;
+    p.cnt = a.cnt;
+    p.off = a.off;
+    p.touched = a.touched;
+    p.n_touched = a.n_touched;
+    p.hq = a.hq;
+    p.hs = a.hqs;
+    p.y = a.y;
+    p.err = a.err;
+    CUtensorMap tar, tas;
+    BMaps4 tb;
+    // gate/up
+    p.mode = kGateUp;
+    p.bn = kBnGateUp;
+    p.ntile_prefix = nl.prefix_small;
+    p.ntile_owner = nl.owner_small;
+    p.m_tiles = (a.I_max + BM - 1) / BM;
+    p.w_scales_routed = a.routed.gu_scales;
+    p.w_scales_shared = a.shared.gu_scales;
+    p.act_scales = a.xqs;
+    p.act_ld = a.H;
+    bool ok = map_packed(&tar, a.routed.gu_codes, a.H, (uint64_t)a.E * 2 * a.I, BM) &&
+              map_terms(tb, a.xq, a.H, a.rows);
+    if (a.shared.gu_codes) ok = ok && map_packed(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s, BM);
+    else tas = tar;
+    if (!ok) return -2;
+    gemm_mx4<<<num_sms, kThreads, smem, st>>>(tar, tas, tb, p);
+    int n = 1;
+    if (mid) cudaEventRecord(mid, st);
+    // down
+    p.mode = kDown;
+    p.bn = kBnDown;
+    p.ntile_prefix = nl.prefix_large;
+    p.ntile_owner = nl.owner_large;
+    p.m_tiles = a.H / BM;
+    p.w_scales_routed = a.routed.d_scales;
+    p.w_scales_shared = a.shared.d_scales;
+    p.act_scales = a.hqs;
+    p.act_ld = a.I_max;
+    ok = map_packed(&tar, a.routed.d_codes, a.I, (uint64_t)a.E * a.H, BM) && map_terms(tb, a.hq, a.I_max, a.rows);
+    if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
+    else tas = tar;
+    if (!ok) return -2;
+    gemm_mx4<<<num_sms, kThreads, smem, st>>>(tar, tas, tb, p);
+    ++n;
+    return cudaPeekAtLastError() == cudaSuccess ? n : -1;
+}
+
+}  // namespace colimoe

@@ -53,7 +53,7 @@ __device__ int block_exclusive_scan(int v, int *smem_warp, int *total) {
 __global__ void __launch_bounds__(1024)
 permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__restrict__ touched,
              int32_t *__restrict__ touched_cost, int32_t *__restrict__ n_touched, int E, int shared_rows,
-             int cost_tokens, NtileLayout nl, bool ntiles) {
+             int cost_tokens, NtileLayout nl, int ntile) {
     __shared__ int smem[33];
     __shared__ int s_nt;
     const int G = E + 1;
@@ -85,7 +85,7 @@ permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__re
         touched_cost[tbase] = cbase;
         s_nt = tbase;
     }
-    if (!ntiles) return;
+    if (!ntile) return;
     // n-tiles of the block-scaled GEMM for both tile sizes, over the touched groups in order
     __syncthreads();
     const int nt = s_nt;
@@ -93,7 +93,7 @@ permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__re
     for (int u0 = 0; u0 < nt; u0 += 1024) {
         const int u = u0 + threadIdx.x;
         const int c = u < nt ? cnt[touched[u]] : 0;
-        const int ns = (c + kNtileSmall - 1) / kNtileSmall, nlg = (c + kNtileLarge - 1) / kNtileLarge;
+        const int ns = (c + ntile - 1) / ntile, nlg = (c + 2 * ntile - 1) / (2 * ntile);
         int tot_s, tot_l;
         const int ex_s = block_exclusive_scan(ns, smem, &tot_s);
         const int ex_l = block_exclusive_scan(nlg, smem, &tot_l);
@@ -171,13 +171,13 @@ permute_gather(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__rest
 }  // namespace
 
 int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, bool gather, int cost_tokens, bool ntiles, Workspace &ws, cudaStream_t st) {
+                   int H, bool gather, int cost_tokens, int ntile, Workspace &ws, cudaStream_t st) {
     const int n = T * top_k;
     const int rows = n + (with_shared ? T : 0);
     if (cudaMemsetAsync(ws.cnt, 0, sizeof(int32_t) * (E + 1), st) != cudaSuccess) return -1;
     permute_count<<<(n + 255) / 256, 256, 0, st>>>(idx, n, ws.cnt);
     permute_scan<<<1, 1024, 0, st>>>(ws.cnt, ws.off, ws.touched, ws.touched_cost, ws.n_touched, E,
-                                     with_shared ? T : 0, cost_tokens, ntile_layout(ws.tile_sched, E, rows), ntiles);
+                                     with_shared ? T : 0, cost_tokens, ntile_layout(ws.tile_sched, E, rows), ntile);
     permute_scatter<<<E + 1, 256, 0, st>>>(idx, T, E, top_k, ws.cnt, ws.off, ws.src_token, ws.inv_row);
     if (!gather) return cudaPeekAtLastError() == cudaSuccess ? 3 : -1;
     const size_t vecs = (size_t)rows * (H / 8);

@@ -9,7 +9,7 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-GEMV, GEMM, AUTO, BF16 = 1, 2, 0, 3
+GEMV, GEMM, AUTO, BF16, MXF4 = 1, 2, 0, 3, 4
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -112,7 +112,7 @@ def test_edge_cases(oracle, wl):
     _assert_ok(rep)
 
 
-@pytest.mark.parametrize("path", [GEMM, BF16, GEMV], ids=["mx", "bf16", "gemv"])
+@pytest.mark.parametrize("path", [MXF4, GEMM, BF16, GEMV], ids=["mxf4", "mx", "bf16", "gemv"])
 @pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T16", "sweep_T128"])
 def test_ffn_paths(oracle, name, path):
     """Each FFN path, forced, against the oracle."""
@@ -126,15 +126,16 @@ def test_ffn_paths(oracle, name, path):
     _custom("gemm_shared_wider", I_s=256),
     _custom("gemm_noshared", I_s=0),
     _custom("gemm_many_rows", T=300, E=4, top_k=2),
+    _custom("gemm_half_stages", T=21, H=640, I=384, I_s=256, E=12, top_k=3),
 ], ids=lambda w: w.name)
-@pytest.mark.parametrize("path", [GEMM, BF16], ids=["mx", "bf16"])
+@pytest.mark.parametrize("path", [MXF4, GEMM, BF16], ids=["mxf4", "mx", "bf16"])
 def test_gemm_edge_cases(oracle, wl, path):
     inputs = S.make_inputs(wl)
     rep, _, _ = _run(oracle, inputs, path)
     _assert_ok(rep)
 
 
-@pytest.mark.parametrize("path", [GEMM, BF16], ids=["mx", "bf16"])
+@pytest.mark.parametrize("path", [MXF4, GEMM, BF16], ids=["mxf4", "mx", "bf16"])
 def test_gemm_matches_gemv(oracle, path):
     """The FFN paths agree with each other within the parity bar on the same routing."""
     inputs = S.make_inputs("sweep_T64")
@@ -187,4 +188,22 @@ def test_forward_host_matches_device(oracle):
     out_host = torch.zeros_like(x_host).pin_memory()
     layer.forward_host(x_host, out_host)
     assert np.array_equal(out_host.numpy().view(np.uint16), outs[0])
+    layer.close()
+
+
+def test_auto_path_is_mxf4():
+    """The automatic choice on a GB300 is the FP4 x FP4 block-scaled GEMM, and the handle reports it."""
+    import torch
+    from routed_moe_fp4_gb300 import colimoe as cm
+    inputs = S.make_inputs("tiny")
+    layer = cm.MoELayer(inputs)
+    assert layer.ffn_path() == cm.COLI_FFN_AUTO
+    x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
+    out = torch.empty_like(x)
+    layer.forward(x, out)
+    torch.cuda.synchronize()
+    assert layer.ffn_path() == cm.COLI_FFN_GEMM_MXF4
+    layer.set_ffn_path(cm.COLI_FFN_GEMV)
+    layer.forward(x, out)
+    assert layer.ffn_path() == cm.COLI_FFN_GEMV
     layer.close()
