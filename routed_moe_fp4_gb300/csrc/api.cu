@@ -149,7 +149,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     if (prof) cudaEventRecord(h->ev[0], st);
 
     n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
-                      ws.scores, ws.idx, ws.w, ws.logit_part, ws.logit_part_floats, h->num_sms, st);
+                      ws.scores, ws.idx, ws.w, ws.logit_part, ws.logit_part_floats, h->num_sms, ws.cnt, E + 1, st);
     if (n < 0) goto launch_fail;
     launches += n;
     if (prof) cudaEventRecord(h->ev[1], st);

@@ -6,6 +6,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "colimoe.h"
 
 namespace colimoe {
@@ -79,15 +81,46 @@ struct FfnArgs {
     int *err;
 };
 
+// Programmatic dependent launch. Every kernel of the library is launched with programmatic
+// stream serialisation (launch_pdl), so its launch and prologue may overlap the kernel before it
+// in the stream. Each kernel therefore begins with pdl_begin() (or, for kernels with an on-chip
+// prologue, pdl_trigger() first and pdl_wait() before its first global-memory access):
+// pdl_trigger lets the next kernel be scheduled once every block of this one has started;
+// pdl_wait returns when the kernel before this one has completed and its writes are visible.
+// Since every kernel waits, completion of one kernel implies completion of all earlier ones.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+    pdl_trigger();
+    pdl_wait();
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Records the text coli_moe_last_error(NULL) returns (printf-style).
 void set_create_error(const char *fmt, ...);
 
 // Launchers. Each returns the number of kernels it enqueued, or -1 on a launch error
 // (the CUDA error is then available from cudaGetLastError()).
-// `partial` ([partial_floats] fp32) holds split-K partial logits for larger T.
+// `partial` ([partial_floats] fp32) holds split-K partial logits for larger T. `zero` (may be
+// null): n_zero ints the router's last kernel clears (the permute histogram).
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
                   int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
-                  int num_sms, cudaStream_t st);
+                  int num_sms, int32_t *zero, int n_zero, cudaStream_t st);
 // `gather`: also copy the activation rows into expert-grouped order (ws.xp). `cost_tokens`: rows
 // per unit of work cost in ws.touched_cost (see permute_scan). `ntile`: when non-zero, also write
 // the block-scaled GEMM's n-tile layout (NtileLayout, tiles of `ntile` and 2 * `ntile` rows) into
@@ -102,20 +135,27 @@ constexpr int kNtileMx = 32;    // E2M1 weights x E4M3 activation terms (gemm_mx
 constexpr int kNtileMx4 = 16;   // E2M1 weights x E2M1 activation terms (gemm_mx4.cu)
 constexpr int kNtileMin = 16;   // the layout below is sized for tiles of at least this many rows
 // The permute scan writes, per tile size, an exclusive prefix of ceil(cnt / size) over the touched
-// groups and the owning group of each tile. A tile size s >= kNtileMin gives at most
-// rows / s + E + 1 tiles.
+// groups, the owning group of each tile, one record per tile ({first row, group | rows << 16},
+// so a kernel decodes a tile with one load) and the number of tiles. A tile size s >= kNtileMin
+// gives at most rows / s + E + 1 tiles.
 struct NtileLayout {
-    int32_t *prefix_small, *owner_small, *prefix_large, *owner_large;
+    int2 *rec_small, *rec_large;
+    int32_t *prefix_small, *owner_small, *prefix_large, *owner_large, *count;   // count[0] small, [1] large
 };
+__host__ __device__ inline size_t ntile_max(int E, int rows) { return (size_t)rows / kNtileMin + (size_t)E + 2; }
 __host__ __device__ inline size_t ntile_layout_ints(int E, int rows) {
-    return 2 * ((size_t)E + 2) + 2 * ((size_t)rows / kNtileMin + (size_t)E + 2);
+    return 4 * ntile_max(E, rows) + 2 * ((size_t)E + 2) + 2 * ntile_max(E, rows) + 2;
 }
 __host__ __device__ inline NtileLayout ntile_layout(void *base, int E, int rows) {
+    const size_t nm = ntile_max(E, rows);
     NtileLayout l;
-    l.prefix_small = static_cast<int32_t *>(base);
+    l.rec_small = static_cast<int2 *>(base);
+    l.rec_large = l.rec_small + nm;
+    l.prefix_small = reinterpret_cast<int32_t *>(l.rec_large + nm);
     l.owner_small = l.prefix_small + E + 2;
-    l.prefix_large = l.owner_small + rows / kNtileMin + E + 2;
+    l.prefix_large = l.owner_small + nm;
     l.owner_large = l.prefix_large + E + 2;
+    l.count = l.owner_large + nm;
     return l;
 }
 // `mid` (may be null): an event recorded between the gate/up and the down kernels.

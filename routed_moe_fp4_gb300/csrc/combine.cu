@@ -11,6 +11,7 @@ namespace {
 __global__ void __launch_bounds__(256)
 combine_kernel(const float *__restrict__ y, const int32_t *__restrict__ inv_row, const float *__restrict__ w,
                int T, int H, int top_k, int shared_base, __nv_bfloat16 *__restrict__ out) {
+    pdl_begin();
     const int t = blockIdx.y;
     const int v = blockIdx.x * blockDim.x + threadIdx.x;   // float4 column index
     if (v >= H / 4) return;
@@ -38,7 +39,7 @@ combine_kernel(const float *__restrict__ y, const int32_t *__restrict__ inv_row,
 int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T, int H, int top_k,
                    bool with_shared, __nv_bfloat16 *out, cudaStream_t st) {
     const dim3 grid((H / 4 + 255) / 256, T);
-    combine_kernel<<<grid, 256, 0, st>>>(y, inv_row, w, T, H, top_k, with_shared ? T * top_k : -1, out);
+    launch_pdl(combine_kernel, grid, dim3(256), 0, st, y, inv_row, w, T, H, top_k, with_shared ? T * top_k : -1, out);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 

@@ -173,6 +173,7 @@ struct BMaps {
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
         const __grid_constant__ BMaps tm_b, const MxParams p) {
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
@@ -208,6 +209,7 @@ gemm_mx(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();   // everything above is on-chip set-up
     const int total_tiles = p.m_tiles * p.ntile_prefix[*p.n_touched];
 
     if (warp == 0) {
@@ -465,6 +467,7 @@ __device__ __forceinline__ uint32_t block_scale_byte(float amax) {
 __global__ void __launch_bounds__(256)
 quant_x_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
              uint8_t *__restrict__ xq, uint8_t *__restrict__ xs) {
+    pdl_begin();
     const int nb = H / 32;
     const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long)rows * nb) return;
@@ -552,7 +555,8 @@ bool mx_available() { return encoder() != nullptr; }
 
 int launch_quant_x(const FfnArgs &a, cudaStream_t st) {
     const long qthreads = (long)a.rows * (a.H / 32);
-    quant_x_rows<<<(unsigned)((qthreads + 255) / 256), 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
+    launch_pdl(quant_x_rows, dim3((unsigned)((qthreads + 255) / 256)), dim3(256), 0, st, a.x, a.H, a.src_token,
+               a.rows, a.xq, a.xqs);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -620,7 +624,7 @@ int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, c
     if (a.shared.gu_codes) ok = ok && map_codes(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s);
     else tas = tar;
     if (!ok) return -2;
-    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb, p);
+    launch_pdl(gemm_mx, dim3(num_sms), dim3(kThreads), smem, st, tar, tas, tb, p);
     ++n;
     if (mid) cudaEventRecord(mid, st);
 
@@ -641,7 +645,7 @@ int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, c
     if (a.shared.d_codes) ok = ok && map_codes(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H);
     else tas = tar;
     if (!ok) return -2;
-    gemm_mx<<<num_sms, kThreads, smem, st>>>(tar, tas, tb, p);
+    launch_pdl(gemm_mx, dim3(num_sms), dim3(kThreads), smem, st, tar, tas, tb, p);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }

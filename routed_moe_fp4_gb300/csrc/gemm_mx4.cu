@@ -21,8 +21,9 @@
 // block per SM; warp roles as in the E4M3 path: TMA producer (warp 0), TMEM owner and MMA issuer
 // (warp 1), scale loaders (warps 2-5; weight row 32q + i reads its scales from lane 32q + i,
 // column (word) * 4 + q; activation row n from lane 32q + n % 32, column n / 32 of its word, in
-// every lane quarter q; the words of one stage sit 4 columns apart), epilogue (warps 6-9). Four stages, double-buffered accumulators, bounded
-// waits. A K that is not a multiple of 256 ends with a half stage.
+// every lane quarter q; the words of one stage sit 4 columns apart; their loads run four stages
+// ahead), epilogue (warps 6-9). Four stages, double-buffered accumulators, bounded waits. A K that
+// is not a multiple of 256 ends with a half stage.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -45,13 +46,15 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 128;             // per accumulator buffer
 constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 32 per stage
 constexpr uint32_t kSfStage = 32;
+constexpr int kSfAhead = 4;                   // stages the scale loads run ahead
 
 enum Mode { kGateUp = 0, kDown = 1 };
 
 struct Mx4Params {
     int E, H, I, I_s, I_max, rows;
     int mode, m_tiles, bn;
-    const int32_t *cnt, *off, *touched, *n_touched, *ntile_prefix, *ntile_owner;
+    const int2 *ntile_rec;              // per n-tile: {first row, group | rows << 16}
+    const int32_t *ntile_count;         // number of n-tiles
     const uint8_t *w_scales_routed, *w_scales_shared;
     const uint8_t *act_scales;          // [kTerms][rows][K/32]
     int act_ld;                         // K of the activation terms (H or I_max)
@@ -67,24 +70,92 @@ struct TileInfo {
     size_t ge;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t) {
+// Tile t = (n-tile t / m_tiles, m-tile t % m_tiles); `rec` is the n-tile's record.
+__device__ __forceinline__ int2 tile_rec(const Mx4Params &p, int t, int total_tiles) {
+    return t < total_tiles ? __ldg(p.ntile_rec + t / p.m_tiles) : make_int2(0, 0);
+}
+
+__device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 rec) {
     TileInfo ti;
     ti.mt = t % p.m_tiles;
-    const int r = t / p.m_tiles;
-    const int u = p.ntile_owner[r];
-    ti.g = p.touched[u];
-    const int nt = r - p.ntile_prefix[u];
+    ti.g = rec.y & 0xFFFF;
     ti.shared = ti.g == p.E;
     ti.Ig = ti.shared ? p.I_s : p.I;
     ti.ge = ti.shared ? 0 : (size_t)ti.g;
-    ti.row0 = p.off[ti.g] + nt * p.bn;
-    ti.n_valid = min(p.bn, p.cnt[ti.g] - nt * p.bn);
+    ti.row0 = rec.x;
+    ti.n_valid = rec.y >> 16;
     ti.valid = p.mode == kGateUp ? ti.mt * BM < ti.Ig : true;
     ti.K = p.mode == kGateUp ? p.H : ti.Ig;
     ti.nk = (ti.K + BK - 1) / BK;
     ti.box = ti.n_valid <= 16 ? 0 : 1;
     ti.bh = 16 << ti.box;
     return ti;
+}
+
+// Scale words of one stage for one loader lane: its gate (a0) and up (a1) weight rows, and the
+// activation rows lane + 32c (c < nbc); nbc == 0 marks an empty ring slot.
+struct SfStage {
+    uint32_t a0[2], a1[2], b[4][2];
+    int nbc;
+};
+
+// Position of a scale loader in the (tile, stage) sequence of its block, with the row pointers of
+// the current tile.
+struct SfCursor {
+    int t, k, nk, K, nbc;
+    const uint8_t *wp0, *wp1, *bp[4];
+};
+
+// Moves the cursor to the first valid tile at or after cur.t; false when there is none.
+__device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int total_tiles, int quad, int lane) {
+    const bool gu = p.mode == kGateUp;
+    for (; c.t < total_tiles; c.t += gridDim.x) {
+        const TileInfo ti = decode_tile(p, c.t, tile_rec(p, c.t, total_tiles));
+        if (!ti.valid) continue;
+        const int kb_row = ti.K / 32, kba = p.act_ld / 32;
+        const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
+        const int rpe = gu ? 2 * ti.Ig : p.H;
+        const size_t wrow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM + quad * 32 + lane;
+        c.wp0 = ws + wrow * kb_row;
+        c.wp1 = gu ? ws + (wrow + ti.Ig) * kb_row : nullptr;
+        c.nbc = (kTerms * ti.bh + 31) / 32;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int n = lane + 32 * q;
+            const int tt = n / ti.bh, j = n % ti.bh;
+            c.bp[q] = (q < c.nbc && j < ti.n_valid) ? p.act_scales + ((size_t)tt * p.rows + ti.row0 + j) * kba
+                                                    : nullptr;
+        }
+        c.k = 0;
+        c.nk = ti.nk;
+        c.K = ti.K;
+        return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ bool sf_next(const Mx4Params &p, SfCursor &c, int total_tiles, int quad, int lane) {
+    if (++c.k < c.nk) return true;
+    c.t += gridDim.x;
+    return sf_tile(p, c, total_tiles, quad, lane);
+}
+
+// Issues the loads of the cursor's stage: 8 scale bytes per row (4 in a final half stage; the
+// missing word reads as scale 1).
+__device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStage &s, int n_a) {
+    const bool half = (c.K - c.k * BK) < BK;
+    auto ld = [&](const uint8_t *q, int w) -> uint32_t {
+        return (q && !(half && w == 1)) ? __ldg(reinterpret_cast<const uint32_t *>(q) + 2 * c.k + w)
+                                        : 0x7F7F7F7Fu;
+    };
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        s.a0[w] = ld(c.wp0, w);
+        s.a1[w] = n_a > 1 ? ld(c.wp1, w) : 0x7F7F7F7Fu;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s.b[q][w] = ld(c.bp[q], w);
+    }
+    s.nbc = c.nbc;
 }
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -148,9 +219,11 @@ struct BMaps4 {
     CUtensorMap m[kTerms][2];   // [term][box height 16 / 32]
 };
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
          const __grid_constant__ BMaps4 tm_b, const Mx4Params p) {
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
@@ -160,8 +233,8 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool gu = p.mode == kGateUp;
-    const int n_a = gu ? 2 : 1;
+    constexpr bool gu = MODE == kGateUp;
+    constexpr int n_a = gu ? 2 : 1;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(ptx::smem_addr(&tma_full[s]), 1);
@@ -184,7 +257,8 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int total_tiles = p.m_tiles * p.ntile_prefix[*p.n_touched];
+    pdl_wait();   // everything above is on-chip set-up
+    const int total_tiles = p.m_tiles * *p.ntile_count;
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
@@ -192,8 +266,11 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             ptx::prefetch_tmap(&tm_a_routed);
             const uint64_t pol = ptx::policy_evict_first();
             uint32_t it = 0;
+            int2 rec = tile_rec(p, blockIdx.x, total_tiles);
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-                const TileInfo ti = decode_tile(p, t);
+                const int2 cur = rec;
+                rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
+                const TileInfo ti = decode_tile(p, t, cur);
                 if (!ti.valid) continue;
                 const uint32_t tx = n_a * kASmem + kTerms * ti.bh * (BK / 2);
                 const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
@@ -218,9 +295,13 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            const uint64_t desc0 = sw128_desc(ptx::smem_addr(smem));   // stage 0, matrix A0
             uint32_t it = 0, tcount = 0;
+            int2 rec = tile_rec(p, blockIdx.x, total_tiles);
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-                const TileInfo ti = decode_tile(p, t);
+                const int2 cur = rec;
+                rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
+                const TileInfo ti = decode_tile(p, t, cur);
                 if (!ti.valid) continue;
                 const uint32_t buf = tcount & 1u, use = tcount >> 1;
                 if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[buf]), (use & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
@@ -229,6 +310,10 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 ++tcount;
                 ptx::tc_fence_after();
                 const int n_mma = kTerms * ti.bh;
+                const uint32_t id0 = idesc_mx4(n_mma, 0), id2 = idesc_mx4(n_mma, 2);
+                const uint32_t d0 = tmem + buf * kAccCols, d1 = d0 + (uint32_t)n_mma;
+                const int nfull = ti.K / BK;                  // full stages; a half stage may follow
+                uint32_t acc = 0;
                 bool ok = true;
                 for (int k = 0; k < ti.nk; ++k, ++it) {
                     const int s = it % NS;
@@ -239,18 +324,21 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sa = ptx::smem_addr(smem + s * kStageBytes);
-                    const uint32_t sf = tmem + kSfCol0 + s * kSfStage;
-                    const int ksteps = min(BK, ti.K - k * BK) / MK;   // 4, or 2 in a final half stage
-                    for (int j = 0; j < ksteps; ++j) {
-                        const uint32_t idesc = idesc_mx4(n_mma, 2 * (j & 1));
-                        const uint64_t bd = sw128_desc(sa + kOffB + j * 32);
-                        for (int a = 0; a < n_a; ++a) {
-                            const uint64_t ad = sw128_desc(sa + (a ? kOffA1 : kOffA0) + j * 32);
-                            const uint32_t d = tmem + buf * kAccCols + (uint32_t)(a * n_mma);
-                            mma_mx4(d, ad, bd, idesc, sf + 8 * a + 4 * (j >> 1), sf + 16 + 4 * (j >> 1),
-                                    (k > 0 || j > 0) ? 1u : 0u);
-                        }
+                    // descriptors of this stage: the start-address field advances by 32 B (2) per MMA
+                    const uint64_t a0 = desc0 + (uint64_t)(s * (kStageBytes >> 4));
+                    const uint64_t a1 = a0 + (kOffA1 >> 4), b = a0 + (kOffB >> 4);
+                    const uint32_t sfa = tmem + kSfCol0 + s * kSfStage, sfb = sfa + 16;
+                    auto step = [&](int j) {
+                        const uint32_t id = (j & 1) ? id2 : id0;
+                        mma_mx4(d0, a0 + 2 * j, b + 2 * j, id, sfa + 4 * (j >> 1), sfb + 4 * (j >> 1), acc);
+                        if (gu) mma_mx4(d1, a1 + 2 * j, b + 2 * j, id, sfa + 8 + 4 * (j >> 1), sfb + 4 * (j >> 1), acc);
+                        acc = 1;
+                    };
+                    step(0);
+                    step(1);
+                    if (k < nfull) {
+                        step(2);
+                        step(3);
                     }
                     ptx::mma_commit(ptx::smem_addr(&empty[s]));
                 }
@@ -262,63 +350,58 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------------ scale loaders
+        // The scale words of stage it + kSfAhead are fetched while stage it is stored, so the
+        // global-load latency overlaps kSfAhead stages of MMA work. Each ring slot keeps its
+        // registers (the loop is unrolled over the slots): nothing waits on a load until the
+        // slot's words are stored.
         const int quad = warp & 3;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-        const int kba = p.act_ld / 32;
-        uint32_t it = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total_tiles && ok && !*abort_flag; t += gridDim.x) {
-            const TileInfo ti = decode_tile(p, t);
-            if (!ti.valid) continue;
-            const int kb_row = ti.K / 32;
-            const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
-            const int rpe = gu ? 2 * ti.Ig : p.H;
-            const size_t wrow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM + quad * 32 + lane;
-            const uint8_t *wp[2] = {ws + wrow * kb_row, n_a > 1 ? ws + (wrow + ti.Ig) * kb_row : nullptr};
-            const int n_mma = kTerms * ti.bh, nbc = (n_mma + 31) / 32;
-            const uint8_t *bp[4];
+        SfCursor cur;
+        cur.t = blockIdx.x;
+        bool live = sf_tile(p, cur, total_tiles, quad, lane);
+        SfStage ring[kSfAhead];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int n = lane + 32 * c;
-                const int tt = n / ti.bh, j = n % ti.bh;
-                bp[c] = (c < nbc && j < ti.n_valid) ? p.act_scales + ((size_t)tt * p.rows + ti.row0 + j) * kba
-                                                    : nullptr;
+        for (int d = 0; d < kSfAhead; ++d) {
+            ring[d].nbc = 0;
+            if (live) {
+                sf_fetch(cur, ring[d], n_a);
+                live = sf_next(p, cur, total_tiles, quad, lane);
             }
-            for (int k = 0; k < ti.nk && ok; ++k) {
-                // this stage's 8 scale bytes per row (4 in a final half stage)
-                const bool half = (ti.K - k * BK) < BK;
-                auto ld = [&](const uint8_t *q, int w) -> uint32_t {
-                    return (q && !(half && w == 1)) ? __ldg(reinterpret_cast<const uint32_t *>(q) + 2 * k + w)
-                                                    : 0x7F7F7F7Fu;
-                };
-                uint32_t a0[2] = {ld(wp[0], 0), ld(wp[0], 1)};
-                uint32_t a1[2] = {ld(wp[1], 0), ld(wp[1], 1)};
-                uint32_t b[4][2];
+        }
+        uint32_t it = 0;
+        bool run = true;
+        while (run) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    b[c][0] = ld(bp[c], 0);
-                    b[c][1] = ld(bp[c], 1);
+            for (int d = 0; d < kSfAhead; ++d) {
+                if (!run || ring[d].nbc == 0 || *abort_flag) {
+                    run = false;
+                    continue;
                 }
                 const int s = it % NS;
                 if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
                                     abort_flag)) {
-                    ok = false;
-                    break;
+                    run = false;
+                    continue;
                 }
                 ptx::tc_fence_after();
                 const uint32_t col = lane_base + kSfCol0 + s * kSfStage;
 #pragma unroll
                 for (int w = 0; w < 2; ++w) {
-                    tmem_st_x1(col + 4 * w + quad, a0[w]);
-                    if (n_a > 1) tmem_st_x1(col + 8 + 4 * w + quad, a1[w]);
+                    tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
+                    if (n_a > 1) tmem_st_x1(col + 8 + 4 * w + quad, ring[d].a1[w]);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
-                        if (c < nbc) tmem_st_x1(col + 16 + 4 * w + c, b[c][w]);
+                        if (c < ring[d].nbc) tmem_st_x1(col + 16 + 4 * w + c, ring[d].b[c][w]);
                 }
                 tmem_st_wait();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
                 ++it;
+                ring[d].nbc = 0;
+                if (live) {
+                    sf_fetch(cur, ring[d], n_a);
+                    live = sf_next(p, cur, total_tiles, quad, lane);
+                }
             }
         }
     } else {
@@ -327,8 +410,11 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         const int m = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t tcount = 0;
+        int2 rec = tile_rec(p, blockIdx.x, total_tiles);
         for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
-            const TileInfo ti = decode_tile(p, t);
+            const int2 cur = rec;
+            rec = tile_rec(p, t + gridDim.x, total_tiles);
+            const TileInfo ti = decode_tile(p, t, cur);
             if (!ti.valid) continue;
             const uint32_t buf = tcount & 1u, use = tcount >> 1;
             if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[buf]), use & 1u, p.err, ptx::kErrWaitAccum, abort_flag))
@@ -396,6 +482,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
 __global__ void __launch_bounds__(256)
 quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
               uint8_t *__restrict__ xq, uint8_t *__restrict__ xs) {
+    pdl_begin();
     const int nb = H / 32;
     const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long)rows * nb) return;
@@ -474,7 +561,8 @@ bool mx4_supported(const FfnArgs &a) { return encoder() != nullptr && a.H % 128 
 
 int launch_quant_x4(const FfnArgs &a, cudaStream_t st) {
     const long threads = (long)a.rows * (a.H / 32);
-    quant_x4_rows<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
+    launch_pdl(quant_x4_rows, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, a.x, a.H, a.src_token, a.rows,
+               a.xq, a.xqs);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -484,7 +572,10 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     const size_t smem = NS * kStageBytes + 1024 + 256;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(gemm_mx4, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_mx4<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(gemm_mx4<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+                cudaSuccess)
             return -1;
         attr = true;
     }
@@ -495,10 +586,6 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     p.I_s = a.I_s;
     p.I_max = a.I_max;
     p.rows = a.rows;
-    p.cnt = a.cnt;
-    p.off = a.off;
-    p.touched = a.touched;
-    p.n_touched = a.n_touched;
     p.hq = a.hq;
     p.hs = a.hqs;
     p.y = a.y;
@@ -508,8 +595,8 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     // gate/up
     p.mode = kGateUp;
     p.bn = kBnGateUp;
-    p.ntile_prefix = nl.prefix_small;
-    p.ntile_owner = nl.owner_small;
+    p.ntile_rec = nl.rec_small;
+    p.ntile_count = nl.count;
     p.m_tiles = (a.I_max + BM - 1) / BM;
     p.w_scales_routed = a.routed.gu_scales;
     p.w_scales_shared = a.shared.gu_scales;
@@ -520,14 +607,14 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     if (a.shared.gu_codes) ok = ok && map_packed(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s, BM);
     else tas = tar;
     if (!ok) return -2;
-    gemm_mx4<<<num_sms, kThreads, smem, st>>>(tar, tas, tb, p);
+    launch_pdl(gemm_mx4<kGateUp>, dim3(num_sms), dim3(kThreads), smem, st, tar, tas, tb, p);
     int n = 1;
     if (mid) cudaEventRecord(mid, st);
     // down
     p.mode = kDown;
     p.bn = kBnDown;
-    p.ntile_prefix = nl.prefix_large;
-    p.ntile_owner = nl.owner_large;
+    p.ntile_rec = nl.rec_large;
+    p.ntile_count = nl.count + 1;
     p.m_tiles = a.H / BM;
     p.w_scales_routed = a.routed.d_scales;
     p.w_scales_shared = a.shared.d_scales;
@@ -537,7 +624,7 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
     else tas = tar;
     if (!ok) return -2;
-    gemm_mx4<<<num_sms, kThreads, smem, st>>>(tar, tas, tb, p);
+    launch_pdl(gemm_mx4<kDown>, dim3(num_sms), dim3(kThreads), smem, st, tar, tas, tb, p);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }

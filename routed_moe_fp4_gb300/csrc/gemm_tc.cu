@@ -158,6 +158,7 @@ __device__ __forceinline__ void dequant_row(const uint8_t *codes, uint8_t *a, in
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_c_routed,
         const __grid_constant__ CUtensorMap tm_c_shared, const GemmParams p) {
+    pdl_trigger();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
@@ -191,6 +192,7 @@ gemm_tc(const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtens
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    pdl_wait();   // everything above is on-chip set-up
     const int total_tiles = p.m_tiles * p.ntile_prefix[*p.n_touched];
     const bool gu = p.mode == kGateUp;
     const uint32_t tx_bytes = kBBytes + (gu ? 2 : 1) * kCBytes;
@@ -391,6 +393,7 @@ struct NtileArgs {
 // n-tile bookkeeping for the grouped GEMM: prefix[u] = sum of ceil(cnt / BN) over touched groups
 // before u, owner[r] = the touched group of n-tile r. One block.
 __global__ void __launch_bounds__(1024) gemm_ntiles(NtileArgs a) {
+    pdl_begin();
     __shared__ int part[1024];
     const int nt = *a.n_touched;
     int carry = 0;
@@ -430,7 +433,7 @@ int launch_ffn_gemm(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     int32_t *prefix = static_cast<int32_t *>(sched);
     int32_t *owner = prefix + a.E + 2;
     NtileArgs na{a.cnt, a.touched, a.n_touched, prefix, owner};
-    gemm_ntiles<<<1, 1024, 0, st>>>(na);
+    launch_pdl(gemm_ntiles, dim3(1), dim3(1024), 0, st, na);
 
     const size_t smem = NS * kStageBytes + 1024 + 256;
     static bool attr = false;
@@ -472,7 +475,7 @@ int launch_ffn_gemm(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     else
         tcs = tcr;
     if (!ok) return -2;
-    gemm_tc<<<num_sms, kThreads, smem, st>>>(tb, tcr, tcs, p);
+    launch_pdl(gemm_tc, dim3(num_sms), dim3(kThreads), smem, st, tb, tcr, tcs, p);
     if (mid) cudaEventRecord(mid, st);
 
     // down: B = h rows [rows][I_max], codes [E*H][I/2]
@@ -490,7 +493,7 @@ int launch_ffn_gemm(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     else
         tcs = tcr;
     if (!ok) return -2;
-    gemm_tc<<<num_sms, kThreads, smem, st>>>(tb, tcr, tcs, p);
+    launch_pdl(gemm_tc, dim3(num_sms), dim3(kThreads), smem, st, tb, tcr, tcs, p);
     return cudaPeekAtLastError() == cudaSuccess ? 3 : -1;
 }
 

@@ -216,6 +216,7 @@ __device__ long item_at_cost(const int32_t *__restrict__ P, int nt, int ipg, lon
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemv_tma(FfnArgs a, int ipg, int nst, uint32_t stage_stride) {
+    pdl_trigger();
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)nst * stage_stride);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * nst);
@@ -229,6 +230,7 @@ gemv_tma(FfnArgs a, int ipg, int nst, uint32_t stage_stride) {
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
+    pdl_wait();   // everything above is on-chip set-up
     if (warp == 0) {   // this block's share of the total cost, as a range of flat items
         const int nt = *a.n_touched;
         const long total = (long)ipg * a.touched_cost[nt];
@@ -322,6 +324,7 @@ gemv_tma(FfnArgs a, int ipg, int nst, uint32_t stage_stride) {
 __global__ void __launch_bounds__(256)
 prep_rows_f16(const __nv_bfloat16 *__restrict__ src, int src_ld, int nrows, int K1, int split, int K2,
               __half *__restrict__ dst, int dst_ld, float *__restrict__ inv) {
+    pdl_begin();
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= nrows) return;
@@ -375,7 +378,7 @@ int launch_mode(const FfnArgs &a, int num_sms, cudaStream_t st) {
     if (cudaFuncSetAttribute(gemv_tma<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return -1;
     const int ipg = MODE == kGateUp ? (a.I_max + kIB - 1) / kIB : a.H / kMB;
-    gemv_tma<MODE><<<num_sms, kThreads, smem, st>>>(a, ipg, nst, stride);
+    launch_pdl(gemv_tma<MODE>, dim3(num_sms), dim3(kThreads), smem, st, a, ipg, nst, stride);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -384,14 +387,14 @@ int launch_mode(const FfnArgs &a, int num_sms, cudaStream_t st) {
 int launch_ffn_gemv(const FfnArgs &a, int num_sms, cudaEvent_t mid, cudaStream_t st) {
     int n = 0, r;
     // tokens -> scaled fp16 (gate/up activations)
-    prep_rows_f16<<<(a.T + 7) / 8, 256, 0, st>>>(a.x, a.H, a.T, a.H, a.T, a.H, a.xh, a.H, a.xinv);
+    launch_pdl(prep_rows_f16, dim3((a.T + 7) / 8), dim3(256), 0, st, a.x, a.H, a.T, a.H, a.T, a.H, a.xh, a.H, a.xinv);
     ++n;
     if ((r = launch_mode<kGateUp>(a, num_sms, st)) < 0) return r;
     n += r;
     if (mid) cudaEventRecord(mid, st);
     // h rows -> scaled fp16 (down activations); shared rows (from T*k on) have I_s columns
-    prep_rows_f16<<<(a.rows + 7) / 8, 256, 0, st>>>(a.h, a.I_max, a.rows, a.I, a.T * a.top_k, a.I_s, a.hh, a.I_max,
-                                                    a.hinv);
+    launch_pdl(prep_rows_f16, dim3((a.rows + 7) / 8), dim3(256), 0, st, (const __nv_bfloat16 *)a.h, a.I_max, a.rows,
+               a.I, a.T * a.top_k, a.I_s, a.hh, a.I_max, a.hinv);
     ++n;
     if ((r = launch_mode<kDown>(a, num_sms, st)) < 0) return r;
     n += r;

@@ -96,7 +96,7 @@ extern "C" int coli_moe_route_static(const void *x_bf16, int32_t T, int32_t H, c
     cudaGetLastError();
     const int n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
                                 d->scratch, idx_out, weights_out, d->scratch + kMaxScores, kMaxPartials, d->num_sms,
-                                static_cast<cudaStream_t>(cuda_stream));
+                                nullptr, 0, static_cast<cudaStream_t>(cuda_stream));
     if (n < 0) {
         set_create_error("route_static: kernel launch failed: %s", cudaGetErrorString(cudaGetLastError()));
         return COLI_ERR_CUDA;

@@ -12,6 +12,7 @@ namespace colimoe {
 namespace {
 
 __global__ void permute_count(const int32_t *__restrict__ idx, int n, int32_t *__restrict__ cnt) {
+    pdl_begin();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
         atomicAdd(&cnt[idx[i]], 1);
 }
@@ -54,6 +55,7 @@ __global__ void __launch_bounds__(1024)
 permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__restrict__ touched,
              int32_t *__restrict__ touched_cost, int32_t *__restrict__ n_touched, int E, int shared_rows,
              int cost_tokens, NtileLayout nl, int ntile) {
+    pdl_begin();
     __shared__ int smem[33];
     __shared__ int s_nt;
     const int G = E + 1;
@@ -98,10 +100,18 @@ permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__re
         const int ex_s = block_exclusive_scan(ns, smem, &tot_s);
         const int ex_l = block_exclusive_scan(nlg, smem, &tot_l);
         if (u < nt) {
+            const int g = touched[u], o = off[g];
             nl.prefix_small[u] = c_small + ex_s;
             nl.prefix_large[u] = c_large + ex_l;
-            for (int r = 0; r < ns; ++r) nl.owner_small[c_small + ex_s + r] = u;
-            for (int r = 0; r < nlg; ++r) nl.owner_large[c_large + ex_l + r] = u;
+            for (int r = 0; r < ns; ++r) {
+                nl.owner_small[c_small + ex_s + r] = u;
+                nl.rec_small[c_small + ex_s + r] = make_int2(o + r * ntile, g | (min(ntile, c - r * ntile) << 16));
+            }
+            for (int r = 0; r < nlg; ++r) {
+                nl.owner_large[c_large + ex_l + r] = u;
+                nl.rec_large[c_large + ex_l + r] =
+                    make_int2(o + r * 2 * ntile, g | (min(2 * ntile, c - r * 2 * ntile) << 16));
+            }
         }
         c_small += tot_s;
         c_large += tot_l;
@@ -109,6 +119,8 @@ permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__re
     if (threadIdx.x == 0) {
         nl.prefix_small[nt] = c_small;
         nl.prefix_large[nt] = c_large;
+        nl.count[0] = c_small;
+        nl.count[1] = c_large;
     }
 }
 
@@ -117,6 +129,7 @@ permute_scan(int32_t *__restrict__ cnt, int32_t *__restrict__ off, int32_t *__re
 __global__ void __launch_bounds__(256)
 permute_scatter(const int32_t *__restrict__ idx, int T, int E, int top_k, const int32_t *__restrict__ cnt,
                 const int32_t *__restrict__ off, int32_t *__restrict__ src_token, int32_t *__restrict__ inv_row) {
+    pdl_begin();
     const int e = blockIdx.x;
     if (e == E) {
         const int base = off[E];
@@ -158,6 +171,7 @@ permute_scatter(const int32_t *__restrict__ idx, int T, int E, int top_k, const 
 __global__ void __launch_bounds__(256)
 permute_gather(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
                __nv_bfloat16 *__restrict__ xp) {
+    pdl_begin();
     const int vec_per_row = H / 8;
     const size_t total = (size_t)rows * vec_per_row;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
@@ -174,15 +188,16 @@ int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared
                    int H, bool gather, int cost_tokens, int ntile, Workspace &ws, cudaStream_t st) {
     const int n = T * top_k;
     const int rows = n + (with_shared ? T : 0);
-    if (cudaMemsetAsync(ws.cnt, 0, sizeof(int32_t) * (E + 1), st) != cudaSuccess) return -1;
-    permute_count<<<(n + 255) / 256, 256, 0, st>>>(idx, n, ws.cnt);
-    permute_scan<<<1, 1024, 0, st>>>(ws.cnt, ws.off, ws.touched, ws.touched_cost, ws.n_touched, E,
-                                     with_shared ? T : 0, cost_tokens, ntile_layout(ws.tile_sched, E, rows), ntile);
-    permute_scatter<<<E + 1, 256, 0, st>>>(idx, T, E, top_k, ws.cnt, ws.off, ws.src_token, ws.inv_row);
+    // ws.cnt was cleared by the router's last kernel
+    launch_pdl(permute_count, dim3((n + 255) / 256), dim3(256), 0, st, idx, n, ws.cnt);
+    launch_pdl(permute_scan, dim3(1), dim3(1024), 0, st, ws.cnt, ws.off, ws.touched, ws.touched_cost, ws.n_touched, E,
+               with_shared ? T : 0, cost_tokens, ntile_layout(ws.tile_sched, E, rows), ntile);
+    launch_pdl(permute_scatter, dim3(E + 1), dim3(256), 0, st, idx, T, E, top_k, (const int32_t *)ws.cnt,
+               (const int32_t *)ws.off, ws.src_token, ws.inv_row);
     if (!gather) return cudaPeekAtLastError() == cudaSuccess ? 3 : -1;
     const size_t vecs = (size_t)rows * (H / 8);
     const int blocks = (int)((vecs + 255) / 256 < 65536 ? (vecs + 255) / 256 : 65536);
-    permute_gather<<<blocks, 256, 0, st>>>(x, H, ws.src_token, rows, ws.xp);
+    launch_pdl(permute_gather, dim3(blocks), dim3(256), 0, st, x, H, (const int32_t *)ws.src_token, rows, ws.xp);
     return cudaPeekAtLastError() == cudaSuccess ? 4 : -1;
 }
 

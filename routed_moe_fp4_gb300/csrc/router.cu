@@ -30,6 +30,7 @@ constexpr int kSmallWarps = 8;
 __global__ void __launch_bounds__(kSmallWarps * 32)
 router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const float *__restrict__ wr,
                     int E, float *__restrict__ scores) {
+    pdl_begin();
     __shared__ float part[kSmallWarps][kSmallTok];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x;
@@ -92,6 +93,7 @@ constexpr int kTileT = 64, kTileE = 64, kTileK = 32;
 __global__ void __launch_bounds__(256)
 router_logits_tiled(const __nv_bfloat16 *__restrict__ x, int T, int H, const float *__restrict__ wr,
                     int E, int hs, float *__restrict__ out) {
+    pdl_begin();
     __shared__ float xs[kTileK][kTileT + 4];
     __shared__ float ws[kTileK][kTileE + 4];
     const int tid = threadIdx.x;
@@ -156,6 +158,7 @@ router_logits_tiled(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
 
 __global__ void __launch_bounds__(256)
 router_split_reduce(const float *__restrict__ part, int n, int splits, float *__restrict__ scores) {
+    pdl_begin();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         float a = part[i];
         for (int z = 1; z < splits; ++z) a += part[(size_t)z * n + i];
@@ -168,7 +171,10 @@ router_split_reduce(const float *__restrict__ part, int n, int splits, float *__
 template <int NPL>
 __global__ void __launch_bounds__(256)
 router_topk(const float *__restrict__ scores, const float *__restrict__ bias, int T, int E, int top_k,
-            int32_t *__restrict__ idx, float *__restrict__ w) {
+            int32_t *__restrict__ idx, float *__restrict__ w, int32_t *__restrict__ zero, int n_zero) {
+    pdl_begin();
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_zero; i += blockDim.x) zero[i] = 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
@@ -245,11 +251,12 @@ router_topk(const float *__restrict__ scores, const float *__restrict__ bias, in
 
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
                   int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
-                  int num_sms, cudaStream_t st) {
+                  int num_sms, int32_t *zero, int n_zero, cudaStream_t st) {
     int n = 0;
+    if (!zero) n_zero = 0;
     if (T < 64) {
         dim3 grid(E, (T + kSmallTok - 1) / kSmallTok);
-        router_logits_small<<<grid, kSmallWarps * 32, 0, st>>>(x, T, H, router_w, E, scores);
+        launch_pdl(router_logits_small, grid, dim3(kSmallWarps * 32), 0, st, x, T, H, router_w, E, scores);
         ++n;
     } else {
         const int tiles = ((T + kTileT - 1) / kTileT) * ((E + kTileE - 1) / kTileE);
@@ -260,23 +267,21 @@ int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, c
         const int hs = ((chunks + splits - 1) / splits) * kTileK;
         splits = (H + hs - 1) / hs;
         dim3 grid((T + kTileT - 1) / kTileT, (E + kTileE - 1) / kTileE, splits);
-        router_logits_tiled<<<grid, 256, 0, st>>>(x, T, H, router_w, E, hs, splits > 1 ? partial : scores);
+        launch_pdl(router_logits_tiled, grid, dim3(256), 0, st, x, T, H, router_w, E, hs,
+                   splits > 1 ? partial : scores);
         ++n;
         if (splits > 1) {
             const int cnt = T * E;
-            router_split_reduce<<<std::min((cnt + 255) / 256, 4 * num_sms), 256, 0, st>>>(partial, cnt, splits,
-                                                                                          scores);
+            launch_pdl(router_split_reduce, dim3(std::min((cnt + 255) / 256, 4 * num_sms)), dim3(256), 0, st,
+                       (const float *)partial, cnt, splits, scores);
             ++n;
         }
     }
     const int npl = (E + 31) / 32;
     const dim3 grid((T + 7) / 8);
-    if (npl <= 1)       router_topk<1><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
-    else if (npl <= 2)  router_topk<2><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
-    else if (npl <= 4)  router_topk<4><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
-    else if (npl <= 8)  router_topk<8><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
-    else if (npl <= 16) router_topk<16><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
-    else                router_topk<32><<<grid, 256, 0, st>>>(scores, router_b, T, E, top_k, idx, w);
+    auto topk = npl <= 1 ? router_topk<1> : npl <= 2 ? router_topk<2> : npl <= 4 ? router_topk<4>
+              : npl <= 8 ? router_topk<8> : npl <= 16 ? router_topk<16> : router_topk<32>;
+    launch_pdl(topk, grid, dim3(256), 0, st, (const float *)scores, router_b, T, E, top_k, idx, w, zero, n_zero);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }
