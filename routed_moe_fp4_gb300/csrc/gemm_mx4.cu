@@ -22,8 +22,9 @@
 // (warp 1), scale loaders (warps 2-5; weight row 32q + i reads its scales from lane 32q + i,
 // column (word) * 4 + q; activation row n from lane 32q + n % 32, column n / 32 of its word, in
 // every lane quarter q; the words of one stage sit 4 columns apart; their loads run four stages
-// ahead), epilogue (warps 6-9). Four stages, double-buffered accumulators, bounded waits. A K that
-// is not a multiple of 256 ends with a half stage.
+// ahead), epilogue (warps 6-9). Four stages, double-buffered accumulators, bounded waits. A stage
+// covers 256 K (512 K for down tiles of up to 16 rows, which leave half of the slot free
+// otherwise); the last stage of a K that is not a multiple of it is partial.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -64,9 +65,11 @@ struct Mx4Params {
     int *err;
 };
 
+// A down tile of at most 16 rows uses wide stages: 512 K, two 128-byte chunks of weights (in the
+// A0 and A1 slots) and of activation terms (two halves of the B slot), eight MMAs.
 struct TileInfo {
-    int g, mt, row0, n_valid, Ig, K, nk, box, bh;
-    bool valid, shared;
+    int g, mt, row0, n_valid, Ig, K, nk, box, bh, kst;
+    bool valid, shared, wide;
     size_t ge;
 };
 
@@ -86,23 +89,30 @@ __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 
     ti.n_valid = rec.y >> 16;
     ti.valid = p.mode == kGateUp ? ti.mt * BM < ti.Ig : true;
     ti.K = p.mode == kGateUp ? p.H : ti.Ig;
-    ti.nk = (ti.K + BK - 1) / BK;
     ti.box = ti.n_valid <= 16 ? 0 : 1;
     ti.bh = 16 << ti.box;
+    ti.wide = p.mode == kDown && ti.box == 0;
+    ti.kst = ti.wide ? 2 * BK : BK;
+    ti.nk = (ti.K + ti.kst - 1) / ti.kst;
     return ti;
 }
 
 // Scale words of one stage for one loader lane: its gate (a0) and up (a1) weight rows, and the
 // activation rows lane + 32c (c < nbc); nbc == 0 marks an empty ring slot.
+// In a wide stage a0 / a1 hold the weight words 0-1 / 2-3, and b[c] / b[c + 2] the words 0-1 / 2-3
+// of activation column c (c < 2).
 struct SfStage {
     uint32_t a0[2], a1[2], b[4][2];
     int nbc;
+    bool wide;
 };
 
 // Position of a scale loader in the (tile, stage) sequence of its block, with the row pointers of
 // the current tile.
 struct SfCursor {
-    int t, k, nk, K, nbc;
+    int t, k, nk, K, nbc, tA, tB;
+    bool wide;
+    int2 recA, recB;                    // records of the next two tiles (tA < tB), loaded ahead
     const uint8_t *wp0, *wp1, *bp[4];
 };
 
@@ -110,8 +120,18 @@ struct SfCursor {
 __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int total_tiles, int quad, int lane) {
     const bool gu = p.mode == kGateUp;
     for (; c.t < total_tiles; c.t += gridDim.x) {
-        const TileInfo ti = decode_tile(p, c.t, tile_rec(p, c.t, total_tiles));
+        const int2 rec = c.t == c.tA ? c.recA : c.t == c.tB ? c.recB : tile_rec(p, c.t, total_tiles);
+        const TileInfo ti = decode_tile(p, c.t, rec);
         if (!ti.valid) continue;
+        if (c.tB == c.t + (int)gridDim.x) {            // keep the next two records in flight
+            c.tA = c.tB;
+            c.recA = c.recB;
+        } else {
+            c.tA = c.t + gridDim.x;
+            c.recA = tile_rec(p, c.tA, total_tiles);
+        }
+        c.tB = c.t + 2 * gridDim.x;
+        c.recB = tile_rec(p, c.tB, total_tiles);
         const int kb_row = ti.K / 32, kba = p.act_ld / 32;
         const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
         const int rpe = gu ? 2 * ti.Ig : p.H;
@@ -129,6 +149,7 @@ __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int tot
         c.k = 0;
         c.nk = ti.nk;
         c.K = ti.K;
+        c.wide = ti.wide;
         return true;
     }
     return false;
@@ -140,22 +161,37 @@ __device__ __forceinline__ bool sf_next(const Mx4Params &p, SfCursor &c, int tot
     return sf_tile(p, c, total_tiles, quad, lane);
 }
 
-// Issues the loads of the cursor's stage: 8 scale bytes per row (4 in a final half stage; the
-// missing word reads as scale 1).
+// Issues the loads of the cursor's stage: 8 scale bytes per row (16 in a wide stage; fewer in the
+// last stage of a K that is not a multiple of the stage; a missing word reads as scale 1).
 __device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStage &s, int n_a) {
-    const bool half = (c.K - c.k * BK) < BK;
+    const int kst = c.wide ? 2 * BK : BK;
+    const int nw = min(kst, c.K - c.k * kst) / 128;         // valid words of this stage (1 to 4)
+    const int w0 = c.k * (kst / 128);
     auto ld = [&](const uint8_t *q, int w) -> uint32_t {
-        return (q && !(half && w == 1)) ? __ldg(reinterpret_cast<const uint32_t *>(q) + 2 * c.k + w)
-                                        : 0x7F7F7F7Fu;
+        return (q && w < nw) ? __ldg(reinterpret_cast<const uint32_t *>(q) + w0 + w) : 0x7F7F7F7Fu;
     };
+    if (c.wide) {
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-        s.a0[w] = ld(c.wp0, w);
-        s.a1[w] = n_a > 1 ? ld(c.wp1, w) : 0x7F7F7F7Fu;
+        for (int w = 0; w < 2; ++w) {
+            s.a0[w] = ld(c.wp0, w);
+            s.a1[w] = ld(c.wp0, w + 2);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) s.b[q][w] = ld(c.bp[q], w);
+            for (int q = 0; q < 2; ++q) {
+                s.b[q][w] = ld(c.bp[q], w);
+                s.b[q + 2][w] = ld(c.bp[q], w + 2);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            s.a0[w] = ld(c.wp0, w);
+            s.a1[w] = n_a > 1 ? ld(c.wp1, w) : 0x7F7F7F7Fu;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s.b[q][w] = ld(c.bp[q], w);
+        }
     }
     s.nbc = c.nbc;
+    s.wide = c.wide;
 }
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -272,7 +308,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
                 const TileInfo ti = decode_tile(p, t, cur);
                 if (!ti.valid) continue;
-                const uint32_t tx = n_a * kASmem + kTerms * ti.bh * (BK / 2);
+                const uint32_t bbytes = kTerms * ti.bh * (BK / 2);   // one 128-byte K chunk of the terms
                 const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
                 const int rpe = gu ? 2 * ti.Ig : p.H;
                 const int arow = (int)ti.ge * rpe + ti.mt * BM;
@@ -283,12 +319,19 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                         break;
                     const uint32_t fb = ptx::smem_addr(&tma_full[s]);
                     const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
-                    ptx::mbar_arrive_expect_tx(fb, tx);
-                    ptx::tma_load_2d_hint(st + kOffA0, ta, k * (BK / 2), arow, fb, pol);
-                    if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, k * (BK / 2), arow + ti.Ig, fb, pol);
-                    for (int tt = 0; tt < kTerms; ++tt)
-                        ptx::tma_load_2d(st + kOffB + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box], k * (BK / 2),
-                                         ti.row0, fb);
+                    const int x0 = k * (ti.kst / 2);                      // byte offset along K
+                    const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;   // second K chunk
+                    ptx::mbar_arrive_expect_tx(fb, (gu || two ? 2 : 1) * kASmem + (two ? 2 : 1) * bbytes);
+                    ptx::tma_load_2d_hint(st + kOffA0, ta, x0, arow, fb, pol);
+                    if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, x0, arow + ti.Ig, fb, pol);
+                    if (two) ptx::tma_load_2d_hint(st + kOffA1, ta, x0 + BK / 2, arow, fb, pol);
+#pragma unroll
+                    for (int tt = 0; tt < kTerms; ++tt) {
+                        ptx::tma_load_2d(st + kOffB + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box], x0, ti.row0, fb);
+                        if (two)
+                            ptx::tma_load_2d(st + kOffB + bbytes + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box],
+                                             x0 + BK / 2, ti.row0, fb);
+                    }
                 }
             }
         }
@@ -312,7 +355,6 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 const int n_mma = kTerms * ti.bh;
                 const uint32_t id0 = idesc_mx4(n_mma, 0), id2 = idesc_mx4(n_mma, 2);
                 const uint32_t d0 = tmem + buf * kAccCols, d1 = d0 + (uint32_t)n_mma;
-                const int nfull = ti.K / BK;                  // full stages; a half stage may follow
                 uint32_t acc = 0;
                 bool ok = true;
                 for (int k = 0; k < ti.nk; ++k, ++it) {
@@ -328,17 +370,34 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     const uint64_t a0 = desc0 + (uint64_t)(s * (kStageBytes >> 4));
                     const uint64_t a1 = a0 + (kOffA1 >> 4), b = a0 + (kOffB >> 4);
                     const uint32_t sfa = tmem + kSfCol0 + s * kSfStage, sfb = sfa + 16;
+                    const int nsteps = min(ti.kst, ti.K - k * ti.kst) / 64;   // 2, 4, 6 or 8
                     auto step = [&](int j) {
                         const uint32_t id = (j & 1) ? id2 : id0;
-                        mma_mx4(d0, a0 + 2 * j, b + 2 * j, id, sfa + 4 * (j >> 1), sfb + 4 * (j >> 1), acc);
-                        if (gu) mma_mx4(d1, a1 + 2 * j, b + 2 * j, id, sfa + 8 + 4 * (j >> 1), sfb + 4 * (j >> 1), acc);
+                        const uint32_t sw = 4 * (j >> 1);                  // scale word j / 2
+                        if (gu) {
+                            mma_mx4(d0, a0 + 2 * j, b + 2 * j, id, sfa + sw, sfb + sw, acc);
+                            mma_mx4(d1, a1 + 2 * j, b + 2 * j, id, sfa + 8 + sw, sfb + sw, acc);
+                        } else if (j < 4) {
+                            mma_mx4(d0, a0 + 2 * j, b + 2 * j, id, sfa + sw, sfb + sw, acc);
+                        } else {                                           // second chunk of a wide stage
+                            constexpr uint64_t kHalfB = (kTerms * 16 * (BK / 2)) >> 4;
+                            mma_mx4(d0, a1 + 2 * (j - 4), b + kHalfB + 2 * (j - 4), id, sfa + sw, sfb + sw, acc);
+                        }
                         acc = 1;
                     };
                     step(0);
                     step(1);
-                    if (k < nfull) {
+                    if (nsteps > 2) {
                         step(2);
                         step(3);
+                    }
+                    if (!gu && nsteps > 4) {
+                        step(4);
+                        step(5);
+                        if (nsteps > 6) {
+                            step(6);
+                            step(7);
+                        }
                     }
                     ptx::mma_commit(ptx::smem_addr(&empty[s]));
                 }
@@ -358,6 +417,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         SfCursor cur;
         cur.t = blockIdx.x;
+        cur.tA = cur.tB = -1;
         bool live = sf_tile(p, cur, total_tiles, quad, lane);
         SfStage ring[kSfAhead];
 #pragma unroll
@@ -385,13 +445,26 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 }
                 ptx::tc_fence_after();
                 const uint32_t col = lane_base + kSfCol0 + s * kSfStage;
+                if (!gu && ring[d].wide) {   // words 0-3, 4 columns apart
 #pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
-                    if (n_a > 1) tmem_st_x1(col + 8 + 4 * w + quad, ring[d].a1[w]);
+                    for (int w = 0; w < 2; ++w) {
+                        tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
+                        tmem_st_x1(col + 8 + 4 * w + quad, ring[d].a1[w]);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (c < ring[d].nbc) tmem_st_x1(col + 16 + 4 * w + c, ring[d].b[c][w]);
+                        for (int c = 0; c < 2; ++c) {
+                            tmem_st_x1(col + 16 + 4 * w + c, ring[d].b[c][w]);
+                            tmem_st_x1(col + 24 + 4 * w + c, ring[d].b[c + 2][w]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
+                        if (n_a > 1) tmem_st_x1(col + 8 + 4 * w + quad, ring[d].a1[w]);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (c < ring[d].nbc) tmem_st_x1(col + 16 + 4 * w + c, ring[d].b[c][w]);
+                    }
                 }
                 tmem_st_wait();
                 ptx::tc_fence_before();
