@@ -259,7 +259,11 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
          const __grid_constant__ BMaps4 tm_b, const Mx4Params p) {
-    pdl_trigger();
+    // The kernel before this one in the stream (quant_x4_rows, or the gate/up launch before the
+    // down launch) signals its dependents only after its own dependency wait, so every kernel up
+    // to the permutation has completed when this one starts: its tile records can be read, and the
+    // first weight stages issued, before the wait. Activation terms and scales, and all writes,
+    // come after it.
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
@@ -293,47 +297,77 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_wait();   // everything above is on-chip set-up
-    const int total_tiles = p.m_tiles * *p.ntile_count;
+    const int total_tiles = p.m_tiles * *p.ntile_count;   // a permutation output: see above
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             ptx::prefetch_tmap(&tm_a_routed);
+            ptx::prefetch_tmap(&tm_a_shared);
             const uint64_t pol = ptx::policy_evict_first();
+            // stage k of tile ti into slot s: the weights (A, with the stage's byte count) and the
+            // activation terms (B) are issued separately
+            auto issue_a = [&](const TileInfo &ti, int k, int s) {
+                const uint32_t bbytes = kTerms * ti.bh * (BK / 2);   // one 128-byte K chunk of the terms
+                const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
+                const int rpe = gu ? 2 * ti.Ig : p.H;
+                const int arow = (int)ti.ge * rpe + ti.mt * BM;
+                const uint32_t fb = ptx::smem_addr(&tma_full[s]);
+                const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
+                const int x0 = k * (ti.kst / 2);                      // byte offset along K
+                const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;   // second K chunk
+                ptx::mbar_arrive_expect_tx(fb, (gu || two ? 2 : 1) * kASmem + (two ? 2 : 1) * bbytes);
+                ptx::tma_load_2d_hint(st + kOffA0, ta, x0, arow, fb, pol);
+                if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, x0, arow + ti.Ig, fb, pol);
+                if (two) ptx::tma_load_2d_hint(st + kOffA1, ta, x0 + BK / 2, arow, fb, pol);
+            };
+            auto issue_b = [&](const TileInfo &ti, int k, int s) {
+                const uint32_t bbytes = kTerms * ti.bh * (BK / 2);
+                const uint32_t fb = ptx::smem_addr(&tma_full[s]);
+                const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
+                const int x0 = k * (ti.kst / 2);
+                const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;
+#pragma unroll
+                for (int tt = 0; tt < kTerms; ++tt) {
+                    ptx::tma_load_2d(st + kOffB + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box], x0, ti.row0, fb);
+                    if (two)
+                        ptx::tma_load_2d(st + kOffB + bbytes + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box],
+                                         x0 + BK / 2, ti.row0, fb);
+                }
+            };
+            // before the wait: the weights of the first stages of the first tile (all slots are free)
+            int t0 = blockIdx.x, pre = 0;
+            int2 rec = tile_rec(p, t0, total_tiles);
+            TileInfo ti0 = decode_tile(p, t0, rec);
+            while (t0 < total_tiles && !ti0.valid) {
+                t0 += gridDim.x;
+                ti0 = decode_tile(p, t0, tile_rec(p, t0, total_tiles));
+            }
+            if (t0 < total_tiles) {
+                pre = min(NS, ti0.nk);
+                for (int k = 0; k < pre; ++k) issue_a(ti0, k, k);
+            }
+            pdl_wait();
+            pdl_trigger();
+            for (int k = 0; k < pre; ++k) issue_b(ti0, k, k);
             uint32_t it = 0;
-            int2 rec = tile_rec(p, blockIdx.x, total_tiles);
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
                 const int2 cur = rec;
                 rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
                 const TileInfo ti = decode_tile(p, t, cur);
                 if (!ti.valid) continue;
-                const uint32_t bbytes = kTerms * ti.bh * (BK / 2);   // one 128-byte K chunk of the terms
-                const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
-                const int rpe = gu ? 2 * ti.Ig : p.H;
-                const int arow = (int)ti.ge * rpe + ti.mt * BM;
                 for (int k = 0; k < ti.nk; ++k, ++it) {
+                    if (t == t0 && k < pre) continue;             // issued above
                     const int s = it % NS;
                     if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
                                         abort_flag))
                         break;
-                    const uint32_t fb = ptx::smem_addr(&tma_full[s]);
-                    const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
-                    const int x0 = k * (ti.kst / 2);                      // byte offset along K
-                    const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;   // second K chunk
-                    ptx::mbar_arrive_expect_tx(fb, (gu || two ? 2 : 1) * kASmem + (two ? 2 : 1) * bbytes);
-                    ptx::tma_load_2d_hint(st + kOffA0, ta, x0, arow, fb, pol);
-                    if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, x0, arow + ti.Ig, fb, pol);
-                    if (two) ptx::tma_load_2d_hint(st + kOffA1, ta, x0 + BK / 2, arow, fb, pol);
-#pragma unroll
-                    for (int tt = 0; tt < kTerms; ++tt) {
-                        ptx::tma_load_2d(st + kOffB + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box], x0, ti.row0, fb);
-                        if (two)
-                            ptx::tma_load_2d(st + kOffB + bbytes + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box],
-                                             x0 + BK / 2, ti.row0, fb);
-                    }
+                    issue_a(ti, k, s);
+                    issue_b(ti, k, s);
                 }
             }
+        } else {
+            pdl_wait();
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
@@ -418,7 +452,14 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         SfCursor cur;
         cur.t = blockIdx.x;
         cur.tA = cur.tB = -1;
-        bool live = sf_tile(p, cur, total_tiles, quad, lane);
+        bool live = sf_tile(p, cur, total_tiles, quad, lane);   // tile records: readable before the wait
+        if (live) {   // this lane's weight-scale rows of the first tile into L2 meanwhile
+            for (int o = 0; o < cur.K / 32; o += 128) {
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(cur.wp0 + o));
+                if (n_a > 1) asm volatile("prefetch.global.L2 [%0];" ::"l"(cur.wp1 + o));
+            }
+        }
+        pdl_wait();
         SfStage ring[kSfAhead];
 #pragma unroll
         for (int d = 0; d < kSfAhead; ++d) {
@@ -479,6 +520,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------------ epilogue
+        pdl_wait();
         const int quad = warp & 3;
         const int m = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
@@ -555,7 +597,10 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
 __global__ void __launch_bounds__(256)
 quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
               uint8_t *__restrict__ xq, uint8_t *__restrict__ xs) {
-    pdl_begin();
+    // signals the next kernel (the gate/up GEMM) only after the wait: that kernel reads the
+    // permutation's tile records before its own wait
+    pdl_wait();
+    pdl_trigger();
     const int nb = H / 32;
     const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long)rows * nb) return;
