@@ -144,20 +144,40 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     int launches = 0, n;
     const FfnKind ffn = pick_ffn(h, T, top_k, packed, shared);
     const bool gemm = ffn == kFfnBf16;
+    const int ntile = ffn == kFfnMx ? kNtileMx : ffn == kFfnMx4 ? kNtileMx4 : 0;
+    const int rows = T * top_k + (with_shared ? T : 0);
     const bool prof = h->profiling;
     h->stage_valid = false;
     if (prof) cudaEventRecord(h->ev[0], st);
 
-    n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
-                      ws.scores, ws.idx, ws.w, ws.logit_part, ws.logit_part_floats, h->num_sms, ws.cnt, E + 1, st);
-    if (n < 0) goto launch_fail;
-    launches += n;
-    if (prof) cudaEventRecord(h->ev[1], st);
-    n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, gemm,
-                       kGemvCostTokens,
-                       ffn == kFfnMx ? kNtileMx : ffn == kFfnMx4 ? kNtileMx4 : 0, ws, st);
-    if (n < 0) goto launch_fail;
-    launches += n;
+    if (T < kSmallRouteTokens) {
+        // logits, then top-k and the whole permutation in one single-block launch
+        n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
+                          ws.scores, ws.idx, ws.w, ws.logit_part, ws.logit_part_floats, h->num_sms, nullptr, 0, st,
+                          false);
+        if (n < 0) goto launch_fail;
+        launches += n;
+        if (prof) cudaEventRecord(h->ev[1], st);
+        n = launch_route_permute_small(router_bias, T, E, top_k, with_shared, kGemvCostTokens, ntile, ws, st);
+        if (n < 0) goto launch_fail;
+        launches += n;
+        if (gemm) {
+            n = launch_gather(static_cast<const __nv_bfloat16 *>(x_bf16), H, rows, ws, st);
+            if (n < 0) goto launch_fail;
+            launches += n;
+        }
+    } else {
+        n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
+                          ws.scores, ws.idx, ws.w, ws.logit_part, ws.logit_part_floats, h->num_sms, ws.cnt, E + 1,
+                          st);
+        if (n < 0) goto launch_fail;
+        launches += n;
+        if (prof) cudaEventRecord(h->ev[1], st);
+        n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, gemm,
+                           kGemvCostTokens, ntile, ws, st);
+        if (n < 0) goto launch_fail;
+        launches += n;
+    }
     {
         FfnArgs a{};
         a.routed = to_set(packed);
@@ -169,7 +189,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         a.I_max = h->I_max;
         a.T = T;
         a.top_k = top_k;
-        a.rows = T * top_k + (with_shared ? T : 0);
+        a.rows = rows;
         a.cnt = ws.cnt;
         a.off = ws.off;
         a.touched = ws.touched;

@@ -120,10 +120,18 @@ void set_create_error(const char *fmt, ...);
 // Launchers. Each returns the number of kernels it enqueued, or -1 on a launch error
 // (the CUDA error is then available from cudaGetLastError()).
 // `partial` ([partial_floats] fp32) holds split-K partial logits for larger T. `zero` (may be
-// null): n_zero ints the router's last kernel clears (the permute histogram).
+// null): n_zero ints the router's last kernel clears (the permute histogram). with_topk false:
+// the logits and scores only (route_permute_small takes the top-k).
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
                   int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
-                  int num_sms, int32_t *zero, int n_zero, cudaStream_t st);
+                  int num_sms, int32_t *zero, int n_zero, cudaStream_t st, bool with_topk = true);
+// Small T: the top-k of A1 and all of A2 (launch_permute with gather = false) in one launch.
+// Returns -2 outside T < kSmallRouteTokens, top_k <= 32, E <= 1024.
+constexpr int kSmallRouteTokens = 64;
+int launch_route_permute_small(const float *router_b, int T, int E, int top_k, bool with_shared, int cost_tokens,
+                               int ntile, Workspace &ws, cudaStream_t st);
+// Copies the activation rows into expert-grouped order (ws.xp) for the bf16 GEMM path.
+int launch_gather(const __nv_bfloat16 *x, int H, int rows, Workspace &ws, cudaStream_t st);
 // `gather`: also copy the activation rows into expert-grouped order (ws.xp). `cost_tokens`: rows
 // per unit of work cost in ws.touched_cost (see permute_scan). `ntile`: when non-zero, also write
 // the block-scaled GEMM's n-tile layout (NtileLayout, tiles of `ntile` and 2 * `ntile` rows) into

@@ -6,6 +6,7 @@
 // the lower expert index; w_j = s_j / S, S the fp32 sum of the chosen s in slot order, one
 // IEEE division each. Built without fast-math: every add, divide and expf is the IEEE/accurate one.
 #include "colimoe_internal.cuh"
+#include "topk.cuh"
 
 #include <float.h>
 
@@ -166,8 +167,7 @@ router_split_reduce(const float *__restrict__ part, int n, int splits, float *__
     }
 }
 
-// Top-k: one warp per token; lane l holds experts l, l+32, ...; k rounds of a warp arg-max on
-// (key descending, expert ascending).
+// Top-k: one warp per token (topk_token).
 template <int NPL>
 __global__ void __launch_bounds__(256)
 router_topk(const float *__restrict__ scores, const float *__restrict__ bias, int T, int E, int top_k,
@@ -178,80 +178,14 @@ router_topk(const float *__restrict__ scores, const float *__restrict__ bias, in
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + warp;
     if (t >= T) return;
-    float key[NPL], sc[NPL];
-    uint32_t taken = 0;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            sc[i] = scores[(size_t)t * E + e];
-            key[i] = __fadd_rn(sc[i], bias ? bias[e] : 0.0f);
-        } else {
-            sc[i] = 0.f;
-            key[i] = -INFINITY;
-            taken |= 1u << i;          // padding slots are never chosen
-        }
-    }
-    float s_sel[32];
-    int e_sel[32];
-    for (int j = 0; j < top_k; ++j) {
-        float bk = -INFINITY, bs = 0.f;
-        int be = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-            const int e = lane + 32 * i;
-            const bool free_ = !((taken >> i) & 1u);
-            if (free_ && (key[i] > bk || (key[i] == bk && e < be))) {
-                bk = key[i];
-                be = e;
-                bs = sc[i];
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-            if (ok > bk || (ok == bk && oe < be)) {
-                bk = ok;
-                be = oe;
-                bs = os;
-            }
-        }
-        if (be == INT_MAX) {           // only NaN keys left: take the lowest free expert
-            int cand = INT_MAX;
-            float cs = 0.f;
-#pragma unroll
-            for (int i = NPL - 1; i >= 0; --i)
-                if (!((taken >> i) & 1u)) { cand = lane + 32 * i; cs = sc[i]; }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const int oc = __shfl_xor_sync(0xffffffffu, cand, o);
-                const float os = __shfl_xor_sync(0xffffffffu, cs, o);
-                if (oc < cand) { cand = oc; cs = os; }
-            }
-            be = cand;
-            bs = cs;
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        s_sel[j] = bs;
-        e_sel[j] = be;
-    }
-    if (lane == 0) {
-        float S = 0.0f;
-        for (int j = 0; j < top_k; ++j) S = __fadd_rn(S, s_sel[j]);
-        for (int j = 0; j < top_k; ++j) {
-            idx[(size_t)t * top_k + j] = e_sel[j];
-            w[(size_t)t * top_k + j] = __fdiv_rn(s_sel[j], S);
-        }
-    }
+    topk_token<NPL>(scores, bias, E, top_k, t, lane, idx, w, nullptr);
 }
 
 }  // namespace
 
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
                   int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
-                  int num_sms, int32_t *zero, int n_zero, cudaStream_t st) {
+                  int num_sms, int32_t *zero, int n_zero, cudaStream_t st, bool with_topk) {
     int n = 0;
     if (!zero) n_zero = 0;
     if (T < 64) {
@@ -277,6 +211,7 @@ int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, c
             ++n;
         }
     }
+    if (!with_topk) return cudaPeekAtLastError() == cudaSuccess ? n : -1;
     const int npl = (E + 31) / 32;
     const dim3 grid((T + 7) / 8);
     auto topk = npl <= 1 ? router_topk<1> : npl <= 2 ? router_topk<2> : npl <= 4 ? router_topk<4>
