@@ -225,10 +225,10 @@ __device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t a) {
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+// Largest of 32 non-negative floats across the warp: their bit patterns order like unsigned
+// integers, so one integer warp reduction serves.
+__device__ __forceinline__ float warp_max_abs(float a) {
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
 }
 
 // UE8M0 byte for an E2M1 term of a block with maximum amax: |v| / 2^(s-127) < 4.
@@ -544,17 +544,16 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v0[j] = v1[j] = 0.f;
 #pragma unroll
-                for (int tt = 0; tt < kTerms; ++tt) {   // add the term columns
-                    uint32_t r[16];
+                for (int tt = 0; tt < kTerms; ++tt) {   // add the term columns (gate and up: one wait)
+                    uint32_t r[16], r1[16];
                     ptx::tmem_ld16(acc + tt * ti.bh + c0, r);
+                    if (gu) ptx::tmem_ld16(acc + ncols + tt * ti.bh + c0, r1);
                     ptx::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 16; ++j) v0[j] += __uint_as_float(r[j]);
                     if (gu) {
-                        ptx::tmem_ld16(acc + ncols + tt * ti.bh + c0, r);
-                        ptx::tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v1[j] += __uint_as_float(r[j]);
+                        for (int j = 0; j < 16; ++j) v1[j] += __uint_as_float(r1[j]);
                     }
                 }
                 for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j) {
@@ -566,7 +565,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     float v = __fdiv_rn(v0[j], 1.0f + expf(-v0[j])) * v1[j];
 #pragma unroll
                     for (int tt = 0; tt < kTerms; ++tt) {
-                        const uint32_t sb = e2m1_scale_byte(warp_max(fabsf(v)));
+                        const uint32_t sb = e2m1_scale_byte(warp_max_abs(fabsf(v)));
                         const float scale = __uint_as_float(sb << 23), inv = __uint_as_float((254u - sb) << 23);
                         float back, unused;
                         const uint32_t code = e2m1_pair(v * inv, 0.f, back, unused) & 0xF;

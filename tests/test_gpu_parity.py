@@ -105,6 +105,9 @@ def _custom(name, **kw):
     _custom("edge_ragged", T=37, H=384, E=16, top_k=3),
     _custom("edge_T1", T=1),
     _custom("edge_many_experts", T=9, E=300, top_k=8, H=256),
+    _custom("edge_k32_T63", T=63, E=64, top_k=32),        # largest single-block routing (63 x 32 slots)
+    _custom("edge_T64", T=64, E=16, top_k=4),             # smallest T of the multi-kernel routing
+    _custom("edge_E1024", T=5, E=1024, top_k=8, H=256),   # widest expert set (NPL = 32)
 ], ids=lambda w: w.name)
 def test_edge_cases(oracle, wl):
     inputs = S.make_inputs(wl)
