@@ -22,7 +22,8 @@
 // (warp 1), scale loaders (warps 2-5; weight row 32q + i reads its scales from lane 32q + i,
 // column (word) * 4 + q; activation row n from lane 32q + n % 32, column n / 32 of its word, in
 // every lane quarter q; the words of one stage sit 4 columns apart; their loads run four stages
-// ahead), epilogue (warps 6-9). Four stages, double-buffered accumulators, bounded waits. A stage
+// ahead), epilogue (warps 6-13: two per lane quarter, taking alternate 8-column groups of the
+// tile's tokens). Four stages, double-buffered accumulators, bounded waits. A stage
 // covers 256 K (512 K for down tiles of up to 16 rows, which leave half of the slot free
 // otherwise); the last stage of a K that is not a multiple of it is partial.
 #include <cuda.h>
@@ -38,7 +39,7 @@ constexpr int BM = 128, BK = 256, MK = 64;     // weight rows, K per stage, K pe
 constexpr int kBnGateUp = kNtileMx4, kBnDown = 2 * kNtileMx4;   // tokens per tile
 constexpr int kTerms = 4;                      // E2M1 terms per activation
 constexpr int NS = 4;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;                  // 14 warps: see the role list above
 constexpr uint32_t kASmem = BM * BK / 2;       // 16 KB: 128 rows x 256 packed codes
 constexpr uint32_t kBSmemMax = kTerms * 32 * (BK / 2);   // 16 KB: up to 4 terms x 32 rows
 constexpr uint32_t kOffA0 = 0, kOffA1 = kASmem, kOffB = 2 * kASmem;
@@ -48,6 +49,7 @@ constexpr uint32_t kAccCols = 128;             // per accumulator buffer
 constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 32 per stage
 constexpr uint32_t kSfStage = 32;
 constexpr int kSfAhead = 4;                   // stages the scale loads run ahead
+constexpr int kEpiWarps = 8;                  // two per TMEM lane quarter, alternate 8-column groups
 
 enum Mode { kGateUp = 0, kDown = 1 };
 
@@ -283,7 +285,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_addr(&acc_full[b]), 1);
-            ptx::mbar_init(ptx::smem_addr(&acc_empty[b]), 4);
+            ptx::mbar_init(ptx::smem_addr(&acc_empty[b]), kEpiWarps);
         }
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
@@ -522,6 +524,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         // ------------------------------------------------------------------ epilogue
         pdl_wait();
         const int quad = warp & 3;
+        const int half = (warp - 6) >> 2;             // this warp's 8-column groups: half, half + 2, ...
         const int m = quad * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t tcount = 0;
@@ -539,24 +542,24 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             const int mrow = ti.mt * BM + m;
             const uint32_t acc = lane_base + buf * kAccCols;
             const int ncols = kTerms * ti.bh;
-            for (int c0 = 0; c0 < ti.n_valid; c0 += 16) {
-                float v0[16], v1[16];
+            for (int c0 = 8 * half; c0 < ti.n_valid; c0 += 16) {
+                float v0[8], v1[8];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v0[j] = v1[j] = 0.f;
+                for (int j = 0; j < 8; ++j) v0[j] = v1[j] = 0.f;
 #pragma unroll
                 for (int tt = 0; tt < kTerms; ++tt) {   // add the term columns (gate and up: one wait)
-                    uint32_t r[16], r1[16];
-                    ptx::tmem_ld16(acc + tt * ti.bh + c0, r);
-                    if (gu) ptx::tmem_ld16(acc + ncols + tt * ti.bh + c0, r1);
+                    uint32_t r[8], r1[8];
+                    ptx::tmem_ld8(acc + tt * ti.bh + c0, r);
+                    if (gu) ptx::tmem_ld8(acc + ncols + tt * ti.bh + c0, r1);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) v0[j] += __uint_as_float(r[j]);
+                    for (int j = 0; j < 8; ++j) v0[j] += __uint_as_float(r[j]);
                     if (gu) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v1[j] += __uint_as_float(r1[j]);
+                        for (int j = 0; j < 8; ++j) v1[j] += __uint_as_float(r1[j]);
                     }
                 }
-                for (int j = 0; j < 16 && c0 + j < ti.n_valid; ++j) {
+                for (int j = 0; j < 8 && c0 + j < ti.n_valid; ++j) {
                     const size_t row = (size_t)ti.row0 + c0 + j;
                     if (!gu) {
                         p.y[row * p.H + mrow] = v0[j];
