@@ -56,6 +56,7 @@ enum Mode { kGateUp = 0, kDown = 1 };
 struct Mx4Params {
     int E, H, I, I_s, I_max, rows;
     int mode, m_tiles, bn;
+    int nbuf;                           // accumulator buffers: 2, or 1 when a gate/up tile needs 256 columns
     const int2 *ntile_rec;              // per n-tile: {first row, group | rows << 16}
     const int32_t *ntile_count;         // number of n-tiles
     const uint8_t *w_scales_routed, *w_scales_shared;
@@ -382,7 +383,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
                 const TileInfo ti = decode_tile(p, t, cur);
                 if (!ti.valid) continue;
-                const uint32_t buf = tcount & 1u, use = tcount >> 1;
+                const uint32_t buf = p.nbuf == 2 ? tcount & 1u : 0u, use = p.nbuf == 2 ? tcount >> 1 : tcount;
                 if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[buf]), (use & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
                                     abort_flag))
                     break;
@@ -534,7 +535,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             rec = tile_rec(p, t + gridDim.x, total_tiles);
             const TileInfo ti = decode_tile(p, t, cur);
             if (!ti.valid) continue;
-            const uint32_t buf = tcount & 1u, use = tcount >> 1;
+            const uint32_t buf = p.nbuf == 2 ? tcount & 1u : 0u, use = p.nbuf == 2 ? tcount >> 1 : tcount;
             if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[buf]), use & 1u, p.err, ptx::kErrWaitAccum, abort_flag))
                 break;
             ++tcount;
@@ -713,10 +714,14 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     CUtensorMap tar, tas;
     BMaps4 tb;
     // gate/up
+    // Many tokens per expert: gate/up tiles of 32 tokens (N = 128 per matrix, half the MMAs per
+    // token) with one accumulator buffer (gate + up fill 256 TMEM columns).
+    const bool gu32 = (long)a.T * a.top_k >= 16L * a.E;
     p.mode = kGateUp;
-    p.bn = kBnGateUp;
-    p.ntile_rec = nl.rec_small;
-    p.ntile_count = nl.count;
+    p.bn = gu32 ? kBnDown : kBnGateUp;
+    p.nbuf = gu32 ? 1 : 2;
+    p.ntile_rec = gu32 ? nl.rec_large : nl.rec_small;
+    p.ntile_count = gu32 ? nl.count + 1 : nl.count;
     p.m_tiles = (a.I_max + BM - 1) / BM;
     p.w_scales_routed = a.routed.gu_scales;
     p.w_scales_shared = a.shared.gu_scales;
@@ -733,6 +738,7 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     // down
     p.mode = kDown;
     p.bn = kBnDown;
+    p.nbuf = 2;
     p.ntile_rec = nl.rec_large;
     p.ntile_count = nl.count + 1;
     p.m_tiles = a.H / BM;
