@@ -180,6 +180,14 @@ COLI_API int32_t coli_moe_last_ffn_path(const coli_moe_t *h);
  * error) to *code and clears it. */
 COLI_API int coli_moe_device_error(coli_moe_t *h, int32_t *code);
 
+/* Limit, in nanoseconds, of the bounded barrier waits inside the COLI_FFN_GEMM_MXF4 kernels
+ * (0 restores the default of two seconds; negative values are rejected). It exists to exercise
+ * the failure path without a fault: with a limit far below a memory latency, a wait runs out,
+ * the kernel records its code in the device error word, lets its copies and MMAs in flight
+ * finish (with the full limit), frees TMEM and returns. The forward's output is then incomplete,
+ * the context stays usable, and later forwards with the default limit are correct. */
+COLI_API int coli_moe_set_wait_limit(coli_moe_t *h, int64_t ns);
+
 /* Stage timing. With profiling enabled (enable != 0) every forward records CUDA events on the
  * handle's stream between its stages; coli_moe_stage_times then synchronises the stream and
  * writes the last forward's stage durations in milliseconds to ms[0..COLI_STAGES-1]:

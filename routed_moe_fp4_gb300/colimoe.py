@@ -23,7 +23,7 @@ COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM, COLI_FFN_GEMM_BF16, COLI_FFN_GEMM_M
 EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "coli_moe_destroy",
             "coli_moe_last_error", "coli_moe_set_ffn_path", "coli_moe_debug_routing",
             "coli_moe_last_launch_count", "coli_moe_last_ffn_path", "coli_moe_set_profiling", "coli_moe_stage_times",
-            "coli_moe_device_error", "coli_moe_route_static")
+            "coli_moe_device_error", "coli_moe_set_wait_limit", "coli_moe_route_static")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
 
@@ -82,6 +82,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_moe_last_launch_count.restype = C.c_int32
     lib.coli_moe_last_ffn_path.argtypes = [vp]
     lib.coli_moe_last_ffn_path.restype = C.c_int32
+    lib.coli_moe_set_wait_limit.argtypes = [vp, C.c_int64]
+    lib.coli_moe_set_wait_limit.restype = C.c_int
     lib.coli_moe_set_profiling.argtypes = [vp, C.c_int32]
     lib.coli_moe_set_profiling.restype = C.c_int
     lib.coli_moe_stage_times.argtypes = [vp, C.POINTER(C.c_float)]
@@ -164,6 +166,10 @@ def coli_moe_last_launch_count(h) -> int:
 
 def coli_moe_last_ffn_path(h) -> int:
     return load().coli_moe_last_ffn_path(h)
+
+
+def coli_moe_set_wait_limit(h, ns: int) -> int:
+    return _check(h, load().coli_moe_set_wait_limit(h, ns))
 
 
 def coli_moe_set_profiling(h, enable: bool) -> int:
@@ -265,6 +271,10 @@ class MoELayer:
 
     def launches(self) -> int:
         return coli_moe_last_launch_count(self.h)
+
+    def set_wait_limit(self, ns: int) -> None:
+        """Limit of the FP4 path's barrier waits in ns (0 = default); a test hook for the failure path."""
+        coli_moe_set_wait_limit(self.h, ns)
 
     def ffn_path(self) -> int:
         """The FFN path the last forward ran (COLI_FFN_*)."""

@@ -24,6 +24,7 @@ struct coli_moe {
     bool last_shared = false;
     int32_t last_launches = 0;
     int32_t last_path = COLI_FFN_AUTO;
+    uint64_t wait_ns = 0;           // coli_moe_set_wait_limit (0 = default)
     bool profiling = false;
     bool stage_valid = false;
     cudaEvent_t ev[COLI_STAGES + 1] = {};
@@ -209,6 +210,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         a.hq = ws.hq;
         a.hqs = ws.hqs;
         a.err = ws.err;
+        a.wait_ns = h->wait_ns;
         if (ffn == kFfnMx || ffn == kFfnMx4) {   // the activation terms belong to the permute stage
             n = ffn == kFfnMx ? launch_quant_x(a, st) : launch_quant_x4(a, st);
             if (n < 0) goto launch_fail;
@@ -438,6 +440,12 @@ int coli_moe_debug_routing(coli_moe_t *h, coli_moe_routing *dst) {
 int32_t coli_moe_last_launch_count(const coli_moe_t *h) { return h ? h->last_launches : 0; }
 
 int32_t coli_moe_last_ffn_path(const coli_moe_t *h) { return h ? h->last_path : COLI_FFN_AUTO; }
+
+int coli_moe_set_wait_limit(coli_moe_t *h, int64_t ns) {
+    if (!h || ns < 0) return COLI_ERR_INVALID_ARG;
+    h->wait_ns = (uint64_t)ns;
+    return COLI_OK;
+}
 
 int coli_moe_device_error(coli_moe_t *h, int32_t *code) {
     if (!h || !code) return COLI_ERR_INVALID_ARG;

@@ -79,6 +79,7 @@ struct FfnArgs {
     float *y;                       // [rows][H]
     uint8_t *xq, *xqs, *hq, *hqs;   // block-scaled paths: activation terms and scales
     int *err;
+    uint64_t wait_ns;               // FP4 path: limit of the pipeline waits (0 = the default, 2 s)
 };
 
 // Programmatic dependent launch. Every kernel of the library is launched with programmatic

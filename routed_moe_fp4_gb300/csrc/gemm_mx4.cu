@@ -66,6 +66,7 @@ struct Mx4Params {
     uint8_t *hs;                        // [kTerms][rows][I_max/32]
     float *y;
     int *err;
+    uint64_t wait_ns;                   // limit of the pipeline waits (the drains always allow the full limit)
 };
 
 // A down tile of at most 16 rows uses wide stages: 512 K, two 128-byte chunks of weights (in the
@@ -363,12 +364,17 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     if (t == t0 && k < pre) continue;             // issued above
                     const int s = it % NS;
                     if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
-                                        abort_flag))
+                                        abort_flag, p.wait_ns))
                         break;
                     issue_a(ti, k, s);
                     issue_b(ti, k, s);
                 }
             }
+            // copies still in flight (only after a wait gave up): let them land before the block
+            // exits, with the full limit
+            const uint32_t issued = it > (uint32_t)pre ? it : (uint32_t)pre;
+            for (uint32_t i = issued > (uint32_t)NS ? issued - NS : 0; i < issued; ++i)
+                ptx::mbar_wait(ptx::smem_addr(&tma_full[i % NS]), (i / NS) & 1u, nullptr, 0, nullptr);
         } else {
             pdl_wait();
         }
@@ -385,7 +391,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 if (!ti.valid) continue;
                 const uint32_t buf = p.nbuf == 2 ? tcount & 1u : 0u, use = p.nbuf == 2 ? tcount >> 1 : tcount;
                 if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[buf]), (use & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
-                                    abort_flag))
+                                    abort_flag, p.wait_ns))
                     break;
                 ++tcount;
                 ptx::tc_fence_after();
@@ -397,8 +403,10 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 for (int k = 0; k < ti.nk; ++k, ++it) {
                     const int s = it % NS;
                     const uint32_t ph = (it / NS) & 1u;
-                    if (!ptx::mbar_wait(ptx::smem_addr(&tma_full[s]), ph, p.err, ptx::kErrWaitFull, abort_flag) ||
-                        !ptx::mbar_wait(ptx::smem_addr(&sf_full[s]), ph, p.err, ptx::kErrWaitFull, abort_flag)) {
+                    if (!ptx::mbar_wait(ptx::smem_addr(&tma_full[s]), ph, p.err, ptx::kErrWaitFull, abort_flag,
+                                        p.wait_ns) ||
+                        !ptx::mbar_wait(ptx::smem_addr(&sf_full[s]), ph, p.err, ptx::kErrWaitFull, abort_flag,
+                                        p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -483,7 +491,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 }
                 const int s = it % NS;
                 if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
-                                    abort_flag)) {
+                                    abort_flag, p.wait_ns)) {
                     run = false;
                     continue;
                 }
@@ -536,7 +544,8 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             const TileInfo ti = decode_tile(p, t, cur);
             if (!ti.valid) continue;
             const uint32_t buf = p.nbuf == 2 ? tcount & 1u : 0u, use = p.nbuf == 2 ? tcount >> 1 : tcount;
-            if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[buf]), use & 1u, p.err, ptx::kErrWaitAccum, abort_flag))
+            if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[buf]), use & 1u, p.err, ptx::kErrWaitAccum, abort_flag,
+                                p.wait_ns))
                 break;
             ++tcount;
             ptx::tc_fence_after();
@@ -707,6 +716,7 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     p.I_s = a.I_s;
     p.I_max = a.I_max;
     p.rows = a.rows;
+    p.wait_ns = a.wait_ns ? a.wait_ns : ptx::kWaitLimitNs;
     p.hq = a.hq;
     p.hs = a.hqs;
     p.y = a.y;

@@ -66,16 +66,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false after kWaitLimitNs (error recorded)
+// Waits for the phase with the given parity to complete; false after limit_ns (error recorded)
 // or as soon as *abort becomes non-zero.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *err, int code,
-                                          volatile int *abort = nullptr) {
+                                          volatile int *abort = nullptr, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (abort && *abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             record_error(err, code);
             if (abort) *abort = 1;
             return false;
