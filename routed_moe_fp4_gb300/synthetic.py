@@ -126,6 +126,9 @@ WORKLOADS: Dict[str, Workload] = {
     "decode": Workload("decode", 8, 4096, 256, 8, 2048, 2048, "normal", margin=1e-3),
     "prefill": Workload("prefill", 512, 4096, 256, 8, 2048, 2048, "normal"),
     "skewed": Workload("skewed", 4096, 7168, 256, 8, 2048, 2048, "zipf"),
+    # the larger V4 shape of the pages (hidden 7168, 384 experts, same MXFP4 layout); top-8 and
+    # I = I_s = 2048 as in the other workloads (the pages give neither for it)
+    "v4pro_decode": Workload("v4pro_decode", 8, 7168, 384, 8, 2048, 2048, "normal"),
 }
 SWEEP_T = (1, 2, 4, 16, 64, 128)
 for _t in SWEEP_T:

@@ -78,6 +78,13 @@ def test_prefill_sampled(oracle):
     _assert_ok(rep)
 
 
+def test_v4pro_decode_all_tokens(oracle):
+    """The V4-Pro shape (E = 384, H = 7168): every token against the oracle."""
+    inputs = S.make_inputs("v4pro_decode")
+    rep, _, _ = _run(oracle, inputs, AUTO)
+    _assert_ok(rep)
+
+
 def test_skewed_sampled(oracle):
     inputs = S.make_inputs("skewed")
     rep, _, routing = _run(oracle, inputs, AUTO, n_tokens=8)
