@@ -124,10 +124,11 @@ COLI_API int coli_moe_forward(coli_moe_t *h, const void *x_bf16, int32_t T,
                      const coli_mxfp4_experts *shared_expert,
                      int32_t top_k, void *out_bf16);
 
-/* The same forward with x and out in HOST memory: copies x to the device, runs the forward and
- * copies the result back, then synchronises the handle's stream before returning. Pinned host
- * buffers give asynchronous copies. Weights and router arguments are device pointers as above.
- * Uses a per-handle device staging buffer sized at create. */
+/* The same forward with x and out in HOST memory, synchronising the handle's stream before
+ * returning. Page-locked (pinned, device-mapped) buffers are used in place: a kernel reads x
+ * across the host link into a per-handle staging buffer and the combine writes out directly.
+ * Other host memory is copied to and from the staging buffers. Weights and router arguments are
+ * device pointers as above. */
 COLI_API int coli_moe_forward_host(coli_moe_t *h, const void *x_bf16_host, int32_t T,
                           const float *router_w, const float *router_bias,
                           const coli_mxfp4_experts *packed_experts,

@@ -371,14 +371,31 @@ int coli_moe_forward_host(coli_moe_t *h, const void *x_bf16_host, int32_t T, con
         return COLI_ERR_INVALID_ARG;
     }
     const size_t bytes = (size_t)T * h->cfg.hidden * sizeof(uint16_t);
-    if (cudaMemcpyAsync(h->ws.x_stage, x_bf16_host, bytes, cudaMemcpyHostToDevice, h->stream) != cudaSuccess) {
+    // Page-locked host buffers are device-mapped: a kernel pulls x across the host link into the
+    // staging buffer (one read of each byte; the forward reads x many times), and the combine
+    // writes out in place. Other host memory goes through copies.
+    cudaPointerAttributes ax, ao;
+    const bool mapped = cudaPointerGetAttributes(&ax, x_bf16_host) == cudaSuccess && ax.type == cudaMemoryTypeHost &&
+                        ax.devicePointer && aligned16(ax.devicePointer) &&
+                        cudaPointerGetAttributes(&ao, out_bf16_host) == cudaSuccess && ao.type == cudaMemoryTypeHost &&
+                        ao.devicePointer && aligned16(ao.devicePointer);
+    cudaGetLastError();
+    void *out_dev = h->ws.out_stage;
+    if (mapped) {
+        if (launch_copy(h->ws.x_stage, ax.devicePointer, bytes, h->num_sms, h->stream) < 0) {
+            set_err(h, "host-to-device copy kernel failed: %s", cudaGetErrorString(cudaGetLastError()));
+            return COLI_ERR_CUDA;
+        }
+        out_dev = ao.devicePointer;
+    } else if (cudaMemcpyAsync(h->ws.x_stage, x_bf16_host, bytes, cudaMemcpyHostToDevice, h->stream) != cudaSuccess) {
         set_err(h, "host-to-device copy failed: %s", cudaGetErrorString(cudaGetLastError()));
         return COLI_ERR_CUDA;
     }
     const int rc = forward_impl(h, h->ws.x_stage, T, router_w, router_bias, packed_experts, shared_expert, top_k,
-                                h->ws.out_stage);
+                                out_dev);
     if (rc != COLI_OK) return rc;
-    if (cudaMemcpyAsync(out_bf16_host, h->ws.out_stage, bytes, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess) {
+    if (!mapped &&
+        cudaMemcpyAsync(out_bf16_host, h->ws.out_stage, bytes, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess) {
         set_err(h, "device-to-host copy failed: %s", cudaGetErrorString(cudaGetLastError()));
         return COLI_ERR_CUDA;
     }

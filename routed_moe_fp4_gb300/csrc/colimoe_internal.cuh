@@ -174,6 +174,8 @@ __host__ __device__ inline NtileLayout ntile_layout(void *base, int E, int rows)
 int launch_ffn_gemv(const FfnArgs &a, int num_sms, cudaEvent_t mid, cudaStream_t st);
 int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T, int H, int top_k,
                    bool with_shared, __nv_bfloat16 *out, cudaStream_t st);
+// Device copy of `bytes` (a multiple of 16, both pointers 16-byte aligned), e.g. from mapped host memory.
+int launch_copy(void *dst, const void *src, size_t bytes, int num_sms, cudaStream_t st);
 
 // Block-scaled MXFP4 tcgen05 GEMM path (gemm_mx.cu): native E2M1 weights x E4M3 activation terms.
 bool mx_available();

@@ -34,7 +34,23 @@ combine_kernel(const float *__restrict__ y, const int32_t *__restrict__ inv_row,
     reinterpret_cast<uint2 *>(out + (size_t)t * H)[v] = packed;
 }
 
+// dst[0..bytes) = src[0..bytes), 16 bytes per thread step (both 16-byte aligned, bytes a multiple
+// of 16); used to pull x from device-mapped host memory.
+__global__ void __launch_bounds__(256) copy16(uint4 *__restrict__ dst, const uint4 *__restrict__ src, size_t n) {
+    pdl_begin();
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
 }  // namespace
+
+int launch_copy(void *dst, const void *src, size_t bytes, int num_sms, cudaStream_t st) {
+    const size_t n = bytes / 16;
+    const size_t blocks = (n + 255) / 256 < (size_t)num_sms * 4 ? (n + 255) / 256 : (size_t)num_sms * 4;
+    launch_pdl(copy16, dim3((unsigned)(blocks ? blocks : 1)), dim3(256), 0, st, static_cast<uint4 *>(dst),
+               static_cast<const uint4 *>(src), n);
+    return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+}
 
 int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T, int H, int top_k,
                    bool with_shared, __nv_bfloat16 *out, cudaStream_t st) {

@@ -188,16 +188,22 @@ def test_bad_arguments_rejected():
     layer.close()
 
 
-def test_forward_host_matches_device(oracle):
+@pytest.mark.parametrize("pinned", [True, False], ids=["mapped", "pageable"])
+def test_forward_host_matches_device(oracle, pinned):
+    """Host buffers give the device forward's bits, read in place when page-locked, else copied."""
     import torch
     from routed_moe_fp4_gb300 import colimoe as cm
     inputs = S.make_inputs("sweep_T4")
     outs, _, _ = P.run_gpu(inputs)
     layer = cm.MoELayer(inputs)
-    x_host = torch.from_numpy(inputs.x.view(np.int16)).pin_memory()
-    out_host = torch.zeros_like(x_host).pin_memory()
-    layer.forward_host(x_host, out_host)
-    assert np.array_equal(out_host.numpy().view(np.uint16), outs[0])
+    x_host = torch.from_numpy(inputs.x.view(np.int16).copy())
+    out_host = torch.zeros_like(x_host)
+    if pinned:
+        x_host, out_host = x_host.pin_memory(), out_host.pin_memory()
+    for _ in range(2):
+        out_host.zero_()
+        layer.forward_host(x_host, out_host)
+        assert np.array_equal(out_host.numpy().view(np.uint16), outs[0])
     layer.close()
 
 
