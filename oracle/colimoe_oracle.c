@@ -323,3 +323,101 @@ void coli_oracle_moe_forward(const uint16_t *x, int32_t T, int32_t H, int32_t E,
     free(slot);
     free(Y);
 }
+
+/* ------------------------------------------------------------------------------------
+ * Expert residency bank: S device slots, each holding one routed expert, and what one
+ * forward does to them. The pages keep the most used routed experts of each layer
+ * resident on the GPU, ranked by usage ("DeepSeek V4 Flash support -- CUDA/VRAM expert
+ * tiering", summary item 1), refill that cache in place, and for a batched prefill route
+ * on the device and refill a transient per-layer bank route-aware in slot-sized groups,
+ * one group's uploads overlapped with the neighbouring group ("the CUDA tier wired into
+ * the DeepSeek V4 engine", the engine-tier and prefill-MoE items).
+ *
+ * Readings (the pages give no rule beyond the above):
+ *  - Cache forward, when T*top_k or E (whichever is smaller) fits in S: touched experts
+ *    already resident compute in place (round 0, with the shared expert); each other
+ *    touched expert, in increasing expert order, takes the slot that is empty or holds an
+ *    untouched expert and is smallest by (occupied, usage of its expert, the forward that
+ *    last used the slot, slot index); usage[e] counts the forwards that routed to e.
+ *    Those refills form round 1.
+ *  - Transient forward otherwise: with G = S/2, the touched experts in increasing order
+ *    form groups of G; group r is round r and takes slots (r mod 2)*G + i, i its place in
+ *    the group, so a group's refill never touches the slots the previous group computes
+ *    on. An expert already in its slot is not copied; one that moves leaves its old slot
+ *    empty.
+ * stats: [0] forwards, [1] touched experts found in their slot, [2] experts copied.
+ * Per expert e: round_of (-1 when untouched), slot_for (the slot it computes from in this
+ * forward), copied (1 when its weights are copied in this forward). */
+static int bank_key_less(int32_t a, int32_t b, const int32_t *expert_in, const uint32_t *usage,
+                         const int32_t *last_use) {
+    const int32_t oa = expert_in[a], ob = expert_in[b];
+    if ((oa >= 0) != (ob >= 0)) return oa < 0;           /* empty slots first */
+    if (oa >= 0) {
+        if (usage[oa] != usage[ob]) return MUT(20) ? usage[oa] > usage[ob] : usage[oa] < usage[ob];
+        if (last_use[a] != last_use[b]) return last_use[a] < last_use[b];
+    }
+    return a < b;
+}
+
+void coli_oracle_bank_plan(int32_t E, int32_t S, int32_t T, int32_t top_k, const int32_t *cnt,
+                           int32_t *slot_of, int32_t *expert_in, uint32_t *usage, int32_t *last_use,
+                           int64_t *stats, int32_t *round_of, int32_t *slot_for, int32_t *copied) {
+    const int32_t step = (int32_t)++stats[0];
+    for (int32_t e = 0; e < E; ++e) {
+        round_of[e] = -1;
+        slot_for[e] = -1;
+        copied[e] = 0;
+        if (cnt[e] > 0) usage[e]++;
+    }
+    const int64_t cap = (int64_t)T * top_k < E ? (int64_t)T * top_k : E;
+    if (cap <= S) {
+        for (int32_t e = 0; e < E; ++e) {                /* resident: compute in place */
+            if (cnt[e] <= 0 || slot_of[e] < 0) continue;
+            round_of[e] = 0;
+            slot_for[e] = slot_of[e];
+            last_use[slot_of[e]] = step;
+            stats[1]++;
+        }
+        for (int32_t e = 0; e < E; ++e) {                /* the rest take the cheapest slots */
+            if (cnt[e] <= 0 || slot_of[e] >= 0) continue;
+            int32_t best = -1;
+            for (int32_t s = 0; s < S; ++s) {
+                const int32_t occ = expert_in[s];
+                if (occ >= 0 && cnt[occ] > 0 && !MUT(19)) continue;
+                if (best < 0 || bank_key_less(s, best, expert_in, usage, last_use)) best = s;
+            }
+            if (best < 0) return;                        /* cannot happen while cap <= S */
+            if (expert_in[best] >= 0) slot_of[expert_in[best]] = -1;
+            expert_in[best] = e;
+            slot_of[e] = best;
+            last_use[best] = step;
+            round_of[e] = 1;
+            slot_for[e] = best;
+            copied[e] = 1;
+            stats[2]++;
+        }
+        return;
+    }
+    const int32_t G = MUT(22) ? S : S / 2;
+    int32_t q = 0;
+    for (int32_t e = 0; e < E; ++e) {
+        if (cnt[e] <= 0) continue;
+        const int32_t r = q / G;
+        const int32_t s = ((r % 2) * G + q % G) % S;     /* below 2G <= S: the modulus only keeps
+                                                           a planted wrong G in bounds */
+        ++q;
+        round_of[e] = r;
+        slot_for[e] = s;
+        last_use[s] = step;
+        if (expert_in[s] == e) {
+            stats[1]++;
+            continue;
+        }
+        if (expert_in[s] >= 0) slot_of[expert_in[s]] = -1;
+        if (slot_of[e] >= 0 && !MUT(21)) expert_in[slot_of[e]] = -1;
+        expert_in[s] = e;
+        slot_of[e] = s;
+        copied[e] = 1;
+        stats[2]++;
+    }
+}

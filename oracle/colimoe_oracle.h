@@ -95,6 +95,15 @@ void coli_oracle_moe_forward(const uint16_t *x, int32_t T, int32_t H, int32_t E,
 int32_t coli_oracle_threads(void);   /* threads an OpenMP region uses (1 without OpenMP) */
 int32_t coli_oracle_mutant(void);    /* planted-mistake id this build carries (0 = none) */
 
+/* --- expert residency bank --- */
+/* One forward's effect on a bank of S device slots (2 <= S <= E) for the touched set
+ * {e : cnt[e] > 0}. State (in/out): slot_of[E] (-1: not resident), expert_in[S] (-1: empty),
+ * usage[E], last_use[S], stats[3] = {forwards, found in place, copied}. Out per expert:
+ * round_of, slot_for, copied. See the definition for the policy and its readings. */
+void coli_oracle_bank_plan(int32_t E, int32_t S, int32_t T, int32_t top_k, const int32_t *cnt,
+                           int32_t *slot_of, int32_t *expert_in, uint32_t *usage, int32_t *last_use,
+                           int64_t *stats, int32_t *round_of, int32_t *slot_for, int32_t *copied);
+
 #ifdef __cplusplus
 }
 #endif

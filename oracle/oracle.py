@@ -18,6 +18,8 @@ _u16p = C.POINTER(C.c_uint16)
 _i32p = C.POINTER(C.c_int32)
 _f32p = C.POINTER(C.c_float)
 _f64p = C.POINTER(C.c_double)
+_u32p = C.POINTER(C.c_uint32)
+_i64p = C.POINTER(C.c_int64)
 
 
 def _p(a: Optional[np.ndarray], t):
@@ -57,6 +59,8 @@ class Oracle:
                                               _f32p, _f32p, C.c_int32,
                                               _u8p, _u8p, _u8p, _u8p, _u8p, _u8p, _u8p, _u8p,
                                               _f32p, _i32p, _f32p, _i32p, _i32p, _i32p, _i32p, _u16p, _f64p]
+        L.coli_oracle_bank_plan.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int32, _i32p,
+                                            _i32p, _i32p, _u32p, _i32p, _i64p, _i32p, _i32p, _i32p]
         L.coli_oracle_threads.restype = C.c_int32
         L.coli_oracle_mutant.restype = C.c_int32
 
@@ -181,6 +185,38 @@ class Oracle:
         rows = int(off[E + 1])
         return dict(s=s, idx=idx, w=w, cnt=cnt, off=off, src_token=src[:rows].copy(), inv_row=inv,
                     out=out, out_f64=out64)
+
+
+class BankState:
+    """Host copy of an expert residency bank's state (the oracle's bank plan updates it)."""
+
+    def __init__(self, E: int, S: int):
+        self.E, self.S = E, S
+        self.slot_of = np.full(E, -1, np.int32)
+        self.expert_in = np.full(S, -1, np.int32)
+        self.usage = np.zeros(E, np.uint32)
+        self.last_use = np.zeros(S, np.int32)
+        self.stats = np.zeros(3, np.int64)
+
+    def copy(self) -> "BankState":
+        c = BankState(self.E, self.S)
+        for k in ("slot_of", "expert_in", "usage", "last_use", "stats"):
+            setattr(c, k, getattr(self, k).copy())
+        return c
+
+
+def bank_plan(o: Oracle, state: BankState, cnt: np.ndarray, T: int, top_k: int):
+    """One forward's effect on the bank (state updated in place); returns per-expert
+    (round_of, slot_for, copied)."""
+    E, S = state.E, state.S
+    cnt = np.ascontiguousarray(cnt[:E], np.int32)
+    rnd = np.zeros(E, np.int32)
+    slot = np.zeros(E, np.int32)
+    cop = np.zeros(E, np.int32)
+    o.lib.coli_oracle_bank_plan(E, S, T, top_k, _p(cnt, _i32p), _p(state.slot_of, _i32p),
+                                _p(state.expert_in, _i32p), _p(state.usage, _u32p), _p(state.last_use, _i32p),
+                                _p(state.stats, _i64p), _p(rnd, _i32p), _p(slot, _i32p), _p(cop, _i32p))
+    return rnd, slot, cop
 
 
 _default: Optional[Oracle] = None

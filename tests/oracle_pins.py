@@ -291,5 +291,178 @@ def pin_round_bf16(o):
         assert got == ref, (v, hex(got), hex(ref))
 
 
+# ---- expert residency bank ---------------------------------------------------------------
+# The bank keeps routed experts in S device slots. The pins check it against bookkeeping kept
+# here from the routing sequence alone: which experts each forward touches, how often each was
+# touched and when last; never against the oracle's own state arrays except to read them out.
+
+def bank_routing(rng, E: int, T: int, k: int, hot=None, p_hot: float = 0.0) -> np.ndarray:
+    """cnt[E + 1] of one forward: each of T tokens picks k distinct experts (expert `hot` first
+    with probability p_hot); cnt[E] = T, the shared expert."""
+    cnt = np.zeros(E + 1, np.int32)
+    for _ in range(T):
+        if hot is not None and rng.random() < p_hot:
+            rest = rng.choice([e for e in range(E) if e != hot], k - 1, replace=False)
+            picks = [hot] + list(rest)
+        else:
+            picks = rng.choice(E, k, replace=False)
+        for e in picks:
+            cnt[e] += 1
+    cnt[E] = T
+    return cnt
+
+
+def _bank_bijection(st):
+    for e in range(st.E):
+        if st.slot_of[e] >= 0:
+            assert st.expert_in[st.slot_of[e]] == e, ("slot_of/expert_in disagree", e)
+    for s in range(st.S):
+        if st.expert_in[s] >= 0:
+            assert st.slot_of[st.expert_in[s]] == s, ("expert_in/slot_of disagree", s)
+
+
+def _bank_run(o, E, S, T, k, forwards, seed, hot=None, p_hot=0.0, check=None):
+    """Runs `forwards` seeded forwards through the oracle's bank plan with independent
+    bookkeeping (usage counts, last forward that touched each expert)."""
+    from oracle.oracle import BankState, bank_plan
+    rng = _rng(seed)
+    st = BankState(E, S)
+    uses = np.zeros(E, np.int64)
+    last = np.zeros(E, np.int64)
+    for f in range(1, forwards + 1):
+        cnt = bank_routing(rng, E, T, k, hot, p_hot)
+        touched = [e for e in range(E) if cnt[e] > 0]
+        before = st.copy()
+        rnd, slot, cop = bank_plan(o, st, cnt, T, k)
+        _bank_bijection(st)
+        assert int(st.stats[0]) == f
+        for e in touched:
+            uses[e] += 1
+        assert np.array_equal(st.usage.astype(np.int64), uses), "usage is not the count of routed forwards"
+        assert int(st.stats[1] - before.stats[1]) + int(st.stats[2] - before.stats[2]) == len(touched)
+        assert int(st.stats[2] - before.stats[2]) == int(cop.sum())
+        assert all(rnd[e] == -1 and cop[e] == 0 for e in range(E) if cnt[e] == 0)
+        if check:
+            check(before, st, cnt, touched, rnd, slot, cop, uses, last)
+        for e in touched:
+            last[e] = f
+    return st
+
+
+def _cache_check(before, st, cnt, touched, rnd, slot, cop, uses, last):
+    resident_before = {e for e in range(st.E) if before.slot_of[e] >= 0}
+    for e in touched:
+        assert st.slot_of[e] >= 0 and slot[e] == st.slot_of[e], ("touched expert not resident", e)
+        hit = e in resident_before
+        assert rnd[e] == (0 if hit else 1) and cop[e] == (0 if hit else 1), ("round/copy", e)
+        if hit:
+            assert st.slot_of[e] == before.slot_of[e], ("a resident expert moved", e)
+    evicted = [e for e in resident_before if st.slot_of[e] < 0]
+    kept = [e for e in resident_before if st.slot_of[e] >= 0 and cnt[e] == 0]
+    for v in evicted:
+        assert cnt[v] == 0, ("a touched expert was evicted", v)
+        # the least used (then least recently used) untouched experts go first
+        for u in kept:
+            assert (uses[v], last[v]) <= (uses[u], last[u]), ("eviction order", v, u)
+    empty = sum(1 for s in range(st.S) if before.expert_in[s] < 0)
+    misses = sum(1 for e in touched if e not in resident_before)
+    assert len(evicted) == max(0, misses - empty), "evicted while a slot was empty"
+
+
+def pin_bank_cache(o):
+    """Cache forwards (T*k <= S): touched experts become resident, resident ones stay in place,
+    and only untouched experts are evicted, least used first."""
+    _bank_run(o, E=24, S=10, T=3, k=3, forwards=40, seed=40, check=_cache_check)
+    _bank_run(o, E=16, S=6, T=2, k=2, forwards=60, seed=41, hot=5, p_hot=0.7, check=_cache_check)
+
+
+def pin_bank_full(o):
+    """A bank with a slot per expert copies each expert once and never evicts."""
+    from oracle.oracle import BankState, bank_plan
+    rng = _rng(42)
+    E = 12
+    st = BankState(E, E)
+    seen = set()
+    for f in range(30):
+        cnt = bank_routing(rng, E, 2, 3)
+        bank_plan(o, st, cnt, 2, 3)
+        seen |= {e for e in range(E) if cnt[e] > 0}
+        assert int(st.stats[2]) == len(seen)
+        assert all(st.slot_of[e] >= 0 for e in seen)
+
+
+def pin_bank_hot_expert(o):
+    """An expert routed to by most forwards, once loaded, is never evicted by a rarely used one."""
+    from oracle.oracle import BankState, bank_plan
+    rng = _rng(43)
+    E, S, hot = 20, 4, 7
+    st = BankState(E, S)
+    for f in range(80):
+        cnt = bank_routing(rng, E, 1, 2, hot=hot, p_hot=0.8)
+        bank_plan(o, st, cnt, 1, 2)
+        if f >= 10:
+            assert st.slot_of[hot] >= 0, ("the most used expert was evicted", f)
+
+
+def _stream_check(before, st, cnt, touched, rnd, slot, cop, uses, last):
+    G = st.S // 2
+    final = {}
+    for q, e in enumerate(touched):
+        r = q // G
+        assert rnd[e] == r, ("round of the q-th touched expert", e)
+        assert slot[e] == (r % 2) * G + q % G, ("slot of the q-th touched expert", e)
+        want_copy = not (r < 2 and before.expert_in[slot[e]] == e)
+        assert cop[e] == int(want_copy), ("copy decision", e)
+        final[int(slot[e])] = e
+    for s in range(st.S):
+        if s in final:
+            assert st.expert_in[s] == final[s], ("last group to use a slot owns it", s)
+        elif before.expert_in[s] >= 0 and cnt[before.expert_in[s]] > 0:
+            assert st.expert_in[s] == -1, ("a moved expert left a copy behind", s)
+        else:
+            assert st.expert_in[s] == before.expert_in[s], ("an unused slot changed", s)
+
+
+def pin_bank_stream(o):
+    """Transient forwards (T*k > S): touched experts in increasing order fill alternate halves
+    of the bank in groups of S/2; a repeated forward finds its last two groups in place."""
+    from oracle.oracle import BankState, bank_plan
+    rng = _rng(44)
+    E, S = 32, 8
+    st = BankState(E, S)
+    uses = np.zeros(E, np.int64)
+    last = np.zeros(E, np.int64)
+    # forward 5 routes 7 tokens x 3 slots to 7 experts (more slots than the bank holds, fewer
+    # experts), among them the one in the last slot, which then moves to a lower slot and must
+    # leave the last slot empty; forward 6 repeats it
+    seq = [(2, 2), (12, 3), (1, 2), (12, 3), (7, 3), (7, 3)]
+    few = None
+    for f, (T, k) in enumerate(seq, start=1):
+        if f == 5:
+            pick = {1, 4, 9, 15, 22, 23, 30}
+            if st.expert_in[S - 1] >= 0:
+                pick = set(sorted(pick - {int(st.expert_in[S - 1])})[:6]) | {int(st.expert_in[S - 1])}
+            few = np.zeros(E + 1, np.int32)
+            few[sorted(pick)] = 3
+            few[E] = 7
+        cnt = few if f >= 5 else bank_routing(rng, E, T, k)
+        touched = [e for e in range(E) if cnt[e] > 0]
+        before = st.copy()
+        rnd, slot, cop = bank_plan(o, st, cnt, T, k)
+        _bank_bijection(st)
+        for e in touched:
+            uses[e] += 1
+        assert np.array_equal(st.usage.astype(np.int64), uses)
+        if min(T * k, E) > S:
+            _stream_check(before, st, cnt, touched, rnd, slot, cop, uses, last)
+        else:
+            _cache_check(before, st, cnt, touched, rnd, slot, cop, uses, last)
+        if f == 6:   # the same two groups again: every expert is already in its slot
+            assert not cop.any(), "a repeated forward recopied experts in place"
+        for e in touched:
+            last[e] = f
+
+
 ALL_PINS = [pin_e2m1_table, pin_e8m0, pin_nibble_order, pin_route_bruteforce, pin_route_weights,
-            pin_permute, pin_dense_swiglu, pin_dense_gated, pin_sigmoid, pin_logits, pin_round_bf16]
+            pin_permute, pin_dense_swiglu, pin_dense_gated, pin_sigmoid, pin_logits, pin_round_bf16,
+            pin_bank_cache, pin_bank_full, pin_bank_hot_expert, pin_bank_stream]
