@@ -311,6 +311,133 @@ def run_ours(args, wl_name: str) -> dict:
     return result if rank == 0 else None
 
 
+def host_link_gbs(nbytes: int = 1 << 30) -> float:
+    """Host-to-device copy rate from page-locked memory (copy engines), GB/s: the measured
+    denominator of the expert bank's refill traffic."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(3):
+        dst.copy_(src, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    return 3 * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
+
+
+def run_bank(args, wl_name: str) -> dict:
+    """The layer with its routed experts in page-locked host memory and a bank of --bank device
+    slots: each step is one forward over a new batch of tokens (so the routing, and the experts the
+    bank must fetch, change from step to step)."""
+    import torch
+    import torch.distributed as dist
+    from routed_moe_fp4_gb300 import build, colimoe as cm
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    inputs = S.make_inputs(wl_name, seed=0)
+    wl = inputs.workload
+    stream = torch.cuda.Stream()
+    layer = cm.MoELayer(inputs, stream=stream)
+    host = cm.HostExperts(inputs.experts)
+    bank = cm.ExpertBank(layer, args.bank, host)
+    if args.copy_blocks:
+        bank.set_copy_blocks(args.copy_blocks)
+    n = args.warmup + args.steps
+    xs = [torch.from_numpy(S.x_batch(0, wl.name, 1 + rank * n + i, wl.T, wl.H).view(np.int16)).cuda()
+          for i in range(n)]
+    out = torch.empty_like(xs[0])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def l2_flush():
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+
+    for i in range(args.warmup):
+        bank.forward(xs[i], out)
+    stream.synchronize()
+    before = bank.state()["stats"].copy()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches = 0
+    clocks = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        l2_flush()
+        starts[i].record(stream)
+        bank.forward(xs[args.warmup + i], out)
+        ends[i].record(stream)
+        launches += layer.launches()
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    after = bank.state()["stats"]
+    ms_per_step = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), device="cuda") / args.steps
+    found, copied = int(after[1] - before[1]), int(after[2] - before[2])
+    eb = S.expert_bytes(wl.H, wl.I)
+    copied_per_step = copied * eb / args.steps
+
+    # end to end: x from page-locked host memory, out back to it, inside the timed region
+    x_host = torch.from_numpy(S.x_batch(0, wl.name, 0, wl.T, wl.H).view(np.int16)).pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(out)
+    e2e_ms = []
+    for i in range(args.steps + 2):
+        l2_flush()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            x_dev.copy_(x_host, non_blocking=True)
+            bank.forward(x_dev, out)
+            out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+        if i >= 2:
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_step = sum(e2e_ms) / len(e2e_ms)
+    link = host_link_gbs()
+    tokens = wl.T * ws
+    result = {
+        "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": FFN_PATHS["mxf4"][4],
+        "data": "synthetic (seeded SplitMix64; MXFP4 experts, bf16 activations; a new token batch every step)",
+        "config": {"workload": f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E}, top_k={wl.top_k}, I={wl.I}, "
+                               f"I_s={wl.I_s}, MXFP4 E2M1 + UE8M0/32; routed experts in page-locked host "
+                               f"memory, expert bank of {args.bank} device slots",
+                   "tokens_per_gpu": wl.T, "ffn_path": "mxf4", "bank_slots": args.bank,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "flushed (512 MiB write) before every timed step"},
+        "roofline": {"kernel": "bank_refill (experts over the host link)", "bound": "host link",
+                     "achieved": copied_per_step / (ms_per_step * 1e-3) / 1e9, "peak": link, "unit": "GB/s",
+                     "frac": copied_per_step / (ms_per_step * 1e-3) / 1e9 / link, "traffic": None,
+                     "peak_source": "measured in this run: page-locked host-to-device copy (copy engines)",
+                     "algorithmic_bytes": copied_per_step},
+        "bank": {"slots": args.bank, "found_in_slot": found, "copied": copied,
+                 "hit_rate": found / max(1, found + copied), "copied_bytes_per_step": copied_per_step,
+                 "copy_blocks": args.copy_blocks or 16},
+        "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_step,
+                "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
+        "gpu_launches": launches,
+        "clocks": clock_info,
+    }
+    bank.close()
+    layer.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
 def oracle_sample(wl_name: str, budget_s: float):
     """Times the oracle's full forward on the workload's tokens, repeated up to `budget_s`."""
     from oracle.oracle import Oracle
@@ -370,12 +497,15 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true", help="no cpu_baseline (profiling runs)")
     ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
                     help="force an FFN path (default: the library's own choice)")
+    ap.add_argument("--bank", type=int, default=0,
+                    help="routed experts in page-locked host memory behind a bank of this many device slots")
+    ap.add_argument("--copy-blocks", type=int, default=0, help="bank: blocks that copy while a round computes")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         res = run_reference(args, args.workload)
     else:
-        res = run_ours(args, args.workload)
+        res = run_bank(args, args.workload) if args.bank else run_ours(args, args.workload)
         if res is not None and not args.skip_cpu:
             res["cpu_baseline"] = oracle_sample(args.workload, args.cpu_budget)
     if res is not None:

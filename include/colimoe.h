@@ -224,6 +224,64 @@ COLI_API int coli_moe_route_static(const void *x_bf16, int32_t T, int32_t H, con
                                    const float *router_bias, int32_t E, int32_t top_k, int32_t *idx_out,
                                    float *weights_out, void *cuda_stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Expert residency bank. The routed experts' master copy stays in page-locked host memory (or any
+ * memory the device can read); a bank of S device slots holds the experts a layer uses most, and
+ * each forward refills it route-aware on the device: the plan, the copies over the host link and
+ * the GEMMs are stream-ordered device work, and the host never waits for the routing.
+ * The pages keep the most used routed experts of each layer resident on the GPU, ranked by usage
+ * ("DeepSeek V4 Flash support -- CUDA/VRAM expert tiering", summary item 1), refill that cache in
+ * place, and for a batched prefill refill a transient per-layer bank in slot-sized groups, one
+ * group's uploads overlapped with the neighbouring group's compute ("the CUDA tier wired into the
+ * DeepSeek V4 engine", What it is: engine tier and prefill MoE).
+ *
+ * Policy, per forward with T tokens and top_k (readings of the pages, which give no more):
+ *  - cache forward, when min(T * top_k, E) <= S: touched experts already resident compute in place
+ *    (round 0, with the shared expert). Each other touched expert, in increasing expert order, is
+ *    copied into the slot that is empty or holds an untouched expert and comes first by (occupied,
+ *    usage of its expert, forward that last used the slot, slot index), where usage counts the
+ *    forwards that routed to the expert; those compute in round 1, their copies overlapping
+ *    round 0.
+ *  - transient forward otherwise: with G = S / 2 the touched experts, in increasing order, form
+ *    groups of G; group r computes in round r from slots (r mod 2) * G + i (i its place in the
+ *    group), and its copies overlap round r - 1. An expert already in its slot is not copied.
+ * Results are bit-identical to coli_moe_forward with the same experts resident in device memory
+ * (the same FP4 path, COLI_FFN_GEMM_MXF4, computes both).
+ */
+typedef struct coli_expert_bank coli_expert_bank_t;
+
+/* Creates a bank of `slots` device slots (2 <= slots <= E) for handle h, bound to h's shapes.
+ * host_experts: the E routed experts in the coli_mxfp4_experts layout, in page-locked host memory
+ * mapped for the device (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped) or in
+ * device memory; pointers 16-byte aligned. The caller owns that memory and keeps it alive and
+ * unchanged for the bank's life. The bank allocates slots x (one expert's bytes) of device memory,
+ * its state and per-round buffers, one copy stream and its events; it starts empty. Synchronises
+ * h's stream. Errors: COLI_ERR_INVALID_ARG (bad slots or pointers, host memory not page-locked),
+ * COLI_ERR_OUT_OF_MEMORY, COLI_ERR_UNSUPPORTED_ARCH (no FP4 tensor-map path on this device). */
+COLI_API int coli_bank_create(coli_moe_t *h, int32_t slots, const coli_mxfp4_experts *host_experts,
+                              coli_expert_bank_t **out);
+/* Waits for the bank's work and frees it. NULL-safe. */
+COLI_API void coli_bank_destroy(coli_expert_bank_t *bank);
+
+/* coli_moe_forward with the routed experts taken from the bank (arguments as there, the shared
+ * expert in device memory). Enqueues on h's stream (and the bank's copy stream, joined back into
+ * h's stream before the combine) and returns without synchronising; allocates nothing. Works
+ * under stream capture. Forwards on one bank must not overlap. */
+COLI_API int coli_moe_forward_banked(coli_moe_t *h, coli_expert_bank_t *bank, const void *x_bf16, int32_t T,
+                                     const float *router_w, const float *router_bias,
+                                     const coli_mxfp4_experts *shared_expert, int32_t top_k, void *out_bf16);
+
+/* Blocks of 1024 threads that copy experts while another round computes (1 .. SMs - 1; default
+ * 16); the GEMM of that round runs on the other SMs. */
+COLI_API int coli_bank_set_copy_blocks(coli_expert_bank_t *bank, int32_t blocks);
+
+/* Bank state after the forwards enqueued so far (synchronises h's stream). Each output may be
+ * NULL: slot_of [E] (slot of a resident expert, -1 if none), expert_in [S] (-1: empty), usage [E]
+ * (forwards that routed to the expert), last_use [S] (the forward, counted from 1, that last used
+ * the slot), stats [3] = {forwards, touched experts found in their slot, experts copied}. */
+COLI_API int coli_bank_state(coli_expert_bank_t *bank, int32_t *slot_of, int32_t *expert_in, uint32_t *usage,
+                             int32_t *last_use, int64_t *stats);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,9 @@ COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM, COLI_FFN_GEMM_BF16, COLI_FFN_GEMM_M
 EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "coli_moe_destroy",
             "coli_moe_last_error", "coli_moe_set_ffn_path", "coli_moe_debug_routing",
             "coli_moe_last_launch_count", "coli_moe_last_ffn_path", "coli_moe_set_profiling", "coli_moe_stage_times",
-            "coli_moe_device_error", "coli_moe_set_wait_limit", "coli_moe_route_static")
+            "coli_moe_device_error", "coli_moe_set_wait_limit", "coli_moe_route_static",
+            "coli_bank_create", "coli_bank_destroy", "coli_moe_forward_banked", "coli_bank_set_copy_blocks",
+            "coli_bank_state")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
 
@@ -92,6 +94,17 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_moe_device_error.restype = C.c_int
     lib.coli_moe_route_static.argtypes = [vp, C.c_int32, C.c_int32, vp, vp, C.c_int32, C.c_int32, vp, vp, vp]
     lib.coli_moe_route_static.restype = C.c_int
+    lib.coli_bank_create.argtypes = [vp, C.c_int32, C.POINTER(coli_mxfp4_experts), C.POINTER(vp)]
+    lib.coli_bank_create.restype = C.c_int
+    lib.coli_bank_destroy.argtypes = [vp]
+    lib.coli_bank_destroy.restype = None
+    lib.coli_moe_forward_banked.argtypes = [vp, vp, vp, C.c_int32, vp, vp, C.POINTER(coli_mxfp4_experts),
+                                            C.c_int32, vp]
+    lib.coli_moe_forward_banked.restype = C.c_int
+    lib.coli_bank_set_copy_blocks.argtypes = [vp, C.c_int32]
+    lib.coli_bank_set_copy_blocks.restype = C.c_int
+    lib.coli_bank_state.argtypes = [vp, vp, vp, vp, vp, vp]
+    lib.coli_bank_state.restype = C.c_int
     _lib = lib
     return lib
 
@@ -199,6 +212,37 @@ def coli_moe_route_static(x_bf16, T: int, H: int, router_w, router_bias, E: int,
     return _check(None, rc)
 
 
+def coli_bank_create(h, slots: int, host_experts: coli_mxfp4_experts) -> C.c_void_p:
+    out = C.c_void_p()
+    _check(h, load().coli_bank_create(h, slots, C.byref(host_experts), C.byref(out)))
+    return out
+
+
+def coli_bank_destroy(bank) -> None:
+    load().coli_bank_destroy(bank)
+
+
+def coli_moe_forward_banked(h, bank, x_bf16, T: int, router_w, router_bias,
+                            shared_expert: Optional[coli_mxfp4_experts], top_k: int, out_bf16) -> int:
+    sh = C.byref(shared_expert) if shared_expert is not None else None
+    return _check(h, load().coli_moe_forward_banked(h, bank, _ptr(x_bf16), T, _ptr(router_w), _ptr(router_bias),
+                                                    sh, top_k, _ptr(out_bf16)))
+
+
+def coli_bank_set_copy_blocks(h, bank, blocks: int) -> int:
+    return _check(h, load().coli_bank_set_copy_blocks(bank, blocks))
+
+
+def coli_bank_state(h, bank, E: int, S: int) -> dict:
+    """The bank's state as numpy arrays (synchronises the handle's stream)."""
+    import numpy as np
+    st = dict(slot_of=np.zeros(E, np.int32), expert_in=np.zeros(S, np.int32), usage=np.zeros(E, np.uint32),
+              last_use=np.zeros(S, np.int32), stats=np.zeros(3, np.int64))
+    _check(h, load().coli_bank_state(bank, *[st[k].ctypes.data for k in
+                                            ("slot_of", "expert_in", "usage", "last_use", "stats")]))
+    return st
+
+
 # ---- convenience: device-resident inputs of a workload -----------------------------------
 
 class DeviceExperts:
@@ -281,6 +325,8 @@ class MoELayer:
         return coli_moe_last_ffn_path(self.h)
 
     def close(self) -> None:
+        for b in list(getattr(self, "_banks", [])):
+            b.close()
         if self.h:
             coli_moe_destroy(self.h)
             self.h = None
@@ -290,3 +336,42 @@ class MoELayer:
             self.close()
         except Exception:
             pass
+
+
+class HostExperts:
+    """MXFP4 expert arrays in page-locked host memory (the device reads them over the host link)."""
+
+    def __init__(self, host):
+        import torch
+        self.tensors = [torch.from_numpy(a).pin_memory() for a in
+                        (host.gate_up_codes, host.gate_up_scales, host.down_codes, host.down_scales)]
+        self.struct = coli_mxfp4_experts(*[t.data_ptr() for t in self.tensors])
+
+
+class ExpertBank:
+    """A bank of device slots over a layer's experts held in page-locked host memory."""
+
+    def __init__(self, layer: "MoELayer", slots: int, host_experts: HostExperts):
+        self.layer, self.slots, self.host = layer, slots, host_experts
+        self.b = coli_bank_create(layer.h, slots, host_experts.struct)
+        if not hasattr(layer, "_banks"):
+            layer._banks = []
+        layer._banks.append(self)
+
+    def forward(self, x, out, T: Optional[int] = None) -> None:
+        L = self.layer
+        T = x.shape[0] if T is None else T
+        coli_moe_forward_banked(L.h, self.b, x, T, L.router_w, L.router_b,
+                                L.shared.struct if L.shared is not None else None, L.top_k, out)
+
+    def set_copy_blocks(self, blocks: int) -> None:
+        coli_bank_set_copy_blocks(self.layer.h, self.b, blocks)
+
+    def state(self) -> dict:
+        return coli_bank_state(self.layer.h, self.b, self.layer.wl.E, self.slots)
+
+    def close(self) -> None:
+        if self.b:
+            coli_bank_destroy(self.b)
+            self.b = None
+            self.layer._banks.remove(self)

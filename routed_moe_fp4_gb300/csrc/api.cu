@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 
 #include "colimoe_internal.cuh"
@@ -103,15 +104,10 @@ FfnKind pick_ffn(const coli_moe_t *h, int T, int top_k, const coli_mxfp4_experts
     return (double)T * top_k / (touched > 0 ? touched : 1.0) > 3.0 ? kFfnBf16 : kFfnGemv;
 }
 
-int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router_w, const float *router_bias,
-                 const coli_mxfp4_experts *packed, const coli_mxfp4_experts *shared, int32_t top_k,
-                 void *out_bf16) {
+// Argument checks every forward shares (T > 0 here).
+int check_forward(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router_w,
+                  const coli_mxfp4_experts *shared, int32_t top_k, const void *out_bf16) {
     const coli_moe_config &c = h->cfg;
-    if (T == 0) {
-        h->last_launches = 0;
-        h->last_path = COLI_FFN_AUTO;
-        return COLI_OK;
-    }
     if (T < 0 || T > c.max_tokens) {
         set_err(h, "T=%d outside [0, max_tokens=%d]", T, c.max_tokens);
         return COLI_ERR_INVALID_ARG;
@@ -128,18 +124,113 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         set_err(h, "out_bf16 may not alias x_bf16");
         return COLI_ERR_INVALID_ARG;
     }
-    if (!valid_experts(packed)) {
-        set_err(h, "packed_experts must hold four non-NULL 16-byte aligned device pointers");
-        return COLI_ERR_INVALID_ARG;
-    }
     if (shared && (c.shared_inter == 0 || !valid_experts(shared))) {
         set_err(h, c.shared_inter == 0 ? "shared_expert given but cfg.shared_inter is 0"
                                        : "shared_expert must hold four non-NULL 16-byte aligned device pointers");
         return COLI_ERR_INVALID_ARG;
     }
+    return COLI_OK;
+}
+
+// A1 router and A2 permute (with the n-tile layout of tile size `ntile` when non-zero, and the
+// activation gather for the bf16 GEMM path). Returns false on a launch error.
+bool run_front(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router_w, const float *router_bias,
+               int32_t top_k, bool with_shared, bool gather, int ntile, int rows, int &launches) {
+    const int E = h->cfg.num_experts, H = h->cfg.hidden;
+    Workspace &ws = h->ws;
+    cudaStream_t st = h->stream;
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(x_bf16);
+    int n;
+    if (T < kSmallRouteTokens) {
+        // logits, then top-k and the whole permutation in one single-block launch
+        n = launch_router(x, T, H, router_w, router_bias, E, top_k, ws.scores, ws.idx, ws.w, ws.logit_part,
+                          ws.logit_part_floats, h->num_sms, nullptr, 0, st, false);
+        if (n < 0) return false;
+        launches += n;
+        if (h->profiling) cudaEventRecord(h->ev[1], st);
+        n = launch_route_permute_small(router_bias, T, E, top_k, with_shared, kGemvCostTokens, ntile, ws, st);
+        if (n < 0) return false;
+        launches += n;
+        if (gather) {
+            n = launch_gather(x, H, rows, ws, st);
+            if (n < 0) return false;
+            launches += n;
+        }
+        return true;
+    }
+    n = launch_router(x, T, H, router_w, router_bias, E, top_k, ws.scores, ws.idx, ws.w, ws.logit_part,
+                      ws.logit_part_floats, h->num_sms, ws.cnt, E + 1, st);
+    if (n < 0) return false;
+    launches += n;
+    if (h->profiling) cudaEventRecord(h->ev[1], st);
+    n = launch_permute(ws.idx, T, E, top_k, with_shared, x, H, gather, kGemvCostTokens, ntile, ws, st);
+    if (n < 0) return false;
+    launches += n;
+    return true;
+}
+
+// The FFN stage's arguments over the handle's workspace.
+FfnArgs ffn_args(coli_moe_t *h, const void *x_bf16, int32_t T, int32_t top_k, int rows,
+                 const coli_mxfp4_experts *packed, const coli_mxfp4_experts *shared) {
+    const coli_moe_config &c = h->cfg;
+    Workspace &ws = h->ws;
+    FfnArgs a{};
+    a.routed = to_set(packed);
+    a.shared = to_set(shared);
+    a.E = c.num_experts;
+    a.H = c.hidden;
+    a.I = c.inter;
+    a.I_s = c.shared_inter;
+    a.I_max = h->I_max;
+    a.T = T;
+    a.top_k = top_k;
+    a.rows = rows;
+    a.cnt = ws.cnt;
+    a.off = ws.off;
+    a.touched = ws.touched;
+    a.n_touched = ws.n_touched;
+    a.touched_cost = ws.touched_cost;
+    a.src_token = ws.src_token;
+    a.x = static_cast<const __nv_bfloat16 *>(x_bf16);
+    a.xp = ws.xp;
+    a.xh = ws.xh;
+    a.xinv = ws.xinv;
+    a.h = ws.h;
+    a.hh = ws.hh;
+    a.hinv = ws.hinv;
+    a.y = ws.y;
+    a.xq = ws.xq;
+    a.xqs = ws.xqs;
+    a.hq = ws.hq;
+    a.hqs = ws.hqs;
+    a.err = ws.err;
+    a.wait_ns = h->wait_ns;
+    return a;
+}
+
+int launch_failed(coli_moe_t *h) {
+    const cudaError_t e = cudaGetLastError();
+    set_err(h, "kernel launch failed: %s", cudaGetErrorString(e));
+    return COLI_ERR_CUDA;
+}
+
+int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router_w, const float *router_bias,
+                 const coli_mxfp4_experts *packed, const coli_mxfp4_experts *shared, int32_t top_k,
+                 void *out_bf16) {
+    if (T == 0) {
+        h->last_launches = 0;
+        h->last_path = COLI_FFN_AUTO;
+        return COLI_OK;
+    }
+    int rc = check_forward(h, x_bf16, T, router_w, shared, top_k, out_bf16);
+    if (rc != COLI_OK) return rc;
+    if (!valid_experts(packed)) {
+        set_err(h, "packed_experts must hold four non-NULL 16-byte aligned device pointers");
+        return COLI_ERR_INVALID_ARG;
+    }
     cudaGetLastError();   // clear a stale error so launch checks below see only our own
     cudaStream_t st = h->stream;
-    const int E = c.num_experts, H = c.hidden;
+    const int H = h->cfg.hidden;
     const bool with_shared = shared != nullptr;
     Workspace &ws = h->ws;
     int launches = 0, n;
@@ -150,70 +241,13 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     const bool prof = h->profiling;
     h->stage_valid = false;
     if (prof) cudaEventRecord(h->ev[0], st);
-
-    if (T < kSmallRouteTokens) {
-        // logits, then top-k and the whole permutation in one single-block launch
-        n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
-                          ws.scores, ws.idx, ws.w, ws.logit_part, ws.logit_part_floats, h->num_sms, nullptr, 0, st,
-                          false);
-        if (n < 0) goto launch_fail;
-        launches += n;
-        if (prof) cudaEventRecord(h->ev[1], st);
-        n = launch_route_permute_small(router_bias, T, E, top_k, with_shared, kGemvCostTokens, ntile, ws, st);
-        if (n < 0) goto launch_fail;
-        launches += n;
-        if (gemm) {
-            n = launch_gather(static_cast<const __nv_bfloat16 *>(x_bf16), H, rows, ws, st);
-            if (n < 0) goto launch_fail;
-            launches += n;
-        }
-    } else {
-        n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
-                          ws.scores, ws.idx, ws.w, ws.logit_part, ws.logit_part_floats, h->num_sms, ws.cnt, E + 1,
-                          st);
-        if (n < 0) goto launch_fail;
-        launches += n;
-        if (prof) cudaEventRecord(h->ev[1], st);
-        n = launch_permute(ws.idx, T, E, top_k, with_shared, static_cast<const __nv_bfloat16 *>(x_bf16), H, gemm,
-                           kGemvCostTokens, ntile, ws, st);
-        if (n < 0) goto launch_fail;
-        launches += n;
-    }
+    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, gemm, ntile, rows, launches))
+        return launch_failed(h);
     {
-        FfnArgs a{};
-        a.routed = to_set(packed);
-        a.shared = to_set(shared);
-        a.E = E;
-        a.H = H;
-        a.I = c.inter;
-        a.I_s = c.shared_inter;
-        a.I_max = h->I_max;
-        a.T = T;
-        a.top_k = top_k;
-        a.rows = rows;
-        a.cnt = ws.cnt;
-        a.off = ws.off;
-        a.touched = ws.touched;
-        a.n_touched = ws.n_touched;
-        a.touched_cost = ws.touched_cost;
-        a.src_token = ws.src_token;
-        a.x = static_cast<const __nv_bfloat16 *>(x_bf16);
-        a.xp = ws.xp;
-        a.xh = ws.xh;
-        a.xinv = ws.xinv;
-        a.h = ws.h;
-        a.hh = ws.hh;
-        a.hinv = ws.hinv;
-        a.y = ws.y;
-        a.xq = ws.xq;
-        a.xqs = ws.xqs;
-        a.hq = ws.hq;
-        a.hqs = ws.hqs;
-        a.err = ws.err;
-        a.wait_ns = h->wait_ns;
+        const FfnArgs a = ffn_args(h, x_bf16, T, top_k, rows, packed, shared);
         if (ffn == kFfnMx || ffn == kFfnMx4) {   // the activation terms belong to the permute stage
             n = ffn == kFfnMx ? launch_quant_x(a, st) : launch_quant_x4(a, st);
-            if (n < 0) goto launch_fail;
+            if (n < 0) return launch_failed(h);
             launches += n;
         }
         if (prof) cudaEventRecord(h->ev[2], st);
@@ -240,12 +274,12 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
         } else {
             n = launch_ffn_gemv(a, h->num_sms, mid, st);
         }
-        if (n < 0) goto launch_fail;
+        if (n < 0) return launch_failed(h);
         launches += n;
     }
     if (prof) cudaEventRecord(h->ev[4], st);
     n = launch_combine(ws.y, ws.inv_row, ws.w, T, H, top_k, with_shared, static_cast<__nv_bfloat16 *>(out_bf16), st);
-    if (n < 0) goto launch_fail;
+    if (n < 0) return launch_failed(h);
     launches += n;
     if (prof) {
         cudaEventRecord(h->ev[5], st);
@@ -258,12 +292,6 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     h->last_path = ffn == kFfnGemv ? COLI_FFN_GEMV : ffn == kFfnMx ? COLI_FFN_GEMM
                  : ffn == kFfnBf16 ? COLI_FFN_GEMM_BF16 : COLI_FFN_GEMM_MXF4;
     return COLI_OK;
-
-launch_fail : {
-    const cudaError_t e = cudaGetLastError();
-    set_err(h, "kernel launch failed: %s", cudaGetErrorString(e));
-    return COLI_ERR_CUDA;
-}
 }
 
 }  // namespace
@@ -506,6 +534,275 @@ int coli_moe_stage_times(coli_moe_t *h, float *ms) {
             return COLI_ERR_CUDA;
         }
     }
+    return COLI_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Expert residency bank (kernels and policy in bank.cu).
+
+struct coli_expert_bank {
+    coli_moe_t *h = nullptr;
+    int S = 0, R = 0, copy_blocks = 16;
+    BankDev dev{};
+    ExpertSet src{};                 // device-accessible addresses of the master experts
+    ExpertSet slots{};               // [S] experts in device memory
+    ExpertBytes eb{};
+    cudaStream_t copy = nullptr;
+    cudaEvent_t ev_plan = nullptr;
+    cudaEvent_t *ev_fill = nullptr, *ev_done = nullptr;   // [R] each
+    void *mem[12] = {};
+};
+
+namespace {
+
+void free_bank(coli_expert_bank_t *b) {
+    if (b->copy) cudaStreamSynchronize(b->copy);
+    for (void *p : b->mem)
+        if (p) cudaFree(p);
+    if (b->ev_plan) cudaEventDestroy(b->ev_plan);
+    for (int r = 0; r < b->R; ++r) {
+        if (b->ev_fill && b->ev_fill[r]) cudaEventDestroy(b->ev_fill[r]);
+        if (b->ev_done && b->ev_done[r]) cudaEventDestroy(b->ev_done[r]);
+    }
+    delete[] b->ev_fill;
+    delete[] b->ev_done;
+    if (b->copy) cudaStreamDestroy(b->copy);
+    delete b;
+}
+
+// The device-readable address of caller memory: mapped page-locked host memory or device memory.
+const uint8_t *device_view(const void *p) {
+    cudaPointerAttributes at;
+    if (!p || cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeHost) return static_cast<const uint8_t *>(at.devicePointer);
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return static_cast<const uint8_t *>(p);
+    return nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+int coli_bank_create(coli_moe_t *h, int32_t slots, const coli_mxfp4_experts *host_experts,
+                     coli_expert_bank_t **out) {
+    if (!h || !out) return COLI_ERR_INVALID_ARG;
+    *out = nullptr;
+    const coli_moe_config &c = h->cfg;
+    const int E = c.num_experts;
+    if (slots < 2 || slots > E) {
+        set_err(h, "bank slots=%d outside [2, E=%d]", slots, E);
+        return COLI_ERR_INVALID_ARG;
+    }
+    if (!valid_experts(host_experts)) {
+        set_err(h, "host_experts must hold four non-NULL 16-byte aligned pointers");
+        return COLI_ERR_INVALID_ARG;
+    }
+    if (!mx4_available()) {
+        set_err(h, "the expert bank runs on the FP4 block-scaled path, which needs a tensor-map encoder");
+        return COLI_ERR_UNSUPPORTED_ARCH;
+    }
+    ExpertSet src;
+    src.gu_codes = device_view(host_experts->gate_up_codes);
+    src.gu_scales = device_view(host_experts->gate_up_scales);
+    src.d_codes = device_view(host_experts->down_codes);
+    src.d_scales = device_view(host_experts->down_scales);
+    if (!src.gu_codes || !src.gu_scales || !src.d_codes || !src.d_scales || !aligned16(src.gu_codes) ||
+        !aligned16(src.gu_scales) || !aligned16(src.d_codes) || !aligned16(src.d_scales)) {
+        set_err(h, "host_experts must be page-locked host memory mapped for the device, or device memory");
+        return COLI_ERR_INVALID_ARG;
+    }
+    coli_expert_bank_t *b = new (std::nothrow) coli_expert_bank_t();
+    if (!b) return COLI_ERR_OUT_OF_MEMORY;
+    b->h = h;
+    b->S = slots;
+    b->src = src;
+    const uint64_t H = c.hidden, I = c.inter;
+    b->eb.seg[0] = 2 * I * (H / 2);
+    b->eb.seg[1] = 2 * I * (H / 32);
+    b->eb.seg[2] = H * (I / 2);
+    b->eb.seg[3] = H * (I / 32);
+    const long cap = std::min<long>((long)c.max_tokens * c.max_top_k, E);
+    const int G = slots / 2;
+    b->R = std::max<int>(2, (int)((cap + G - 1) / G));
+    const int rows = c.max_tokens * c.max_top_k + c.max_tokens;
+    BankDev &d = b->dev;
+    d.E = E;
+    d.S = slots;
+    d.R = b->R;
+    d.nm = ntile_max(E, rows);
+    bool ok = true;
+    auto get = [&](int i, size_t bytes) -> void * {
+        if (ok && cudaMalloc(&b->mem[i], bytes + 256) != cudaSuccess) ok = false;
+        return ok ? b->mem[i] : nullptr;
+    };
+    b->slots.gu_codes = static_cast<const uint8_t *>(get(0, slots * b->eb.seg[0]));
+    b->slots.gu_scales = static_cast<const uint8_t *>(get(1, slots * b->eb.seg[1]));
+    b->slots.d_codes = static_cast<const uint8_t *>(get(2, slots * b->eb.seg[2]));
+    b->slots.d_scales = static_cast<const uint8_t *>(get(3, slots * b->eb.seg[3]));
+    d.slot_of = static_cast<int32_t *>(get(4, sizeof(int32_t) * E));
+    d.expert_in = static_cast<int32_t *>(get(5, sizeof(int32_t) * slots));
+    d.usage = static_cast<uint32_t *>(get(6, sizeof(uint32_t) * E));
+    d.last_use = static_cast<int32_t *>(get(7, sizeof(int32_t) * slots));
+    d.stats = static_cast<long long *>(get(8, sizeof(long long) * 4));
+    d.copies = static_cast<int2 *>(get(9, sizeof(int2) * (size_t)b->R * slots));
+    d.ncopy = static_cast<int32_t *>(get(10, sizeof(int32_t) * (size_t)b->R + sizeof(int32_t) * 2 * b->R));
+    d.counts = d.ncopy ? d.ncopy + b->R : nullptr;
+    int2 *recs = static_cast<int2 *>(get(11, sizeof(int2) * 2 * d.nm * (size_t)b->R));
+    d.rec_small = recs;
+    d.rec_large = recs ? recs + d.nm * (size_t)b->R : nullptr;
+    if (ok) {
+        cudaStream_t st = h->stream;
+        ok = cudaMemsetAsync(d.slot_of, 0xFF, sizeof(int32_t) * E, st) == cudaSuccess &&
+             cudaMemsetAsync(d.expert_in, 0xFF, sizeof(int32_t) * slots, st) == cudaSuccess &&
+             cudaMemsetAsync(d.usage, 0, sizeof(uint32_t) * E, st) == cudaSuccess &&
+             cudaMemsetAsync(d.last_use, 0, sizeof(int32_t) * slots, st) == cudaSuccess &&
+             cudaMemsetAsync(d.stats, 0, sizeof(long long) * 4, st) == cudaSuccess &&
+             cudaStreamSynchronize(st) == cudaSuccess;
+    }
+    if (ok) ok = cudaStreamCreateWithFlags(&b->copy, cudaStreamNonBlocking) == cudaSuccess;
+    if (ok) {
+        b->ev_fill = new (std::nothrow) cudaEvent_t[b->R]();
+        b->ev_done = new (std::nothrow) cudaEvent_t[b->R]();
+        ok = b->ev_fill && b->ev_done &&
+             cudaEventCreateWithFlags(&b->ev_plan, cudaEventDisableTiming) == cudaSuccess;
+        for (int r = 0; ok && r < b->R; ++r)
+            ok = cudaEventCreateWithFlags(&b->ev_fill[r], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&b->ev_done[r], cudaEventDisableTiming) == cudaSuccess;
+    }
+    if (!ok) {
+        cudaGetLastError();
+        free_bank(b);
+        set_err(h, "bank allocation failed (%d slots)", slots);
+        return COLI_ERR_OUT_OF_MEMORY;
+    }
+    b->copy_blocks = std::min(16, h->num_sms - 1);
+    *out = b;
+    return COLI_OK;
+}
+
+void coli_bank_destroy(coli_expert_bank_t *bank) {
+    if (!bank) return;
+    cudaStreamSynchronize(bank->h->stream);
+    free_bank(bank);
+}
+
+int coli_bank_set_copy_blocks(coli_expert_bank_t *bank, int32_t blocks) {
+    if (!bank || blocks < 1 || blocks > bank->h->num_sms - 1) {
+        if (bank) set_err(bank->h, "copy blocks %d outside [1, SMs - 1]", blocks);
+        return COLI_ERR_INVALID_ARG;
+    }
+    bank->copy_blocks = blocks;
+    return COLI_OK;
+}
+
+int coli_bank_state(coli_expert_bank_t *bank, int32_t *slot_of, int32_t *expert_in, uint32_t *usage,
+                    int32_t *last_use, int64_t *stats) {
+    if (!bank) return COLI_ERR_INVALID_ARG;
+    coli_moe_t *h = bank->h;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) {
+        set_err(h, "stream error: %s", cudaGetErrorString(cudaGetLastError()));
+        return COLI_ERR_CUDA;
+    }
+    const BankDev &d = bank->dev;
+    struct Copy {
+        void *dst;
+        const void *src;
+        size_t bytes;
+    } copies[] = {{slot_of, d.slot_of, sizeof(int32_t) * d.E}, {expert_in, d.expert_in, sizeof(int32_t) * d.S},
+                  {usage, d.usage, sizeof(uint32_t) * d.E},     {last_use, d.last_use, sizeof(int32_t) * d.S},
+                  {stats, d.stats, sizeof(int64_t) * 3}};
+    for (const Copy &c : copies) {
+        if (!c.dst) continue;
+        if (cudaMemcpy(c.dst, c.src, c.bytes, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            set_err(h, "copy failed: %s", cudaGetErrorString(cudaGetLastError()));
+            return COLI_ERR_CUDA;
+        }
+    }
+    return COLI_OK;
+}
+
+int coli_moe_forward_banked(coli_moe_t *h, coli_expert_bank_t *bank, const void *x_bf16, int32_t T,
+                            const float *router_w, const float *router_bias,
+                            const coli_mxfp4_experts *shared_expert, int32_t top_k, void *out_bf16) {
+    if (!h) return COLI_ERR_INVALID_ARG;
+    if (!bank || bank->h != h) {
+        set_err(h, "bank is NULL or belongs to another handle");
+        return COLI_ERR_INVALID_ARG;
+    }
+    if (T == 0) {
+        h->last_launches = 0;
+        return COLI_OK;
+    }
+    int rc = check_forward(h, x_bf16, T, router_w, shared_expert, top_k, out_bf16);
+    if (rc != COLI_OK) return rc;
+    cudaGetLastError();
+    cudaStream_t st = h->stream, cs = bank->copy;
+    const int E = h->cfg.num_experts, S = bank->S;
+    const bool with_shared = shared_expert != nullptr;
+    const int rows = T * top_k + (with_shared ? T : 0);
+    const long cap = std::min<long>((long)T * top_k, E);
+    const bool cache = cap <= S;
+    const int G = cache ? S : S / 2;
+    const int R = cache ? 2 : (int)((cap + G - 1) / G);
+    int launches = 0, n;
+    h->stage_valid = false;
+    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, false, kNtileMx4, rows, launches))
+        return launch_failed(h);
+    Workspace &ws = h->ws;
+    n = launch_bank_plan(bank->dev, ws.cnt, ws.off, cache, G, R, kNtileMx4, ws.err, st);
+    if (n < 0) return launch_failed(h);
+    launches += n;
+    FfnArgs a = ffn_args(h, x_bf16, T, top_k, rows, nullptr, shared_expert);
+    a.routed = bank->slots;
+    a.w_slots = S;
+    n = launch_quant_x4(a, st);
+    if (n < 0) return launch_failed(h);
+    launches += n;
+    if (cudaEventRecord(bank->ev_plan, st) != cudaSuccess || cudaStreamWaitEvent(cs, bank->ev_plan, 0) != cudaSuccess)
+        return launch_failed(h);
+    // Refills on the copy stream: round r's copies overlap round r - 1's GEMMs. A round's copies
+    // may reuse slots of round r - 2 only, so they wait for that round's down projection.
+    auto refill = [&](int r) -> bool {
+        if (r >= 2 && cudaStreamWaitEvent(cs, bank->ev_done[r - 2], 0) != cudaSuccess) return false;
+        const int blocks = r == 0 ? h->num_sms : bank->copy_blocks;   // round 0's copies run alone
+        if (launch_bank_refill(bank->dev, r, bank->src, bank->slots, bank->eb, blocks, ws.err, cs) < 0) return false;
+        ++launches;
+        return cudaEventRecord(bank->ev_fill[r], cs) == cudaSuccess;
+    };
+    const int first_fill = cache ? 1 : 0;   // a cache forward's round 0 computes resident experts
+    for (int r = first_fill; r < std::min(R, 2); ++r)
+        if (!refill(r)) return launch_failed(h);
+    for (int r = 0; r < R; ++r) {
+        const bool waits = r >= first_fill;
+        if (waits && cudaStreamWaitEvent(st, bank->ev_fill[r], 0) != cudaSuccess) return launch_failed(h);
+        const NtileLayout nl = bank_round_layout(bank->dev, r);
+        a.tiles = &nl;
+        a.grid = r + 1 < R ? h->num_sms - bank->copy_blocks : 0;   // the copy blocks take the rest
+        a.pdl_gate_up = !waits;
+        n = launch_ffn_mx4(a, h->num_sms, nullptr, nullptr, st);
+        if (n == -2) {
+            set_err(h, "FP4 block-scaled GEMM path unavailable (needs a tensor-map encoder)");
+            return COLI_ERR_INVALID_ARG;
+        }
+        if (n < 0) return launch_failed(h);
+        launches += n;
+        if (cudaEventRecord(bank->ev_done[r], st) != cudaSuccess) return launch_failed(h);
+        if (r + 2 < R && !refill(r + 2)) return launch_failed(h);
+    }
+    n = launch_combine(ws.y, ws.inv_row, ws.w, T, h->cfg.hidden, top_k, with_shared,
+                       static_cast<__nv_bfloat16 *>(out_bf16), st);
+    if (n < 0) return launch_failed(h);
+    launches += n;
+    h->last_T = T;
+    h->last_k = top_k;
+    h->last_shared = with_shared;
+    h->last_launches = launches;
+    h->last_path = COLI_FFN_GEMM_MXF4;
     return COLI_OK;
 }
 

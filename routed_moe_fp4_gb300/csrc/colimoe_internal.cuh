@@ -55,6 +55,8 @@ struct Workspace {
     size_t tile_sched_bytes = 0;
 };
 
+struct NtileLayout;
+
 // Arguments of the expert FFN stage: groups 0..E-1 are the routed experts, group E the
 // shared expert. Group g owns rows [off[g], off[g] + cnt[g]) of xp / h / y.
 struct FfnArgs {
@@ -80,6 +82,13 @@ struct FfnArgs {
     uint8_t *xq, *xqs, *hq, *hqs;   // block-scaled paths: activation terms and scales
     int *err;
     uint64_t wait_ns;               // FP4 path: limit of the pipeline waits (0 = the default, 2 s)
+    // FP4 path over an expert bank (bank.cu): the tile layout of one round, whose records name
+    // bank slots instead of experts; the number of slots `routed` holds; the grid (0 = one block
+    // per SM); false when the gate/up launch must not overlap the kernel before it.
+    const NtileLayout *tiles = nullptr;
+    int w_slots = 0;
+    int grid = 0;
+    bool pdl_gate_up = true;
 };
 
 // Programmatic dependent launch. Every kernel of the library is launched with programmatic
@@ -99,9 +108,11 @@ __device__ __forceinline__ void pdl_begin() {
     pdl_wait();
 }
 
+// `pdl` false: an ordinary launch, which starts only after all earlier work of the stream (and
+// the events it waits on) has completed; griddepcontrol.wait then returns at once.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                              Args &&...args) {
+inline cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args &&...args) {
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
@@ -111,8 +122,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+    return launch_k(true, kernel, grid, block, smem, st, std::forward<Args>(args)...);
 }
 
 // Records the text coli_moe_last_error(NULL) returns (printf-style).
@@ -176,6 +193,41 @@ int launch_combine(const float *y, const int32_t *inv_row, const float *w, int T
                    bool with_shared, __nv_bfloat16 *out, cudaStream_t st);
 // Device copy of `bytes` (a multiple of 16, both pointers 16-byte aligned), e.g. from mapped host memory.
 int launch_copy(void *dst, const void *src, size_t bytes, int num_sms, cudaStream_t st);
+
+// Expert residency bank (bank.cu). Device state and per-round buffers of one bank.
+struct BankDev {
+    int E, S, R;                    // experts, slots, rounds the buffers hold
+    size_t nm;                      // n-tiles per round and tile size (ntile_max)
+    int32_t *slot_of;               // [E] slot of a resident expert, -1 otherwise
+    int32_t *expert_in;             // [S] expert in a slot, -1 when empty
+    uint32_t *usage;                // [E] forwards that routed to the expert
+    int32_t *last_use;              // [S] the forward that last used the slot
+    long long *stats;               // [3] forwards, experts found in place, experts copied
+    int2 *copies;                   // [R][S] {expert, slot} refills of each round
+    int32_t *ncopy;                 // [R]
+    int2 *rec_small, *rec_large;    // [R][nm] n-tile records of each round ({row0, slot | n << 16})
+    int32_t *counts;                // [R][2] small and large n-tile counts of each round
+};
+// Byte sizes of one expert's four arrays (gate/up codes and scales, down codes and scales).
+struct ExpertBytes {
+    uint64_t seg[4];
+};
+// The layout of round r's tiles, as the FP4 GEMM reads it.
+inline NtileLayout bank_round_layout(const BankDev &b, int r) {
+    NtileLayout l{};
+    l.rec_small = b.rec_small + (size_t)r * b.nm;
+    l.rec_large = b.rec_large + (size_t)r * b.nm;
+    l.count = b.counts + 2 * r;
+    return l;
+}
+// Plans one forward over the bank from the permutation's cnt/off (after the permute, same
+// stream): cache forward when `cache`, else transient groups of G slots; R rounds are cleared.
+int launch_bank_plan(const BankDev &b, const int32_t *cnt, const int32_t *off, bool cache, int G, int R, int ntile,
+                     int *err, cudaStream_t st);
+// Copies round r's refills from the source experts (device-accessible, e.g. mapped host memory)
+// into their slots.
+int launch_bank_refill(const BankDev &b, int r, const ExpertSet &src, const ExpertSet &dst, const ExpertBytes &eb,
+                       int blocks, int *err, cudaStream_t st);
 
 // Block-scaled MXFP4 tcgen05 GEMM path (gemm_mx.cu): native E2M1 weights x E4M3 activation terms.
 bool mx_available();

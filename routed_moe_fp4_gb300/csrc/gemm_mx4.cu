@@ -698,7 +698,9 @@ int launch_quant_x4(const FfnArgs &a, cudaStream_t st) {
 
 int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
     if (!mx4_supported(a)) return -2;
-    const NtileLayout nl = ntile_layout(sched, a.E, a.rows);
+    const NtileLayout nl = a.tiles ? *a.tiles : ntile_layout(sched, a.E, a.rows);
+    const uint64_t slots = a.w_slots ? a.w_slots : a.E;   // weight sets the routed arrays hold
+    const dim3 grid(a.grid ? a.grid : num_sms);
     const size_t smem = NS * kStageBytes + 1024 + 256;
     static bool attr = false;
     if (!attr) {
@@ -737,12 +739,12 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     p.w_scales_shared = a.shared.gu_scales;
     p.act_scales = a.xqs;
     p.act_ld = a.H;
-    bool ok = map_packed(&tar, a.routed.gu_codes, a.H, (uint64_t)a.E * 2 * a.I, BM) &&
+    bool ok = map_packed(&tar, a.routed.gu_codes, a.H, slots * 2 * a.I, BM) &&
               map_terms(tb, a.xq, a.H, a.rows);
     if (a.shared.gu_codes) ok = ok && map_packed(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_pdl(gemm_mx4<kGateUp>, dim3(num_sms), dim3(kThreads), smem, st, tar, tas, tb, p);
+    launch_k(a.pdl_gate_up, gemm_mx4<kGateUp>, grid, dim3(kThreads), smem, st, tar, tas, tb, p);
     int n = 1;
     if (mid) cudaEventRecord(mid, st);
     // down
@@ -756,11 +758,11 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     p.w_scales_shared = a.shared.d_scales;
     p.act_scales = a.hqs;
     p.act_ld = a.I_max;
-    ok = map_packed(&tar, a.routed.d_codes, a.I, (uint64_t)a.E * a.H, BM) && map_terms(tb, a.hq, a.I_max, a.rows);
+    ok = map_packed(&tar, a.routed.d_codes, a.I, slots * a.H, BM) && map_terms(tb, a.hq, a.I_max, a.rows);
     if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_pdl(gemm_mx4<kDown>, dim3(num_sms), dim3(kThreads), smem, st, tar, tas, tb, p);
+    launch_pdl(gemm_mx4<kDown>, grid, dim3(kThreads), smem, st, tar, tas, tb, p);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }

@@ -7,6 +7,7 @@
 // run. Group E is the shared expert with rows off[E] + t for every token t. The activation rows
 // are gathered into that order (xp) for the expert FFN.
 #include "colimoe_internal.cuh"
+#include "block_scan.cuh"
 #include "topk.cuh"
 
 namespace colimoe {
@@ -16,36 +17,6 @@ __global__ void permute_count(const int32_t *__restrict__ idx, int n, int32_t *_
     pdl_begin();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
         atomicAdd(&cnt[idx[i]], 1);
-}
-
-// Exclusive block scan of one value per thread (blockDim.x == 1024). Returns the exclusive
-// prefix; *total receives the block sum.
-__device__ int block_exclusive_scan(int v, int *smem_warp, int *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-    }
-    if (lane == 31) smem_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = smem_warp[lane];
-        int wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o) wi += n;
-        }
-        smem_warp[lane] = wi - w;          // exclusive prefix of warp sums
-        if (lane == 31) smem_warp[32] = wi;
-    }
-    __syncthreads();
-    const int res = smem_warp[warp] + incl - v;
-    *total = smem_warp[32];
-    __syncthreads();
-    return res;
 }
 
 // One block of 1024 threads; groups g = 0..E (E <= 1024 + shared handled as the last entry).

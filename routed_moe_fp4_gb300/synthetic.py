@@ -184,6 +184,15 @@ def x_row(seed: int, wl_name: str, t: int, H: int, attempt: int = 0) -> np.ndarr
     return f32_to_bf16_bits(z.astype(np.float32))
 
 
+def x_batch(seed: int, wl_name: str, batch: int, T: int, H: int) -> np.ndarray:
+    """A further batch of T token rows (bf16 bits [T, H]) of a workload, batch >= 1: a stream of
+    distinct batches, as successive forwards of a layer see them."""
+    if T == 0:
+        return np.zeros((0, H), np.uint16)
+    return np.stack([f32_to_bf16_bits(normal(stream_key(seed, wl_name, "x-batch", batch, t), H).astype(np.float32))
+                     for t in range(T)])
+
+
 def _expert_arrays(seed: int, tag: str, e: int, H: int, I: int):
     gu_c = random_bytes(stream_key(seed, tag, e, "gate_up_codes"), 2 * I * H // 2).reshape(2 * I, H // 2)
     gu_s = scale_bytes(stream_key(seed, tag, e, "gate_up_scales"), 2 * I * H // 32).reshape(2 * I, H // 32)
