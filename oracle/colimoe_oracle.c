@@ -421,3 +421,39 @@ void coli_oracle_bank_plan(int32_t E, int32_t S, int32_t T, int32_t top_k, const
         stats[2]++;
     }
 }
+
+/* ------------------------------------------------------------------------------------
+ * FP8 dense projection. The pages give the model's dense weights as FP8 E4M3 with one scale
+ * per 128 x 128 block ("DeepSeek V4 Flash CPU inference with NVMe expert streaming", the
+ * review question on config-driven V4 sizes), and move the five per-layer dense matmuls to
+ * the GPU with numerics identical to the CPU path ("DeepSeek V4 Flash support -- CUDA/VRAM
+ * expert tiering", the dense-on-GPU tier comment). E4M3 is the OCP 8-bit float: sign, four
+ * exponent bits with bias 7, three mantissa bits, subnormals at exponent 0, no infinities,
+ * S.1111.111 is NaN. Reading: a block scale multiplies its block's decoded values. */
+double coli_oracle_e4m3(int code) {
+    code &= 255;
+    const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double mag;
+    if (e == 0 && !MUT(24)) mag = ldexp(m / 8.0, -6);
+    else mag = ldexp(1.0 + m / 8.0, e - (MUT(23) ? 8 : 7));
+    return sign ? -mag : mag;
+}
+
+void coli_oracle_fp8_linear(const uint16_t *x, int32_t T, int32_t K, const uint8_t *w, const float *w_scale,
+                            int32_t N, uint16_t *out, double *out_f64) {
+    const int64_t kb = (K + 127) / 128, nb = (N + 127) / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < (int64_t)T * N; ++i) {
+        const int64_t t = i / N, n = i % N;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            int64_t si = (n / 128) * kb + k / 128;
+            if (MUT(25)) si = (k / 128) * nb + n / 128;
+            if (MUT(26)) si = (n / 128) * kb;
+            acc += coli_oracle_bf16(x[t * K + k]) * coli_oracle_e4m3(w[n * K + k]) * (double)w_scale[si];
+        }
+        out[i] = coli_oracle_round_bf16(acc);
+        if (out_f64) out_f64[i] = acc;
+    }
+}

@@ -104,6 +104,14 @@ void coli_oracle_bank_plan(int32_t E, int32_t S, int32_t T, int32_t top_k, const
                            int32_t *slot_of, int32_t *expert_in, uint32_t *usage, int32_t *last_use,
                            int64_t *stats, int32_t *round_of, int32_t *slot_for, int32_t *copied);
 
+/* --- FP8 dense projection --- */
+double coli_oracle_e4m3(int code);          /* value of an OCP E4M3 byte (NaN for S.1111.111) */
+/* out[t][n] = round_bf16(sum_k x[t][k] * e4m3(w[n][k]) * w_scale[n/128][k/128]) in fp64.
+ * x bf16 bits [T][K]; w E4M3 codes [N][K]; w_scale fp32 [ceil(N/128)][ceil(K/128)];
+ * out_f64 (may be NULL) receives the unrounded sums. OpenMP over outputs when built with it. */
+void coli_oracle_fp8_linear(const uint16_t *x, int32_t T, int32_t K, const uint8_t *w, const float *w_scale,
+                            int32_t N, uint16_t *out, double *out_f64);
+
 #ifdef __cplusplus
 }
 #endif

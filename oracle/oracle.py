@@ -61,6 +61,9 @@ class Oracle:
                                               _f32p, _i32p, _f32p, _i32p, _i32p, _i32p, _i32p, _u16p, _f64p]
         L.coli_oracle_bank_plan.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int32, _i32p,
                                             _i32p, _i32p, _u32p, _i32p, _i64p, _i32p, _i32p, _i32p]
+        L.coli_oracle_e4m3.restype = C.c_double
+        L.coli_oracle_e4m3.argtypes = [C.c_int]
+        L.coli_oracle_fp8_linear.argtypes = [_u16p, C.c_int32, C.c_int32, _u8p, _f32p, C.c_int32, _u16p, _f64p]
         L.coli_oracle_threads.restype = C.c_int32
         L.coli_oracle_mutant.restype = C.c_int32
 
@@ -73,6 +76,22 @@ class Oracle:
 
     def mxfp4(self, codes: np.ndarray, scales: np.ndarray, K: int, row: int, k: int) -> float:
         return self.lib.coli_oracle_mxfp4(_p(codes, _u8p), _p(scales, _u8p), K, row, k)
+
+    def e4m3(self, code: int) -> float:
+        return self.lib.coli_oracle_e4m3(code)
+
+    def fp8_linear(self, x: np.ndarray, w: np.ndarray, w_scale: np.ndarray):
+        """out bf16 bits [T, N] and fp64 sums of x [T, K] (bf16 bits) times the E4M3 block-scaled w [N, K]."""
+        x = np.ascontiguousarray(x, np.uint16)
+        w = np.ascontiguousarray(w, np.uint8)
+        sc = np.ascontiguousarray(w_scale, np.float32)
+        T, K = x.shape
+        N = w.shape[0]
+        out = np.zeros((T, N), np.uint16)
+        out64 = np.zeros((T, N), np.float64)
+        self.lib.coli_oracle_fp8_linear(_p(x, _u16p), T, K, _p(w, _u8p), _p(sc, _f32p), N, _p(out, _u16p),
+                                        _p(out64, _f64p))
+        return out, out64
 
     def bf16(self, bits: int) -> float:
         return self.lib.coli_oracle_bf16(bits)

@@ -463,6 +463,65 @@ def pin_bank_stream(o):
             last[e] = f
 
 
+# ---- FP8 dense projection -----------------------------------------------------------------
+
+def e4m3_values() -> dict:
+    """Every finite OCP E4M3 value by construction: normals (1 + m/8) * 2^(e - 7) for exponent
+    fields 1..15 (mantissa 7 excluded at 15, that code is NaN), subnormals (m/8) * 2^-6."""
+    vals = {}
+    for sign in (0, 1):
+        for e in range(16):
+            for m in range(8):
+                if e == 15 and m == 7:
+                    continue
+                mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+                vals[(sign << 7) | (e << 3) | m] = -mag if sign else mag
+    return vals
+
+
+def pin_e4m3(o):
+    """E4M3 against the OCP FP8 spec: 1.0 = 0x38, max 448 = 0x7E, smallest subnormal 2^-9,
+    smallest normal 2^-6, NaN at S.1111.111, and every code by its fields."""
+    fixed = {0x38: 1.0, 0x7E: 448.0, 0xFE: -448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6, 0x00: 0.0, 0x40: 2.0,
+             0x30: 0.5, 0x3C: 1.5, 0x07: 7 * 2.0 ** -9}
+    for c, v in fixed.items():
+        assert o.e4m3(c) == v, (hex(c), o.e4m3(c), v)
+    assert math.isnan(o.e4m3(0x7F)) and math.isnan(o.e4m3(0xFF))
+    for c, v in e4m3_values().items():
+        assert o.e4m3(c) == v, (hex(c), o.e4m3(c), v)
+
+
+def fp8_case(rng, T, K, N, pow2_scales=False):
+    """x bf16 bits [T, K], E4M3 codes [N, K] (no NaN codes), fp32 block scales."""
+    x = random_bf16(rng, (T, K))
+    w = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    w[(w & 0x7F) == 0x7F] ^= 1                        # NaN codes -> 0x7E / 0xFE
+    nb, kb = -(-N // 128), -(-K // 128)
+    if pow2_scales:
+        sc = (2.0 ** rng.integers(-12, -4, (nb, kb))).astype(np.float32)
+    else:
+        sc = (rng.uniform(1.0, 2.0, (nb, kb)) * 2.0 ** rng.integers(-12, -4, (nb, kb))).astype(np.float32)
+    return x, w, sc
+
+
+def pin_fp8_linear(o):
+    """The projection equals numpy's matmul of the bf16 activations and the weights decoded by
+    their E4M3 fields, each 128 x 128 block multiplied by its scale (blocks 2 x 3: a transposed or
+    dropped block index fails)."""
+    rng = _rng(50)
+    table = np.zeros(256)
+    for c, v in e4m3_values().items():
+        table[c] = v
+    for T, K, N in ((3, 384, 256), (1, 128, 128), (5, 256, 384)):
+        x, w, sc = fp8_case(rng, T, K, N)
+        W = table[w] * np.repeat(np.repeat(sc.astype(np.float64), 128, 0), 128, 1)[:N, :K]
+        ref = bf16_to_f64(x) @ W.T
+        out, out64 = o.fp8_linear(x, w, sc)
+        assert np.allclose(out64, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), (T, K, N)
+        for v, b in zip(ref.ravel()[:64], out.ravel()[:64]):
+            assert b == nearest_bf16_bits(float(v))
+
+
 ALL_PINS = [pin_e2m1_table, pin_e8m0, pin_nibble_order, pin_route_bruteforce, pin_route_weights,
             pin_permute, pin_dense_swiglu, pin_dense_gated, pin_sigmoid, pin_logits, pin_round_bf16,
-            pin_bank_cache, pin_bank_full, pin_bank_hot_expert, pin_bank_stream]
+            pin_bank_cache, pin_bank_full, pin_bank_hot_expert, pin_bank_stream, pin_e4m3, pin_fp8_linear]
