@@ -439,6 +439,112 @@ def run_bank(args, wl_name: str) -> dict:
     return result if rank == 0 else None
 
 
+def run_dense(args, name: str) -> dict:
+    """The FP8 dense projection: each step is one projection of the workload's T token rows."""
+    import torch
+    import torch.distributed as dist
+    from routed_moe_fp4_gb300 import build, colimoe as cm
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    inputs = S.make_dense_inputs(name)
+    wl = inputs.workload
+    stream = torch.cuda.Stream()
+    layer = cm.DenseLayer(inputs, stream=stream)
+    x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
+    out = torch.empty((wl.T, wl.N), dtype=torch.int16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def l2_flush():
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+
+    for _ in range(args.warmup):
+        layer.forward(x, out)
+    stream.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        l2_flush()
+        starts[i].record(stream)
+        layer.forward(x, out)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), device="cuda") / args.steps
+    assert layer.device_error() == 0
+
+    x_host = torch.from_numpy(inputs.x.view(np.int16).copy()).pin_memory()
+    out_host = torch.empty((wl.T, wl.N), dtype=torch.int16).pin_memory()
+    e2e = []
+    for i in range(args.steps + 2):
+        l2_flush()
+        stream.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            x.copy_(x_host, non_blocking=True)
+            layer.forward(x, out)
+            out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
+        if i >= 2:
+            e2e.append((time.perf_counter() - t0) * 1e3)
+    e2e_ms = sum(e2e) / len(e2e)
+
+    hbm_gbs, bf16_tf, peak_kind = _peaks()
+    fp8_tf = 2.0 * bf16_tf                       # nominal FP8 / bf16 dense ratio (4.5 / 2.25)
+    nbytes = wl.N * wl.K + 4 * (wl.N // 128) * (wl.K // 128) + 2 * wl.T * wl.K + 2 * wl.T * wl.N
+    flops = 2.0 * wl.T * wl.N * wl.K
+    t_hbm, t_tc = nbytes / (hbm_gbs * 1e9), flops / (fp8_tf * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": hbm_gbs, "unit": "GB/s",
+                "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": nbytes}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": fp8_tf, "unit": "TFLOP/s",
+                "peak_source": f"{peak_kind} bf16_tflops x 2 (nominal FP8/bf16 ratio)", "algorithmic_flops": flops}
+    roof.update({"kernel": "gemm_fp8 (with its activation split)", "frac": roof["achieved"] / roof["peak"],
+                 "traffic": None, "kernel_ms": ms})
+    tokens = wl.T * ws
+    res = {
+        "metric": "FP8 dense projection tokens/s at 1 GB300", "value": tokens / (ms * 1e-3), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 weights x two e4m3 activation terms, fp32 accumulate, fp32 block-scale folding",
+        "data": "synthetic (seeded SplitMix64; E4M3 weights with fp32 128x128 block scales, bf16 activations)",
+        "config": {"workload": f"{wl.name}: T={wl.T}, K={wl.K}, N={wl.N}, E4M3 + fp32 scale per 128x128",
+                   "tokens_per_gpu": wl.T, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "flushed (512 MiB write) before every timed step"},
+        "roofline": roof,
+        "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clock_info,
+    }
+    if not args.skip_cpu and rank == 0:
+        from oracle.oracle import Oracle
+        o = Oracle()
+        rows, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_budget:
+            o.fp8_linear(inputs.x[: min(8, wl.T)], inputs.w, inputs.w_scale)
+            rows += min(8, wl.T)
+        el = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": rows / el, "unit": "tokens/s", "cores": o.threads(), "kind": "oracle",
+                               "sample": f"{rows} token rows of {wl.name} through the oracle, {el:.1f} s"}
+    layer.close()
+    if ws > 1:
+        dist.destroy_process_group()
+    return res if rank == 0 else None
+
+
 def oracle_sample(wl_name: str, budget_s: float):
     """Times the oracle's full forward on the workload's tokens, repeated up to `budget_s`."""
     from oracle.oracle import Oracle
@@ -501,12 +607,18 @@ def main():
     ap.add_argument("--bank", type=int, default=0,
                     help="routed experts in page-locked host memory behind a bank of this many device slots")
     ap.add_argument("--copy-blocks", type=int, default=0, help="bank: blocks that copy while a round computes")
+    ap.add_argument("--dense", default="", choices=[""] + sorted(S.DENSE_WORKLOADS),
+                    help="time the FP8 dense projection on this workload instead of the MoE layer")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         res = run_reference(args, args.workload)
     else:
-        res = run_bank(args, args.workload) if args.bank else run_ours(args, args.workload)
+        if args.dense:
+            res = run_dense(args, args.dense)
+            args.skip_cpu = True                 # run_dense times its own oracle sample
+        else:
+            res = run_bank(args, args.workload) if args.bank else run_ours(args, args.workload)
         if res is not None and not args.skip_cpu:
             res["cpu_baseline"] = oracle_sample(args.workload, args.cpu_budget)
     if res is not None:

@@ -282,6 +282,32 @@ COLI_API int coli_bank_set_copy_blocks(coli_expert_bank_t *bank, int32_t blocks)
 COLI_API int coli_bank_state(coli_expert_bank_t *bank, int32_t *slot_of, int32_t *expert_in, uint32_t *usage,
                              int32_t *last_use, int64_t *stats);
 
+/* ---------------------------------------------------------------------------------------------
+ * FP8 dense projection: out[t][n] = bf16(sum_k x[t][k] * e4m3(w[n][k]) * w_scale[n/128][k/128]),
+ * the weight format the pages give for the model's dense matrices: FP8 E4M3 with one fp32 scale
+ * per 128 x 128 block ("DeepSeek V4 Flash CPU inference with NVMe expert streaming", the review
+ * question on config-driven V4 sizes; the five per-layer dense matmuls of "DeepSeek V4 Flash
+ * support -- CUDA/VRAM expert tiering", dense-on-GPU tier comment). E4M3 is the OCP 8-bit float
+ * (bias 7, subnormals, max 448, S.1111.111 NaN); the output is the exact sum rounded once, up to the
+ * activation split (x enters as two E4M3 terms under a per-token power-of-two scale, about 2^-9
+ * relative per element) and fp32 accumulation.
+ *
+ * A dense handle holds the workspace for up to max_tokens rows of up to max_k features and is
+ * bound to one stream. Layout: x bf16 [T][K], w E4M3 codes [N][K] (K-major rows), w_scale fp32
+ * [N/128][K/128], out bf16 [T][N]; all device pointers owned by the caller; K and N multiples of 128.
+ * coli_dense_forward enqueues two kernels on the stream, returns without synchronising and
+ * allocates nothing; forwards on one handle must not overlap on the device. */
+typedef struct coli_dense coli_dense_t;
+COLI_API int coli_dense_create(int32_t max_tokens, int32_t max_k, void *cuda_stream, coli_dense_t **out);
+COLI_API int coli_dense_forward(coli_dense_t *d, const void *x_bf16, int32_t T, int32_t K, const uint8_t *w_e4m3,
+                                const float *w_scale, int32_t N, void *out_bf16);
+COLI_API void coli_dense_destroy(coli_dense_t *d);
+/* Text of the last error on d (or of the last failed coli_dense_create when d is NULL). */
+COLI_API const char *coli_dense_last_error(const coli_dense_t *d);
+/* Synchronises d's stream, returns the device error word (0: none; a bounded wait that ran out
+ * records its code, as for coli_moe_device_error) and clears it. */
+COLI_API int coli_dense_device_error(coli_dense_t *d, int32_t *code);
+
 #ifdef __cplusplus
 }
 #endif

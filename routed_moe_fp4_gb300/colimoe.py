@@ -25,7 +25,8 @@ EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "col
             "coli_moe_last_launch_count", "coli_moe_last_ffn_path", "coli_moe_set_profiling", "coli_moe_stage_times",
             "coli_moe_device_error", "coli_moe_set_wait_limit", "coli_moe_route_static",
             "coli_bank_create", "coli_bank_destroy", "coli_moe_forward_banked", "coli_bank_set_copy_blocks",
-            "coli_bank_state")
+            "coli_bank_state", "coli_dense_create", "coli_dense_forward", "coli_dense_destroy",
+            "coli_dense_last_error", "coli_dense_device_error")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
 
@@ -105,6 +106,16 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_bank_set_copy_blocks.restype = C.c_int
     lib.coli_bank_state.argtypes = [vp, vp, vp, vp, vp, vp]
     lib.coli_bank_state.restype = C.c_int
+    lib.coli_dense_create.argtypes = [C.c_int32, C.c_int32, vp, C.POINTER(vp)]
+    lib.coli_dense_create.restype = C.c_int
+    lib.coli_dense_forward.argtypes = [vp, vp, C.c_int32, C.c_int32, vp, vp, C.c_int32, vp]
+    lib.coli_dense_forward.restype = C.c_int
+    lib.coli_dense_destroy.argtypes = [vp]
+    lib.coli_dense_destroy.restype = None
+    lib.coli_dense_last_error.argtypes = [vp]
+    lib.coli_dense_last_error.restype = C.c_char_p
+    lib.coli_dense_device_error.argtypes = [vp, C.POINTER(C.c_int32)]
+    lib.coli_dense_device_error.restype = C.c_int
     _lib = lib
     return lib
 
@@ -375,3 +386,68 @@ class ExpertBank:
             coli_bank_destroy(self.b)
             self.b = None
             self.layer._banks.remove(self)
+
+
+# ---- FP8 dense projection -----------------------------------------------------------------
+
+def coli_dense_last_error(d=None) -> str:
+    return load().coli_dense_last_error(d).decode()
+
+
+def _dcheck(d, rc: int) -> int:
+    if rc != COLI_OK:
+        raise ColiError(rc, coli_dense_last_error(d))
+    return rc
+
+
+def coli_dense_create(max_tokens: int, max_k: int, cuda_stream=None) -> C.c_void_p:
+    st = getattr(cuda_stream, "cuda_stream", cuda_stream)
+    out = C.c_void_p()
+    _dcheck(None, load().coli_dense_create(max_tokens, max_k, st, C.byref(out)))
+    return out
+
+
+def coli_dense_forward(d, x_bf16, T: int, K: int, w_e4m3, w_scale, N: int, out_bf16) -> int:
+    return _dcheck(d, load().coli_dense_forward(d, _ptr(x_bf16), T, K, _ptr(w_e4m3), _ptr(w_scale), N,
+                                                _ptr(out_bf16)))
+
+
+def coli_dense_destroy(d) -> None:
+    load().coli_dense_destroy(d)
+
+
+def coli_dense_device_error(d) -> int:
+    code = C.c_int32(0)
+    _dcheck(d, load().coli_dense_device_error(d, C.byref(code)))
+    return code.value
+
+
+class DenseLayer:
+    """A dense handle plus device copies of one FP8 projection's weights (E4M3 codes, block scales)."""
+
+    def __init__(self, inputs, max_tokens: Optional[int] = None, stream=None, device="cuda"):
+        import torch
+        wl = inputs.workload
+        self.wl = wl
+        self.w = torch.from_numpy(inputs.w).to(device)
+        self.w_scale = torch.from_numpy(inputs.w_scale).to(device)
+        self.stream = stream
+        self.d = coli_dense_create(max_tokens or max(wl.T, 1), wl.K, stream)
+
+    def forward(self, x, out, T: Optional[int] = None) -> None:
+        T = x.shape[0] if T is None else T
+        coli_dense_forward(self.d, x, T, self.wl.K, self.w, self.w_scale, self.wl.N, out)
+
+    def device_error(self) -> int:
+        return coli_dense_device_error(self.d)
+
+    def close(self) -> None:
+        if self.d:
+            coli_dense_destroy(self.d)
+            self.d = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -229,6 +229,23 @@ int launch_bank_plan(const BankDev &b, const int32_t *cnt, const int32_t *off, b
 int launch_bank_refill(const BankDev &b, int r, const ExpertSet &src, const ExpertSet &dst, const ExpertBytes &eb,
                        int blocks, int *err, cudaStream_t st);
 
+// FP8 dense projection (gemm_fp8.cu): out [T][N] bf16 = x [T][K] bf16 times the E4M3 weights
+// w [N][K] with fp32 scales w_scale [N/128][K/128]; K and N multiples of 128. xq ([2][T][K]) and
+// xs ([T]) are workspace for the two E4M3 terms of x and the per-token scales.
+struct DenseArgs {
+    const __nv_bfloat16 *x;
+    int T, K, N;
+    const uint8_t *w;
+    const float *w_scale;
+    uint8_t *xq;
+    float *xs;
+    __nv_bfloat16 *out;
+    int *err;
+    uint64_t wait_ns;
+};
+bool fp8_available();
+int launch_dense_fp8(const DenseArgs &a, int num_sms, cudaStream_t st);
+
 // Block-scaled MXFP4 tcgen05 GEMM path (gemm_mx.cu): native E2M1 weights x E4M3 activation terms.
 bool mx_available();
 bool mx_supported(const FfnArgs &a);

@@ -264,3 +264,55 @@ def make_inputs(name, seed: int = 0, T: Optional[int] = None, with_experts: bool
 def expert_bytes(H: int, I: int) -> int:
     """Bytes of one MXFP4 expert (gate, up and down matrices with their scales)."""
     return 3 * H * I // 2 + 3 * H * I // 32
+
+
+# --------------------------------------------------------------------------------------
+# FP8 dense projections (y = x W^T, W E4M3 with one fp32 scale per 128 x 128 block)
+
+
+@dataclasses.dataclass(frozen=True)
+class DenseWorkload:
+    name: str
+    T: int
+    K: int            # input features (x columns, W columns)
+    N: int            # output features (W rows)
+
+
+# One per-layer dense projection of the hidden-4096 model (a 4096 x 4096 matrix: the pages name
+# the five projections but not their sizes), in decode and prefill, plus a small ragged case.
+DENSE_WORKLOADS: Dict[str, DenseWorkload] = {
+    "dense_tiny": DenseWorkload("dense_tiny", 5, 384, 256),
+    "dense_decode": DenseWorkload("dense_decode", 8, 4096, 4096),
+    "dense_prefill": DenseWorkload("dense_prefill", 512, 4096, 4096),
+}
+
+
+@dataclasses.dataclass
+class DenseInputs:
+    workload: DenseWorkload
+    x: np.ndarray          # uint16 bf16 bits [T, K]
+    w: np.ndarray          # uint8 E4M3 codes [N, K]
+    w_scale: np.ndarray    # float32 [ceil(N/128), ceil(K/128)]
+
+
+def e4m3_codes(key: int, count: int) -> np.ndarray:
+    """E4M3 bytes shaped like block-quantised weights, built from their bit fields: a random sign,
+    exponent field 14 - floor(|N(0, 2.5)|) clipped to [0, 14], a uniform 3-bit mantissa."""
+    z = np.abs(normal(key, count))
+    e = np.clip(14 - np.floor(2.5 * z), 0, 14).astype(np.uint8)
+    r = random_bytes(_mix64_int(key ^ 0x3C3C3C3C3C3C3C3C), count)
+    return ((r & np.uint8(0x80)) | (e << np.uint8(3)) | (r & np.uint8(7))).astype(np.uint8)
+
+
+def make_dense_inputs(name, seed: int = 0, T: Optional[int] = None) -> DenseInputs:
+    wl = DENSE_WORKLOADS[name] if isinstance(name, str) else name
+    if T is not None:
+        wl = dataclasses.replace(wl, T=T)
+    x = np.stack([x_row(seed, wl.name, t, wl.K) for t in range(wl.T)]) if wl.T > 0 \
+        else np.zeros((0, wl.K), np.uint16)
+    w = e4m3_codes(stream_key(seed, wl.name, "w"), wl.N * wl.K).reshape(wl.N, wl.K)
+    nb, kb = -(-wl.N // 128), -(-wl.K // 128)
+    u = uniform01(stream_key(seed, wl.name, "w_scale_m"), nb * kb)
+    p = np.floor(uniform01(stream_key(seed, wl.name, "w_scale_e"), nb * kb) * 5)
+    sc = ((1.0 + u) * 2.0 ** (-14 + p)).astype(np.float32).reshape(nb, kb)
+    return DenseInputs(wl, x, w, sc)
