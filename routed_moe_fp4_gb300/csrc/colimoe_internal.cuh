@@ -240,9 +240,12 @@ struct DenseArgs {
     uint8_t *xq;
     float *xs;
     __nv_bfloat16 *out;
+    float *part;          // split-K partial sums: min(max_tokens, kSplitMaxTokens) x 128 x SMs floats
+    int *cnt;             // SMs split-K arrival counters
     int *err;
     uint64_t wait_ns;
 };
+constexpr int kSplitMaxTokens = 64;   // the FP8 GEMM splits K only up to this many tokens
 bool fp8_available();
 int launch_dense_fp8(const DenseArgs &a, int num_sms, cudaStream_t st);
 

@@ -16,6 +16,8 @@ struct coli_dense {
     int num_sms = 0;
     uint8_t *xq = nullptr;     // [2][max_tokens][max_k] E4M3 terms of x
     float *xs = nullptr;       // [max_tokens] token scales
+    float *part = nullptr;     // split-K partial sums
+    int *cnt = nullptr;        // split-K arrival counters [SMs]
     int *err = nullptr;        // device error word
     uint64_t wait_ns = 0;
     char msg[256] = {0};
@@ -38,6 +40,8 @@ bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 void free_dense(coli_dense_t *d) {
     if (d->xq) cudaFree(d->xq);
     if (d->xs) cudaFree(d->xs);
+    if (d->part) cudaFree(d->part);
+    if (d->cnt) cudaFree(d->cnt);
     if (d->err) cudaFree(d->err);
     delete d;
 }
@@ -76,7 +80,10 @@ int coli_dense_create(int32_t max_tokens, int32_t max_k, void *cuda_stream, coli
     d->stream = static_cast<cudaStream_t>(cuda_stream);
     d->num_sms = prop.multiProcessorCount;
     const size_t tk = (size_t)max_tokens * max_k;
+    const size_t part = (size_t)(max_tokens < kSplitMaxTokens ? max_tokens : kSplitMaxTokens) * 128 * d->num_sms;
     if (cudaMalloc(&d->xq, 2 * tk + 256) != cudaSuccess || cudaMalloc(&d->xs, 4 * (size_t)max_tokens + 256) != cudaSuccess ||
+        cudaMalloc(&d->part, 4 * part + 256) != cudaSuccess || cudaMalloc(&d->cnt, 4 * (size_t)d->num_sms + 256) != cudaSuccess ||
+        cudaMemset(d->cnt, 0, 4 * (size_t)d->num_sms) != cudaSuccess ||
         cudaMalloc(&d->err, 256) != cudaSuccess || cudaMemset(d->err, 0, sizeof(int)) != cudaSuccess) {
         cudaGetLastError();
         free_dense(d);
@@ -115,6 +122,8 @@ int coli_dense_forward(coli_dense_t *d, const void *x_bf16, int32_t T, int32_t K
     a.xq = d->xq;
     a.xs = d->xs;
     a.out = static_cast<__nv_bfloat16 *>(out_bf16);
+    a.part = d->part;
+    a.cnt = d->cnt;
     a.err = d->err;
     a.wait_ns = d->wait_ns;
     const int n = launch_dense_fp8(a, d->num_sms, d->stream);

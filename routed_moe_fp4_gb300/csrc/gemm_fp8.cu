@@ -40,12 +40,43 @@ constexpr int kTmemCols = 512;
 
 struct Fp8Params {
     int T, K, N, n_blocks, t_tiles;
+    int ksplit, kper;              // K split into ksplit ranges of kper 128-blocks (ksplit 1: none)
     const float *w_scale;          // [N/128][K/128]
     const float *x_scale;          // [T] 2^e per token
     __nv_bfloat16 *out;            // [T][N]
+    float *part;                   // [ksplit][T][N] partial sums of a split K
+    int *cnt;                      // [n_blocks * t_tiles] arrivals of the splits of a tile
     int *err;
     uint64_t wait_ns;
 };
+
+// Tile `tile` = (K range sp, token block tb, weight block nb), weight blocks fastest.
+struct Fp8Tile {
+    int nb, tb, sp, k0, k1, id;
+};
+__device__ __forceinline__ Fp8Tile fp8_tile(const Fp8Params &p, int tile) {
+    Fp8Tile t;
+    const int per = p.n_blocks * p.t_tiles, r = tile % per;
+    t.sp = tile / per;
+    t.nb = r % p.n_blocks;
+    t.tb = r / p.n_blocks;
+    t.id = r;
+    t.k0 = t.sp * p.kper;
+    t.k1 = min(p.K / KB, t.k0 + p.kper);
+    return t;
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     uint64_t d = (uint64_t)((saddr & 0x3FFFF) >> 4);
@@ -82,6 +113,7 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
              *drain = bar + 2 * NS + 4;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2 * NS + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = abort_flag + 1;
     constexpr int NC = 2 * BN;                                // MMA N: both terms
     constexpr uint32_t kBBytes = NC * KB;
 
@@ -107,43 +139,42 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int nk = p.K / KB;
-    const int total = p.n_blocks * p.t_tiles;
+    const int total = p.n_blocks * p.t_tiles * p.ksplit;
 
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
             ptx::prefetch_tmap(&tm_w);
             const uint64_t pol = ptx::policy_evict_first();
-            auto issue_w = [&](int tile, int k, int s) {
+            auto issue_w = [&](const Fp8Tile &tl, int k, int s) {
                 const uint32_t fb = ptx::smem_addr(&full[s]);
                 ptx::mbar_arrive_expect_tx(fb, kASmem + kBBytes);
-                ptx::tma_load_2d_hint(ptx::smem_addr(smem + s * kStageBytes), &tm_w, k * KB,
-                                      (tile % p.n_blocks) * BM, fb, pol);
+                ptx::tma_load_2d_hint(ptx::smem_addr(smem + s * kStageBytes), &tm_w, k * KB, tl.nb * BM, fb, pol);
             };
-            auto issue_x = [&](int tile, int k, int s) {
+            auto issue_x = [&](const Fp8Tile &tl, int k, int s) {
                 const uint32_t fb = ptx::smem_addr(&full[s]);
                 const uint32_t st = ptx::smem_addr(smem + s * kStageBytes) + kASmem;
-                const int t0 = (tile / p.n_blocks) * BN;
-                ptx::tma_load_2d(st, &tm_x0, k * KB, t0, fb);
-                ptx::tma_load_2d(st + BN * KB, &tm_x1, k * KB, t0, fb);
+                ptx::tma_load_2d(st, &tm_x0, k * KB, tl.tb * BN, fb);
+                ptx::tma_load_2d(st + BN * KB, &tm_x1, k * KB, tl.tb * BN, fb);
             };
             const int first = blockIdx.x;
-            const int pre = first < total ? min(NS, nk) : 0;
-            for (int k = 0; k < pre; ++k) issue_w(first, k, k);
+            const Fp8Tile tf = fp8_tile(p, first);
+            const int pre = first < total ? min(NS, tf.k1 - tf.k0) : 0;
+            for (int k = 0; k < pre; ++k) issue_w(tf, tf.k0 + k, k);
             pdl_wait();
             pdl_trigger();
-            for (int k = 0; k < pre; ++k) issue_x(first, k, k);
+            for (int k = 0; k < pre; ++k) issue_x(tf, tf.k0 + k, k);
             uint32_t it = 0;
             for (int tile = first; tile < total && !*abort_flag; tile += gridDim.x) {
-                for (int k = 0; k < nk; ++k, ++it) {
-                    if (tile == first && k < pre) continue;
+                const Fp8Tile tl = fp8_tile(p, tile);
+                for (int k = tl.k0; k < tl.k1; ++k, ++it) {
+                    if (tile == first && k - tl.k0 < pre) continue;
                     const int s = it % NS;
                     if (!ptx::mbar_wait(ptx::smem_addr(&empty[s]), ((it / NS) & 1u) ^ 1u, p.err, ptx::kErrWaitEmpty,
                                         abort_flag, p.wait_ns))
                         break;
-                    issue_w(tile, k, s);
-                    issue_x(tile, k, s);
+                    issue_w(tl, k, s);
+                    issue_x(tl, k, s);
                 }
             }
             const uint32_t issued = it > (uint32_t)pre ? it : (uint32_t)pre;
@@ -161,7 +192,8 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
             uint32_t it = 0, u = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
-                for (int k = 0; k < nk; ++k, ++it, ++u) {
+                const Fp8Tile tl = fp8_tile(p, tile);
+                for (int k = tl.k0; k < tl.k1; ++k, ++it, ++u) {
                     const int s = it % NS, b = u & 1;
                     if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[b]), ((u >> 1) & 1u) ^ 1u, p.err,
                                         ptx::kErrWaitAccum, abort_flag, p.wait_ns) ||
@@ -190,19 +222,22 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
         const int quad = warp & 3, half = (warp - 2) >> 2;
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t u = 0;
-        for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-            const int nb = tile % p.n_blocks, t0 = (tile / p.n_blocks) * BN + half * H2;
-            const int n = nb * BM + quad * 32 + lane;
-            const float *wsc = p.w_scale + (size_t)nb * nk;
+        // Every epilogue warp walks every tile of the block, also after an abort (its waits then
+        // return at once), so that the split-K named barriers below are always met by all eight.
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const Fp8Tile tl = fp8_tile(p, tile);
+            const int t0 = tl.tb * BN + half * H2;
+            const int n = tl.nb * BM + quad * 32 + lane;
+            const float *wsc = p.w_scale + (size_t)tl.nb * (p.K / KB);
             float acc[H2];
 #pragma unroll
             for (int j = 0; j < H2; ++j) acc[j] = 0.f;
-            float s_next = __ldg(wsc);
+            float s_next = __ldg(wsc + tl.k0);
             bool ok = true;
-            for (int k = 0; k < nk; ++k, ++u) {
+            for (int k = tl.k0; k < tl.k1; ++k, ++u) {
                 const int b = u & 1;
                 const float s = s_next;
-                if (k + 1 < nk) s_next = __ldg(wsc + k + 1);
+                if (k + 1 < tl.k1) s_next = __ldg(wsc + k + 1);
                 if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[b]), (u >> 1) & 1u, p.err, ptx::kErrWaitAccum,
                                     abort_flag, p.wait_ns)) {
                     ok = false;
@@ -210,25 +245,68 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
                 }
                 ptx::tc_fence_after();
                 const uint32_t base = lane_base + b * NC + half * H2;
+                if constexpr (H2 >= 32) {
 #pragma unroll
-                for (int c = 0; c < H2; c += 8) {
-                    uint32_t r0[8], r1[8];
-                    ptx::tmem_ld8(base + c, r0);
-                    ptx::tmem_ld8(base + BN + c, r1);
-                    ptx::tmem_ld_wait();
+                    for (int c = 0; c < H2; c += 32) {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld32(base + c, r0);
+                        tmem_ld32(base + BN + c, r1);
+                        ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[c + j] = fmaf(s, __uint_as_float(r0[j]) + __uint_as_float(r1[j]), acc[c + j]);
+                        for (int j = 0; j < 32; ++j)
+                            acc[c + j] = fmaf(s, __uint_as_float(r0[j]) + __uint_as_float(r1[j]), acc[c + j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < H2; c += 8) {
+                        uint32_t r0[8], r1[8];
+                        ptx::tmem_ld8(base + c, r0);
+                        ptx::tmem_ld8(base + BN + c, r1);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            acc[c + j] = fmaf(s, __uint_as_float(r0[j]) + __uint_as_float(r1[j]), acc[c + j]);
+                    }
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&acc_empty[b]));
             }
-            if (!ok) break;
+            if (p.ksplit == 1) {
+                if (!ok) continue;
 #pragma unroll
-            for (int j = 0; j < H2; ++j) {
-                const int t = t0 + j;
-                if (t < p.T) p.out[(size_t)t * p.N + n] = __float2bfloat16_rn(acc[j] * __ldg(p.x_scale + t));
+                for (int j = 0; j < H2; ++j) {
+                    const int t = t0 + j;
+                    if (t < p.T) p.out[(size_t)t * p.N + n] = __float2bfloat16_rn(acc[j] * __ldg(p.x_scale + t));
+                }
+                continue;
             }
+            // Split K: every split stores its partial sums; the last split of the tile to arrive adds
+            // them in split order (the same result whichever arrives last) and writes out.
+            if (ok) {
+#pragma unroll
+                for (int j = 0; j < H2; ++j)
+                    if (t0 + j < p.T) p.part[((size_t)tl.sp * p.T + t0 + j) * p.N + n] = acc[j];
+            }
+            __threadfence();
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+            if (warp == 2 && lane == 0)
+                *last_flag = !*abort_flag && atomicAdd(p.cnt + tl.id, 1) == p.ksplit - 1;
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
+            if (*last_flag && ok) {
+                __threadfence();
+#pragma unroll
+                for (int j = 0; j < H2; ++j) {
+                    const int t = t0 + j;
+                    if (t >= p.T) continue;
+                    float sum = 0.f;
+                    for (int s2 = 0; s2 < p.ksplit; ++s2)
+                        sum += s2 == tl.sp ? acc[j] : __ldcg(p.part + ((size_t)s2 * p.T + t) * p.N + n);
+                    p.out[(size_t)t * p.N + n] = __float2bfloat16_rn(sum * __ldg(p.x_scale + t));
+                }
+                if (warp == 2 && lane == 0) p.cnt[tl.id] = 0;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");   // last_flag reuse
         }
     }
 
@@ -242,10 +320,14 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
 
 // x [T][K] bf16 -> two E4M3 terms [2][T][K] and the token scale 2^e ([T]): e = floor(log2 max|x|) - 7,
 // so |x| 2^-e < 256 (within E4M3's 448); q1 = e4m3(x 2^-e), q2 = e4m3(x 2^-e - q1). One block per token.
+// Block 0 also clears the split-K arrival counters (left non-zero only by a forward that gave up).
 __global__ void __launch_bounds__(256) quant_x_e4m3(const __nv_bfloat16 *__restrict__ x, int T, int K,
-                                                    uint8_t *__restrict__ xq, float *__restrict__ xs) {
+                                                    uint8_t *__restrict__ xq, float *__restrict__ xs, int *cnt,
+                                                    int n_cnt) {
     pdl_wait();
     pdl_trigger();
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_cnt; i += 256) cnt[i] = 0;
     const int t = blockIdx.x;
     const __nv_bfloat16 *row = x + (size_t)t * K;
     float amax = 0.f;
@@ -337,12 +419,21 @@ int launch_gemm(const DenseArgs &a, int num_sms, cudaStream_t st) {
     p.N = a.N;
     p.n_blocks = a.N / BM;
     p.t_tiles = (a.T + BN - 1) / BN;
+    // Few tiles (small T): split K so that every SM streams weights; the partials fit the
+    // workspace because ksplit x n_blocks <= SMs.
+    const int nk = a.K / KB, tiles0 = p.n_blocks * p.t_tiles;
+    int ksplit = 1;
+    if (a.T <= kSplitMaxTokens && 2 * tiles0 <= num_sms) ksplit = min(nk, num_sms / tiles0);
+    p.kper = (nk + ksplit - 1) / ksplit;
+    p.ksplit = (nk + p.kper - 1) / p.kper;
+    p.part = a.part;
+    p.cnt = a.cnt;
     p.w_scale = a.w_scale;
     p.x_scale = a.xs;
     p.out = a.out;
     p.err = a.err;
     p.wait_ns = a.wait_ns ? a.wait_ns : ptx::kWaitLimitNs;
-    const int tiles = p.n_blocks * p.t_tiles;
+    const int tiles = tiles0 * p.ksplit;
     launch_pdl(gemm_fp8<BN>, dim3(tiles < num_sms ? tiles : num_sms), dim3(kThreads), smem, st, tw, tx0, tx1, p);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
@@ -353,7 +444,7 @@ bool fp8_available() { return encoder() != nullptr; }
 
 int launch_dense_fp8(const DenseArgs &a, int num_sms, cudaStream_t st) {
     if (!encoder()) return -2;
-    launch_pdl(quant_x_e4m3, dim3(a.T), dim3(256), 0, st, a.x, a.T, a.K, a.xq, a.xs);
+    launch_pdl(quant_x_e4m3, dim3(a.T), dim3(256), 0, st, a.x, a.T, a.K, a.xq, a.xs, a.cnt, num_sms);
     if (cudaPeekAtLastError() != cudaSuccess) return -1;
     // tokens per tile: 16 for decode-sized T, else 64 or 128 (the MMA's N is twice that)
     const int n = a.T <= 16 ? launch_gemm<16>(a, num_sms, st)
