@@ -31,11 +31,18 @@ namespace {
 
 constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int KB = 128;            // K per stage: one scale block, one 128-byte swizzle row
-constexpr int NS = 4;              // pipeline stages
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kASmem = BM * KB;                       // 16 KB
-constexpr uint32_t kStageBytes = kASmem + 2 * 128 * KB;    // + two terms of up to 128 tokens
+// Per token-tile size BN: a stage holds the weights and both terms of BN tokens; as many stages
+// as fit in 200 KB (more bytes in flight when the stages are small); as many TMEM
+// accumulator buffers (2 x BN columns each) as fit in 512 columns, up to 8, so the tensor cores
+// can run ahead of the fold.
+template <int BN> struct Fp8Cfg {
+    static constexpr uint32_t kStage = kASmem + 2 * BN * KB;
+    static constexpr int NS = (200 * 1024) / kStage > 12 ? 12 : (200 * 1024) / kStage;
+    static constexpr int NBUF = 512 / (2 * BN) > 8 ? 8 : 512 / (2 * BN);
+};
 constexpr int kTmemCols = 512;
 
 struct Fp8Params {
@@ -108,10 +115,12 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
     // weights (which no kernel of this forward writes) may be loaded before this kernel's wait.
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr int NS = Fp8Cfg<BN>::NS, NBUF = Fp8Cfg<BN>::NBUF;
+    constexpr uint32_t kStageBytes = Fp8Cfg<BN>::kStage;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
-    uint64_t *full = bar, *empty = bar + NS, *acc_full = bar + 2 * NS, *acc_empty = bar + 2 * NS + 2,
-             *drain = bar + 2 * NS + 4;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2 * NS + 5);
+    uint64_t *full = bar, *empty = bar + NS, *acc_full = bar + 2 * NS, *acc_empty = bar + 2 * NS + NBUF,
+             *drain = bar + 2 * NS + 2 * NBUF;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = abort_flag + 1;
     constexpr int NC = 2 * BN;                                // MMA N: both terms
@@ -123,7 +132,7 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
             ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NBUF; ++b) {
             ptx::mbar_init(ptx::smem_addr(&acc_full[b]), 1);
             ptx::mbar_init(ptx::smem_addr(&acc_empty[b]), kEpiWarps);
         }
@@ -194,8 +203,8 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
             for (int tile = blockIdx.x; tile < total && ok && !*abort_flag; tile += gridDim.x) {
                 const Fp8Tile tl = fp8_tile(p, tile);
                 for (int k = tl.k0; k < tl.k1; ++k, ++it, ++u) {
-                    const int s = it % NS, b = u & 1;
-                    if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[b]), ((u >> 1) & 1u) ^ 1u, p.err,
+                    const int s = it % NS, b = u % NBUF;
+                    if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[b]), ((u / NBUF) & 1u) ^ 1u, p.err,
                                         ptx::kErrWaitAccum, abort_flag, p.wait_ns) ||
                         !ptx::mbar_wait(ptx::smem_addr(&full[s]), (it / NS) & 1u, p.err, ptx::kErrWaitFull,
                                         abort_flag, p.wait_ns)) {
@@ -235,10 +244,10 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
             float s_next = __ldg(wsc + tl.k0);
             bool ok = true;
             for (int k = tl.k0; k < tl.k1; ++k, ++u) {
-                const int b = u & 1;
+                const int b = u % NBUF;
                 const float s = s_next;
                 if (k + 1 < tl.k1) s_next = __ldg(wsc + k + 1);
-                if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[b]), (u >> 1) & 1u, p.err, ptx::kErrWaitAccum,
+                if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[b]), (u / NBUF) & 1u, p.err, ptx::kErrWaitAccum,
                                     abort_flag, p.wait_ns)) {
                     ok = false;
                     break;
@@ -402,7 +411,7 @@ bool map_bytes(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint
 
 template <int BN>
 int launch_gemm(const DenseArgs &a, int num_sms, cudaStream_t st) {
-    const size_t smem = NS * kStageBytes + 1024 + 256;
+    const size_t smem = Fp8Cfg<BN>::NS * Fp8Cfg<BN>::kStage + 1024 + 512;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(gemm_fp8<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
