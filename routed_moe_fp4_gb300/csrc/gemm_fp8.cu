@@ -281,7 +281,7 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&acc_empty[b]));
             }
-            if (p.ksplit == 1) {
+            if (BN > kSplitMaxTokens || p.ksplit == 1) {   // the host splits K only for small T
                 if (!ok) continue;
 #pragma unroll
                 for (int j = 0; j < H2; ++j) {
@@ -304,15 +304,23 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
             asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
             if (*last_flag && ok) {
                 __threadfence();
+                // sum[j] over the splits in split order; each split's H2 values are loaded together
+                float sum[H2];
 #pragma unroll
-                for (int j = 0; j < H2; ++j) {
-                    const int t = t0 + j;
-                    if (t >= p.T) continue;
-                    float sum = 0.f;
-                    for (int s2 = 0; s2 < p.ksplit; ++s2)
-                        sum += s2 == tl.sp ? acc[j] : __ldcg(p.part + ((size_t)s2 * p.T + t) * p.N + n);
-                    p.out[(size_t)t * p.N + n] = __float2bfloat16_rn(sum * __ldg(p.x_scale + t));
+                for (int j = 0; j < H2; ++j) sum[j] = 0.f;
+                for (int s2 = 0; s2 < p.ksplit; ++s2) {
+                    float v[H2];
+#pragma unroll
+                    for (int j = 0; j < H2; ++j)
+                        v[j] = s2 == tl.sp ? acc[j]
+                             : t0 + j < p.T ? __ldcg(p.part + ((size_t)s2 * p.T + t0 + j) * p.N + n) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < H2; ++j) sum[j] += v[j];
                 }
+#pragma unroll
+                for (int j = 0; j < H2; ++j)
+                    if (t0 + j < p.T)
+                        p.out[(size_t)(t0 + j) * p.N + n] = __float2bfloat16_rn(sum[j] * __ldg(p.x_scale + t0 + j));
                 if (warp == 2 && lane == 0) p.cnt[tl.id] = 0;
             }
             asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");   // last_flag reuse
