@@ -15,9 +15,10 @@
 // This runs while the tensor cores fill the other buffer. The token scale 2^e is applied once,
 // when out is written.
 //
-// Roles (320 threads, one persistent block per SM): warp 0 issues TMA, warp 1 allocates TMEM and
-// issues MMAs, warps 2-9 fold the partial sums (two warps per TMEM lane quarter, each taking half
-// of the tile's tokens). Tiles are 128 weight rows x BN tokens; every wait is bounded.
+// Roles (one persistent block per SM): warp 0 issues TMA, warp 1 allocates TMEM and issues MMAs,
+// the other warps fold the partial sums: 8 of them (16 for 128-token tiles), each TMEM lane
+// quarter shared by 2 (4) warps that split the tile's tokens. Tiles are 128 weight rows x BN
+// tokens; every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -31,14 +32,14 @@ namespace {
 
 constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int KB = 128;            // K per stage: one scale block, one 128-byte swizzle row
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kASmem = BM * KB;                       // 16 KB
 // Per token-tile size BN: a stage holds the weights and both terms of BN tokens; as many stages
 // as fit in 200 KB (more bytes in flight when the stages are small); as many TMEM
 // accumulator buffers (2 x BN columns each) as fit in 512 columns, up to 8, so the tensor cores
 // can run ahead of the fold.
 template <int BN> struct Fp8Cfg {
+    static constexpr int EPI = BN >= 128 ? 16 : 8;         // fold warps
+    static constexpr int THREADS = 64 + 32 * EPI;
     static constexpr uint32_t kStage = kASmem + 2 * BN * KB;
     static constexpr int NS = (200 * 1024) / kStage > 12 ? 12 : (200 * 1024) / kStage;
     static constexpr int NBUF = 512 / (2 * BN) > 8 ? 8 : 512 / (2 * BN);
@@ -108,14 +109,14 @@ __device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint3
 }
 
 template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Fp8Cfg<BN>::THREADS, 1)
 gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x0,
          const __grid_constant__ CUtensorMap tm_x1, const Fp8Params p) {
     // The quantisation kernel before this one signals only after its own dependency wait, so the
     // weights (which no kernel of this forward writes) may be loaded before this kernel's wait.
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int NS = Fp8Cfg<BN>::NS, NBUF = Fp8Cfg<BN>::NBUF;
+    constexpr int NS = Fp8Cfg<BN>::NS, NBUF = Fp8Cfg<BN>::NBUF, kEpiWarps = Fp8Cfg<BN>::EPI;
     constexpr uint32_t kStageBytes = Fp8Cfg<BN>::kStage;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + NS * kStageBytes);
     uint64_t *full = bar, *empty = bar + NS, *acc_full = bar + 2 * NS, *acc_empty = bar + 2 * NS + NBUF,
@@ -227,8 +228,8 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
     } else {
         // ------------------------------------------------------------------ fold + store
         pdl_wait();
-        constexpr int H2 = BN / 2;                             // tokens of this warp
-        const int quad = warp & 3, half = (warp - 2) >> 2;
+        constexpr int H2 = BN / (kEpiWarps / 4);               // tokens of this warp
+        const int quad = warp & 3, half = (warp - 2) >> 2;     // lane quarter, token slice
         const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
         uint32_t u = 0;
         // Every epilogue warp walks every tile of the block, also after an abort (its waits then
@@ -254,28 +255,25 @@ gemm_fp8(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUten
                 }
                 ptx::tc_fence_after();
                 const uint32_t base = lane_base + b * NC + half * H2;
-                if constexpr (H2 >= 32) {
+                // columns per TMEM load: 32, or 16 when 16 fold warps share the registers
+                constexpr int CH = H2 < 16 ? 8 : (kEpiWarps > 8 || H2 < 32) ? 16 : 32;
 #pragma unroll
-                    for (int c = 0; c < H2; c += 32) {
-                        uint32_t r0[32], r1[32];
+                for (int c = 0; c < H2; c += CH) {
+                    uint32_t r0[CH], r1[CH];
+                    if constexpr (CH == 32) {
                         tmem_ld32(base + c, r0);
                         tmem_ld32(base + BN + c, r1);
-                        ptx::tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            acc[c + j] = fmaf(s, __uint_as_float(r0[j]) + __uint_as_float(r1[j]), acc[c + j]);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < H2; c += 8) {
-                        uint32_t r0[8], r1[8];
+                    } else if constexpr (CH == 16) {
+                        ptx::tmem_ld16(base + c, r0);
+                        ptx::tmem_ld16(base + BN + c, r1);
+                    } else {
                         ptx::tmem_ld8(base + c, r0);
                         ptx::tmem_ld8(base + BN + c, r1);
-                        ptx::tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            acc[c + j] = fmaf(s, __uint_as_float(r0[j]) + __uint_as_float(r1[j]), acc[c + j]);
                     }
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < CH; ++j)
+                        acc[c + j] = fmaf(s, __uint_as_float(r0[j]) + __uint_as_float(r1[j]), acc[c + j]);
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -451,7 +449,8 @@ int launch_gemm(const DenseArgs &a, int num_sms, cudaStream_t st) {
     p.err = a.err;
     p.wait_ns = a.wait_ns ? a.wait_ns : ptx::kWaitLimitNs;
     const int tiles = tiles0 * p.ksplit;
-    launch_pdl(gemm_fp8<BN>, dim3(tiles < num_sms ? tiles : num_sms), dim3(kThreads), smem, st, tw, tx0, tx1, p);
+    launch_pdl(gemm_fp8<BN>, dim3(tiles < num_sms ? tiles : num_sms), dim3(Fp8Cfg<BN>::THREADS), smem, st, tw, tx0,
+               tx1, p);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
