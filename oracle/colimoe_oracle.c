@@ -457,3 +457,74 @@ void coli_oracle_fp8_linear(const uint16_t *x, int32_t T, int32_t K, const uint8
         if (out_f64) out_f64[i] = acc;
     }
 }
+
+/* ------------------------------------------------------------------------------------
+ * NVFP4 experts: E2M1 elements with an E4M3 scale per 16 elements along K and one fp32 scale
+ * per matrix (NVIDIA's two-level FP4 format; the pages use MXFP4 only, so this is the format
+ * variant of the same layer). Element value = e2m1(code) * e4m3(scale byte) * global. */
+double coli_oracle_nvfp4(const uint8_t *codes, const uint8_t *scales, float global, int64_t K, int64_t row,
+                         int64_t k) {
+    const uint8_t byte = codes[row * (K / 2) + k / 2];
+    const int code = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
+    const int64_t si = MUT(27) ? row * (K / 16) + k / 32 : row * (K / 16) + k / 16;
+    return E2M1_TABLE[code] * coli_oracle_e4m3(scales[si]) * (MUT(28) ? 1.0 : (double)global);
+}
+
+static void expert_row_nv(const uint16_t *x_row, int32_t H, int32_t I, const uint8_t *gu_codes,
+                          const uint8_t *gu_scales, float gu_global, const uint8_t *d_codes,
+                          const uint8_t *d_scales, float d_global, double *y) {
+    double *xv = (double *)malloc(sizeof(double) * (size_t)H);
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    for (int32_t k = 0; k < H; ++k) xv[k] = coli_oracle_bf16(x_row[k]);
+    for (int32_t i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int32_t k = 0; k < H; ++k) {
+            g += coli_oracle_nvfp4(gu_codes, gu_scales, gu_global, H, i, k) * xv[k];
+            u += coli_oracle_nvfp4(gu_codes, gu_scales, gu_global, H, (int64_t)I + i, k) * xv[k];
+        }
+        h[i] = g / (1.0 + exp(-g)) * u;
+    }
+    for (int32_t m = 0; m < H; ++m) {
+        double acc = 0.0;
+        for (int32_t i = 0; i < I; ++i) acc += coli_oracle_nvfp4(d_codes, d_scales, d_global, I, m, i) * h[i];
+        y[m] = acc;
+    }
+    free(h);
+    free(xv);
+}
+
+void coli_oracle_tokens_output_nv(const uint16_t *x, int32_t H, int32_t I, int32_t I_s,
+                                  const int32_t *idx, const float *w, int32_t top_k,
+                                  const uint8_t *gu_codes, const uint8_t *gu_scales, const float *gu_global,
+                                  const uint8_t *d_codes, const uint8_t *d_scales, const float *d_global,
+                                  const uint8_t *sh_gu_codes, const uint8_t *sh_gu_scales, float sh_gu_global,
+                                  const uint8_t *sh_d_codes, const uint8_t *sh_d_scales, float sh_d_global,
+                                  const int32_t *tokens, int32_t n_tokens, uint16_t *out, double *out_f64) {
+    const int64_t gu_c = 2LL * I * (H / 2), gu_s = 2LL * I * (H / 16);
+    const int64_t d_c = (int64_t)H * (I / 2), d_s = (int64_t)H * (I / 16);
+    const int with_shared = sh_gu_codes != NULL && I_s > 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int32_t n = 0; n < n_tokens; ++n) {
+        int32_t t = tokens[n];
+        const uint16_t *xr = x + (int64_t)t * H;
+        double *ys = (double *)malloc(sizeof(double) * (size_t)H * (size_t)(top_k + 1));
+        const double **slot = (const double **)malloc(sizeof(double *) * (size_t)top_k);
+        for (int32_t j = 0; j < top_k; ++j) {
+            int64_t e = idx[(int64_t)t * top_k + j];
+            double *yj = ys + (int64_t)j * H;
+            expert_row_nv(xr, H, I, off_ptr(gu_codes, e, gu_c), off_ptr(gu_scales, e, gu_s), gu_global[e],
+                          off_ptr(d_codes, e, d_c), off_ptr(d_scales, e, d_s), d_global[e], yj);
+            slot[j] = yj;
+        }
+        double *ysh = NULL;
+        if (with_shared) {
+            ysh = ys + (int64_t)top_k * H;
+            expert_row_nv(xr, H, I_s, sh_gu_codes, sh_gu_scales, sh_gu_global, sh_d_codes, sh_d_scales,
+                          sh_d_global, ysh);
+        }
+        combine_row(H, top_k, w + (int64_t)t * top_k, slot, ysh, out + (int64_t)n * H,
+                    out_f64 ? out_f64 + (int64_t)n * H : NULL);
+        free(slot);
+        free(ys);
+    }
+}

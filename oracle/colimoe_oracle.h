@@ -112,6 +112,21 @@ double coli_oracle_e4m3(int code);          /* value of an OCP E4M3 byte (NaN fo
 void coli_oracle_fp8_linear(const uint16_t *x, int32_t T, int32_t K, const uint8_t *w, const float *w_scale,
                             int32_t N, uint16_t *out, double *out_f64);
 
+/* --- NVFP4 experts (format variant) --- */
+/* One weight of an NVFP4 matrix: e2m1(code) * e4m3(scale of its group of 16 along K) * global;
+ * codes [R][K/2] (low nibble = even k), scales [R][K/16] E4M3 bytes. */
+double coli_oracle_nvfp4(const uint8_t *codes, const uint8_t *scales, float global, int64_t K, int64_t row,
+                         int64_t k);
+/* coli_oracle_tokens_output with NVFP4 experts: scales [E][rows][K/16], one fp32 global per
+ * expert and matrix (gate/up, down); the shared expert's globals as scalars. */
+void coli_oracle_tokens_output_nv(const uint16_t *x, int32_t H, int32_t I, int32_t I_s,
+                                  const int32_t *idx, const float *w, int32_t top_k,
+                                  const uint8_t *gu_codes, const uint8_t *gu_scales, const float *gu_global,
+                                  const uint8_t *d_codes, const uint8_t *d_scales, const float *d_global,
+                                  const uint8_t *sh_gu_codes, const uint8_t *sh_gu_scales, float sh_gu_global,
+                                  const uint8_t *sh_d_codes, const uint8_t *sh_d_scales, float sh_d_global,
+                                  const int32_t *tokens, int32_t n_tokens, uint16_t *out, double *out_f64);
+
 #ifdef __cplusplus
 }
 #endif

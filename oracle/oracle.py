@@ -64,6 +64,12 @@ class Oracle:
         L.coli_oracle_e4m3.restype = C.c_double
         L.coli_oracle_e4m3.argtypes = [C.c_int]
         L.coli_oracle_fp8_linear.argtypes = [_u16p, C.c_int32, C.c_int32, _u8p, _f32p, C.c_int32, _u16p, _f64p]
+        L.coli_oracle_nvfp4.restype = C.c_double
+        L.coli_oracle_nvfp4.argtypes = [_u8p, _u8p, C.c_float, C.c_int64, C.c_int64, C.c_int64]
+        L.coli_oracle_tokens_output_nv.argtypes = [_u16p, C.c_int32, C.c_int32, C.c_int32, _i32p, _f32p, C.c_int32,
+                                                   _u8p, _u8p, _f32p, _u8p, _u8p, _f32p,
+                                                   _u8p, _u8p, C.c_float, _u8p, _u8p, C.c_float,
+                                                   _i32p, C.c_int32, _u16p, _f64p]
         L.coli_oracle_threads.restype = C.c_int32
         L.coli_oracle_mutant.restype = C.c_int32
 
@@ -173,6 +179,34 @@ class Oracle:
             _p(experts.gate_up_codes, _u8p), _p(experts.gate_up_scales, _u8p),
             _p(experts.down_codes, _u8p), _p(experts.down_scales, _u8p),
             *[_p(a, _u8p) for a in sh], _p(tok, _i32p), len(tok), _p(out, _u16p), _p(out64, _f64p))
+        return out, out64
+
+    def nvfp4(self, codes: np.ndarray, scales: np.ndarray, glob: float, K: int, row: int, k: int) -> float:
+        return self.lib.coli_oracle_nvfp4(_p(codes, _u8p), _p(scales, _u8p), glob, K, row, k)
+
+    def tokens_output_nv(self, x: np.ndarray, idx: np.ndarray, w: np.ndarray, experts, shared,
+                         tokens: Sequence[int]):
+        """tokens_output with NVFP4 experts (synthetic.NVFP4Experts)."""
+        T, H = x.shape
+        k = idx.shape[1]
+        I = experts.gate_up_codes.shape[1] // 2
+        I_s = shared.gate_up_codes.shape[1] // 2 if shared is not None else 0
+        tok = np.ascontiguousarray(np.asarray(tokens, np.int32))
+        out = np.zeros((len(tok), H), np.uint16)
+        out64 = np.zeros((len(tok), H), np.float64)
+        if shared is None:
+            sh = [None, None, 0.0, None, None, 0.0]
+        else:
+            sh = [_p(shared.gate_up_codes, _u8p), _p(shared.gate_up_scales, _u8p), float(shared.gate_up_global[0]),
+                  _p(shared.down_codes, _u8p), _p(shared.down_scales, _u8p), float(shared.down_global[0])]
+        self.lib.coli_oracle_tokens_output_nv(
+            _p(x, _u16p), H, I, I_s, _p(np.ascontiguousarray(idx, np.int32), _i32p),
+            _p(np.ascontiguousarray(w, np.float32), _f32p), k,
+            _p(experts.gate_up_codes, _u8p), _p(experts.gate_up_scales, _u8p),
+            _p(np.ascontiguousarray(experts.gate_up_global, np.float32), _f32p),
+            _p(experts.down_codes, _u8p), _p(experts.down_scales, _u8p),
+            _p(np.ascontiguousarray(experts.down_global, np.float32), _f32p),
+            *sh, _p(tok, _i32p), len(tok), _p(out, _u16p), _p(out64, _f64p))
         return out, out64
 
     def moe_forward(self, x: np.ndarray, router_w: np.ndarray, router_b: Optional[np.ndarray], top_k: int,

@@ -316,3 +316,54 @@ def make_dense_inputs(name, seed: int = 0, T: Optional[int] = None) -> DenseInpu
     p = np.floor(uniform01(stream_key(seed, wl.name, "w_scale_e"), nb * kb) * 5)
     sc = ((1.0 + u) * 2.0 ** (-14 + p)).astype(np.float32).reshape(nb, kb)
     return DenseInputs(wl, x, w, sc)
+
+
+# --------------------------------------------------------------------------------------
+# NVFP4 experts (the format variant): E2M1 codes, an E4M3 scale per 16 elements along K and
+# one fp32 scale per matrix.
+
+
+@dataclasses.dataclass
+class NVFP4Experts:
+    gate_up_codes: np.ndarray   # uint8 [E, 2I, H/2]
+    gate_up_scales: np.ndarray  # uint8 [E, 2I, H/16] E4M3
+    gate_up_global: np.ndarray  # float32 [E]
+    down_codes: np.ndarray      # uint8 [E, H, I/2]
+    down_scales: np.ndarray     # uint8 [E, H, I/16] E4M3
+    down_global: np.ndarray     # float32 [E]
+
+    @property
+    def nbytes(self) -> int:
+        return sum(a.nbytes for a in (self.gate_up_codes, self.gate_up_scales, self.gate_up_global,
+                                      self.down_codes, self.down_scales, self.down_global))
+
+
+def e4m3_scale_bytes(key: int, count: int) -> np.ndarray:
+    """Positive E4M3 scale bytes from their fields: exponent field uniform in 4..8 (2^-3 .. 2^1),
+    mantissa uniform in 0..7."""
+    r = u64_stream(key, count)
+    e = np.uint64(4) + (((r >> np.uint64(32)) * np.uint64(5)) >> np.uint64(32))
+    m = r & np.uint64(7)
+    return ((e << np.uint64(3)) | m).astype(np.uint8)
+
+
+def make_nv_experts(seed: int, tag: str, E: int, H: int, I: int) -> NVFP4Experts:
+    gu_c = np.stack([random_bytes(stream_key(seed, tag, e, "nv_gate_up_codes"), I * H).reshape(2 * I, H // 2)
+                     for e in range(E)])
+    gu_s = np.stack([e4m3_scale_bytes(stream_key(seed, tag, e, "nv_gate_up_scales"), 2 * I * H // 16)
+                     .reshape(2 * I, H // 16) for e in range(E)])
+    d_c = np.stack([random_bytes(stream_key(seed, tag, e, "nv_down_codes"), H * I // 2).reshape(H, I // 2)
+                    for e in range(E)])
+    d_s = np.stack([e4m3_scale_bytes(stream_key(seed, tag, e, "nv_down_scales"), H * I // 16).reshape(H, I // 16)
+                    for e in range(E)])
+    g = (1.0 + uniform01(stream_key(seed, tag, "nv_global"), 2 * E)) * 2.0 ** -6
+    return NVFP4Experts(gu_c, gu_s, g[:E].astype(np.float32), d_c, d_s, g[E:].astype(np.float32))
+
+
+def make_nv_inputs(name, seed: int = 0, T: Optional[int] = None) -> MoEInputs:
+    """A workload's tokens and router with NVFP4 experts in place of the MXFP4 ones."""
+    base = make_inputs(name, seed=seed, T=T, with_experts=False)
+    wl = base.workload
+    experts = make_nv_experts(seed, wl.name + "/nv_experts", wl.E, wl.H, wl.I)
+    shared = make_nv_experts(seed, wl.name + "/nv_shared", 1, wl.H, wl.I_s) if wl.I_s > 0 else None
+    return dataclasses.replace(base, experts=experts, shared=shared)

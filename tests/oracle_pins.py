@@ -522,6 +522,56 @@ def pin_fp8_linear(o):
             assert b == nearest_bf16_bits(float(v))
 
 
+# ---- NVFP4 experts ---------------------------------------------------------------------------
+
+def decode_nvfp4(codes: np.ndarray, scales: np.ndarray, glob: float) -> np.ndarray:
+    """[R, K] values from E2M1 fields, E4M3 scale fields per 16 along K and the matrix scale."""
+    R, K2 = codes.shape
+    K = 2 * K2
+    e2 = np.array([e2m1_from_fields(c) for c in range(16)])
+    e4 = np.zeros(256)
+    for c, v in e4m3_values().items():
+        e4[c] = v
+    lo, hi = codes & 15, codes >> 4
+    vals = np.empty((R, K))
+    vals[:, 0::2] = e2[lo]
+    vals[:, 1::2] = e2[hi]
+    return vals * np.repeat(e4[scales], 16, axis=1) * float(glob)
+
+
+def pin_nvfp4_decode(o):
+    """Single weights against the E2M1 and E4M3 field decoders, in both nibbles and across
+    16-element groups (a 32-element group or a missing matrix scale fails)."""
+    rng = _rng(60)
+    R, K = 3, 64
+    codes = rng.integers(0, 256, (R, K // 2), dtype=np.uint8)
+    scales = rng.integers(0x20, 0x50, (R, K // 16), dtype=np.uint8)
+    ref = decode_nvfp4(codes, scales, 0.375)
+    for r in range(R):
+        for k in range(K):
+            assert o.nvfp4(codes, scales, 0.375, K, r, k) == ref[r, k], (r, k)
+
+
+def pin_nvfp4_dense_swiglu(o):
+    """One expert, top-1, no shared expert: the routed layer reduces to a dense SwiGLU MLP over the
+    independently decoded NVFP4 weights (numpy), to fp64 rounding."""
+    from routed_moe_fp4_gb300 import synthetic as S
+    rng = _rng(61)
+    H, I, T = 128, 64, 3
+    ex = S.make_nv_experts(61, "pin", 1, H, I)
+    x = random_bf16(rng, (T, H))
+    idx = np.zeros((T, 1), np.int32)
+    w = np.ones((T, 1), np.float32)
+    out, out64 = o.tokens_output_nv(x, idx, w, ex, None, list(range(T)))
+    Wgu = decode_nvfp4(ex.gate_up_codes[0], ex.gate_up_scales[0], ex.gate_up_global[0])
+    Wd = decode_nvfp4(ex.down_codes[0], ex.down_scales[0], ex.down_global[0])
+    xv = bf16_to_f64(x)
+    g, u = xv @ Wgu[:I].T, xv @ Wgu[I:].T
+    ref = (g / (1.0 + np.exp(-g)) * u) @ Wd.T
+    assert np.allclose(out64, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
+
+
 ALL_PINS = [pin_e2m1_table, pin_e8m0, pin_nibble_order, pin_route_bruteforce, pin_route_weights,
             pin_permute, pin_dense_swiglu, pin_dense_gated, pin_sigmoid, pin_logits, pin_round_bf16,
-            pin_bank_cache, pin_bank_full, pin_bank_hot_expert, pin_bank_stream, pin_e4m3, pin_fp8_linear]
+            pin_bank_cache, pin_bank_full, pin_bank_hot_expert, pin_bank_stream, pin_e4m3, pin_fp8_linear,
+            pin_nvfp4_decode, pin_nvfp4_dense_swiglu]
