@@ -283,6 +283,27 @@ COLI_API int coli_bank_state(coli_expert_bank_t *bank, int32_t *slot_of, int32_t
                              int32_t *last_use, int64_t *stats);
 
 /* ---------------------------------------------------------------------------------------------
+ * NVFP4 experts (the format variant of the layer; the pages use MXFP4 only). Same layer, with each
+ * matrix stored as E2M1 codes (the layout above), one E4M3 scale byte per 16 elements along K
+ * (positive values; [rows][K/16]) and one fp32 scale per matrix: element = e2m1(code) *
+ * e4m3(scale) * global. The weights go to the tensor cores as stored (tcgen05 kind::mxf4nvf4,
+ * scale_vec::4X); the activations are split into four E2M1 terms with E4M3 scales per 16 under a
+ * power-of-two scale per term and row. */
+typedef struct {
+    const uint8_t *gate_up_codes;        /* [E][2I][H/2] */
+    const uint8_t *gate_up_scales;       /* [E][2I][H/16] E4M3 */
+    const float *gate_up_global;         /* [E] fp32, one per expert's gate/up matrix */
+    const uint8_t *down_codes;           /* [E][H][I/2] */
+    const uint8_t *down_scales;          /* [E][H][I/16] E4M3 */
+    const float *down_global;            /* [E] fp32 */
+} coli_nvfp4_experts;                    /* all device pointers; the shared expert: E = 1 */
+
+/* coli_moe_forward with NVFP4 experts (H and I up to 8192). Same conventions and errors. */
+COLI_API int coli_moe_forward_nvfp4(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router_w,
+                                    const float *router_bias, const coli_nvfp4_experts *packed_experts,
+                                    const coli_nvfp4_experts *shared_expert, int32_t top_k, void *out_bf16);
+
+/* ---------------------------------------------------------------------------------------------
  * FP8 dense projection: out[t][n] = bf16(sum_k x[t][k] * e4m3(w[n][k]) * w_scale[n/128][k/128]),
  * the weight format the pages give for the model's dense matrices: FP8 E4M3 with one fp32 scale
  * per 128 x 128 block ("DeepSeek V4 Flash CPU inference with NVMe expert streaming", the review

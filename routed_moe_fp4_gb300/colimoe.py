@@ -26,7 +26,7 @@ EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "col
             "coli_moe_device_error", "coli_moe_set_wait_limit", "coli_moe_route_static",
             "coli_bank_create", "coli_bank_destroy", "coli_moe_forward_banked", "coli_bank_set_copy_blocks",
             "coli_bank_state", "coli_dense_create", "coli_dense_forward", "coli_dense_destroy",
-            "coli_dense_last_error", "coli_dense_device_error")
+            "coli_dense_last_error", "coli_dense_device_error", "coli_moe_forward_nvfp4")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
 
@@ -39,6 +39,11 @@ class coli_moe_config(C.Structure):
 class coli_mxfp4_experts(C.Structure):
     _fields_ = [("gate_up_codes", C.c_void_p), ("gate_up_scales", C.c_void_p),
                 ("down_codes", C.c_void_p), ("down_scales", C.c_void_p)]
+
+
+class coli_nvfp4_experts(C.Structure):
+    _fields_ = [("gate_up_codes", C.c_void_p), ("gate_up_scales", C.c_void_p), ("gate_up_global", C.c_void_p),
+                ("down_codes", C.c_void_p), ("down_scales", C.c_void_p), ("down_global", C.c_void_p)]
 
 
 class coli_moe_routing(C.Structure):
@@ -106,6 +111,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_bank_set_copy_blocks.restype = C.c_int
     lib.coli_bank_state.argtypes = [vp, vp, vp, vp, vp, vp]
     lib.coli_bank_state.restype = C.c_int
+    lib.coli_moe_forward_nvfp4.argtypes = [vp, vp, C.c_int32, vp, vp, C.POINTER(coli_nvfp4_experts),
+                                           C.POINTER(coli_nvfp4_experts), C.c_int32, vp]
+    lib.coli_moe_forward_nvfp4.restype = C.c_int
     lib.coli_dense_create.argtypes = [C.c_int32, C.c_int32, vp, C.POINTER(vp)]
     lib.coli_dense_create.restype = C.c_int
     lib.coli_dense_forward.argtypes = [vp, vp, C.c_int32, C.c_int32, vp, vp, C.c_int32, vp]
@@ -347,6 +355,47 @@ class MoELayer:
             self.close()
         except Exception:
             pass
+
+
+def coli_moe_forward_nvfp4(h, x_bf16, T: int, router_w, router_bias, packed_experts: coli_nvfp4_experts,
+                           shared_expert: Optional[coli_nvfp4_experts], top_k: int, out_bf16) -> int:
+    sh = C.byref(shared_expert) if shared_expert is not None else None
+    return _check(h, load().coli_moe_forward_nvfp4(h, _ptr(x_bf16), T, _ptr(router_w), _ptr(router_bias),
+                                                   C.byref(packed_experts), sh, top_k, _ptr(out_bf16)))
+
+
+class DeviceNvExperts:
+    """NVFP4 expert arrays (synthetic.NVFP4Experts) copied to the device, with the ABI struct."""
+
+    def __init__(self, host, device="cuda"):
+        import torch
+        self.tensors = [torch.from_numpy(a).to(device) for a in
+                        (host.gate_up_codes, host.gate_up_scales, host.gate_up_global,
+                         host.down_codes, host.down_scales, host.down_global)]
+        self.struct = coli_nvfp4_experts(*[t.data_ptr() for t in self.tensors])
+
+
+class NvMoELayer(MoELayer):
+    """MoELayer over NVFP4 experts: forward() runs coli_moe_forward_nvfp4."""
+
+    def __init__(self, inputs, max_tokens: Optional[int] = None, stream=None, device="cuda"):
+        import torch
+        wl = inputs.workload
+        self.wl = wl
+        self.top_k = wl.top_k
+        self.router_w = torch.from_numpy(inputs.router_w).to(device)
+        self.router_b = None if inputs.router_b is None else torch.from_numpy(inputs.router_b).to(device)
+        self.experts = DeviceNvExperts(inputs.experts, device)
+        self.shared = DeviceNvExperts(inputs.shared, device) if inputs.shared is not None else None
+        cfg = coli_moe_config(wl.E, wl.H, wl.I, wl.I_s if inputs.shared is not None else 0,
+                              max_tokens or max(wl.T, 1), wl.top_k)
+        self.stream = stream
+        self.h = coli_moe_create(cfg, stream)
+
+    def forward(self, x, out, T: Optional[int] = None) -> None:
+        T = x.shape[0] if T is None else T
+        coli_moe_forward_nvfp4(self.h, x, T, self.router_w, self.router_b, self.experts.struct,
+                               self.shared.struct if self.shared is not None else None, self.top_k, out)
 
 
 class HostExperts:

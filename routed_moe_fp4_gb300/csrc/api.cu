@@ -47,7 +47,7 @@ void set_err(coli_moe_t *h, const char *fmt, ...) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_ws(Workspace &ws) {
-    void *ptrs[] = {ws.xq, ws.xqs, ws.hq, ws.hqs, ws.scores, ws.logit_part, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
+    void *ptrs[] = {ws.xq, ws.xqs, ws.hq, ws.hqs, ws.xg, ws.hg, ws.hf, ws.scores, ws.logit_part, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
                     ws.n_touched, ws.xp, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
                     ws.out_stage, ws.tile_sched};
     for (void *p : ptrs)
@@ -203,6 +203,9 @@ FfnArgs ffn_args(coli_moe_t *h, const void *x_bf16, int32_t T, int32_t top_k, in
     a.xqs = ws.xqs;
     a.hq = ws.hq;
     a.hqs = ws.hqs;
+    a.xg = ws.xg;
+    a.hg = ws.hg;
+    a.hf = ws.hf;
     a.err = ws.err;
     a.wait_ns = h->wait_ns;
     return a;
@@ -362,8 +365,9 @@ int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **
               alloc(&ws.hinv, rows) && alloc(&ws.err, 4) && alloc(&ws.x_stage, Tm * H) &&
               alloc(&ws.out_stage, Tm * H);
     if (ok)
-        ok = alloc(&ws.xq, 2 * rows * H) && alloc(&ws.xqs, 4 * rows * (H / 32)) &&
-             alloc(&ws.hq, 3 * rows * (size_t)h->I_max) && alloc(&ws.hqs, 4 * rows * (size_t)(h->I_max / 32));
+        ok = alloc(&ws.xq, 2 * rows * H) && alloc(&ws.xqs, 4 * rows * (H / 16)) &&
+             alloc(&ws.hq, 3 * rows * (size_t)h->I_max) && alloc(&ws.hqs, 4 * rows * (size_t)(h->I_max / 16)) &&
+             alloc(&ws.xg, 4 * rows) && alloc(&ws.hg, 4 * rows) && alloc(&ws.hf, rows * (size_t)h->I_max);
     if (ok) ok = cudaMemset(ws.err, 0, sizeof(int)) == cudaSuccess;
     if (ok) {
         ws.tile_sched_bytes = gemm_sched_bytes((int)E, (int)rows);
@@ -538,6 +542,76 @@ int coli_moe_stage_times(coli_moe_t *h, float *ms) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// NVFP4 experts.
+
+namespace {
+
+bool valid_nv(const coli_nvfp4_experts *e) {
+    return e && e->gate_up_codes && e->gate_up_scales && e->gate_up_global && e->down_codes && e->down_scales &&
+           e->down_global && aligned16(e->gate_up_codes) && aligned16(e->gate_up_scales) &&
+           aligned16(e->down_codes) && aligned16(e->down_scales);
+}
+
+ExpertSet nv_set(const coli_nvfp4_experts *e) {
+    ExpertSet s{};
+    if (e) {
+        s.gu_codes = e->gate_up_codes;
+        s.gu_scales = e->gate_up_scales;
+        s.d_codes = e->down_codes;
+        s.d_scales = e->down_scales;
+        s.gu_global = e->gate_up_global;
+        s.d_global = e->down_global;
+    }
+    return s;
+}
+
+}  // namespace
+
+extern "C" int coli_moe_forward_nvfp4(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router_w,
+                                      const float *router_bias, const coli_nvfp4_experts *packed,
+                                      const coli_nvfp4_experts *shared, int32_t top_k, void *out_bf16) {
+    if (!h) return COLI_ERR_INVALID_ARG;
+    if (T == 0) {
+        h->last_launches = 0;
+        return COLI_OK;
+    }
+    int rc = check_forward(h, x_bf16, T, router_w, nullptr, top_k, out_bf16);
+    if (rc != COLI_OK) return rc;
+    if (!valid_nv(packed) || (shared && (h->cfg.shared_inter == 0 || !valid_nv(shared)))) {
+        set_err(h, "NVFP4 experts need six non-NULL pointers (codes and scales 16-byte aligned), and a shared "
+                   "expert only with cfg.shared_inter > 0");
+        return COLI_ERR_INVALID_ARG;
+    }
+    cudaGetLastError();
+    const bool with_shared = shared != nullptr;
+    const int rows = T * top_k + (with_shared ? T : 0);
+    int launches = 0;
+    h->stage_valid = false;
+    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, false, kNtileMx4, rows, launches))
+        return launch_failed(h);
+    FfnArgs a = ffn_args(h, x_bf16, T, top_k, rows, nullptr, nullptr);
+    a.routed = nv_set(packed);
+    a.shared = nv_set(shared);
+    int n = launch_ffn_nv4(a, h->num_sms, h->ws.tile_sched, h->stream);
+    if (n == -2) {
+        set_err(h, "NVFP4 path unavailable (needs a tensor-map encoder, H and I up to 8192)");
+        return COLI_ERR_INVALID_ARG;
+    }
+    if (n < 0) return launch_failed(h);
+    launches += n;
+    n = launch_combine(h->ws.y, h->ws.inv_row, h->ws.w, T, h->cfg.hidden, top_k, with_shared,
+                       static_cast<__nv_bfloat16 *>(out_bf16), h->stream);
+    if (n < 0) return launch_failed(h);
+    launches += n;
+    h->last_T = T;
+    h->last_k = top_k;
+    h->last_shared = with_shared;
+    h->last_launches = launches;
+    h->last_path = COLI_FFN_GEMM_MXF4;
+    return COLI_OK;
+}
 
 // ------------------------------------------------------------------------------------------------
 // Expert residency bank (kernels and policy in bank.cu).

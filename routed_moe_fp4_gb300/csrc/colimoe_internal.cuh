@@ -13,11 +13,14 @@
 namespace colimoe {
 
 // One expert set in the packed MXFP4 layout (see colimoe.h).
+// NVFP4 sets (the format variant) use the same codes, E4M3 scales per 16 ([E][rows][K/16]) and
+// one fp32 scale per expert and matrix (gu_global, d_global: [E] device arrays, else null).
 struct ExpertSet {
     const uint8_t *gu_codes;    // [E][2I][H/2]
     const uint8_t *gu_scales;   // [E][2I][H/32]
     const uint8_t *d_codes;     // [E][H][I/2]
     const uint8_t *d_scales;    // [E][H][I/32]
+    const float *gu_global = nullptr, *d_global = nullptr;
 };
 
 // Device workspace, sized at create for (max_tokens, max_top_k).
@@ -41,9 +44,12 @@ struct Workspace {
     // E2M1 terms ([4][rows][H/2]); three E4M3 terms of h ([3][rows][I_max]) or four packed E2M1
     // terms ([4][rows][I_max/2]); UE8M0 scales per 32 elements, [terms][rows][K/32].
     uint8_t *xq = nullptr;          // 2 * rows * H bytes
-    uint8_t *xqs = nullptr;         // 4 * rows * H/32
+    uint8_t *xqs = nullptr;         // 4 * rows * H/16 (per 32 on the MXFP4 paths)
     uint8_t *hq = nullptr;          // 3 * rows * I_max
-    uint8_t *hqs = nullptr;         // 4 * rows * I_max/32
+    uint8_t *hqs = nullptr;         // 4 * rows * I_max/16 (per 32 on the MXFP4 paths)
+    float *xg = nullptr;            // NVFP4 path: [4][rows] power-of-two scale per x term and row
+    float *hg = nullptr;            // [4][rows] the same for the h terms
+    float *hf = nullptr;            // [rows][I_max] fp32 h between the NVFP4 GEMMs
     __half *xh = nullptr;           // [Tm][H] tokens as scaled fp16, permuted unit layout (GEMV path)
     float *xinv = nullptr;          // [Tm] inverse scales of xh
     __half *hh = nullptr;           // [Tm*km + Tm][I_max] h rows as scaled fp16 (GEMV path)
@@ -80,6 +86,7 @@ struct FfnArgs {
     float *hinv;
     float *y;                       // [rows][H]
     uint8_t *xq, *xqs, *hq, *hqs;   // block-scaled paths: activation terms and scales
+    float *xg, *hg, *hf;            // NVFP4 path: per (term, row) scales of x and h, fp32 h
     int *err;
     uint64_t wait_ns;               // FP4 path: limit of the pipeline waits (0 = the default, 2 s)
     // FP4 path over an expert bank (bank.cu): the tile layout of one round, whose records name
@@ -263,6 +270,10 @@ bool mx4_supported(const FfnArgs &a);
 int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
 // Expert-grouped activation rows -> four packed E2M1 terms + UE8M0 scales (ws.xq / ws.xqs).
 int launch_quant_x4(const FfnArgs &a, cudaStream_t st);
+// NVFP4 variant (routed and shared sets carry E4M3 scales per 16 and fp32 globals): x terms with
+// E4M3 scales per 16 and a power-of-two scale per (term, row), both GEMMs, and the h terms
+// between them. Returns the kernels enqueued, -1 on a launch error, -2 when unsupported.
+int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaStream_t st);
 
 // Grouped tcgen05 GEMM path with weights dequantised to bf16 in shared memory (gemm_tc.cu).
 size_t gemm_sched_bytes(int E, int max_rows);

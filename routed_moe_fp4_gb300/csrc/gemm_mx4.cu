@@ -46,9 +46,10 @@ constexpr uint32_t kOffA0 = 0, kOffA1 = kASmem, kOffB = 2 * kASmem;
 constexpr uint32_t kStageBytes = 2 * kASmem + kBSmemMax;   // 49152
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 128;             // per accumulator buffer
-constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 32 per stage
+constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 32 per stage (64 for NVFP4)
 constexpr uint32_t kSfStage = 32;
-constexpr int kSfAhead = 4;                   // stages the scale loads run ahead
+constexpr uint32_t kSfStageNv = 64;
+constexpr int kSfAhead = 4;                   // stages the scale loads run ahead (2 for NVFP4)
 constexpr int kEpiWarps = 8;                  // two per TMEM lane quarter, alternate 8-column groups
 
 enum Mode { kGateUp = 0, kDown = 1 };
@@ -67,6 +68,11 @@ struct Mx4Params {
     float *y;
     int *err;
     uint64_t wait_ns;                   // limit of the pipeline waits (the drains always allow the full limit)
+    // NVFP4: E4M3 scales per 16 on both operands (act_scales [kTerms][rows][K/16]), the experts'
+    // fp32 matrix scales, the activations' power-of-two scales per (term, row), and fp32 h out
+    int nv;
+    const float *w_global_routed, *w_global_shared, *act_global;
+    float *hf;
 };
 
 // A down tile of at most 16 rows uses wide stages: 512 K, two 128-byte chunks of weights (in the
@@ -95,7 +101,7 @@ __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 
     ti.K = p.mode == kGateUp ? p.H : ti.Ig;
     ti.box = ti.n_valid <= 16 ? 0 : 1;
     ti.bh = 16 << ti.box;
-    ti.wide = p.mode == kDown && ti.box == 0;
+    ti.wide = !p.nv && p.mode == kDown && ti.box == 0;
     ti.kst = ti.wide ? 2 * BK : BK;
     ti.nk = (ti.K + ti.kst - 1) / ti.kst;
     return ti;
@@ -105,8 +111,10 @@ __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 
 // activation rows lane + 32c (c < nbc); nbc == 0 marks an empty ring slot.
 // In a wide stage a0 / a1 hold the weight words 0-1 / 2-3, and b[c] / b[c + 2] the words 0-1 / 2-3
 // of activation column c (c < 2).
-struct SfStage {
-    uint32_t a0[2], a1[2], b[4][2];
+// NVFP4 stages hold four words per operand row (one per 64-K MMA) and are never wide.
+template <bool NV> struct SfStageT {
+    static constexpr int W = NV ? 4 : 2;
+    uint32_t a0[W], a1[W], b[4][W];
     int nbc;
     bool wide;
 };
@@ -136,7 +144,8 @@ __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int tot
         }
         c.tB = c.t + 2 * gridDim.x;
         c.recB = tile_rec(p, c.tB, total_tiles);
-        const int kb_row = ti.K / 32, kba = p.act_ld / 32;
+        const int sdiv = p.nv ? 16 : 32;                 // elements per scale byte
+        const int kb_row = ti.K / sdiv, kba = p.act_ld / sdiv;
         const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
         const int rpe = gu ? 2 * ti.Ig : p.H;
         const size_t wrow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM + quad * 32 + lane;
@@ -167,7 +176,25 @@ __device__ __forceinline__ bool sf_next(const Mx4Params &p, SfCursor &c, int tot
 
 // Issues the loads of the cursor's stage: 8 scale bytes per row (16 in a wide stage; fewer in the
 // last stage of a K that is not a multiple of the stage; a missing word reads as scale 1).
-__device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStage &s, int n_a) {
+template <bool NV>
+__device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStageT<NV> &s, int n_a) {
+    if constexpr (NV) {   // four words (16 scale bytes) per row and stage; a missing word reads as 1.0
+        const int nw = min(BK, c.K - c.k * BK) / 64;
+        const int w0 = c.k * 4;
+        auto ld = [&](const uint8_t *q, int w) -> uint32_t {
+            return (q && w < nw) ? __ldg(reinterpret_cast<const uint32_t *>(q) + w0 + w) : 0x38383838u;
+        };
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            s.a0[w] = ld(c.wp0, w);
+            s.a1[w] = n_a > 1 ? ld(c.wp1, w) : 0x38383838u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) s.b[q][w] = ld(c.bp[q], w);
+        }
+        s.nbc = c.nbc;
+        s.wide = false;
+        return;
+    } else {
     const int kst = c.wide ? 2 * BK : BK;
     const int nw = min(kst, c.K - c.k * kst) / 128;         // valid words of this stage (1 to 4)
     const int w0 = c.k * (kst / 128);
@@ -196,6 +223,7 @@ __device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStage &s, int n_a)
     }
     s.nbc = c.nbc;
     s.wide = c.wide;
+    }
 }
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -219,6 +247,20 @@ __device__ __forceinline__ void mma_mx4(uint32_t d, uint64_t a, uint64_t b, uint
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
         " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+
+// kind::mxf4nvf4 with UE4M3 scales per 16 (scale_vec::4X): one scale word per row per MMA.
+__device__ __forceinline__ uint32_t idesc_nv4(int N) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_nv4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
         ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
         : "memory");
 }
@@ -259,7 +301,7 @@ struct BMaps4 {
     CUtensorMap m[kTerms][2];   // [term][box height 16 / 32]
 };
 
-template <int MODE>
+template <int MODE, bool NV = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
          const __grid_constant__ BMaps4 tm_b, const Mx4Params p) {
@@ -414,8 +456,19 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     // descriptors of this stage: the start-address field advances by 32 B (2) per MMA
                     const uint64_t a0 = desc0 + (uint64_t)(s * (kStageBytes >> 4));
                     const uint64_t a1 = a0 + (kOffA1 >> 4), b = a0 + (kOffB >> 4);
-                    const uint32_t sfa = tmem + kSfCol0 + s * kSfStage, sfb = sfa + 16;
                     const int nsteps = min(ti.kst, ti.K - k * ti.kst) / 64;   // 2, 4, 6 or 8
+                    if constexpr (NV) {   // one scale word per MMA, four words per operand and stage
+                        const uint32_t sfa = tmem + kSfCol0 + s * kSfStageNv, sfb = sfa + 32;
+                        const uint32_t idn = idesc_nv4(n_mma);
+                        for (int j = 0; j < nsteps; ++j) {
+                            mma_nv4(d0, a0 + 2 * j, b + 2 * j, idn, sfa + 4 * j, sfb + 4 * j, acc);
+                            if (gu) mma_nv4(d1, a1 + 2 * j, b + 2 * j, idn, sfa + 16 + 4 * j, sfb + 4 * j, acc);
+                            acc = 1;
+                        }
+                        ptx::mma_commit(ptx::smem_addr(&empty[s]));
+                        continue;
+                    }
+                    const uint32_t sfa = tmem + kSfCol0 + s * kSfStage, sfb = sfa + 16;
                     auto step = [&](int j) {
                         const uint32_t id = (j & 1) ? id2 : id0;
                         const uint32_t sw = 4 * (j >> 1);                  // scale word j / 2
@@ -471,9 +524,10 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             }
         }
         pdl_wait();
-        SfStage ring[kSfAhead];
+        constexpr int kAhead = NV ? 2 : kSfAhead;
+        SfStageT<NV> ring[kAhead];
 #pragma unroll
-        for (int d = 0; d < kSfAhead; ++d) {
+        for (int d = 0; d < kAhead; ++d) {
             ring[d].nbc = 0;
             if (live) {
                 sf_fetch(cur, ring[d], n_a);
@@ -484,7 +538,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         bool run = true;
         while (run) {
 #pragma unroll
-            for (int d = 0; d < kSfAhead; ++d) {
+            for (int d = 0; d < kAhead; ++d) {
                 if (!run || ring[d].nbc == 0 || *abort_flag) {
                     run = false;
                     continue;
@@ -496,8 +550,17 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     continue;
                 }
                 ptx::tc_fence_after();
-                const uint32_t col = lane_base + kSfCol0 + s * kSfStage;
-                if (!gu && ring[d].wide) {   // words 0-3, 4 columns apart
+                const uint32_t col = lane_base + kSfCol0 + s * (NV ? kSfStageNv : kSfStage);
+                if constexpr (NV) {   // A0 words at +4w, A1 at +16 + 4w, activation words at +32 + 4w
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
+                        if (n_a > 1) tmem_st_x1(col + 16 + 4 * w + quad, ring[d].a1[w]);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (c < ring[d].nbc) tmem_st_x1(col + 32 + 4 * w + c, ring[d].b[c][w]);
+                    }
+                } else if (!gu && ring[d].wide) {   // words 0-3, 4 columns apart
 #pragma unroll
                     for (int w = 0; w < 2; ++w) {
                         tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
@@ -552,6 +615,8 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             const int mrow = ti.mt * BM + m;
             const uint32_t acc = lane_base + buf * kAccCols;
             const int ncols = kTerms * ti.bh;
+            // NVFP4: the matrix scale of this tile's expert
+            const float wg = NV ? __ldg(ti.shared ? p.w_global_shared : p.w_global_routed + ti.ge) : 1.f;
             for (int c0 = 8 * half; c0 < ti.n_valid; c0 += 16) {
                 float v0[8], v1[8];
 #pragma unroll
@@ -561,18 +626,28 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     uint32_t r[8], r1[8];
                     ptx::tmem_ld8(acc + tt * ti.bh + c0, r);
                     if (gu) ptx::tmem_ld8(acc + ncols + tt * ti.bh + c0, r1);
+                    float ag[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)   // NVFP4: the term's power-of-two scale for that row
+                        ag[j] = NV && c0 + j < ti.n_valid
+                                    ? __ldg(p.act_global + (size_t)tt * p.rows + ti.row0 + c0 + j) : 1.f;
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v0[j] += __uint_as_float(r[j]);
+                    for (int j = 0; j < 8; ++j) v0[j] = fmaf(__uint_as_float(r[j]), ag[j], v0[j]);
                     if (gu) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) v1[j] += __uint_as_float(r1[j]);
+                        for (int j = 0; j < 8; ++j) v1[j] = fmaf(__uint_as_float(r1[j]), ag[j], v1[j]);
                     }
                 }
                 for (int j = 0; j < 8 && c0 + j < ti.n_valid; ++j) {
                     const size_t row = (size_t)ti.row0 + c0 + j;
                     if (!gu) {
-                        p.y[row * p.H + mrow] = v0[j];
+                        p.y[row * p.H + mrow] = NV ? v0[j] * wg : v0[j];
+                        continue;
+                    }
+                    if constexpr (NV) {   // h in fp32; the next kernel splits it into terms
+                        const float g = v0[j] * wg, u = v1[j] * wg;
+                        p.hf[row * p.I_max + mrow] = __fdiv_rn(g, 1.0f + expf(-g)) * u;
                         continue;
                     }
                     float v = __fdiv_rn(v0[j], 1.0f + expf(-v0[j])) * v1[j];
@@ -651,6 +726,107 @@ quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restr
     }
 }
 
+// NVFP4 activation terms: rows -> four E2M1 terms, each with an E4M3 scale per 16 elements under
+// a power-of-two scale per (term, row): G = 2^ceil(log2(max|v| / (6 * 448))) keeps every group's
+// scale max|v_group| / (6 G), rounded up to an E4M3 value, within E4M3's range, and |v| / (scale
+// G) <= 6 within E2M1's. The next term takes the exact residual. x rows are gathered through
+// src_token (K = H); h rows come from the gate/up launch in fp32, K = I for routed rows and I_s
+// for the shared expert's rows (from off[E] on). One block of 128 threads per row; a thread owns
+// whole groups, up to four (K <= 8192).
+template <bool FROM_X>
+__global__ void __launch_bounds__(128)
+quant_rows_nv(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ hf, const int32_t *__restrict__ src_token,
+              const int32_t *__restrict__ off_shared, int K_routed, int K_shared, int ld_in, int rows, int ld_out,
+              uint8_t *__restrict__ q, uint8_t *__restrict__ qs, float *__restrict__ gs) {
+    pdl_wait();
+    pdl_trigger();
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const int K = FROM_X ? K_routed : (row >= *off_shared ? K_shared : K_routed);
+    const int ng = K / 16;
+    float v[4][16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int g = tid + 128 * i;
+#pragma unroll
+        for (int e = 0; e < 16; e += 8) {
+            if (g < ng) {
+                if constexpr (FROM_X) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(x + (size_t)src_token[row] * ld_in + g * 16 + e);
+                    const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 f = __bfloat1622float2(h2[j]);
+                        v[i][e + 2 * j] = f.x;
+                        v[i][e + 2 * j + 1] = f.y;
+                    }
+                } else {
+                    const float4 a = *reinterpret_cast<const float4 *>(hf + (size_t)row * ld_in + g * 16 + e);
+                    const float4 b = *reinterpret_cast<const float4 *>(hf + (size_t)row * ld_in + g * 16 + e + 4);
+                    v[i][e] = a.x; v[i][e + 1] = a.y; v[i][e + 2] = a.z; v[i][e + 3] = a.w;
+                    v[i][e + 4] = b.x; v[i][e + 5] = b.y; v[i][e + 6] = b.z; v[i][e + 7] = b.w;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[i][e + j] = 0.f;
+            }
+        }
+    }
+    __shared__ float red[4];
+    for (int t = 0; t < kTerms; ++t) {
+        float am[4], tm = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            am[i] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) am[i] = fmaxf(am[i], fabsf(v[i][e]));
+            tm = fmaxf(tm, am[i]);
+        }
+        tm = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(tm)));
+        if ((tid & 31) == 0) red[tid >> 5] = tm;
+        __syncthreads();
+        const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+        __syncthreads();
+        // G = 2^ceil(log2(M / 2688)) as an fp32 bit pattern (M = 0: G = 1)
+        float G = 1.f;
+        if (M > 0.f) {
+            const float r = M * (1.0f / 2688.0f);
+            uint32_t eb = (__float_as_uint(r) >> 23) & 0xFF;
+            if ((__float_as_uint(r) & 0x7FFFFF) != 0 || eb == 0) ++eb;   // round the power up
+            G = __uint_as_float(min(max(eb, 1u), 254u) << 23);
+        }
+        if (tid == 0) gs[(size_t)t * rows + row] = G;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int g = tid + 128 * i;
+            if (g >= ng) continue;
+            // the group's E4M3 scale: am / (6 G) rounded up to an E4M3 value (0 for an empty group)
+            const float ratio = am[i] / (6.0f * G);
+            uint16_t sb2;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(sb2) : "f"(0.f), "f"(ratio));
+            uint32_t sb = sb2 & 0xFF, back;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"((uint16_t)sb));
+            if (__half2float(__ushort_as_half((uint16_t)(back & 0xFFFF))) < ratio) {   // next code up
+                ++sb;
+                asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"((uint16_t)sb));
+            }
+            const float scale = __half2float(__ushort_as_half((uint16_t)(back & 0xFFFF))) * G;
+            qs[((size_t)t * rows + row) * (ld_out / 16) + g] = (uint8_t)sb;
+            uint32_t packed[2] = {0, 0};
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                float b0 = 0.f, b1 = 0.f;
+                uint32_t code = 0;
+                if (scale > 0.f) code = e2m1_pair(__fdiv_rn(v[i][e], scale), __fdiv_rn(v[i][e + 1], scale), b0, b1);
+                v[i][e] -= b0 * scale;
+                v[i][e + 1] -= b1 * scale;
+                packed[e >> 3] |= code << (4 * (e & 7));
+            }
+            *reinterpret_cast<uint2 *>(q + ((size_t)t * rows + row) * (ld_out / 2) + g * 8) =
+                make_uint2(packed[0], packed[1]);
+        }
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -696,7 +872,10 @@ int launch_quant_x4(const FfnArgs &a, cudaStream_t st) {
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
-int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
+namespace {
+
+template <bool NV>
+int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
     if (!mx4_supported(a)) return -2;
     const NtileLayout nl = a.tiles ? *a.tiles : ntile_layout(sched, a.E, a.rows);
     const uint64_t slots = a.w_slots ? a.w_slots : a.E;   // weight sets the routed arrays hold
@@ -704,9 +883,9 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     const size_t smem = NS * kStageBytes + 1024 + 256;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(gemm_mx4<kGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        if (cudaFuncSetAttribute(gemm_mx4<kGateUp, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
                 cudaSuccess ||
-            cudaFuncSetAttribute(gemm_mx4<kDown>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaFuncSetAttribute(gemm_mx4<kDown, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
                 cudaSuccess)
             return -1;
         attr = true;
@@ -723,6 +902,8 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     p.hs = a.hqs;
     p.y = a.y;
     p.err = a.err;
+    p.nv = NV ? 1 : 0;
+    p.hf = a.hf;
     CUtensorMap tar, tas;
     BMaps4 tb;
     // gate/up
@@ -737,16 +918,25 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     p.m_tiles = (a.I_max + BM - 1) / BM;
     p.w_scales_routed = a.routed.gu_scales;
     p.w_scales_shared = a.shared.gu_scales;
+    p.w_global_routed = a.routed.gu_global;
+    p.w_global_shared = a.shared.gu_global;
     p.act_scales = a.xqs;
+    p.act_global = a.xg;
     p.act_ld = a.H;
     bool ok = map_packed(&tar, a.routed.gu_codes, a.H, slots * 2 * a.I, BM) &&
               map_terms(tb, a.xq, a.H, a.rows);
     if (a.shared.gu_codes) ok = ok && map_packed(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_k(a.pdl_gate_up, gemm_mx4<kGateUp>, grid, dim3(kThreads), smem, st, tar, tas, tb, p);
+    launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV>, grid, dim3(kThreads), smem, st, tar, tas, tb, p);
     int n = 1;
     if (mid) cudaEventRecord(mid, st);
+    if constexpr (NV) {   // h (fp32) -> four terms with E4M3 scales per 16 under a scale per (term, row)
+        launch_pdl(quant_rows_nv<false>, dim3((unsigned)a.rows), dim3(128), 0, st, (const __nv_bfloat16 *)nullptr,
+                   (const float *)a.hf, (const int32_t *)nullptr, a.off + a.E, a.I, a.I_s, a.I_max, a.rows, a.I_max,
+                   a.hq, a.hqs, a.hg);
+        ++n;
+    }
     // down
     p.mode = kDown;
     p.bn = kBnDown;
@@ -756,15 +946,33 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     p.m_tiles = a.H / BM;
     p.w_scales_routed = a.routed.d_scales;
     p.w_scales_shared = a.shared.d_scales;
+    p.w_global_routed = a.routed.d_global;
+    p.w_global_shared = a.shared.d_global;
     p.act_scales = a.hqs;
+    p.act_global = a.hg;
     p.act_ld = a.I_max;
     ok = map_packed(&tar, a.routed.d_codes, a.I, slots * a.H, BM) && map_terms(tb, a.hq, a.I_max, a.rows);
     if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_pdl(gemm_mx4<kDown>, grid, dim3(kThreads), smem, st, tar, tas, tb, p);
+    launch_pdl(gemm_mx4<kDown, NV>, grid, dim3(kThreads), smem, st, tar, tas, tb, p);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
+}
+
+}  // namespace
+
+int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
+    return launch_ffn_impl<false>(a, num_sms, sched, mid, st);
+}
+
+int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaStream_t st) {
+    if (a.H > 8192 || a.I_max > 8192 || !a.routed.gu_global || !a.routed.d_global) return -2;
+    launch_pdl(quant_rows_nv<true>, dim3((unsigned)a.rows), dim3(128), 0, st, a.x, (const float *)nullptr,
+               a.src_token, a.off + a.E, a.H, a.H, a.H, a.rows, a.H, a.xq, a.xqs, a.xg);
+    if (cudaPeekAtLastError() != cudaSuccess) return -1;
+    const int n = launch_ffn_impl<true>(a, num_sms, sched, nullptr, st);
+    return n < 0 ? n : n + 1;
 }
 
 }  // namespace colimoe
