@@ -88,6 +88,7 @@ __device__ __forceinline__ int2 tile_rec(const Mx4Params &p, int t, int total_ti
     return t < total_tiles ? __ldg(p.ntile_rec + t / p.m_tiles) : make_int2(0, 0);
 }
 
+template <bool NV>
 __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 rec) {
     TileInfo ti;
     ti.mt = t % p.m_tiles;
@@ -101,7 +102,7 @@ __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 
     ti.K = p.mode == kGateUp ? p.H : ti.Ig;
     ti.box = ti.n_valid <= 16 ? 0 : 1;
     ti.bh = 16 << ti.box;
-    ti.wide = !p.nv && p.mode == kDown && ti.box == 0;
+    ti.wide = !NV && p.mode == kDown && ti.box == 0;
     ti.kst = ti.wide ? 2 * BK : BK;
     ti.nk = (ti.K + ti.kst - 1) / ti.kst;
     return ti;
@@ -129,11 +130,12 @@ struct SfCursor {
 };
 
 // Moves the cursor to the first valid tile at or after cur.t; false when there is none.
+template <bool NV>
 __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int total_tiles, int quad, int lane) {
     const bool gu = p.mode == kGateUp;
     for (; c.t < total_tiles; c.t += gridDim.x) {
         const int2 rec = c.t == c.tA ? c.recA : c.t == c.tB ? c.recB : tile_rec(p, c.t, total_tiles);
-        const TileInfo ti = decode_tile(p, c.t, rec);
+        const TileInfo ti = decode_tile<NV>(p, c.t, rec);
         if (!ti.valid) continue;
         if (c.tB == c.t + (int)gridDim.x) {            // keep the next two records in flight
             c.tA = c.tB;
@@ -144,7 +146,7 @@ __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int tot
         }
         c.tB = c.t + 2 * gridDim.x;
         c.recB = tile_rec(p, c.tB, total_tiles);
-        const int sdiv = p.nv ? 16 : 32;                 // elements per scale byte
+        constexpr int sdiv = NV ? 16 : 32;               // elements per scale byte
         const int kb_row = ti.K / sdiv, kba = p.act_ld / sdiv;
         const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
         const int rpe = gu ? 2 * ti.Ig : p.H;
@@ -168,10 +170,11 @@ __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int tot
     return false;
 }
 
+template <bool NV>
 __device__ __forceinline__ bool sf_next(const Mx4Params &p, SfCursor &c, int total_tiles, int quad, int lane) {
     if (++c.k < c.nk) return true;
     c.t += gridDim.x;
-    return sf_tile(p, c, total_tiles, quad, lane);
+    return sf_tile<NV>(p, c, total_tiles, quad, lane);
 }
 
 // Issues the loads of the cursor's stage: 8 scale bytes per row (16 in a wide stage; fewer in the
@@ -384,10 +387,10 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             // before the wait: the weights of the first stages of the first tile (all slots are free)
             int t0 = blockIdx.x, pre = 0;
             int2 rec = tile_rec(p, t0, total_tiles);
-            TileInfo ti0 = decode_tile(p, t0, rec);
+            TileInfo ti0 = decode_tile<NV>(p, t0, rec);
             while (t0 < total_tiles && !ti0.valid) {
                 t0 += gridDim.x;
-                ti0 = decode_tile(p, t0, tile_rec(p, t0, total_tiles));
+                ti0 = decode_tile<NV>(p, t0, tile_rec(p, t0, total_tiles));
             }
             if (t0 < total_tiles) {
                 pre = min(NS, ti0.nk);
@@ -400,7 +403,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
                 const int2 cur = rec;
                 rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
-                const TileInfo ti = decode_tile(p, t, cur);
+                const TileInfo ti = decode_tile<NV>(p, t, cur);
                 if (!ti.valid) continue;
                 for (int k = 0; k < ti.nk; ++k, ++it) {
                     if (t == t0 && k < pre) continue;             // issued above
@@ -429,7 +432,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
                 const int2 cur = rec;
                 rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
-                const TileInfo ti = decode_tile(p, t, cur);
+                const TileInfo ti = decode_tile<NV>(p, t, cur);
                 if (!ti.valid) continue;
                 const uint32_t buf = p.nbuf == 2 ? tcount & 1u : 0u, use = p.nbuf == 2 ? tcount >> 1 : tcount;
                 if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[buf]), (use & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
@@ -516,7 +519,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         SfCursor cur;
         cur.t = blockIdx.x;
         cur.tA = cur.tB = -1;
-        bool live = sf_tile(p, cur, total_tiles, quad, lane);   // tile records: readable before the wait
+        bool live = sf_tile<NV>(p, cur, total_tiles, quad, lane);   // tile records: readable before the wait
         if (live) {   // this lane's weight-scale rows of the first tile into L2 meanwhile
             for (int o = 0; o < cur.K / 32; o += 128) {
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(cur.wp0 + o));
@@ -531,7 +534,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             ring[d].nbc = 0;
             if (live) {
                 sf_fetch(cur, ring[d], n_a);
-                live = sf_next(p, cur, total_tiles, quad, lane);
+                live = sf_next<NV>(p, cur, total_tiles, quad, lane);
             }
         }
         uint32_t it = 0;
@@ -588,7 +591,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 ring[d].nbc = 0;
                 if (live) {
                     sf_fetch(cur, ring[d], n_a);
-                    live = sf_next(p, cur, total_tiles, quad, lane);
+                    live = sf_next<NV>(p, cur, total_tiles, quad, lane);
                 }
             }
         }
@@ -604,7 +607,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
             const int2 cur = rec;
             rec = tile_rec(p, t + gridDim.x, total_tiles);
-            const TileInfo ti = decode_tile(p, t, cur);
+            const TileInfo ti = decode_tile<NV>(p, t, cur);
             if (!ti.valid) continue;
             const uint32_t buf = p.nbuf == 2 ? tcount & 1u : 0u, use = p.nbuf == 2 ? tcount >> 1 : tcount;
             if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[buf]), use & 1u, p.err, ptx::kErrWaitAccum, abort_flag,
@@ -615,8 +618,8 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             const int mrow = ti.mt * BM + m;
             const uint32_t acc = lane_base + buf * kAccCols;
             const int ncols = kTerms * ti.bh;
-            // NVFP4: the matrix scale of this tile's expert
-            const float wg = NV ? __ldg(ti.shared ? p.w_global_shared : p.w_global_routed + ti.ge) : 1.f;
+            float wg = 1.f;   // NVFP4: the matrix scale of this tile's expert
+            if constexpr (NV) wg = __ldg(ti.shared ? p.w_global_shared : p.w_global_routed + ti.ge);
             for (int c0 = 8 * half; c0 < ti.n_valid; c0 += 16) {
                 float v0[8], v1[8];
 #pragma unroll
@@ -626,23 +629,34 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     uint32_t r[8], r1[8];
                     ptx::tmem_ld8(acc + tt * ti.bh + c0, r);
                     if (gu) ptx::tmem_ld8(acc + ncols + tt * ti.bh + c0, r1);
-                    float ag[8];
+                    if constexpr (NV) {   // each term column times its power-of-two scale for that row
+                        float ag[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)   // NVFP4: the term's power-of-two scale for that row
-                        ag[j] = NV && c0 + j < ti.n_valid
-                                    ? __ldg(p.act_global + (size_t)tt * p.rows + ti.row0 + c0 + j) : 1.f;
-                    ptx::tmem_ld_wait();
+                        for (int j = 0; j < 8; ++j)
+                            ag[j] = c0 + j < ti.n_valid
+                                        ? __ldg(p.act_global + (size_t)tt * p.rows + ti.row0 + c0 + j) : 0.f;
+                        ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v0[j] = fmaf(__uint_as_float(r[j]), ag[j], v0[j]);
-                    if (gu) {
+                        for (int j = 0; j < 8; ++j) v0[j] = fmaf(__uint_as_float(r[j]), ag[j], v0[j]);
+                        if (gu) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) v1[j] = fmaf(__uint_as_float(r1[j]), ag[j], v1[j]);
+                            for (int j = 0; j < 8; ++j) v1[j] = fmaf(__uint_as_float(r1[j]), ag[j], v1[j]);
+                        }
+                    } else {
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v0[j] += __uint_as_float(r[j]);
+                        if (gu) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) v1[j] += __uint_as_float(r1[j]);
+                        }
                     }
                 }
                 for (int j = 0; j < 8 && c0 + j < ti.n_valid; ++j) {
                     const size_t row = (size_t)ti.row0 + c0 + j;
                     if (!gu) {
-                        p.y[row * p.H + mrow] = NV ? v0[j] * wg : v0[j];
+                        if constexpr (NV) p.y[row * p.H + mrow] = v0[j] * wg;
+                        else p.y[row * p.H + mrow] = v0[j];
                         continue;
                     }
                     if constexpr (NV) {   // h in fp32; the next kernel splits it into terms
