@@ -116,11 +116,13 @@ FFN_PATHS = {
     "mx": (2, "gemm_mx", (2, 1.0), (3, 1.0), "mxfp4 e2m1 x e4m3 activation terms, fp32 accumulate"),
     "bf16": (3, "gemm_tc", None, None, "mxfp4 e2m1 dequantised to bf16, bf16 tensor cores, fp32 accumulate"),
     "mxf4": (4, "gemm_mx4", (4, 0.5), (4, 0.5), "mxfp4 e2m1 x e2m1 activation terms, fp32 accumulate"),
+    "nvf4": (4, "gemm_mx4", (4, 0.5), (4, 0.5),
+             "nvfp4 e2m1 (e4m3 scale per 16, fp32 per matrix) x e2m1 activation terms, fp32 accumulate"),
 }
 PATH_BY_ABI = {v[0]: k for k, v in FFN_PATHS.items()}
 
 
-def algorithmic_bytes(wl, routing: dict, path: str = "mxf4") -> dict:
+def algorithmic_bytes(wl, routing: dict, path: str = "mxf4", group: int = 32) -> dict:
     """Bytes each stage of a block-scaled path must move at least once (touched experts from cnt).
 
     gate/up: the touched experts' gate and up codes + scales, the activation terms of x (+ scales)
@@ -133,12 +135,12 @@ def algorithmic_bytes(wl, routing: dict, path: str = "mxf4") -> dict:
     touched = int((cnt[:E] > 0).sum())
     shared = 1 if I_s > 0 else 0
     Imax = max(I, I_s)
-    gu_per = lambda i: 2 * i * (H // 2 + H // 32)        # gate+up codes and scales
-    dn_per = lambda i: H * (i // 2 + i // 32)
+    gu_per = lambda i: 2 * i * (H // 2 + H // group)     # gate+up codes and scales (one per group)
+    dn_per = lambda i: H * (i // 2 + i // group)
     rows = T * k + T * shared
     (nx, bx), (nh, bh) = FFN_PATHS[path][2] or (2, 1.0), FFN_PATHS[path][3] or (3, 1.0)
-    x_terms = int(nx * rows * (H * bx + H // 32))
-    h_terms = int(nh * rows * (Imax * bh + Imax // 32))
+    x_terms = int(nx * rows * (H * bx + H // group))
+    h_terms = int(nh * rows * (Imax * bh + Imax // group))
     weights = touched * (gu_per(I) + dn_per(I)) + shared * (gu_per(I_s) + dn_per(I_s))
     gate_up = touched * gu_per(I) + shared * gu_per(I_s) + x_terms + h_terms
     down = touched * dn_per(I) + shared * dn_per(I_s) + h_terms + rows * H * 4
@@ -184,11 +186,12 @@ def run_ours(args, wl_name: str) -> dict:
     if ws > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     build.build()
-    inputs = S.make_inputs(wl_name, seed=0)
+    nv = args.format == "nvfp4"
+    inputs = S.make_nv_inputs(wl_name) if nv else S.make_inputs(wl_name, seed=0)
     wl = inputs.workload
     stream = torch.cuda.Stream()
-    layer = cm.MoELayer(inputs, stream=stream)
-    if args.ffn_path != "auto":
+    layer = (cm.NvMoELayer if nv else cm.MoELayer)(inputs, stream=stream)
+    if args.ffn_path != "auto" and not nv:
         layer.set_ffn_path(FFN_PATHS[args.ffn_path][0])
     x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
     out = torch.empty_like(x)
@@ -263,24 +266,36 @@ def run_ours(args, wl_name: str) -> dict:
     except RuntimeError as e:                  # capture not possible: say so, keep the eager numbers
         graph_info = {"unavailable": str(e).splitlines()[0][:200]}
 
-    # end to end: host buffers through coli_moe_forward_host
+    # end to end: host buffers through coli_moe_forward_host (the NVFP4 layer: the same copies
+    # around coli_moe_forward_nvfp4)
+    def host_step():
+        if not nv:
+            layer.forward_host(x_host, out_host)
+            return
+        with torch.cuda.stream(stream):
+            x.copy_(x_host, non_blocking=True)
+            layer.forward(x, out)
+            out_host.copy_(out, non_blocking=True)
+        stream.synchronize()
     for _ in range(2):
-        layer.forward_host(x_host, out_host)
+        host_step()
     e2e_ms = []
     for _ in range(args.steps):
         l2_flush()
         stream.synchronize()
         t0 = time.perf_counter()
-        layer.forward_host(x_host, out_host)
+        host_step()
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
     e2e_step = sum(e2e_ms) / len(e2e_ms)
 
     routing = layer.routing(wl.T)
-    ab = algorithmic_bytes(wl, routing, path)
+    if nv:
+        path = "nvf4"
+    ab = algorithmic_bytes(wl, routing, path, group=16 if nv else 32)
     hbm_gbs, bf16_tf, peak_kind = _peaks()
     dom = "ffn_gate_up"            # the largest kernel: the FFN GEMM's gate/up launch
     achieved = ab[dom] / (stages[dom] * 1e-3) / 1e9
-    traffic = profiled_traffic(kernel, wl.name)
+    traffic = None if nv else profiled_traffic(kernel, wl.name)
     tokens = wl.T * ws
     result = {
         "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
@@ -288,7 +303,8 @@ def run_ours(args, wl_name: str) -> dict:
         "scaling": "weak", "vs_baseline": None, "dtype": FFN_PATHS[path][4],
         "data": "synthetic (seeded SplitMix64; MXFP4 experts, bf16 activations)",
         "config": {"workload": f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E}, top_k={wl.top_k}, I={wl.I}, "
-                               f"I_s={wl.I_s}, MXFP4 E2M1 + UE8M0/32", "tokens_per_gpu": wl.T,
+                               f"I_s={wl.I_s}, " + ("NVFP4 E2M1 + E4M3/16 + fp32 per matrix" if nv
+                                                    else "MXFP4 E2M1 + UE8M0/32"), "tokens_per_gpu": wl.T,
                    "ffn_path": path, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed (512 MiB write) before every timed step"},
         "roofline": {"kernel": f"{kernel} (gate/up launch)", "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
@@ -604,6 +620,8 @@ def main():
     ap.add_argument("--skip-cpu", action="store_true", help="no cpu_baseline (profiling runs)")
     ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
                     help="force an FFN path (default: the library's own choice)")
+    ap.add_argument("--format", default="mxfp4", choices=["mxfp4", "nvfp4"],
+                    help="expert weight format of the MoE layer (nvfp4: the format variant)")
     ap.add_argument("--bank", type=int, default=0,
                     help="routed experts in page-locked host memory behind a bank of this many device slots")
     ap.add_argument("--copy-blocks", type=int, default=0, help="bank: blocks that copy while a round computes")

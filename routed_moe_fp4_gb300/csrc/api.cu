@@ -588,23 +588,35 @@ extern "C" int coli_moe_forward_nvfp4(coli_moe_t *h, const void *x_bf16, int32_t
     const bool with_shared = shared != nullptr;
     const int rows = T * top_k + (with_shared ? T : 0);
     int launches = 0;
+    cudaStream_t st = h->stream;
+    const bool prof = h->profiling;
     h->stage_valid = false;
-    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, false, kNtileMx4, rows, launches))
-        return launch_failed(h);
     FfnArgs a = ffn_args(h, x_bf16, T, top_k, rows, nullptr, nullptr);
     a.routed = nv_set(packed);
     a.shared = nv_set(shared);
-    int n = launch_ffn_nv4(a, h->num_sms, h->ws.tile_sched, h->stream);
-    if (n == -2) {
+    if (!nv4_supported(a)) {
         set_err(h, "NVFP4 path unavailable (needs a tensor-map encoder, H and I up to 8192)");
         return COLI_ERR_INVALID_ARG;
     }
+    if (prof) cudaEventRecord(h->ev[0], st);
+    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, false, kNtileMx4, rows, launches))
+        return launch_failed(h);
+    int n = launch_quant_x_nv(a, st);
     if (n < 0) return launch_failed(h);
     launches += n;
+    if (prof) cudaEventRecord(h->ev[2], st);
+    n = launch_ffn_nv4(a, h->num_sms, h->ws.tile_sched, prof ? h->ev[3] : nullptr, st);
+    if (n < 0) return launch_failed(h);
+    launches += n;
+    if (prof) cudaEventRecord(h->ev[4], st);
     n = launch_combine(h->ws.y, h->ws.inv_row, h->ws.w, T, h->cfg.hidden, top_k, with_shared,
-                       static_cast<__nv_bfloat16 *>(out_bf16), h->stream);
+                       static_cast<__nv_bfloat16 *>(out_bf16), st);
     if (n < 0) return launch_failed(h);
     launches += n;
+    if (prof) {
+        cudaEventRecord(h->ev[5], st);
+        h->stage_valid = true;
+    }
     h->last_T = T;
     h->last_k = top_k;
     h->last_shared = with_shared;

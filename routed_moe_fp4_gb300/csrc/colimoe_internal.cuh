@@ -270,10 +270,13 @@ bool mx4_supported(const FfnArgs &a);
 int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
 // Expert-grouped activation rows -> four packed E2M1 terms + UE8M0 scales (ws.xq / ws.xqs).
 int launch_quant_x4(const FfnArgs &a, cudaStream_t st);
-// NVFP4 variant (routed and shared sets carry E4M3 scales per 16 and fp32 globals): x terms with
-// E4M3 scales per 16 and a power-of-two scale per (term, row), both GEMMs, and the h terms
-// between them. Returns the kernels enqueued, -1 on a launch error, -2 when unsupported.
-int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaStream_t st);
+// NVFP4 variant (routed and shared sets carry E4M3 scales per 16 and fp32 globals): the x terms
+// (E4M3 scales per 16 under a power-of-two scale per (term, row)); then both GEMMs with the h
+// terms between them (`mid`, may be null, is recorded after the gate/up launch). Each returns the
+// kernels enqueued, -1 on a launch error; launch_ffn_nv4 -2 when the shapes are unsupported.
+bool nv4_supported(const FfnArgs &a);
+int launch_quant_x_nv(const FfnArgs &a, cudaStream_t st);
+int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
 
 // Grouped tcgen05 GEMM path with weights dequantised to bf16 in shared memory (gemm_tc.cu).
 size_t gemm_sched_bytes(int E, int max_rows);

@@ -68,9 +68,12 @@ struct Mx4Params {
     float *y;
     int *err;
     uint64_t wait_ns;                   // limit of the pipeline waits (the drains always allow the full limit)
-    // NVFP4: E4M3 scales per 16 on both operands (act_scales [kTerms][rows][K/16]), the experts'
-    // fp32 matrix scales, the activations' power-of-two scales per (term, row), and fp32 h out
-    int nv;
+};
+
+// NVFP4 launches only (a separate parameter, so that the MXFP4 kernels keep their parameter
+// layout): the experts' fp32 matrix scales, the activations' power-of-two scales per (term, row)
+// ([kTerms][rows]), and fp32 h out of the gate/up launch. act_scales then holds E4M3 bytes per 16.
+struct NvParams {
     const float *w_global_routed, *w_global_shared, *act_global;
     float *hf;
 };
@@ -307,7 +310,7 @@ struct BMaps4 {
 template <int MODE, bool NV = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
-         const __grid_constant__ BMaps4 tm_b, const Mx4Params p) {
+         const __grid_constant__ BMaps4 tm_b, const Mx4Params p, const __grid_constant__ NvParams q) {
     // The kernel before this one in the stream (quant_x4_rows, or the gate/up launch before the
     // down launch) signals its dependents only after its own dependency wait, so every kernel up
     // to the permutation has completed when this one starts: its tile records can be read, and the
@@ -619,7 +622,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             const uint32_t acc = lane_base + buf * kAccCols;
             const int ncols = kTerms * ti.bh;
             float wg = 1.f;   // NVFP4: the matrix scale of this tile's expert
-            if constexpr (NV) wg = __ldg(ti.shared ? p.w_global_shared : p.w_global_routed + ti.ge);
+            if constexpr (NV) wg = __ldg(ti.shared ? q.w_global_shared : q.w_global_routed + ti.ge);
             for (int c0 = 8 * half; c0 < ti.n_valid; c0 += 16) {
                 float v0[8], v1[8];
 #pragma unroll
@@ -634,7 +637,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             ag[j] = c0 + j < ti.n_valid
-                                        ? __ldg(p.act_global + (size_t)tt * p.rows + ti.row0 + c0 + j) : 0.f;
+                                        ? __ldg(q.act_global + (size_t)tt * p.rows + ti.row0 + c0 + j) : 0.f;
                         ptx::tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 8; ++j) v0[j] = fmaf(__uint_as_float(r[j]), ag[j], v0[j]);
@@ -661,7 +664,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     }
                     if constexpr (NV) {   // h in fp32; the next kernel splits it into terms
                         const float g = v0[j] * wg, u = v1[j] * wg;
-                        p.hf[row * p.I_max + mrow] = __fdiv_rn(g, 1.0f + expf(-g)) * u;
+                        q.hf[row * p.I_max + mrow] = __fdiv_rn(g, 1.0f + expf(-g)) * u;
                         continue;
                     }
                     float v = __fdiv_rn(v0[j], 1.0f + expf(-v0[j])) * v1[j];
@@ -916,8 +919,8 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     p.hs = a.hqs;
     p.y = a.y;
     p.err = a.err;
-    p.nv = NV ? 1 : 0;
-    p.hf = a.hf;
+    NvParams q{};
+    q.hf = a.hf;
     CUtensorMap tar, tas;
     BMaps4 tb;
     // gate/up
@@ -932,17 +935,17 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     p.m_tiles = (a.I_max + BM - 1) / BM;
     p.w_scales_routed = a.routed.gu_scales;
     p.w_scales_shared = a.shared.gu_scales;
-    p.w_global_routed = a.routed.gu_global;
-    p.w_global_shared = a.shared.gu_global;
+    q.w_global_routed = a.routed.gu_global;
+    q.w_global_shared = a.shared.gu_global;
     p.act_scales = a.xqs;
-    p.act_global = a.xg;
+    q.act_global = a.xg;
     p.act_ld = a.H;
     bool ok = map_packed(&tar, a.routed.gu_codes, a.H, slots * 2 * a.I, BM) &&
               map_terms(tb, a.xq, a.H, a.rows);
     if (a.shared.gu_codes) ok = ok && map_packed(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV>, grid, dim3(kThreads), smem, st, tar, tas, tb, p);
+    launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q);
     int n = 1;
     if (mid) cudaEventRecord(mid, st);
     if constexpr (NV) {   // h (fp32) -> four terms with E4M3 scales per 16 under a scale per (term, row)
@@ -960,16 +963,16 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     p.m_tiles = a.H / BM;
     p.w_scales_routed = a.routed.d_scales;
     p.w_scales_shared = a.shared.d_scales;
-    p.w_global_routed = a.routed.d_global;
-    p.w_global_shared = a.shared.d_global;
+    q.w_global_routed = a.routed.d_global;
+    q.w_global_shared = a.shared.d_global;
     p.act_scales = a.hqs;
-    p.act_global = a.hg;
+    q.act_global = a.hg;
     p.act_ld = a.I_max;
     ok = map_packed(&tar, a.routed.d_codes, a.I, slots * a.H, BM) && map_terms(tb, a.hq, a.I_max, a.rows);
     if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_pdl(gemm_mx4<kDown, NV>, grid, dim3(kThreads), smem, st, tar, tas, tb, p);
+    launch_pdl(gemm_mx4<kDown, NV>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }
@@ -980,13 +983,19 @@ int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, 
     return launch_ffn_impl<false>(a, num_sms, sched, mid, st);
 }
 
-int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaStream_t st) {
-    if (a.H > 8192 || a.I_max > 8192 || !a.routed.gu_global || !a.routed.d_global) return -2;
+bool nv4_supported(const FfnArgs &a) {
+    return mx4_supported(a) && a.H <= 8192 && a.I_max <= 8192 && a.routed.gu_global && a.routed.d_global;
+}
+
+int launch_quant_x_nv(const FfnArgs &a, cudaStream_t st) {
     launch_pdl(quant_rows_nv<true>, dim3((unsigned)a.rows), dim3(128), 0, st, a.x, (const float *)nullptr,
                a.src_token, a.off + a.E, a.H, a.H, a.H, a.rows, a.H, a.xq, a.xqs, a.xg);
-    if (cudaPeekAtLastError() != cudaSuccess) return -1;
-    const int n = launch_ffn_impl<true>(a, num_sms, sched, nullptr, st);
-    return n < 0 ? n : n + 1;
+    return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
+}
+
+int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
+    if (!nv4_supported(a)) return -2;
+    return launch_ffn_impl<true>(a, num_sms, sched, mid, st);
 }
 
 }  // namespace colimoe
