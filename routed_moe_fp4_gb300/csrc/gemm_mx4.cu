@@ -530,7 +530,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             }
         }
         pdl_wait();
-        constexpr int kAhead = NV ? 2 : kSfAhead;
+        constexpr int kAhead = NV ? 3 : kSfAhead;
         SfStageT<NV> ring[kAhead];
 #pragma unroll
         for (int d = 0; d < kAhead; ++d) {
@@ -828,12 +828,14 @@ quant_rows_nv(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ hf,
             }
             const float scale = __half2float(__ushort_as_half((uint16_t)(back & 0xFFFF))) * G;
             qs[((size_t)t * rows + row) * (ld_out / 16) + g] = (uint8_t)sb;
+            // codes of v / scale (by the rounded reciprocal: a quotient a hair above 6 saturates,
+            // and the next term takes whatever this one leaves)
+            const float inv = scale > 0.f ? __frcp_rn(scale) : 0.f;
             uint32_t packed[2] = {0, 0};
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
                 float b0 = 0.f, b1 = 0.f;
-                uint32_t code = 0;
-                if (scale > 0.f) code = e2m1_pair(__fdiv_rn(v[i][e], scale), __fdiv_rn(v[i][e + 1], scale), b0, b1);
+                const uint32_t code = e2m1_pair(v[i][e] * inv, v[i][e + 1] * inv, b0, b1);
                 v[i][e] -= b0 * scale;
                 v[i][e + 1] -= b1 * scale;
                 packed[e >> 3] |= code << (4 * (e & 7));
