@@ -128,6 +128,7 @@ template <bool NV> struct SfStageT {
 struct SfCursor {
     int t, k, nk, K, nbc, tA, tB;
     bool wide;
+    bool vw, va;                        // NVFP4: weight / activation scale rows are 16-byte aligned
     int2 recA, recB;                    // records of the next two tiles (tA < tB), loaded ahead
     const uint8_t *wp0, *wp1, *bp[4];
 };
@@ -168,6 +169,8 @@ __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int tot
         c.nk = ti.nk;
         c.K = ti.K;
         c.wide = ti.wide;
+        c.vw = kb_row % 16 == 0;
+        c.va = kba % 16 == 0;
         return true;
     }
     return false;
@@ -187,16 +190,28 @@ __device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStageT<NV> &s, int
     if constexpr (NV) {   // four words (16 scale bytes) per row and stage; a missing word reads as 1.0
         const int nw = min(BK, c.K - c.k * BK) / 64;
         const int w0 = c.k * 4;
-        auto ld = [&](const uint8_t *q, int w) -> uint32_t {
-            return (q && w < nw) ? __ldg(reinterpret_cast<const uint32_t *>(q) + w0 + w) : 0x38383838u;
+        // a full stage of a 16-byte aligned row is one 16-byte load; other rows, and the last stage
+        // of a K that is not a multiple of 256, load word by word
+        auto ld4 = [&](const uint8_t *q, bool vec, uint32_t (&o)[4]) {
+            if (!q) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) o[w] = 0x38383838u;
+            } else if (vec && nw == 4) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(q) + c.k);
+                o[0] = v.x;
+                o[1] = v.y;
+                o[2] = v.z;
+                o[3] = v.w;
+            } else {
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    o[w] = w < nw ? __ldg(reinterpret_cast<const uint32_t *>(q) + w0 + w) : 0x38383838u;
+            }
         };
+        ld4(c.wp0, c.vw, s.a0);
+        ld4(n_a > 1 ? c.wp1 : nullptr, c.vw, s.a1);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            s.a0[w] = ld(c.wp0, w);
-            s.a1[w] = n_a > 1 ? ld(c.wp1, w) : 0x38383838u;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) s.b[q][w] = ld(c.bp[q], w);
-        }
+        for (int q = 0; q < 4; ++q) ld4(c.bp[q], c.va, s.b[q]);
         s.nbc = c.nbc;
         s.wide = false;
         return;
@@ -273,6 +288,16 @@ __device__ __forceinline__ void mma_nv4(uint32_t d, uint64_t a, uint64_t b, uint
 
 __device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t a) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
+}
+
+// 32 lanes x 16 consecutive columns.
+__device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -530,7 +555,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             }
         }
         pdl_wait();
-        constexpr int kAhead = NV ? 3 : kSfAhead;
+        constexpr int kAhead = NV ? 2 : kSfAhead;
         SfStageT<NV> ring[kAhead];
 #pragma unroll
         for (int d = 0; d < kAhead; ++d) {
@@ -558,14 +583,20 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 ptx::tc_fence_after();
                 const uint32_t col = lane_base + kSfCol0 + s * (NV ? kSfStageNv : kSfStage);
                 if constexpr (NV) {   // A0 words at +4w, A1 at +16 + 4w, activation words at +32 + 4w
+                    // Lane 32q + i reads only column 4w + q of a weight group, so each word is
+                    // written to all four columns of its group: one 16-column store per operand.
+                    uint32_t r[16];
 #pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
-                        if (n_a > 1) tmem_st_x1(col + 16 + 4 * w + quad, ring[d].a1[w]);
+                    for (int j = 0; j < 16; ++j) r[j] = ring[d].a0[j >> 2];
+                    tmem_st_x16(col, r);
+                    if (n_a > 1) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < ring[d].nbc) tmem_st_x1(col + 32 + 4 * w + c, ring[d].b[c][w]);
+                        for (int j = 0; j < 16; ++j) r[j] = ring[d].a1[j >> 2];
+                        tmem_st_x16(col + 16, r);
                     }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) r[j] = ring[d].b[j & 3][j >> 2];
+                    tmem_st_x16(col + 32, r);
                 } else if (!gu && ring[d].wide) {   // words 0-3, 4 columns apart
 #pragma unroll
                     for (int w = 0; w < 2; ++w) {
