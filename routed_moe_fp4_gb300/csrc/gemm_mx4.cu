@@ -222,7 +222,33 @@ __device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStageT<NV> &s, int
     auto ld = [&](const uint8_t *q, int w) -> uint32_t {
         return (q && w < nw) ? __ldg(reinterpret_cast<const uint32_t *>(q) + w0 + w) : 0x7F7F7F7Fu;
     };
-    if (c.wide) {
+    // full stages of 16-byte aligned rows: one 8-byte (16 in a wide stage) load per row
+    if (c.wide && nw == 4 && c.vw && c.va) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4 *>(c.wp0) + c.k);
+        s.a0[0] = a.x;
+        s.a0[1] = a.y;
+        s.a1[0] = a.z;
+        s.a1[1] = a.w;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint4 v = c.bp[q] ? __ldg(reinterpret_cast<const uint4 *>(c.bp[q]) + c.k)
+                                    : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            s.b[q][0] = v.x;
+            s.b[q][1] = v.y;
+            s.b[q + 2][0] = v.z;
+            s.b[q + 2][1] = v.w;
+        }
+    } else if (!c.wide && nw == 2 && c.vw && c.va) {
+        auto ld2 = [&](const uint8_t *q, uint32_t (&o)[2]) {
+            const uint2 v = q ? __ldg(reinterpret_cast<const uint2 *>(q) + c.k) : make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+            o[0] = v.x;
+            o[1] = v.y;
+        };
+        ld2(c.wp0, s.a0);
+        ld2(n_a > 1 ? c.wp1 : nullptr, s.a1);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ld2(c.bp[q], s.b[q]);
+    } else if (c.wide) {
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
             s.a0[w] = ld(c.wp0, w);
@@ -597,26 +623,19 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
 #pragma unroll
                     for (int j = 0; j < 16; ++j) r[j] = ring[d].b[j & 3][j >> 2];
                     tmem_st_x16(col + 32, r);
-                } else if (!gu && ring[d].wide) {   // words 0-3, 4 columns apart
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
-                        tmem_st_x1(col + 8 + 4 * w + quad, ring[d].a1[w]);
-#pragma unroll
-                        for (int c = 0; c < 2; ++c) {
-                            tmem_st_x1(col + 16 + 4 * w + c, ring[d].b[c][w]);
-                            tmem_st_x1(col + 24 + 4 * w + c, ring[d].b[c + 2][w]);
-                        }
-                    }
                 } else {
+                    // Weight words 0-3 (a0 then a1; in a wide stage a1 holds words 2-3) at +4w, each
+                    // written to its whole 4-column group (lane 32q + i reads column 4w + q); the
+                    // activation words of column group c at +16 + 4w + c (a wide stage's words 2-3
+                    // at +24 + 4w + c). Columns a stage does not use take any value.
+                    uint32_t r[16];
 #pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        tmem_st_x1(col + 4 * w + quad, ring[d].a0[w]);
-                        if (n_a > 1) tmem_st_x1(col + 8 + 4 * w + quad, ring[d].a1[w]);
+                    for (int j = 0; j < 16; ++j) r[j] = j < 8 ? ring[d].a0[(j >> 2) & 1] : ring[d].a1[(j >> 2) & 1];
+                    tmem_st_x16(col, r);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            if (c < ring[d].nbc) tmem_st_x1(col + 16 + 4 * w + c, ring[d].b[c][w]);
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        r[j] = j < 8 ? ring[d].b[j & 3][(j >> 2) & 1] : ring[d].b[((j & 3) + 2) & 3][(j >> 2) & 1];
+                    tmem_st_x16(col + 16, r);
                 }
                 tmem_st_wait();
                 ptx::tc_fence_before();
