@@ -72,3 +72,40 @@ def test_create_without_gpu_is_an_error_not_a_fallback(lib):
     out = C.c_void_p()
     rc = lib.coli_moe_create(C.byref(cfg), None, C.byref(out))
     assert rc == cm.COLI_ERR_UNSUPPORTED_ARCH and out.value is None
+
+
+def test_null_arguments_of_the_bank_dense_and_nvfp4_calls(lib):
+    from routed_moe_fp4_gb300 import colimoe as cm
+    out = C.c_void_p(1)
+    assert lib.coli_bank_create(None, 4, None, C.byref(out)) == cm.COLI_ERR_INVALID_ARG
+    assert lib.coli_bank_create(None, 4, None, None) == cm.COLI_ERR_INVALID_ARG
+    lib.coli_bank_destroy(None)                      # no-op
+    assert lib.coli_bank_set_copy_blocks(None, 4) == cm.COLI_ERR_INVALID_ARG
+    assert lib.coli_bank_state(None, None, None, None, None, None) == cm.COLI_ERR_INVALID_ARG
+    assert lib.coli_moe_forward_banked(None, None, None, 1, None, None, None, 1, None) == cm.COLI_ERR_INVALID_ARG
+    assert lib.coli_moe_forward_nvfp4(None, None, 1, None, None, None, None, 1, None) == cm.COLI_ERR_INVALID_ARG
+    assert lib.coli_dense_create(4, 256, None, None) == cm.COLI_ERR_INVALID_ARG
+    assert lib.coli_dense_forward(None, None, 1, 128, None, None, 128, None) == cm.COLI_ERR_INVALID_ARG
+    lib.coli_dense_destroy(None)                     # no-op
+    code = C.c_int32(0)
+    assert lib.coli_dense_device_error(None, C.byref(code)) == cm.COLI_ERR_INVALID_ARG
+    assert isinstance(cm.coli_dense_last_error(None), str)
+
+
+def test_dense_create_rejects_bad_sizes(lib):
+    from routed_moe_fp4_gb300 import colimoe as cm
+    for max_tokens, max_k in ((0, 256), (4, 100), (4, 0), (4, 64)):
+        out = C.c_void_p(1)
+        assert lib.coli_dense_create(max_tokens, max_k, None, C.byref(out)) == cm.COLI_ERR_INVALID_ARG
+        assert out.value is None
+        assert "invalid dense config" in cm.coli_dense_last_error(None)
+
+
+def test_dense_create_without_gpu_is_an_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("this host has a GPU")
+    from routed_moe_fp4_gb300 import colimoe as cm
+    out = C.c_void_p()
+    assert lib.coli_dense_create(4, 256, None, C.byref(out)) == cm.COLI_ERR_UNSUPPORTED_ARCH
+    assert out.value is None

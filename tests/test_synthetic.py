@@ -69,3 +69,29 @@ def test_calibration_present():
     assert -1.25 < slope < -0.95, slope
     inp = S.make_inputs("skewed", 0, T=1, with_experts=False)
     assert np.array_equal(inp.router_b, np.array(cal["skewed_router_bias"], np.float32))
+
+
+def test_dense_inputs_have_no_nan_codes_and_positive_scales():
+    from routed_moe_fp4_gb300 import synthetic as S
+    d = S.make_dense_inputs("dense_tiny")
+    assert d.w.shape == (256, 384) and d.w_scale.shape == (2, 3) and d.x.shape == (5, 384)
+    assert not np.any((d.w & 0x7F) == 0x7F), "E4M3 NaN code in the weights"
+    assert np.all(d.w_scale > 0) and np.all(np.isfinite(d.w_scale))
+    assert np.array_equal(d.w, S.make_dense_inputs("dense_tiny").w), "not seeded"
+
+
+def test_nvfp4_experts_scale_bytes():
+    from routed_moe_fp4_gb300 import synthetic as S
+    ex = S.make_nv_experts(0, "t", 2, 256, 128)
+    assert ex.gate_up_scales.shape == (2, 256, 16) and ex.down_scales.shape == (2, 256, 8)
+    e = (ex.gate_up_scales >> 3) & 15
+    assert e.min() >= 4 and e.max() <= 8 and not np.any(ex.gate_up_scales & 0x80)
+    assert np.all((ex.gate_up_global >= 2.0 ** -6) & (ex.gate_up_global < 2.0 ** -5))
+
+
+def test_x_batches_are_distinct_streams():
+    from routed_moe_fp4_gb300 import synthetic as S
+    a = S.x_batch(0, "decode", 1, 4, 256)
+    b = S.x_batch(0, "decode", 2, 4, 256)
+    assert a.shape == (4, 256) and not np.array_equal(a, b)
+    assert np.array_equal(a, S.x_batch(0, "decode", 1, 4, 256))
