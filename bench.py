@@ -576,9 +576,35 @@ def oracle_sample(wl_name: str, budget_s: float):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return {"value": n_tok / el, "unit": "tokens/s", "cores": o.threads(), "kind": "oracle",
-            "sample": f"{runs} full oracle forward(s) of the {wl.name} workload ({wl.T} tokens each), "
-                      f"{el:.1f} s"}
+    res = {"value": n_tok / el, "unit": "tokens/s", "cores": o.threads(), "kind": "oracle",
+           "sample": f"{runs} full oracle forward(s) of the {wl.name} workload ({wl.T} tokens each), "
+                     f"{el:.1f} s", "cpu_model": cpu_model()}
+    # the same oracle built without OpenMP, on one core, for a third of the budget
+    o1 = Oracle(openmp=False)
+    n1, t1 = 0, time.perf_counter()
+    while True:
+        o1.moe_forward(inputs.x, inputs.router_w, inputs.router_b, wl.top_k, inputs.experts, inputs.shared)
+        n1 += wl.T
+        el1 = time.perf_counter() - t1
+        if el1 >= budget_s / 3:
+            break
+    res["single_thread"] = {"value": n1 / el1, "unit": "tokens/s", "cores": 1,
+                            "sample": f"{n1 // wl.T} forward(s), {el1:.1f} s"}
+    return res
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo), or the machine type."""
+    import platform
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
 
 
 def run_reference(args, wl_name: str):
