@@ -116,10 +116,11 @@ FFN_PATHS = {
     "mx": (2, "gemm_mx", (2, 1.0), (3, 1.0), "mxfp4 e2m1 x e4m3 activation terms, fp32 accumulate"),
     "bf16": (3, "gemm_tc", None, None, "mxfp4 e2m1 dequantised to bf16, bf16 tensor cores, fp32 accumulate"),
     "mxf4": (4, "gemm_mx4", (4, 0.5), (4, 0.5), "mxfp4 e2m1 x e2m1 activation terms, fp32 accumulate"),
-    "nvf4": (4, "gemm_mx4", (4, 0.5), (4, 0.5),
+    # the NVFP4 layer (coli_moe_forward_nvfp4) is not an FFN path of coli_moe_forward: no ABI value
+    "nvf4": (None, "gemm_mx4", (4, 0.5), (4, 0.5),
              "nvfp4 e2m1 (e4m3 scale per 16, fp32 per matrix) x e2m1 activation terms, fp32 accumulate"),
 }
-PATH_BY_ABI = {v[0]: k for k, v in FFN_PATHS.items()}
+PATH_BY_ABI = {v[0]: k for k, v in FFN_PATHS.items() if v[0] is not None}
 
 
 def algorithmic_bytes(wl, routing: dict, path: str = "mxf4", group: int = 32) -> dict:
@@ -644,7 +645,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--skip-cpu", action="store_true", help="no cpu_baseline (profiling runs)")
-    ap.add_argument("--ffn-path", default="auto", choices=sorted(FFN_PATHS),
+    ap.add_argument("--ffn-path", default="auto", choices=sorted(PATH_BY_ABI.values()),
                     help="force an FFN path (default: the library's own choice)")
     ap.add_argument("--format", default="mxfp4", choices=["mxfp4", "nvfp4"],
                     help="expert weight format of the MoE layer (nvfp4: the format variant)")
