@@ -12,6 +12,14 @@ arm; one oracle forward of a bounded token sample per step).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 Under torchrun every rank runs an independent replica (no collective on the data path).
+
+Other lines (same contract, their own metric or config):
+  --format nvfp4          the layer with NVFP4 experts (coli_moe_forward_nvfp4)
+  --bank S                routed experts in page-locked host memory behind S device slots, a new
+                          token batch every step (roofline: the refill against the measured
+                          host-to-device copy rate)
+  --dense NAME            the FP8 E4M3 dense projection (coli_dense_forward) on a dense workload
+  --ffn-path P            force one FFN path of coli_moe_forward (path comparisons)
 """
 from __future__ import annotations
 
