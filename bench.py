@@ -158,11 +158,12 @@ def algorithmic_bytes(wl, routing: dict, path: str = "mxf4", group: int = 32) ->
             "layer": weights + E * H * 4 + 2 * T * H * 2}
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per gate/up launch from a committed ncu summary (profiles/<kernel>_<workload>.json),
-    or None when the kernel's source has changed since the counters were taken."""
+def profiled_traffic(kernel: str, workload: str, profile: str = ""):
+    """DRAM bytes per gate/up launch from a committed ncu summary (profiles/<profile>_<workload>.json,
+    profile defaulting to the kernel's source stem), or None when the kernel's source has changed
+    since the counters were taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
+    path = os.path.join(ROOT, "profiles", f"{profile or kernel}_{workload}.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
@@ -304,7 +305,7 @@ def run_ours(args, wl_name: str) -> dict:
     hbm_gbs, bf16_tf, peak_kind = _peaks()
     dom = "ffn_gate_up"            # the largest kernel: the FFN GEMM's gate/up launch
     achieved = ab[dom] / (stages[dom] * 1e-3) / 1e9
-    traffic = None if nv else profiled_traffic(kernel, wl.name)
+    traffic = profiled_traffic(kernel, wl.name, "gemm_mx4_nv" if nv else kernel)
     tokens = wl.T * ws
     result = {
         "metric": METRIC, "value": tokens / (ms_per_step * 1e-3), "unit": "tokens/s", "n_gpus": ws,
