@@ -1,0 +1,147 @@
+"""The benchmark's host logic on CPU: the reference arm's JSON line, the byte arithmetic of the
+roofline, the gate on committed ncu counters and the clock record's parsing."""
+import hashlib
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from routed_moe_fp4_gb300 import synthetic as S  # noqa: E402
+
+
+def _run_bench(*args, env_extra=None):
+    env = dict(os.environ, **(env_extra or {}))
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, env=env,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_one_contract_line():
+    p = _run_bench("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1")
+    assert p.returncode == 0, p.stderr
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["steps"] == 2 and d["warmup"] == 3          # warm-up is raised to at least 3
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert abs(d["value"] - 4 / (d["ms_per_step"] * 1e-3)) < 1e-6 * d["value"]
+    assert d["config"]["workload"].startswith("tiny:")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    p = _run_bench("--impl", "reference", "--workload", "tiny", "--steps", "1",
+                   env_extra={"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert p.returncode == 0, p.stderr
+    assert p.stdout.strip() == ""
+
+
+def _routing(wl, touched):
+    cnt = np.zeros(wl.E + 1, np.int32)
+    cnt[:touched] = 1
+    return {"cnt": cnt}
+
+
+def test_layer_bytes_match_the_expert_sizes_of_the_scope_table():
+    # one expert's three MXFP4 matrices, H*I*(1/2 + 1/32) bytes each: 13,369,344 B at
+    # H 4096 x I 2048 and 23,396,352 B at H 7168 x I 2048 (the per-config table of the scope)
+    for name, per_expert in (("decode", 13_369_344), ("skewed", 23_396_352)):
+        wl = S.WORKLOADS[name]
+        for touched in (1, 62, wl.E):
+            b = bench.algorithmic_bytes(wl, _routing(wl, touched))
+            assert b["touched_experts"] == touched
+            extra = wl.E * wl.H * 4 + 2 * wl.T * wl.H * 2          # router weights, x in, out
+            assert b["layer"] == (touched + 1) * per_expert + extra
+
+
+def test_gate_up_and_down_bytes_split_the_weights():
+    wl = S.WORKLOADS["decode"]
+    b = bench.algorithmic_bytes(wl, _routing(wl, 62))
+    rows = wl.T * wl.top_k + wl.T
+    # four E2M1 terms of x and of h, each with a UE8M0 byte per 32
+    x_terms = 4 * rows * (wl.H // 2 + wl.H // 32)
+    h_terms = 4 * rows * (wl.I // 2 + wl.I // 32)
+    gu_w = 63 * 2 * wl.I * (wl.H // 2 + wl.H // 32)
+    dn_w = 63 * wl.H * (wl.I // 2 + wl.I // 32)
+    assert b["ffn_gate_up"] == gu_w + x_terms + h_terms
+    assert b["ffn_down"] == dn_w + h_terms + rows * wl.H * 4
+    assert gu_w + dn_w == 63 * 13_369_344
+    # the E2M1 x E4M3 path moves two and three one-byte terms instead
+    b2 = bench.algorithmic_bytes(wl, _routing(wl, 62), path="mx")
+    assert b2["ffn_gate_up"] == gu_w + 2 * rows * (wl.H + wl.H // 32) + 3 * rows * (wl.I + wl.I // 32)
+    # NVFP4: scale bytes per 16 elements
+    b3 = bench.algorithmic_bytes(wl, _routing(wl, 62), path="nvf4", group=16)
+    assert b3["layer"] - b["layer"] == 63 * 3 * wl.H * wl.I // 32
+
+
+def test_committed_counters_are_used_only_for_the_source_they_were_taken_on(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    src_dir = tmp_path / "routed_moe_fp4_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    src = src_dir / "kern.cu"
+    src.write_bytes(b"__global__ void k() {}\n")
+    prof = {"source_sha256": hashlib.sha256(src.read_bytes()).hexdigest(),
+            "gate_up": {"dram_read_bytes": 1000, "dram_write_bytes": 24}}
+    (tmp_path / "profiles" / "kern_decode.json").write_text(json.dumps(prof))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("kern", "decode") == 1024
+    assert bench.profiled_traffic("kern", "prefill") is None          # no counters for it
+    src.write_bytes(b"__global__ void k() { }\n")                       # the kernel changed
+    assert bench.profiled_traffic("kern", "decode") is None
+
+
+def test_committed_decode_counters_name_an_existing_source():
+    with open(os.path.join(ROOT, "profiles", "gemm_mx4_decode.json")) as f:
+        prof = json.load(f)
+    assert len(prof["source_sha256"]) == 64
+    assert prof["gate_up"]["dram_read_bytes"] > 0
+
+
+class _FakeProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def test_clock_record_parsing():
+    cs = bench.ClockSampler(0)
+    cs.proc = _FakeProc()
+    cs.lines = [
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2055, 2070, 1350.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1980, 2070, 1399.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "garbled line",
+        "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    r = cs.stop()
+    assert r["sm_mhz"] == 2055 and r["sm_max_mhz"] == 2070 and r["samples"] == 3
+    assert r["reasons"] == ["sw_power_cap"]
+    cs2 = bench.ClockSampler(0)
+    cs2.proc = _FakeProc()
+    cs2.lines = ["0, 1500, 2070, 800, 0x8, Active, Not Active, Active, Not Active"]
+    assert cs2.stop()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+
+
+def test_clock_record_without_nvidia_smi():
+    assert bench.ClockSampler(0).stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_ffn_path_names_are_unique_per_abi_value():
+    abi = [v[0] for v in bench.FFN_PATHS.values() if v[0] is not None]
+    assert len(abi) == len(set(abi))
+    assert bench.PATH_BY_ABI[4] == "mxf4" and "nvf4" not in bench.PATH_BY_ABI.values()
+
