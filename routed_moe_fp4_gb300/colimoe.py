@@ -129,14 +129,19 @@ def load(path: str = LIB_PATH) -> C.CDLL:
 
 
 def _ptr(t) -> Optional[int]:
-    """Device/host address of a torch tensor, numpy array or int (None stays None)."""
+    """Device/host address of a torch tensor, numpy array or int (None stays None). The library
+    reads every array as dense rows, so a strided view is refused rather than misread."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
     if hasattr(t, "data_ptr"):
+        if not t.is_contiguous():
+            raise ValueError("the library takes contiguous row-major tensors; pass .contiguous()")
         return t.data_ptr()
     if hasattr(t, "ctypes"):
+        if not t.flags["C_CONTIGUOUS"]:
+            raise ValueError("the library takes C-contiguous arrays; pass np.ascontiguousarray(a)")
         return t.ctypes.data
     raise TypeError(f"cannot take the address of {type(t)}")
 

@@ -109,3 +109,20 @@ def test_dense_create_without_gpu_is_an_error_not_a_fallback(lib):
     out = C.c_void_p()
     assert lib.coli_dense_create(4, 256, None, C.byref(out)) == cm.COLI_ERR_UNSUPPORTED_ARCH
     assert out.value is None
+
+
+def test_binding_refuses_strided_views():
+    import numpy as np
+    import torch
+    from routed_moe_fp4_gb300 import colimoe as cm
+    t = torch.zeros((8, 16), dtype=torch.int16)
+    assert cm._ptr(t) == t.data_ptr() and cm._ptr(t[2:5]) == t[2:5].data_ptr()
+    with pytest.raises(ValueError):
+        cm._ptr(t.t())
+    with pytest.raises(ValueError):
+        cm._ptr(t[:, ::2])
+    a = np.zeros((8, 16), np.uint8)
+    assert cm._ptr(a) == a.ctypes.data
+    with pytest.raises(ValueError):
+        cm._ptr(a[:, 1:])
+    assert cm._ptr(None) is None and cm._ptr(1234) == 1234
