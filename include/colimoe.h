@@ -135,7 +135,8 @@ COLI_API int coli_moe_forward_host(coli_moe_t *h, const void *x_bf16_host, int32
                           const coli_mxfp4_experts *shared_expert,
                           int32_t top_k, void *out_bf16_host);
 
-/* Releases the handle and its workspace (synchronises its stream first). NULL is a no-op. */
+/* Releases the handle and its workspace (synchronises its stream first). NULL is a no-op. Every
+ * expert bank created on h must be destroyed first: a bank keeps h's stream and shapes. */
 COLI_API void coli_moe_destroy(coli_moe_t *h);
 
 /* Text of the last error on this handle (or of the last failed create when h is NULL). The
@@ -260,7 +261,8 @@ typedef struct coli_expert_bank coli_expert_bank_t;
  * COLI_ERR_OUT_OF_MEMORY, COLI_ERR_UNSUPPORTED_ARCH (no FP4 tensor-map path on this device). */
 COLI_API int coli_bank_create(coli_moe_t *h, int32_t slots, const coli_mxfp4_experts *host_experts,
                               coli_expert_bank_t **out);
-/* Waits for the bank's work and frees it. NULL-safe. */
+/* Waits for the bank's work and frees it. NULL-safe. Call it before coli_moe_destroy of the
+ * bank's handle. */
 COLI_API void coli_bank_destroy(coli_expert_bank_t *bank);
 
 /* coli_moe_forward with the routed experts taken from the bank (arguments as there, the shared
