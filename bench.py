@@ -325,6 +325,8 @@ def run_ours(args, wl_name: str) -> dict:
                            "achieved_gbs": ab["layer"] / (ms_per_step * 1e-3) / 1e9,
                            "frac": ab["layer"] / (ms_per_step * 1e-3) / 1e9 / hbm_gbs},
         "stages_ms": stages, "touched_experts": ab["touched_experts"],
+        # per-step spread of the timed region on this rank (value and ms_per_step use the mean)
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
         "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_step,
                 "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
         "graph": graph_info,
