@@ -75,6 +75,10 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        # the timed region starts once nvidia-smi reports (its first query takes a while)
+        t0 = time.perf_counter()
+        while not self.lines and self.proc.poll() is None and time.perf_counter() - t0 < 3.0:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -107,6 +111,146 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class NvmlPoller:
+    """Polls the SM clock and the clock-event reasons through NVML's read-only queries every
+    millisecond. A timed region of a few milliseconds falls between two of nvidia-smi's 100 ms
+    samples; this poller sees it. Sets nothing on the GPU."""
+    NVML_CLOCK_SM = 1
+    # clock-event reason bits of nvml.h that slow the clocks (idle, application-clock setting,
+    # sync boost and display setting are left out)
+    REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+               (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
+
+    def __init__(self, device_ids, lib=None, period_s: float = 0.001):
+        """device_ids: candidates to find the GPU by, tried in order, each ("uuid", "GPU-..."),
+        ("pci", "00000000:01:00.0") or ("index", n)."""
+        self.ids = list(device_ids)
+        self.lib = lib
+        self.period = period_s
+        self.handle = None
+        self.samples = []
+        self.max_mhz = None
+        self.error = None
+        self._stop = threading.Event()
+        self._thread = None
+
+    def start(self) -> bool:
+        import ctypes as C
+        try:
+            if self.lib is None:
+                self.lib = C.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            h = C.c_void_p()
+            for kind, v in self.ids:
+                if kind == "uuid":
+                    rc = self.lib.nvmlDeviceGetHandleByUUID(v.encode(), C.byref(h))
+                elif kind == "pci":
+                    rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(v.encode(), C.byref(h))
+                else:
+                    rc = self.lib.nvmlDeviceGetHandleByIndex_v2(C.c_uint(int(v)), C.byref(h))
+                if rc == 0:
+                    self.handle = h
+                    break
+            if self.handle is None:
+                raise OSError("no NVML handle for the device")
+            mx = C.c_uint()
+            if self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.NVML_CLOCK_SM, C.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError) as e:
+            self.error = str(e).splitlines()[0][:120] if str(e) else type(e).__name__
+            self.handle = None
+            return False
+        self._thread = threading.Thread(target=self._poll, daemon=True)
+        self._thread.start()
+        return True
+
+    def _poll(self):
+        import ctypes as C
+        clk, rs = C.c_uint(), C.c_ulonglong()
+        while not self._stop.is_set():
+            ok_c = self.lib.nvmlDeviceGetClockInfo(self.handle, self.NVML_CLOCK_SM, C.byref(clk)) == 0
+            ok_r = self._reasons(self.handle, C.byref(rs)) == 0
+            if ok_c:
+                self.samples.append((float(clk.value), int(rs.value) if ok_r else 0))
+            time.sleep(self.period)
+
+    def stop(self):
+        """The clock record of the polled window, or None when NVML was not usable."""
+        if self._thread is None:
+            return None
+        self._stop.set()
+        self._thread.join(timeout=2)
+        try:
+            self.lib.nvmlShutdown()
+        except AttributeError:
+            pass
+        if not self.samples:
+            return None
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz if self.max_mhz else max(c for c, _ in self.samples),
+                "sm_min_mhz": min(c for c, _ in self.samples),
+                "reasons": [n for b, n in self.REASONS if bits & b], "samples": len(self.samples)}
+
+
+def nvml_ids(device: int):
+    """Ways to find CUDA device `device` in NVML (whose numbering can differ from CUDA's)."""
+    import torch
+    ids = []
+    p = torch.cuda.get_device_properties(device)
+    u = str(getattr(p, "uuid", "") or "")
+    if u:
+        ids.append(("uuid", u if u.startswith("GPU-") else "GPU-" + u))
+    if hasattr(p, "pci_bus_id"):
+        ids.append(("pci", f"{getattr(p, 'pci_domain_id', 0):08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"))
+    ids.append(("index", device))
+    return ids
+
+
+class Clocks:
+    """The clock record of a timed region: NVML polled every millisecond inside the region, and
+    the nvidia-smi query line of the profiling recipe beside it (100 ms samples)."""
+
+    def __init__(self, device: int, nvml_lib=None, smi: bool = True, ids=None):
+        self.smi = ClockSampler(device) if smi else None
+        self.device = device
+        self.nvml_lib = nvml_lib
+        self.ids = ids
+        self.nvml = None
+
+    def start(self):
+        if self.smi is not None:
+            self.smi.start()
+        try:
+            ids = self.ids if self.ids is not None else nvml_ids(self.device)
+        except (RuntimeError, AssertionError, AttributeError):
+            ids = [("index", self.device)]
+        self.nvml = NvmlPoller(ids, lib=self.nvml_lib)
+        self.nvml.start()
+
+    def stop(self) -> dict:
+        # NVML first: its window closes with the timed region (nvidia-smi's stop waits 0.25 s)
+        nv = self.nvml.stop() if self.nvml is not None else None
+        smi = self.smi.stop() if self.smi is not None else None
+        if nv is None:
+            out = dict(smi or {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"]})
+            out["source"] = "nvidia-smi, 100 ms samples" + (
+                f" (NVML: {self.nvml.error})" if self.nvml is not None and self.nvml.error else "")
+            return out
+        reasons = set(nv["reasons"])
+        if smi:
+            reasons |= {r for r in smi.get("reasons", []) if r != "nvidia-smi unavailable"}
+        out = dict(nv, reasons=sorted(reasons), source="NVML every 1 ms inside the timed region")
+        if smi:
+            out["smi"] = smi
+        return out
 
 
 def _dist():
@@ -224,7 +368,7 @@ def run_ours(args, wl_name: str) -> dict:
     # timed: device-resident inputs
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    clocks = Clocks(local)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -395,7 +539,7 @@ def run_bank(args, wl_name: str) -> dict:
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     launches = 0
-    clocks = ClockSampler(local)
+    clocks = Clocks(local)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -495,7 +639,7 @@ def run_dense(args, name: str) -> dict:
     stream.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    clocks = Clocks(local)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()

@@ -145,3 +145,82 @@ def test_ffn_path_names_are_unique_per_abi_value():
     assert len(abi) == len(set(abi))
     assert bench.PATH_BY_ABI[4] == "mxf4" and "nvf4" not in bench.PATH_BY_ABI.values()
 
+
+
+class _FakeNvml:
+    """Stands in for libnvidia-ml: a GPU found by UUID, an SM clock sequence and reason bits."""
+
+    def __init__(self, clocks, reasons, uuid="GPU-abc"):
+        self.clocks, self.reasons, self.uuid = list(clocks), list(reasons), uuid
+        self.i = 0
+        self.shutdown = False
+
+    def nvmlInit_v2(self):
+        return 0
+
+    def nvmlDeviceGetHandleByUUID(self, u, h):
+        if u.decode() != self.uuid:
+            return 13
+        h._obj.value = 1234
+        return 0
+
+    def nvmlDeviceGetHandleByPciBusId_v2(self, bus, h):
+        return 13
+
+    def nvmlDeviceGetHandleByIndex_v2(self, i, h):
+        return 13
+
+    def nvmlDeviceGetMaxClockInfo(self, h, kind, out):
+        out._obj.value = 2070
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, out):
+        out._obj.value = self.clocks[min(self.i, len(self.clocks) - 1)]
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h, out):
+        out._obj.value = self.reasons[min(self.i, len(self.reasons) - 1)]
+        self.i += 1
+        return 0
+
+    def nvmlShutdown(self):
+        self.shutdown = True
+        return 0
+
+
+def _poll(fake, ids, n):
+    import time
+    p = bench.NvmlPoller(ids, lib=fake, period_s=0.0005)
+    assert p.start()
+    t0 = time.perf_counter()
+    while len(p.samples) < n and time.perf_counter() - t0 < 5:
+        time.sleep(0.001)
+    return p.stop()
+
+
+def test_nvml_poller_reads_clocks_and_reasons():
+    fake = _FakeNvml([2070, 2055, 1980, 2070], [0x1, 0x4, 0x4 | 0x40, 0x0])
+    r = _poll(fake, [("pci", "0:1:0.0"), ("uuid", "GPU-abc")], 4)
+    assert fake.shutdown and r["samples"] >= 4 and r["sm_max_mhz"] == 2070
+    assert r["sm_min_mhz"] == 1980 and 1980 <= r["sm_mhz"] <= 2070
+    # the idle bit (0x1) is not a slowdown; power cap and hardware thermal are
+    assert r["reasons"] == ["sw_power_cap", "hw_thermal_slowdown"]
+
+
+def test_nvml_poller_without_a_matching_device():
+    p = bench.NvmlPoller([("uuid", "GPU-other"), ("index", 3)], lib=_FakeNvml([2070], [0]))
+    assert not p.start() and p.error and p.stop() is None
+
+
+def test_clock_record_prefers_the_in_region_nvml_samples():
+    c = bench.Clocks(0, nvml_lib=_FakeNvml([1900], [0x8]), smi=False, ids=[("uuid", "GPU-abc")])
+    c.start()
+    import time
+    time.sleep(0.02)
+    r = c.stop()
+    assert r["source"].startswith("NVML") and r["sm_mhz"] == 1900 and r["reasons"] == ["hw_slowdown"]
+    # no NVML: the record says where its numbers come from
+    c2 = bench.Clocks(0, nvml_lib=_FakeNvml([1900], [0], uuid="GPU-x"), smi=False, ids=[("uuid", "GPU-y")])
+    c2.start()
+    r2 = c2.stop()
+    assert r2["sm_mhz"] is None and "no NVML handle" in r2["source"]
