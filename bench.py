@@ -302,6 +302,31 @@ def algorithmic_bytes(wl, routing: dict, path: str = "mxf4", group: int = 32) ->
             "layer": weights + E * H * 4 + 2 * T * H * 2}
 
 
+# FP4 dense tensor rate over bf16 dense, from the nominal per-GPU figures (13.5 and 2.25 PFLOP/s)
+FP4_OVER_BF16 = 6.0
+
+
+def algorithmic_flops(wl) -> float:
+    """The layer's multiply-adds x 2: gate, up and down (6 H I per row) for T*k routed rows and
+    T shared rows, plus the router logits (2 T E H)."""
+    return 6.0 * wl.H * (wl.T * wl.top_k * wl.I + wl.T * wl.I_s) + 2.0 * wl.T * wl.E * wl.H
+
+
+def layer_roofline(layer_bytes: int, flops: float, ms: float, hbm_gbs: float, bf16_tflops: float,
+                   peak_kind: str) -> dict:
+    """The layer against both rooflines: HBM (its minimum bytes) and the FP4 tensor rate (its
+    flops; measured bf16 peak x the nominal FP4/bf16 ratio). frac_combined is
+    max(bytes / bandwidth, flops / FP4 peak) / time: whichever bound binds."""
+    s = ms * 1e-3
+    fp4 = bf16_tflops * FP4_OVER_BF16
+    t_hbm, t_tc = layer_bytes / (hbm_gbs * 1e9), flops / (fp4 * 1e12)
+    return {"bytes": layer_bytes, "ms": ms, "achieved_gbs": layer_bytes / s / 1e9,
+            "frac": layer_bytes / s / 1e9 / hbm_gbs, "flops": flops, "achieved_tflops": flops / s / 1e12,
+            "fp4_peak_tflops": fp4, "tensor_frac": flops / s / 1e12 / fp4,
+            "frac_combined": max(t_hbm, t_tc) / s, "binding": "hbm" if t_hbm >= t_tc else "tensor",
+            "peak_source": f"{peak_kind} hbm_gbs; {peak_kind} bf16_tflops x {FP4_OVER_BF16:g} (nominal FP4/bf16)"}
+
+
 def profiled_traffic(kernel: str, workload: str, profile: str = ""):
     """DRAM bytes per gate/up launch from a committed ncu summary (profiles/<profile>_<workload>.json,
     profile defaulting to the kernel's source stem), or None when the kernel's source has changed
@@ -465,9 +490,8 @@ def run_ours(args, wl_name: str) -> dict:
                      "unit": "GB/s", "frac": achieved / hbm_gbs, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": ab[dom],
                      "kernel_ms": stages[dom]},
-        "layer_roofline": {"bytes": ab["layer"], "ms": ms_per_step,
-                           "achieved_gbs": ab["layer"] / (ms_per_step * 1e-3) / 1e9,
-                           "frac": ab["layer"] / (ms_per_step * 1e-3) / 1e9 / hbm_gbs},
+        "layer_roofline": layer_roofline(ab["layer"], algorithmic_flops(wl), ms_per_step, hbm_gbs, bf16_tf,
+                                         peak_kind),
         "stages_ms": stages, "touched_experts": ab["touched_experts"],
         # per-step spread of the timed region on this rank (value and ms_per_step use the mean)
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},

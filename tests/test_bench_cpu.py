@@ -224,3 +224,23 @@ def test_clock_record_prefers_the_in_region_nvml_samples():
     c2.start()
     r2 = c2.stop()
     assert r2["sm_mhz"] is None and "no NVML handle" in r2["source"]
+
+
+def test_layer_flops_match_the_scope_table():
+    # algorithmic flops = T (k + 1) 6 H I + 2 T E H, as tabulated per configuration in the scope
+    for name, gflop, rel in (("decode", 3.6, 0.02), ("prefill", 233.0, 0.005), ("skewed", 3262.0, 0.001),
+                             ("sweep_T1", 0.79, 0.02), ("sweep_T128", 101.5, 0.005)):
+        got = bench.algorithmic_flops(S.WORKLOADS[name]) / 1e9
+        assert abs(got - gflop) <= rel * gflop, (name, got)
+
+
+def test_layer_roofline_takes_the_binding_bound():
+    # decode-like: bytes bind; 847 MB in 0.18 ms against 6782 GB/s
+    r = bench.layer_roofline(846_594_048, 3.64e9, 0.18, 6782.1, 1879.7, "measured")
+    assert r["binding"] == "hbm" and abs(r["frac"] - 846_594_048 / 0.18e-3 / 6782.1e9) < 1e-12
+    assert r["frac_combined"] == r["frac"] and r["fp4_peak_tflops"] == 1879.7 * 6
+    # compute-heavy: 3.26 TFLOP and 1 GB in 1 ms; the FP4 bound (0.289 ms) exceeds the HBM one
+    r = bench.layer_roofline(1_000_000_000, 3.26e12, 1.0, 6782.1, 1879.7, "measured")
+    assert r["binding"] == "tensor"
+    assert abs(r["frac_combined"] - 3.26e12 / (1879.7 * 6e12) / 1e-3) < 1e-12
+    assert abs(r["tensor_frac"] - r["frac_combined"]) < 1e-12
