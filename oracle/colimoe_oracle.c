@@ -500,9 +500,9 @@ void coli_oracle_tokens_output_nv(const uint16_t *x, int32_t H, int32_t I, int32
                                   const uint8_t *sh_gu_codes, const uint8_t *sh_gu_scales, float sh_gu_global,
                                   const uint8_t *sh_d_codes, const uint8_t *sh_d_scales, float sh_d_global,
                                   const int32_t *tokens, int32_t n_tokens, uint16_t *out, double *out_f64) {
-    const int64_t gu_c = 2LL * I * (H / 2), gu_s = 2LL * I * (H / 16);
+    const int64_t gu_c = 2LL * I * (H / 2), gu_s = 2LL * I * (H / (MUT(29) ? 32 : 16));
     const int64_t d_c = (int64_t)H * (I / 2), d_s = (int64_t)H * (I / 16);
-    const int with_shared = sh_gu_codes != NULL && I_s > 0;
+    const int with_shared = sh_gu_codes != NULL && I_s > 0 && !MUT(31);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t n = 0; n < n_tokens; ++n) {
         int32_t t = tokens[n];
@@ -512,7 +512,8 @@ void coli_oracle_tokens_output_nv(const uint16_t *x, int32_t H, int32_t I, int32
         for (int32_t j = 0; j < top_k; ++j) {
             int64_t e = idx[(int64_t)t * top_k + j];
             double *yj = ys + (int64_t)j * H;
-            expert_row_nv(xr, H, I, off_ptr(gu_codes, e, gu_c), off_ptr(gu_scales, e, gu_s), gu_global[e],
+            expert_row_nv(xr, H, I, off_ptr(gu_codes, e, gu_c), off_ptr(gu_scales, e, gu_s),
+                          gu_global[MUT(30) ? 0 : e],
                           off_ptr(d_codes, e, d_c), off_ptr(d_scales, e, d_s), d_global[e], yj);
             slot[j] = yj;
         }

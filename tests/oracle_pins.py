@@ -571,7 +571,41 @@ def pin_nvfp4_dense_swiglu(o):
     assert np.allclose(out64, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
 
 
+def pin_nvfp4_gated(o):
+    """Four NVFP4 experts, top-2 with given weights, and the shared expert: each token's output is
+    the shared expert's dense SwiGLU plus the weighted SwiGLUs of its two experts, each expert with
+    its own codes, scales and matrix scales (numpy over independently decoded weights)."""
+    from routed_moe_fp4_gb300 import synthetic as S
+    rng = _rng(62)
+    H, I, I_s, E, T, k = 64, 32, 64, 4, 5, 2
+    ex = S.make_nv_experts(62, "pin-gated", E, H, I)
+    sh = S.make_nv_experts(62, "pin-gated-shared", 1, H, I_s)
+    # distinct matrix scales per expert, so that taking another expert's scale shows
+    ex.gate_up_global[:] = np.float32(2.0) ** np.arange(E, dtype=np.float32) * np.float32(0.75)
+    ex.down_global[:] = np.float32(0.5) ** np.arange(E, dtype=np.float32)
+    x = random_bf16(rng, (T, H))
+    idx = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32)
+    w = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    out, out64 = o.tokens_output_nv(x, idx, w, ex, sh, list(range(T)))
+    xv = bf16_to_f64(x)
+
+    def mlp(e_set, e):
+        Wgu = decode_nvfp4(e_set.gate_up_codes[e], e_set.gate_up_scales[e], e_set.gate_up_global[e])
+        Wd = decode_nvfp4(e_set.down_codes[e], e_set.down_scales[e], e_set.down_global[e])
+        n = Wgu.shape[0] // 2
+        g, u = xv @ Wgu[:n].T, xv @ Wgu[n:].T
+        return (g / (1.0 + np.exp(-g)) * u) @ Wd.T
+
+    ys = [mlp(ex, e) for e in range(E)]
+    ref = mlp(sh, 0)
+    for t in range(T):
+        for j in range(k):
+            ref[t] = ref[t] + float(w[t, j]) * ys[idx[t, j]][t]
+    err = np.abs(out64 - ref).max() / np.sqrt((ref ** 2).mean())
+    assert err < 1e-12, err
+
+
 ALL_PINS = [pin_e2m1_table, pin_e8m0, pin_nibble_order, pin_route_bruteforce, pin_route_weights,
             pin_permute, pin_dense_swiglu, pin_dense_gated, pin_sigmoid, pin_logits, pin_round_bf16,
             pin_bank_cache, pin_bank_full, pin_bank_hot_expert, pin_bank_stream, pin_e4m3, pin_fp8_linear,
-            pin_nvfp4_decode, pin_nvfp4_dense_swiglu]
+            pin_nvfp4_decode, pin_nvfp4_dense_swiglu, pin_nvfp4_gated]
