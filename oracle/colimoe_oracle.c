@@ -251,8 +251,8 @@ void coli_oracle_tokens_output(const uint16_t *x, int32_t H, int32_t I, int32_t 
                                const int32_t *tokens, int32_t n_tokens,
                                uint16_t *out, double *out_f64) {
     const int64_t gu_c = 2LL * I * (H / 2), gu_s = 2LL * I * (H / 32);
-    const int64_t d_c = (int64_t)H * (I / 2), d_s = (int64_t)H * (I / 32);
-    const int with_shared = sh_gu_codes != NULL && I_s > 0;
+    const int64_t d_c = (int64_t)H * (I / 2), d_s = (int64_t)H * (I / (MUT(32) ? 16 : 32));
+    const int with_shared = sh_gu_codes != NULL && I_s > 0 && !MUT(33);
 #pragma omp parallel for schedule(dynamic, 1)
     for (int32_t n = 0; n < n_tokens; ++n) {
         int32_t t = tokens[n];

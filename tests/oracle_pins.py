@@ -256,6 +256,34 @@ def pin_dense_gated(o):
             assert r["out"][t, m] == nearest_bf16_bits(float(r["out_f64"][t, m]))
 
 
+def pin_tokens_output(o):
+    """The token-by-token output for given routing (what the GPU parity checks compare with):
+    four experts, top-2 with given weights and the shared expert, against numpy SwiGLUs over
+    independently decoded weights combined by the weights."""
+    rng = _rng(7)
+    T, H, E, k, I, I_s = 5, 64, 4, 2, 64, 32
+    x = random_bf16(rng, (T, H))
+    ex = _Experts([tiny_expert(rng, H, I) for _ in range(E)])
+    sh = _Experts([tiny_expert(rng, H, I_s)])
+    idx = np.array([rng.permutation(E)[:k] for _ in range(T)], np.int32)
+    w = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    toks = [4, 0, 2]
+    out, out64 = o.tokens_output(x, idx, w, ex, sh, toks)
+    xf = bf16_to_f64(x)
+    ys = [dense_swiglu(xf, ex.gate_up_codes[e], ex.gate_up_scales[e], ex.down_codes[e], ex.down_scales[e])
+          for e in range(E)]
+    ref = dense_swiglu(xf, sh.gate_up_codes[0], sh.gate_up_scales[0], sh.down_codes[0], sh.down_scales[0])
+    for t in range(T):
+        for j in range(k):
+            ref[t] = ref[t] + float(w[t, j]) * ys[idx[t, j]][t]
+    ref = ref[toks]
+    err = np.abs(out64 - ref).max() / np.sqrt((ref ** 2).mean())
+    assert err < 1e-12, err
+    for n in range(len(toks)):
+        for m in range(0, H, 5):
+            assert out[n, m] == nearest_bf16_bits(float(out64[n, m]))
+
+
 def pin_sigmoid(o):
     """sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4, symmetry, increasing in the logit."""
     z = np.array([0.0, math.log(3.0), -math.log(3.0), 2.5, -2.5, 10.0, -10.0, 1e-3, -1e-3])
@@ -606,6 +634,6 @@ def pin_nvfp4_gated(o):
 
 
 ALL_PINS = [pin_e2m1_table, pin_e8m0, pin_nibble_order, pin_route_bruteforce, pin_route_weights,
-            pin_permute, pin_dense_swiglu, pin_dense_gated, pin_sigmoid, pin_logits, pin_round_bf16,
+            pin_permute, pin_dense_swiglu, pin_dense_gated, pin_tokens_output, pin_sigmoid, pin_logits, pin_round_bf16,
             pin_bank_cache, pin_bank_full, pin_bank_hot_expert, pin_bank_stream, pin_e4m3, pin_fp8_linear,
             pin_nvfp4_decode, pin_nvfp4_dense_swiglu, pin_nvfp4_gated]

@@ -5,7 +5,7 @@ from oracle import build as obuild
 from oracle.oracle import Oracle
 from tests import oracle_pins as P
 
-MUTANTS = list(range(1, 32))
+MUTANTS = list(range(1, 34))
 
 
 @pytest.mark.parametrize("pin", P.ALL_PINS, ids=lambda f: f.__name__)
