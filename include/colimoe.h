@@ -178,7 +178,10 @@ COLI_API int32_t coli_moe_last_ffn_path(const coli_moe_t *h);
 /* Device error word. Kernels that wait on barriers bound every wait (about two seconds); a wait
  * that runs out makes the kernel stop, record a code here (1: waiting for a weight stage,
  * 2: waiting for a free stage, 3: waiting for an MMA, 4: waiting for an accumulator) and return,
- * leaving that forward's output incomplete. Synchronises the stream, writes the code (0 = no
+ * leaving that forward's output incomplete. Banked forwards (coli_moe_forward_banked) also record
+ * 21 when a cache forward finds no free slot and 22 when a refill entry names an expert or slot
+ * out of range; neither happens for arguments the host accepted, and the entry is skipped rather
+ * than copied. The first code recorded is kept. Synchronises the stream, writes the code (0 = no
  * error) to *code and clears it. */
 COLI_API int coli_moe_device_error(coli_moe_t *h, int32_t *code);
 
