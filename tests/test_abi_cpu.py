@@ -126,3 +126,23 @@ def test_binding_refuses_strided_views():
     with pytest.raises(ValueError):
         cm._ptr(a[:, 1:])
     assert cm._ptr(None) is None and cm._ptr(1234) == 1234
+
+
+def test_header_is_plain_c_with_only_stdint(tmp_path):
+    """The ABI header includes only <stdint.h> and compiles as strict C99 and as C++."""
+    import shutil
+    import subprocess
+    hdr = os.path.join(ROOT, "include", "colimoe.h")
+    with open(hdr) as f:
+        includes = re.findall(r"^\s*#\s*include\s*[<\"]([^>\"]+)[>\"]", f.read(), re.M)
+    assert includes == ["stdint.h"]
+    src = tmp_path / "use.c"
+    src.write_text('#include "colimoe.h"\nint main(void) { coli_moe_config c = {1, 128, 128, 0, 1, 1}; (void)c;'
+                   ' const char *(*f)(const coli_moe_t *) = coli_moe_last_error; (void)f; return 0; }\n')
+    for cc, std in (("gcc", "-std=c99"), ("g++", "-std=c++17")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not found")
+        r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                            "-x", "c" if cc == "gcc" else "c++", f"-I{os.path.join(ROOT, 'include')}", str(src)],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
