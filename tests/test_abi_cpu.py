@@ -146,3 +146,28 @@ def test_header_is_plain_c_with_only_stdint(tmp_path):
                             "-x", "c" if cc == "gcc" else "c++", f"-I{os.path.join(ROOT, 'include')}", str(src)],
                            capture_output=True, text=True)
         assert r.returncode == 0, r.stderr
+
+
+def test_route_static_checks_arguments_before_the_device(lib):
+    """Bad sizes, oversize scratch and NULL or misaligned pointers are rejected before any CUDA
+    call; valid arguments without a GPU give an error code, never a host fallback."""
+    from routed_moe_fp4_gb300 import colimoe as cm
+    lib_fn = lib.coli_moe_route_static
+    buf = (C.c_uint8 * 4096)()
+    base = (C.addressof(buf) + 15) & ~15                 # a 16-byte aligned host address
+    good = dict(x=base, T=4, H=256, w=base, b=None, E=8, k=2, idx=base, wt=base)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return lib_fn(a["x"], a["T"], a["H"], a["w"], a["b"], a["E"], a["k"], a["idx"], a["wt"], None)
+
+    assert call(T=0) == cm.COLI_OK                        # nothing to do
+    for bad in (dict(T=-1), dict(E=0), dict(E=1025), dict(H=100), dict(H=0), dict(k=0), dict(k=9),
+                dict(k=33, E=64), dict(T=2048, E=256), dict(x=None), dict(w=None), dict(idx=None),
+                dict(wt=None), dict(x=base + 2), dict(w=base + 4)):
+        assert call(**bad) == cm.COLI_ERR_INVALID_ARG, bad
+        assert "route_static" in cm.coli_moe_last_error(None)
+    assert "scratch limit" in (call(T=2048, E=256), cm.coli_moe_last_error(None))[1]
+    import torch
+    if not torch.cuda.is_available():
+        assert call() in (cm.COLI_ERR_CUDA, cm.COLI_ERR_UNSUPPORTED_ARCH)
