@@ -115,7 +115,7 @@ COLI_API int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli
  *   shared_expert  the shared expert (E = 1, I = cfg.shared_inter), or NULL for none; must be
  *                  NULL when cfg.shared_inter == 0
  *   top_k          1..cfg.max_top_k
- *   out_bf16       device, bf16 [T][H], 16-byte aligned; may not alias x_bf16
+ *   out_bf16       device, bf16 [T][H], 16-byte aligned; may not overlap x_bf16
  * Errors: COLI_ERR_INVALID_ARG for bad arguments (nothing enqueued), COLI_ERR_CUDA when a launch
  * fails. Device-side execution errors surface on the stream as usual in CUDA. */
 COLI_API int coli_moe_forward(coli_moe_t *h, const void *x_bf16, int32_t T,

@@ -120,8 +120,10 @@ int check_forward(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rou
         set_err(h, "x, router_w and out must be non-NULL, 16-byte aligned device pointers");
         return COLI_ERR_INVALID_ARG;
     }
-    if (x_bf16 == out_bf16) {
-        set_err(h, "out_bf16 may not alias x_bf16");
+    const size_t bytes = (size_t)T * (size_t)c.hidden * sizeof(uint16_t);
+    const uintptr_t xb = reinterpret_cast<uintptr_t>(x_bf16), ob = reinterpret_cast<uintptr_t>(out_bf16);
+    if (xb < ob + bytes && ob < xb + bytes) {   // the combine writes out while x may still be read
+        set_err(h, "out_bf16 may not overlap x_bf16");
         return COLI_ERR_INVALID_ARG;
     }
     if (shared && (c.shared_inter == 0 || !valid_experts(shared))) {

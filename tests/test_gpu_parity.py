@@ -185,6 +185,13 @@ def test_bad_arguments_rejected():
         cm.coli_moe_forward(layer.h, x, 4, layer.router_w, None, layer.experts.struct, None, 3, out)
     with pytest.raises(cm.ColiError):
         cm.coli_moe_forward(layer.h, x, 4, layer.router_w, None, layer.experts.struct, None, 2, x)
+    # out may not overlap x even in part; adjacent buffers are fine
+    buf = torch.zeros((8, 256), dtype=torch.int16, device="cuda")
+    with pytest.raises(cm.ColiError) as e:
+        cm.coli_moe_forward(layer.h, buf[:4], 4, layer.router_w, None, layer.experts.struct, None, 2, buf[2:6])
+    assert e.value.code == cm.COLI_ERR_INVALID_ARG and "overlap" in str(e.value)
+    cm.coli_moe_forward(layer.h, buf[:4], 4, layer.router_w, None, layer.experts.struct, None, 2, buf[4:])
+    torch.cuda.synchronize()
     layer.close()
 
 
