@@ -122,7 +122,7 @@ int check_forward(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rou
     }
     const size_t bytes = (size_t)T * (size_t)c.hidden * sizeof(uint16_t);
     const uintptr_t xb = reinterpret_cast<uintptr_t>(x_bf16), ob = reinterpret_cast<uintptr_t>(out_bf16);
-    if (xb < ob + bytes && ob < xb + bytes) {   // the combine writes out while x may still be read
+    if (xb < ob + bytes && ob < xb + bytes) {   // x is const across the ABI: writing out may not touch it
         set_err(h, "out_bf16 may not overlap x_bf16");
         return COLI_ERR_INVALID_ARG;
     }
