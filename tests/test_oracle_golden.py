@@ -75,3 +75,15 @@ def test_bank_sequence_matches_stored(oracle):
         assert cop.tolist() == want["copied"]
         for key in ("slot_of", "expert_in", "usage", "last_use", "stats"):
             assert getattr(state, key).tolist() == want[key], key
+
+
+def test_skewed_popularity_is_what_the_stored_bias_routes_to(oracle):
+    """The stored Zipf bias, routed by the oracle over the skewed workload's 4096 tokens, gives
+    exactly the stored slot counts per popularity rank."""
+    cal = S.calibration()
+    wl = S.WORKLOADS["skewed"]
+    inp = S.make_inputs("skewed", 0, with_experts=False)
+    idx, _ = oracle.route(oracle.scores(inp.x, inp.router_w), inp.router_b, wl.top_k)
+    cnt = np.bincount(idx.reshape(-1), minlength=wl.E)
+    order = np.argsort(S.zipf_rank(0, wl.E))
+    assert cnt[order].tolist() == cal["skewed_slots_by_rank"]
