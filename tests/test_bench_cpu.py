@@ -54,9 +54,9 @@ def _routing(wl, touched):
     return {"cnt": cnt}
 
 
-def test_layer_bytes_match_the_expert_sizes_of_the_scope_table():
-    # one expert's three MXFP4 matrices, H*I*(1/2 + 1/32) bytes each: 13,369,344 B at
-    # H 4096 x I 2048 and 23,396,352 B at H 7168 x I 2048 (the per-config table of the scope)
+def test_layer_bytes_match_the_expert_sizes():
+    # one expert's three MXFP4 matrices, H*I*(1/2 + 1/32) bytes each, worked out by hand:
+    # 3 x 4096 x 2048 x 17/32 = 13,369,344 B and 3 x 7168 x 2048 x 17/32 = 23,396,352 B
     for name, per_expert in (("decode", 13_369_344), ("skewed", 23_396_352)):
         wl = S.WORKLOADS[name]
         for touched in (1, 62, wl.E):
@@ -226,8 +226,9 @@ def test_clock_record_prefers_the_in_region_nvml_samples():
     assert r2["sm_mhz"] is None and "no NVML handle" in r2["source"]
 
 
-def test_layer_flops_match_the_scope_table():
-    # algorithmic flops = T (k + 1) 6 H I + 2 T E H, as tabulated per configuration in the scope
+def test_layer_flops_match_the_closed_form():
+    # algorithmic flops = T (k + 1) 6 H I + 2 T E H, worked out by hand per workload: decode
+    # 8 x 9 x 6 x 4096 x 2048 + 2 x 8 x 256 x 4096 = 3.64 GFLOP, skewed 3.262 TFLOP, ...
     for name, gflop, rel in (("decode", 3.6, 0.02), ("prefill", 233.0, 0.005), ("skewed", 3262.0, 0.001),
                              ("sweep_T1", 0.79, 0.02), ("sweep_T128", 101.5, 0.005)):
         got = bench.algorithmic_flops(S.WORKLOADS[name]) / 1e9
