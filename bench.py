@@ -265,9 +265,7 @@ def _dist():
 FFN_PATHS = {
     "auto": (0, None, None, None, None),
     "gemv": (1, "gemv", None, None, "mxfp4 e2m1 weights dequantised to fp16, fp16 x fp16 FMA, fp32 sums"),
-    "mx": (2, "gemm_mx", (2, 1.0), (3, 1.0), "mxfp4 e2m1 x e4m3 activation terms, fp32 accumulate"),
-    "bf16": (3, "gemm_tc", None, None, "mxfp4 e2m1 dequantised to bf16, bf16 tensor cores, fp32 accumulate"),
-    "mxf4": (4, "gemm_mx4", (4, 0.5), (4, 0.5), "mxfp4 e2m1 x e2m1 activation terms, fp32 accumulate"),
+    "mxf4": (2, "gemm_mx4", (4, 0.5), (4, 0.5), "mxfp4 e2m1 x e2m1 activation terms, fp32 accumulate"),
     # the NVFP4 layer (coli_moe_forward_nvfp4) is not an FFN path of coli_moe_forward: no ABI value
     "nvf4": (None, "gemm_mx4", (4, 0.5), (4, 0.5),
              "nvfp4 e2m1 (e4m3 scale per 16, fp32 per matrix) x e2m1 activation terms, fp32 accumulate"),
@@ -353,6 +351,93 @@ def max_over_ranks(value: float, device=None) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+# The other configurations of the scope table, timed beside the headline line in the same run:
+# the prefill chunk, the skewed prefill, the batched-decode sweep (with the CUDA-core GEMV beside
+# the tensor-core path, for the crossover) and the V4-Pro-sized decode.
+CONFIG_PASS = ("prefill", "skewed", *[f"sweep_T{t}" for t in S.SWEEP_T], "v4pro_decode")
+
+
+def config_target(name: str):
+    """(roofline fraction the configuration is judged on, target): the decode shapes against HBM,
+    the prefill shapes against max(bytes / bandwidth, flops / FP4 rate)."""
+    if name in ("prefill", "skewed"):
+        return "frac_combined", 0.50
+    return "frac", 0.70
+
+
+def time_steps(layer, x, out, stream, flush, steps: int, warmup: int, local: int):
+    """Device time of `steps` forwards, each after an L2 flush outside its CUDA events, with the
+    clocks polled over the timed region. Returns ([ms per step], clock record)."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        layer.forward(x, out)
+    stream.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    clocks = Clocks(local, smi=False)
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        layer.forward(x, out)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], clocks.stop()
+
+
+def config_entry(name: str, steps: int, warmup: int, local: int, flush_buf, gemv: bool) -> dict:
+    """One configuration: mean and median step time, tokens/s, the layer against its rooflines
+    and its target, clocks; with `gemv` the CUDA-core GEMV path timed the same way."""
+    import torch
+    from routed_moe_fp4_gb300 import colimoe as cm
+    inputs = S.make_inputs(name, seed=0)
+    wl = inputs.workload
+    stream = torch.cuda.Stream()
+    layer = cm.MoELayer(inputs, stream=stream)
+    x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
+    out = torch.empty_like(x)
+
+    def flush():
+        with torch.cuda.stream(stream):
+            flush_buf.fill_(1.0)
+    hbm_gbs, bf16_tf, kind = _peaks()
+    ms, ci = time_steps(layer, x, out, stream, flush, steps, warmup, local)
+    routing = layer.routing(wl.T)
+    ab = algorithmic_bytes(wl, routing, "mxf4")
+    mean = sum(ms) / len(ms)
+    lr = layer_roofline(ab["layer"], algorithmic_flops(wl), mean, hbm_gbs, bf16_tf, kind)
+    key, target = config_target(name)
+    entry = {"workload": f"T={wl.T}, H={wl.H}, E={wl.E}, top_k={wl.top_k}, I={wl.I}, I_s={wl.I_s}, bias {wl.bias}",
+             "ms_per_step": mean, "ms_median": statistics.median(ms), "tokens_per_s": wl.T / (mean * 1e-3),
+             "touched_experts": ab["touched_experts"],
+             "layer_roofline": {k: lr[k] for k in ("bytes", "frac", "flops", "tensor_frac", "frac_combined",
+                                                   "binding")},
+             "target": {"on": key, "at_least": target, "met": bool(lr[key] >= target)},
+             "clocks": {k: ci.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")}}
+    if gemv:
+        layer.set_ffn_path(cm.COLI_FFN_GEMV)
+        gms, _ = time_steps(layer, x, out, stream, flush, steps, warmup, local)
+        gmean = sum(gms) / len(gms)
+        entry["gemv"] = {"ms_per_step": gmean, "frac": ab["layer"] / (gmean * 1e-3) / 1e9 / hbm_gbs}
+    layer.close()
+    del x, out, layer
+    torch.cuda.empty_cache()
+    return entry
+
+
+def run_config_pass(local: int, steps: int = 10, warmup: int = 3) -> dict:
+    import torch
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    res = {n: config_entry(n, steps, warmup, local, flush_buf, gemv=n.startswith("sweep_")) for n in CONFIG_PASS}
+    sweep = [(int(n[len("sweep_T"):]), e) for n, e in res.items() if n.startswith("sweep_")]
+    faster = [t for t, e in sorted(sweep) if e["ms_per_step"] < e["gemv"]["ms_per_step"]]
+    res["crossover"] = {"tensor_core_path_faster_from_T": faster[0] if faster else None,
+                        "note": "the FP4 tensor-core GEMM against the CUDA-core GEMV, same inputs and routing"}
+    return res
 
 
 def run_ours(args, wl_name: str) -> dict:
@@ -503,6 +588,8 @@ def run_ours(args, wl_name: str) -> dict:
         "clocks": clock_info,
     }
     layer.close()
+    if ws == 1 and not nv and not args.skip_configs:
+        result["configs"] = run_config_pass(local)
     if ws > 1:
         dist.destroy_process_group()
     return result if rank == 0 else None
@@ -776,16 +863,43 @@ def oracle_sample(wl_name: str, budget_s: float):
     return res
 
 
-def cpu_model() -> str:
-    """The host CPU's model name (from /proc/cpuinfo), or the machine type."""
+# Arm CPU part numbers (MIDR_EL1 PartNum, implementer 0x41) of the cores these hosts carry.
+_ARM_PARTS = {0xD40: "Neoverse-V1", 0xD49: "Neoverse-N2", 0xD4F: "Neoverse-V2", 0xD83: "Neoverse-V3",
+              0xD8E: "Neoverse-N3"}
+
+
+def cpu_model(cpuinfo: str = "/proc/cpuinfo") -> str:
+    """The host CPU's model: the "model name" line of /proc/cpuinfo where there is one (x86), else
+    `lscpu`'s "Model name", else the Arm implementer and part number (Grace: Neoverse-V2), else the
+    machine type."""
     import platform
+    import subprocess
+    fields = {}
     try:
-        with open("/proc/cpuinfo") as f:
+        with open(cpuinfo) as f:
             for line in f:
-                key = line.split(":")[0].strip().lower()
-                if key in ("model name", "cpu model", "hardware"):
-                    return line.split(":", 1)[1].strip()
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
     except OSError:
+        pass
+    for key in ("model name", "cpu model", "hardware"):
+        if fields.get(key):
+            return fields[key]
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                name = line.split(":", 1)[1].strip()
+                if name and name != "-":
+                    return name
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        impl, part = int(fields["cpu implementer"], 16), int(fields["cpu part"], 16)
+        name = _ARM_PARTS.get(part, f"part 0x{part:03x}") if impl == 0x41 else f"implementer 0x{impl:02x} part 0x{part:03x}"
+        return f"Arm {name}" if impl == 0x41 else name
+    except (KeyError, ValueError):
         pass
     return platform.machine()
 
@@ -827,6 +941,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(S.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--skip-cpu", action="store_true", help="no cpu_baseline (profiling runs)")
+    ap.add_argument("--skip-configs", action="store_true",
+                    help="no per-configuration pass beside the headline line (profiling runs)")
     ap.add_argument("--ffn-path", default="auto", choices=sorted(PATH_BY_ABI.values()),
                     help="force an FFN path (default: the library's own choice)")
     ap.add_argument("--format", default="mxfp4", choices=["mxfp4", "nvfp4"],

@@ -60,18 +60,15 @@ enum {
 
 /* FFN path selection for coli_moe_set_ffn_path. */
 enum {
-    COLI_FFN_AUTO = 0,      /* COLI_FFN_GEMM_MXF4 when a tensor-map encoder is available, else the
-                               other block-scaled GEMM, else GEMV / bf16 GEMM */
-    COLI_FFN_GEMV = 1,      /* weight-streaming GEMV kernels on the CUDA cores */
-    COLI_FFN_GEMM = 2,      /* block-scaled tcgen05 GEMM: E2M1 weights straight from HBM to the tensor
-                               cores (kind::mxf8f6f4), activations as exact E4M3 terms; needs 32-byte
-                               aligned code pointers. Follows the hardware's UE8M0 decoding, which
-                               differs from the format above only for scale bytes 0 and 255. */
-    COLI_FFN_GEMM_BF16 = 3, /* tcgen05 GEMM with the weights dequantised to bf16 in shared memory */
-    COLI_FFN_GEMM_MXF4 = 4, /* block-scaled tcgen05 GEMM with FP4 on both sides (kind::mxf4, 64 K per
+    COLI_FFN_AUTO = 0,      /* COLI_FFN_GEMM_MXF4 whenever a tensor-map encoder is available (always on
+                               a GB300 with its driver), else COLI_FFN_GEMV */
+    COLI_FFN_GEMV = 1,      /* weight-streaming GEMV kernels on the CUDA cores: the small-T comparison
+                               path of the crossover measurement */
+    COLI_FFN_GEMM_MXF4 = 2, /* block-scaled tcgen05 GEMM with FP4 on both sides (kind::mxf4, 64 K per
                                instruction): E2M1 weights from HBM as stored, activations as four
-                               E2M1 terms with UE8M0 scales per 32 elements (about 2e-4 relative
-                               error on x and h). Same UE8M0 decoding note as COLI_FFN_GEMM. */
+                               E2M1 terms with UE8M0 scales per 32 elements (about 3e-4 RMS relative
+                               error on x and h). Follows the hardware's UE8M0 decoding, which
+                               differs from the format above only for scale bytes 0 and 255. */
 };
 
 typedef struct coli_moe coli_moe_t;
@@ -143,7 +140,7 @@ COLI_API void coli_moe_destroy(coli_moe_t *h);
  * string stays valid until the next call on the same handle. Never returns NULL. */
 COLI_API const char *coli_moe_last_error(const coli_moe_t *h);
 
-/* Forces the FFN path (COLI_FFN_AUTO / _GEMV / _GEMM / _GEMM_BF16 / _GEMM_MXF4). Returns
+/* Forces the FFN path (COLI_FFN_AUTO / _GEMV / _GEMM_MXF4). Returns
  * COLI_ERR_INVALID_ARG for an unknown value. All paths compute the same result within rounding. */
 COLI_API int coli_moe_set_ffn_path(coli_moe_t *h, int32_t path);
 
@@ -171,7 +168,7 @@ COLI_API int coli_moe_debug_routing(coli_moe_t *h, coli_moe_routing *dst);
 /* Kernel launches the last forward enqueued (for launch accounting). */
 COLI_API int32_t coli_moe_last_launch_count(const coli_moe_t *h);
 
-/* FFN path (COLI_FFN_GEMV / _GEMM / _GEMM_BF16 / _GEMM_MXF4) the last forward ran; COLI_FFN_AUTO
+/* FFN path (COLI_FFN_GEMV / _GEMM_MXF4) the last forward ran; COLI_FFN_AUTO
  * before the first forward, after a forward with T = 0, or for a NULL handle. */
 COLI_API int32_t coli_moe_last_ffn_path(const coli_moe_t *h);
 
@@ -205,7 +202,9 @@ COLI_API int coli_moe_stage_times(coli_moe_t *h, float *ms);
 /* Routing with no device allocation. Runs the router of coli_moe_forward (A1: scores, bias-
  * adjusted top-k, renormalised weights) on the given stream and writes idx_out [T][top_k] (int32)
  * and weights_out [T][top_k] (fp32), device pointers owned by the caller, identical to the idx and
- * weights coli_moe_forward computes for the same inputs. The pages have no counterpart to this call.
+ * weights coli_moe_forward computes for the same inputs, whatever max_tokens the forward's handle
+ * was created with: both calls choose the router's split of H from T, E, H and the SM count alone,
+ * and so add the same partial logits in the same order. The pages have no counterpart to this call.
  *
  * Who it is for: callers that cannot let a library allocate device memory while they route -- code
  * running while a CUDA graph is being captured, runtimes whose own pool owns all device memory,

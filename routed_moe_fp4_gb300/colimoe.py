@@ -18,7 +18,7 @@ COLI_ERR_INVALID_ARG = -1
 COLI_ERR_UNSUPPORTED_ARCH = -2
 COLI_ERR_OUT_OF_MEMORY = -3
 COLI_ERR_CUDA = -4
-COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM, COLI_FFN_GEMM_BF16, COLI_FFN_GEMM_MXF4 = 0, 1, 2, 3, 4
+COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM_MXF4 = 0, 1, 2
 
 EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "coli_moe_destroy",
             "coli_moe_last_error", "coli_moe_set_ffn_path", "coli_moe_debug_routing",

@@ -48,7 +48,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 void free_ws(Workspace &ws) {
     void *ptrs[] = {ws.xq, ws.xqs, ws.hq, ws.hqs, ws.xg, ws.hg, ws.hf, ws.scores, ws.logit_part, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
-                    ws.n_touched, ws.xp, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
+                    ws.n_touched, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
                     ws.out_stage, ws.tile_sched};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -77,31 +77,18 @@ ExpertSet to_set(const coli_mxfp4_experts *e) {
     return s;
 }
 
-enum FfnKind { kFfnGemv, kFfnMx, kFfnBf16, kFfnMx4 };
-
-bool mx_pointers_ok(const coli_mxfp4_experts *r, const coli_mxfp4_experts *s) {
-    auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; };
-    return al(r->gate_up_codes) && al(r->down_codes) && (!s || (al(s->gate_up_codes) && al(s->down_codes)));
-}
+enum FfnKind { kFfnGemv, kFfnMx4 };
 
 // The FFN kernels a forward uses: the FP4 x FP4 block-scaled GEMM whenever it can run (weights go
-// to the tensor cores as stored, 64 K per instruction, at every token count); then the E2M1 x E4M3
-// block-scaled GEMM; otherwise the bf16 GEMM when tokens per touched expert are many, the GEMV
-// when they are few.
-FfnKind pick_ffn(const coli_moe_t *h, int T, int top_k, const coli_mxfp4_experts *r, const coli_mxfp4_experts *s) {
+// to the tensor cores as stored, 64 K per instruction, at every token count); the CUDA-core GEMV
+// only when forced, or when no tensor-map encoder is available.
+FfnKind pick_ffn(const coli_moe_t *h) {
     switch (h->ffn_path) {
         case COLI_FFN_GEMV: return kFfnGemv;
-        case COLI_FFN_GEMM: return kFfnMx;
-        case COLI_FFN_GEMM_BF16: return kFfnBf16;
         case COLI_FFN_GEMM_MXF4: return kFfnMx4;
         default: break;
     }
-    if (mx4_available()) return kFfnMx4;
-    if (mx_available() && mx_pointers_ok(r, s)) return kFfnMx;
-    if (!gemm_available()) return kFfnGemv;
-    const double E = h->cfg.num_experts;
-    const double touched = E * (1.0 - pow(1.0 - (double)top_k / E, (double)T));
-    return (double)T * top_k / (touched > 0 ? touched : 1.0) > 3.0 ? kFfnBf16 : kFfnGemv;
+    return mx4_available() ? kFfnMx4 : kFfnGemv;
 }
 
 // Argument checks every forward shares (T > 0 here).
@@ -134,10 +121,10 @@ int check_forward(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rou
     return COLI_OK;
 }
 
-// A1 router and A2 permute (with the n-tile layout of tile size `ntile` when non-zero, and the
-// activation gather for the bf16 GEMM path). Returns false on a launch error.
+// A1 router and A2 permute (with the n-tile layout of tile size `ntile` when non-zero). Returns
+// false on a launch error.
 bool run_front(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router_w, const float *router_bias,
-               int32_t top_k, bool with_shared, bool gather, int ntile, int rows, int &launches) {
+               int32_t top_k, bool with_shared, int ntile, int &launches) {
     const int E = h->cfg.num_experts, H = h->cfg.hidden;
     Workspace &ws = h->ws;
     cudaStream_t st = h->stream;
@@ -146,26 +133,21 @@ bool run_front(coli_moe_t *h, const void *x_bf16, int32_t T, const float *router
     if (T < kSmallRouteTokens) {
         // logits, then top-k and the whole permutation in one single-block launch
         n = launch_router(x, T, H, router_w, router_bias, E, top_k, ws.scores, ws.idx, ws.w, ws.logit_part,
-                          ws.logit_part_floats, h->num_sms, nullptr, 0, st, false);
+                          h->num_sms, nullptr, 0, ws.err, st, false);
         if (n < 0) return false;
         launches += n;
         if (h->profiling) cudaEventRecord(h->ev[1], st);
         n = launch_route_permute_small(router_bias, T, E, top_k, with_shared, kGemvCostTokens, ntile, ws, st);
         if (n < 0) return false;
         launches += n;
-        if (gather) {
-            n = launch_gather(x, H, rows, ws, st);
-            if (n < 0) return false;
-            launches += n;
-        }
         return true;
     }
     n = launch_router(x, T, H, router_w, router_bias, E, top_k, ws.scores, ws.idx, ws.w, ws.logit_part,
-                      ws.logit_part_floats, h->num_sms, ws.cnt, E + 1, st);
+                      h->num_sms, ws.cnt, E + 1, ws.err, st);
     if (n < 0) return false;
     launches += n;
     if (h->profiling) cudaEventRecord(h->ev[1], st);
-    n = launch_permute(ws.idx, T, E, top_k, with_shared, x, H, gather, kGemvCostTokens, ntile, ws, st);
+    n = launch_permute(ws.idx, T, E, top_k, with_shared, kGemvCostTokens, ntile, ws, st);
     if (n < 0) return false;
     launches += n;
     return true;
@@ -194,7 +176,6 @@ FfnArgs ffn_args(coli_moe_t *h, const void *x_bf16, int32_t T, int32_t top_k, in
     a.touched_cost = ws.touched_cost;
     a.src_token = ws.src_token;
     a.x = static_cast<const __nv_bfloat16 *>(x_bf16);
-    a.xp = ws.xp;
     a.xh = ws.xh;
     a.xinv = ws.xinv;
     a.h = ws.h;
@@ -239,19 +220,18 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     const bool with_shared = shared != nullptr;
     Workspace &ws = h->ws;
     int launches = 0, n;
-    const FfnKind ffn = pick_ffn(h, T, top_k, packed, shared);
-    const bool gemm = ffn == kFfnBf16;
-    const int ntile = ffn == kFfnMx ? kNtileMx : ffn == kFfnMx4 ? kNtileMx4 : 0;
+    const FfnKind ffn = pick_ffn(h);
+    const int ntile = ffn == kFfnMx4 ? mx4_ntile(T, top_k, h->cfg.num_experts, H) : 0;
     const int rows = T * top_k + (with_shared ? T : 0);
     const bool prof = h->profiling;
     h->stage_valid = false;
     if (prof) cudaEventRecord(h->ev[0], st);
-    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, gemm, ntile, rows, launches))
+    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, ntile, launches))
         return launch_failed(h);
     {
         const FfnArgs a = ffn_args(h, x_bf16, T, top_k, rows, packed, shared);
-        if (ffn == kFfnMx || ffn == kFfnMx4) {   // the activation terms belong to the permute stage
-            n = ffn == kFfnMx ? launch_quant_x(a, st) : launch_quant_x4(a, st);
+        if (ffn == kFfnMx4) {   // the activation terms belong to the permute stage
+            n = launch_quant_x4(a, st);
             if (n < 0) return launch_failed(h);
             launches += n;
         }
@@ -261,19 +241,6 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
             n = launch_ffn_mx4(a, h->num_sms, ws.tile_sched, mid, st);
             if (n == -2) {
                 set_err(h, "FP4 block-scaled GEMM path unavailable (needs a tensor-map encoder)");
-                return COLI_ERR_INVALID_ARG;
-            }
-        } else if (ffn == kFfnMx) {
-            n = launch_ffn_mx(a, h->num_sms, ws.tile_sched, mid, st);
-            if (n == -2) {
-                set_err(h, "block-scaled GEMM path unavailable (needs 32-byte aligned code pointers and a "
-                           "tensor-map encoder)");
-                return COLI_ERR_INVALID_ARG;
-            }
-        } else if (gemm) {
-            n = launch_ffn_gemm(a, h->num_sms, ws.tile_sched, mid, st);
-            if (n == -2) {
-                set_err(h, "tensor-core grouped GEMM path is not available for this configuration");
                 return COLI_ERR_INVALID_ARG;
             }
         } else {
@@ -294,8 +261,7 @@ int forward_impl(coli_moe_t *h, const void *x_bf16, int32_t T, const float *rout
     h->last_k = top_k;
     h->last_shared = with_shared;
     h->last_launches = launches;
-    h->last_path = ffn == kFfnGemv ? COLI_FFN_GEMV : ffn == kFfnMx ? COLI_FFN_GEMM
-                 : ffn == kFfnBf16 ? COLI_FFN_GEMM_BF16 : COLI_FFN_GEMM_MXF4;
+    h->last_path = ffn == kFfnGemv ? COLI_FFN_GEMV : COLI_FFN_GEMM_MXF4;
     return COLI_OK;
 }
 
@@ -358,23 +324,20 @@ int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **
     const size_t Tm = c.max_tokens, km = c.max_top_k, E = c.num_experts, H = c.hidden;
     const size_t rows = Tm * km + Tm;
     Workspace &ws = h->ws;
-    ws.logit_part_floats = 4 * (Tm > 1024 ? Tm : 1024) * E;
-    bool ok = alloc(&ws.scores, Tm * E) && alloc(&ws.logit_part, ws.logit_part_floats) && alloc(&ws.idx, Tm * km) && alloc(&ws.w, Tm * km) &&
+    bool ok = alloc(&ws.scores, Tm * E) && alloc(&ws.logit_part, kRouterPartialFloats) && alloc(&ws.idx, Tm * km) && alloc(&ws.w, Tm * km) &&
               alloc(&ws.inv_row, Tm * km) && alloc(&ws.src_token, rows) && alloc(&ws.cnt, E + 1) &&
               alloc(&ws.off, E + 2) && alloc(&ws.touched, E + 1) && alloc(&ws.touched_cost, E + 2) && alloc(&ws.n_touched, 4) &&
-              alloc(&ws.xp, rows * H) && alloc(&ws.h, rows * (size_t)h->I_max) && alloc(&ws.y, rows * H) &&
+              alloc(&ws.h, rows * (size_t)h->I_max) && alloc(&ws.y, rows * H) &&
               alloc(&ws.xh, Tm * H) && alloc(&ws.xinv, Tm) && alloc(&ws.hh, rows * (size_t)h->I_max) &&
               alloc(&ws.hinv, rows) && alloc(&ws.err, 4) && alloc(&ws.x_stage, Tm * H) &&
               alloc(&ws.out_stage, Tm * H);
     if (ok)
         ok = alloc(&ws.xq, 2 * rows * H) && alloc(&ws.xqs, 4 * rows * (H / 16)) &&
-             alloc(&ws.hq, 3 * rows * (size_t)h->I_max) && alloc(&ws.hqs, 4 * rows * (size_t)(h->I_max / 16)) &&
+             alloc(&ws.hq, 2 * rows * (size_t)h->I_max) && alloc(&ws.hqs, 4 * rows * (size_t)(h->I_max / 16)) &&
              alloc(&ws.xg, 4 * rows) && alloc(&ws.hg, 4 * rows) && alloc(&ws.hf, rows * (size_t)h->I_max);
     if (ok) ok = cudaMemset(ws.err, 0, sizeof(int)) == cudaSuccess;
     if (ok) {
-        ws.tile_sched_bytes = gemm_sched_bytes((int)E, (int)rows);
-        const size_t mx_bytes = ntile_layout_ints((int)E, (int)rows) * sizeof(int32_t);
-        if (mx_bytes > ws.tile_sched_bytes) ws.tile_sched_bytes = mx_bytes;
+        ws.tile_sched_bytes = ntile_layout_ints((int)E, (int)rows) * sizeof(int32_t);
         ok = cudaMalloc(&ws.tile_sched, ws.tile_sched_bytes + 256) == cudaSuccess;
     }
     if (!ok) {
@@ -601,7 +564,7 @@ extern "C" int coli_moe_forward_nvfp4(coli_moe_t *h, const void *x_bf16, int32_t
         return COLI_ERR_INVALID_ARG;
     }
     if (prof) cudaEventRecord(h->ev[0], st);
-    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, false, kNtileMx4, rows, launches))
+    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, kNtileMx4, launches))
         return launch_failed(h);
     int n = launch_quant_x_nv(a, st);
     if (n < 0) return launch_failed(h);
@@ -839,7 +802,7 @@ int coli_moe_forward_banked(coli_moe_t *h, coli_expert_bank_t *bank, const void 
     const int R = cache ? 2 : (int)((cap + G - 1) / G);
     int launches = 0, n;
     h->stage_valid = false;
-    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, false, kNtileMx4, rows, launches))
+    if (!run_front(h, x_bf16, T, router_w, router_bias, top_k, with_shared, kNtileMx4, launches))
         return launch_failed(h);
     Workspace &ws = h->ws;
     n = launch_bank_plan(bank->dev, ws.cnt, ws.off, cache, G, R, kNtileMx4, ws.err, st);

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -26,8 +27,7 @@ struct ExpertSet {
 // Device workspace, sized at create for (max_tokens, max_top_k).
 struct Workspace {
     float *scores = nullptr;        // [Tm][E]
-    float *logit_part = nullptr;    // [logit_part_floats] split-K partial router logits
-    size_t logit_part_floats = 0;
+    float *logit_part = nullptr;    // [kRouterPartialFloats] split-K partial router logits
     int32_t *idx = nullptr;         // [Tm][km]
     float *w = nullptr;             // [Tm][km]
     int32_t *inv_row = nullptr;     // [Tm][km]
@@ -37,16 +37,15 @@ struct Workspace {
     int32_t *touched = nullptr;     // [E+1] non-empty groups, ascending
     int32_t *touched_cost = nullptr;  // [E+2] exclusive prefix of per-group work cost
     int32_t *n_touched = nullptr;   // [1]
-    __nv_bfloat16 *xp = nullptr;    // [Tm*km + Tm][H] expert-grouped activation rows
-    __nv_bfloat16 *h = nullptr;     // [Tm*km + Tm][I_max] SwiGLU output rows
+    __nv_bfloat16 *h = nullptr;     // [Tm*km + Tm][I_max] SwiGLU output rows (GEMV path)
     float *y = nullptr;             // [Tm*km + Tm][H] expert output rows
-    // Activation terms of the block-scaled paths: two E4M3 terms of x ([2][rows][H]) or four packed
-    // E2M1 terms ([4][rows][H/2]); three E4M3 terms of h ([3][rows][I_max]) or four packed E2M1
-    // terms ([4][rows][I_max/2]); UE8M0 scales per 32 elements, [terms][rows][K/32].
+    // Activation terms of the block-scaled path: four packed E2M1 terms of x ([4][rows][H/2]) and
+    // of h ([4][rows][I_max/2]); scales per 32 elements (UE8M0) or per 16 (E4M3, NVFP4 layer),
+    // [terms][rows][K/32 or K/16].
     uint8_t *xq = nullptr;          // 2 * rows * H bytes
-    uint8_t *xqs = nullptr;         // 4 * rows * H/16 (per 32 on the MXFP4 paths)
-    uint8_t *hq = nullptr;          // 3 * rows * I_max
-    uint8_t *hqs = nullptr;         // 4 * rows * I_max/16 (per 32 on the MXFP4 paths)
+    uint8_t *xqs = nullptr;         // 4 * rows * H/16
+    uint8_t *hq = nullptr;          // 2 * rows * I_max
+    uint8_t *hqs = nullptr;         // 4 * rows * I_max/16
     float *xg = nullptr;            // NVFP4 path: [4][rows] power-of-two scale per x term and row
     float *hg = nullptr;            // [4][rows] the same for the h terms
     float *hf = nullptr;            // [rows][I_max] fp32 h between the NVFP4 GEMMs
@@ -57,7 +56,7 @@ struct Workspace {
     int *err = nullptr;             // device error word (0 = none), see sm103_ptx.cuh
     __nv_bfloat16 *x_stage = nullptr;    // [Tm][H] forward_host input staging
     __nv_bfloat16 *out_stage = nullptr;  // [Tm][H] forward_host output staging
-    void *tile_sched = nullptr;     // grouped-GEMM tile schedule (see gemm_tc.cu)
+    void *tile_sched = nullptr;     // n-tile layout of the block-scaled GEMM (NtileLayout)
     size_t tile_sched_bytes = 0;
 };
 
@@ -78,7 +77,6 @@ struct FfnArgs {
     const int32_t *touched_cost;    // [n_touched + 1] exclusive prefix of per-group cost
     const int32_t *src_token;
     const __nv_bfloat16 *x;         // [T][H] input tokens
-    const __nv_bfloat16 *xp;        // [rows][H] expert-grouped activation rows (GEMM path)
     __half *xh;                     // GEMV path: scaled fp16 tokens and inverse scales
     float *xinv;
     __nv_bfloat16 *h;               // [rows][I_max]
@@ -142,32 +140,40 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Records the text coli_moe_last_error(NULL) returns (printf-style).
 void set_create_error(const char *fmt, ...);
 
+// A 2-D tensor map (cuTensorMapEncodeTiled, taken from the driver at first use): `rows` rows of
+// `inner` elements of type dt, `row_bytes` apart, boxes of box_inner x box_rows. False when the
+// driver offers no encoder or rejects the arguments (base and row_bytes must be 16-byte aligned).
+bool tensor_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
 // Launchers. Each returns the number of kernels it enqueued, or -1 on a launch error
 // (the CUDA error is then available from cudaGetLastError()).
-// `partial` ([partial_floats] fp32) holds split-K partial logits for larger T. `zero` (may be
-// null): n_zero ints the router's last kernel clears (the permute histogram). with_topk false:
-// the logits and scores only (route_permute_small takes the top-k).
+// `partial` holds split-K partial logits for larger T: at least kRouterPartialFloats fp32. The
+// split count depends only on (T, E, H, num_sms) and keeps splits * T * E within that fixed cap,
+// so every caller that passes such a buffer adds the partial logits in the same order and gets
+// bit-identical scores. `zero` (may be null): n_zero ints the router's last kernel clears (the
+// permute histogram). `err` (may be null): the device error word the tensor-core logits kernel
+// records a timed-out wait in. with_topk false: the logits and scores only (route_permute_small
+// takes the top-k).
+constexpr size_t kRouterPartialFloats = size_t(1) << 20;   // 4 MiB
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
-                  int E, int top_k, float *scores, int32_t *idx, float *w, float *partial, size_t partial_floats,
-                  int num_sms, int32_t *zero, int n_zero, cudaStream_t st, bool with_topk = true);
+                  int E, int top_k, float *scores, int32_t *idx, float *w, float *partial,
+                  int num_sms, int32_t *zero, int n_zero, int *err, cudaStream_t st, bool with_topk = true);
 // Small T: the top-k of A1 and all of A2 (launch_permute with gather = false) in one launch.
 // Returns -2 outside T < kSmallRouteTokens, top_k <= 32, E <= 1024.
 constexpr int kSmallRouteTokens = 64;
 int launch_route_permute_small(const float *router_b, int T, int E, int top_k, bool with_shared, int cost_tokens,
                                int ntile, Workspace &ws, cudaStream_t st);
-// Copies the activation rows into expert-grouped order (ws.xp) for the bf16 GEMM path.
-int launch_gather(const __nv_bfloat16 *x, int H, int rows, Workspace &ws, cudaStream_t st);
-// `gather`: also copy the activation rows into expert-grouped order (ws.xp). `cost_tokens`: rows
-// per unit of work cost in ws.touched_cost (see permute_scan). `ntile`: when non-zero, also write
-// the block-scaled GEMM's n-tile layout (NtileLayout, tiles of `ntile` and 2 * `ntile` rows) into
-// ws.tile_sched.
-int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, bool gather, int cost_tokens, int ntile, Workspace &ws, cudaStream_t st);
+// `cost_tokens`: rows per unit of work cost in ws.touched_cost (see permute_scan). `ntile`: when
+// non-zero, also write the block-scaled GEMM's n-tile layout (NtileLayout, tiles of `ntile` and
+// 2 * `ntile` rows) into ws.tile_sched.
+int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, int cost_tokens, int ntile,
+                   Workspace &ws, cudaStream_t st);
 // Rows per cost unit the GEMV kernels assume.
 constexpr int kGemvCostTokens = 4;
 
-// Token tiles of the block-scaled GEMMs: gate/up tiles of n rows, down tiles of 2n rows.
-constexpr int kNtileMx = 32;    // E2M1 weights x E4M3 activation terms (gemm_mx.cu)
+// Token tiles of the block-scaled GEMM: gate/up tiles of n rows, down tiles of 2n rows; with many
+// rows per expert both launches take 48-row tiles (the records of 2 x 24).
 constexpr int kNtileMx4 = 16;   // E2M1 weights x E2M1 activation terms (gemm_mx4.cu)
 constexpr int kNtileMin = 16;   // the layout below is sized for tiles of at least this many rows
 // The permute scan writes, per tile size, an exclusive prefix of ceil(cnt / size) over the touched
@@ -256,17 +262,12 @@ constexpr int kSplitMaxTokens = 64;   // the FP8 GEMM splits K only up to this m
 bool fp8_available();
 int launch_dense_fp8(const DenseArgs &a, int num_sms, cudaStream_t st);
 
-// Block-scaled MXFP4 tcgen05 GEMM path (gemm_mx.cu): native E2M1 weights x E4M3 activation terms.
-bool mx_available();
-bool mx_supported(const FfnArgs &a);
-int launch_ffn_mx(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
-// Expert-grouped activation rows -> two E4M3 terms + UE8M0 scales (ws.xq / ws.xqs).
-int launch_quant_x(const FfnArgs &a, cudaStream_t st);
-
 // Block-scaled tcgen05 GEMM path with FP4 on both sides (gemm_mx4.cu): E2M1 weights x four E2M1
 // activation terms.
 bool mx4_available();
 bool mx4_supported(const FfnArgs &a);
+// The n-tile size the permutation must lay out for a forward of the MXFP4 layer (see kNtileMx4).
+int mx4_ntile(int T, int top_k, int E, int H);
 int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
 // Expert-grouped activation rows -> four packed E2M1 terms + UE8M0 scales (ws.xq / ws.xqs).
 int launch_quant_x4(const FfnArgs &a, cudaStream_t st);
@@ -277,10 +278,5 @@ int launch_quant_x4(const FfnArgs &a, cudaStream_t st);
 bool nv4_supported(const FfnArgs &a);
 int launch_quant_x_nv(const FfnArgs &a, cudaStream_t st);
 int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
-
-// Grouped tcgen05 GEMM path with weights dequantised to bf16 in shared memory (gemm_tc.cu).
-size_t gemm_sched_bytes(int E, int max_rows);
-bool gemm_available();
-int launch_ffn_gemm(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
 
 }  // namespace colimoe

@@ -18,14 +18,24 @@
 // are stacked along N (term t at activation rows [t * bh, (t + 1) * bh)); the epilogue adds them.
 //
 // Tiles: 128 weight rows (M) x 16 (gate/up) or up to 32 (down) tokens of one group. One persistent
-// block per SM; warp roles as in the E4M3 path: TMA producer (warp 0), TMEM owner and MMA issuer
-// (warp 1), scale loaders (warps 2-5; weight row 32q + i reads its scales from lane 32q + i,
-// column (word) * 4 + q; activation row n from lane 32q + n % 32, column n / 32 of its word, in
-// every lane quarter q; the words of one stage sit 4 columns apart; their loads run four stages
-// ahead), epilogue (warps 6-13: two per lane quarter, taking alternate 8-column groups of the
-// tile's tokens). Four stages, double-buffered accumulators, bounded waits. A stage
-// covers 256 K (512 K for down tiles of up to 16 rows, which leave half of the slot free
-// otherwise); the last stage of a K that is not a multiple of it is partial.
+// block per SM; warp roles: TMA producer (warp 0), TMEM owner and MMA issuer (warp 1), scale
+// loaders (warps 2-5; weight row 32q + i reads its scales from lane 32q + i, column (word) * 4 + q;
+// activation row n from lane 32q + n % 32, column n / 32 of its word, in every lane quarter q; the
+// words of one stage sit 4 columns apart; their loads run four stages ahead), epilogue (warps
+// 6-13: two per lane quarter, taking alternate 8-column groups of the tile's tokens). Four stages,
+// double-buffered accumulators, bounded waits. A stage covers 256 K (512 K for down tiles of up to
+// 16 rows, which leave half of the slot free otherwise); the last stage of a K that is not a
+// multiple of it is partial.
+//
+// Big tiles, for launches with many rows per expert (48 on average or more): the tensor pipe then
+// bounds the launch, and with 16- or 32-token tiles every expert's weights are read into shared
+// memory once per tile, more often than the L2 can serve at the pipe's rate. A big tile holds 48
+// tokens (N = 4 x 48 = 192 per MMA) and two 128-row weight matrices that share them: the gate and
+// up rows of 128 i-values, or two consecutive 128-row blocks of the down matrix (256 rows of
+// hidden). Both accumulators (2 x 192 TMEM columns) live in one buffer; the scale factors take
+// columns 384-511. The epilogue first moves its sums of the term columns into registers and frees
+// the buffer, so the next tile's MMAs start while it computes. In the scale area an activation
+// word has 8 columns (a row n < 192 reads column n / 32 of its word).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -38,15 +48,23 @@ namespace {
 constexpr int BM = 128, BK = 256, MK = 64;     // weight rows, K per stage, K per MMA
 constexpr int kBnGateUp = kNtileMx4, kBnDown = 2 * kNtileMx4;   // tokens per tile
 constexpr int kTerms = 4;                      // E2M1 terms per activation
-constexpr int NS = 4;
 constexpr int kThreads = 448;                  // 14 warps: see the role list above
+constexpr int kBnBig = 48;                     // tokens of a big tile
 constexpr uint32_t kASmem = BM * BK / 2;       // 16 KB: 128 rows x 256 packed codes
-constexpr uint32_t kBSmemMax = kTerms * 32 * (BK / 2);   // 16 KB: up to 4 terms x 32 rows
 constexpr uint32_t kOffA0 = 0, kOffA1 = kASmem, kOffB = 2 * kASmem;
-constexpr uint32_t kStageBytes = 2 * kASmem + kBSmemMax;   // 49152
+// A stage: two weight tiles and up to 4 terms x 32 rows (48 in big tiles), a multiple of 1024 bytes.
+// Small-tile launches keep the smaller stage, which leaves more of the SM's unified L1 to the
+// scale loaders' reads.
+template <bool BIG> constexpr uint32_t stage_bytes() { return 2 * kASmem + kTerms * (BIG ? kBnBig : 32) * (BK / 2); }
+// Ring stages: four; three for big tiles, whose 56 KB stages would otherwise leave the unified L1
+// too small to hold the scale loaders' sectors between stages.
+template <bool BIG> constexpr int num_stages() { return BIG ? 3 : 4; }
+template <bool BIG> constexpr size_t smem_bytes() { return num_stages<BIG>() * (size_t)stage_bytes<BIG>() + 1024 + 256; }
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = 128;             // per accumulator buffer
-constexpr uint32_t kSfCol0 = 256;              // scale-factor columns: 32 per stage (64 for NVFP4)
+constexpr uint32_t kAccCols = 128;             // per accumulator buffer (two buffers; big tiles: one)
+// Scale-factor columns, 32 per stage (64 for NVFP4): after the two 128-column accumulator buffers,
+// or after the 384 accumulator columns of a big tile.
+template <bool BIG> constexpr uint32_t sf_col0() { return BIG ? 384 : 256; }
 constexpr uint32_t kSfStage = 32;
 constexpr uint32_t kSfStageNv = 64;
 constexpr int kSfAhead = 4;                   // stages the scale loads run ahead (2 for NVFP4)
@@ -57,7 +75,7 @@ enum Mode { kGateUp = 0, kDown = 1 };
 struct Mx4Params {
     int E, H, I, I_s, I_max, rows;
     int mode, m_tiles, bn;
-    int nbuf;                           // accumulator buffers: 2, or 1 when a gate/up tile needs 256 columns
+    int nbuf;                           // accumulator buffers: 2, or 1 when a tile needs more than 128 columns
     const int2 *ntile_rec;              // per n-tile: {first row, group | rows << 16}
     const int32_t *ntile_count;         // number of n-tiles
     const uint8_t *w_scales_routed, *w_scales_shared;
@@ -86,12 +104,14 @@ struct TileInfo {
     size_t ge;
 };
 
+
+
 // Tile t = (n-tile t / m_tiles, m-tile t % m_tiles); `rec` is the n-tile's record.
 __device__ __forceinline__ int2 tile_rec(const Mx4Params &p, int t, int total_tiles) {
     return t < total_tiles ? __ldg(p.ntile_rec + t / p.m_tiles) : make_int2(0, 0);
 }
 
-template <bool NV>
+template <bool NV, bool BIG>
 __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 rec) {
     TileInfo ti;
     ti.mt = t % p.m_tiles;
@@ -103,9 +123,9 @@ __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 
     ti.n_valid = rec.y >> 16;
     ti.valid = p.mode == kGateUp ? ti.mt * BM < ti.Ig : true;
     ti.K = p.mode == kGateUp ? p.H : ti.Ig;
-    ti.box = ti.n_valid <= 16 ? 0 : 1;
-    ti.bh = 16 << ti.box;
-    ti.wide = !NV && p.mode == kDown && ti.box == 0;
+    ti.box = ti.n_valid <= 16 ? 0 : ti.n_valid <= 32 ? 1 : 2;   // 48-row boxes in big tiles only
+    ti.bh = 16 * (ti.box + 1);
+    ti.wide = !NV && p.mode == kDown && ti.box == 0 && !BIG;
     ti.kst = ti.wide ? 2 * BK : BK;
     ti.nk = (ti.K + ti.kst - 1) / ti.kst;
     return ti;
@@ -116,9 +136,10 @@ __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 
 // In a wide stage a0 / a1 hold the weight words 0-1 / 2-3, and b[c] / b[c + 2] the words 0-1 / 2-3
 // of activation column c (c < 2).
 // NVFP4 stages hold four words per operand row (one per 64-K MMA) and are never wide.
-template <bool NV> struct SfStageT {
+template <bool NV, bool BIG> struct SfStageT {
     static constexpr int W = NV ? 4 : 2;
-    uint32_t a0[W], a1[W], b[4][W];
+    static constexpr int C = BIG ? 6 : 4;   // activation column groups: 4 x 48 rows in a big tile
+    uint32_t a0[W], a1[W], b[C][W];
     int nbc;
     bool wide;
 };
@@ -130,16 +151,16 @@ struct SfCursor {
     bool wide;
     bool vw, va;                        // NVFP4: weight / activation scale rows are 16-byte aligned
     int2 recA, recB;                    // records of the next two tiles (tA < tB), loaded ahead
-    const uint8_t *wp0, *wp1, *bp[4];
+    const uint8_t *wp0, *wp1, *bp[6];
 };
 
 // Moves the cursor to the first valid tile at or after cur.t; false when there is none.
-template <bool NV>
+template <bool NV, bool BIG>
 __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int total_tiles, int quad, int lane) {
     const bool gu = p.mode == kGateUp;
     for (; c.t < total_tiles; c.t += gridDim.x) {
         const int2 rec = c.t == c.tA ? c.recA : c.t == c.tB ? c.recB : tile_rec(p, c.t, total_tiles);
-        const TileInfo ti = decode_tile<NV>(p, c.t, rec);
+        const TileInfo ti = decode_tile<NV, BIG>(p, c.t, rec);
         if (!ti.valid) continue;
         if (c.tB == c.t + (int)gridDim.x) {            // keep the next two records in flight
             c.tA = c.tB;
@@ -154,12 +175,13 @@ __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int tot
         const int kb_row = ti.K / sdiv, kba = p.act_ld / sdiv;
         const uint8_t *ws = ti.shared ? p.w_scales_shared : p.w_scales_routed;
         const int rpe = gu ? 2 * ti.Ig : p.H;
-        const size_t wrow = ti.ge * (size_t)rpe + (size_t)ti.mt * BM + quad * 32 + lane;
+        const int mrows = BIG && !gu ? 2 * BM : BM;       // rows of the tile's m-block
+        const size_t wrow = ti.ge * (size_t)rpe + (size_t)ti.mt * mrows + quad * 32 + lane;
         c.wp0 = ws + wrow * kb_row;
-        c.wp1 = gu ? ws + (wrow + ti.Ig) * kb_row : nullptr;
+        c.wp1 = gu ? ws + (wrow + ti.Ig) * kb_row : BIG ? ws + (wrow + BM) * kb_row : nullptr;
         c.nbc = (kTerms * ti.bh + 31) / 32;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < SfStageT<NV, BIG>::C; ++q) {
             const int n = lane + 32 * q;
             const int tt = n / ti.bh, j = n % ti.bh;
             c.bp[q] = (q < c.nbc && j < ti.n_valid) ? p.act_scales + ((size_t)tt * p.rows + ti.row0 + j) * kba
@@ -176,17 +198,17 @@ __device__ __forceinline__ bool sf_tile(const Mx4Params &p, SfCursor &c, int tot
     return false;
 }
 
-template <bool NV>
+template <bool NV, bool BIG>
 __device__ __forceinline__ bool sf_next(const Mx4Params &p, SfCursor &c, int total_tiles, int quad, int lane) {
     if (++c.k < c.nk) return true;
     c.t += gridDim.x;
-    return sf_tile<NV>(p, c, total_tiles, quad, lane);
+    return sf_tile<NV, BIG>(p, c, total_tiles, quad, lane);
 }
 
 // Issues the loads of the cursor's stage: 8 scale bytes per row (16 in a wide stage; fewer in the
 // last stage of a K that is not a multiple of the stage; a missing word reads as scale 1).
-template <bool NV>
-__device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStageT<NV> &s, int n_a) {
+template <bool NV, bool BIG>
+__device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStageT<NV, BIG> &s, int n_a) {
     if constexpr (NV) {   // four words (16 scale bytes) per row and stage; a missing word reads as 1.0
         const int nw = min(BK, c.K - c.k * BK) / 64;
         const int w0 = c.k * 4;
@@ -247,7 +269,7 @@ __device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStageT<NV> &s, int
         ld2(c.wp0, s.a0);
         ld2(n_a > 1 ? c.wp1 : nullptr, s.a1);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) ld2(c.bp[q], s.b[q]);
+        for (int q = 0; q < SfStageT<NV, BIG>::C; ++q) ld2(c.bp[q], s.b[q]);
     } else if (c.wide) {
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
@@ -265,7 +287,7 @@ __device__ __forceinline__ void sf_fetch(const SfCursor &c, SfStageT<NV> &s, int
             s.a0[w] = ld(c.wp0, w);
             s.a1[w] = n_a > 1 ? ld(c.wp1, w) : 0x7F7F7F7Fu;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) s.b[q][w] = ld(c.bp[q], w);
+            for (int q = 0; q < SfStageT<NV, BIG>::C; ++q) s.b[q][w] = ld(c.bp[q], w);
         }
     }
     s.nbc = c.nbc;
@@ -354,14 +376,36 @@ __device__ __forceinline__ uint32_t e2m1_pair(float lo, float hi, float &blo, fl
     return b;
 }
 
-struct BMaps4 {
-    CUtensorMap m[kTerms][2];   // [term][box height 16 / 32]
+// One token's value of h at i = mrow (lane = i mod 32): SwiGLU of the gate and up sums, then four
+// E2M1 terms, each with its UE8M0 scale per 32 consecutive i (one warp), stored to hq / hs. Called
+// by all lanes of a warp together. Not inlined: a big tile's epilogue finishes 24 tokens per warp,
+// and as many inlined copies overflow the instruction cache the MMA and TMA warps share.
+__device__ __noinline__ void finish_h(float g, float u, size_t row, int mrow, int lane, uint8_t *hq, uint8_t *hs,
+                                      int rows, int I_max) {
+    float v = __fdiv_rn(g, 1.0f + expf(-g)) * u;
+#pragma unroll
+    for (int tt = 0; tt < kTerms; ++tt) {
+        const uint32_t sb = e2m1_scale_byte(warp_max_abs(fabsf(v)));
+        const float scale = __uint_as_float(sb << 23), inv = __uint_as_float((254u - sb) << 23);
+        float back, unused;
+        const uint32_t code = e2m1_pair(v * inv, 0.f, back, unused) & 0xF;
+        v -= back * scale;
+        const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+        if ((lane & 1) == 0) hq[((size_t)tt * rows + row) * (I_max / 2) + mrow / 2] = (uint8_t)(code | (hi << 4));
+        if (lane == 0) hs[((size_t)tt * rows + row) * (I_max / 32) + mrow / 32] = (uint8_t)sb;
+    }
+}
+
+template <bool BIG> struct BMaps4 {
+    CUtensorMap m[kTerms][BIG ? 3 : 2];   // [term][box height 16 / 32 / 48]
 };
 
-template <int MODE, bool NV = false>
+template <int MODE, bool NV, bool BIG>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
-         const __grid_constant__ BMaps4 tm_b, const Mx4Params p, const __grid_constant__ NvParams q) {
+         const __grid_constant__ BMaps4<BIG> tm_b, const Mx4Params p, const __grid_constant__ NvParams q) {
+    constexpr uint32_t kStageBytes = stage_bytes<BIG>(), kSfCol0 = sf_col0<BIG>();
+    constexpr int NS = num_stages<BIG>();
     // The kernel before this one in the stream (quant_x4_rows, or the gate/up launch before the
     // down launch) signals its dependents only after its own dependency wait, so every kernel up
     // to the permutation has completed when this one starts: its tile records can be read, and the
@@ -377,7 +421,8 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr bool gu = MODE == kGateUp;
-    constexpr int n_a = gu ? 2 : 1;
+    constexpr int n_a = gu || BIG ? 2 : 1;          // weight matrices: gate and up, or two down row blocks
+    constexpr int mrows = BIG && !gu ? 2 * BM : BM; // weight rows of one m-tile
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(ptx::smem_addr(&tma_full[s]), 1);
@@ -414,14 +459,14 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 const uint32_t bbytes = kTerms * ti.bh * (BK / 2);   // one 128-byte K chunk of the terms
                 const CUtensorMap *ta = ti.shared ? &tm_a_shared : &tm_a_routed;
                 const int rpe = gu ? 2 * ti.Ig : p.H;
-                const int arow = (int)ti.ge * rpe + ti.mt * BM;
+                const int arow = (int)ti.ge * rpe + ti.mt * mrows;
                 const uint32_t fb = ptx::smem_addr(&tma_full[s]);
                 const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
                 const int x0 = k * (ti.kst / 2);                      // byte offset along K
                 const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;   // second K chunk
-                ptx::mbar_arrive_expect_tx(fb, (gu || two ? 2 : 1) * kASmem + (two ? 2 : 1) * bbytes);
+                ptx::mbar_arrive_expect_tx(fb, (n_a == 2 || two ? 2 : 1) * kASmem + (two ? 2 : 1) * bbytes);
                 ptx::tma_load_2d_hint(st + kOffA0, ta, x0, arow, fb, pol);
-                if (gu) ptx::tma_load_2d_hint(st + kOffA1, ta, x0, arow + ti.Ig, fb, pol);
+                if (n_a == 2) ptx::tma_load_2d_hint(st + kOffA1, ta, x0, arow + (gu ? ti.Ig : BM), fb, pol);
                 if (two) ptx::tma_load_2d_hint(st + kOffA1, ta, x0 + BK / 2, arow, fb, pol);
             };
             auto issue_b = [&](const TileInfo &ti, int k, int s) {
@@ -441,10 +486,10 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             // before the wait: the weights of the first stages of the first tile (all slots are free)
             int t0 = blockIdx.x, pre = 0;
             int2 rec = tile_rec(p, t0, total_tiles);
-            TileInfo ti0 = decode_tile<NV>(p, t0, rec);
+            TileInfo ti0 = decode_tile<NV, BIG>(p, t0, rec);
             while (t0 < total_tiles && !ti0.valid) {
                 t0 += gridDim.x;
-                ti0 = decode_tile<NV>(p, t0, tile_rec(p, t0, total_tiles));
+                ti0 = decode_tile<NV, BIG>(p, t0, tile_rec(p, t0, total_tiles));
             }
             if (t0 < total_tiles) {
                 pre = min(NS, ti0.nk);
@@ -457,7 +502,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
                 const int2 cur = rec;
                 rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
-                const TileInfo ti = decode_tile<NV>(p, t, cur);
+                const TileInfo ti = decode_tile<NV, BIG>(p, t, cur);
                 if (!ti.valid) continue;
                 for (int k = 0; k < ti.nk; ++k, ++it) {
                     if (t == t0 && k < pre) continue;             // issued above
@@ -486,7 +531,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
                 const int2 cur = rec;
                 rec = tile_rec(p, t + gridDim.x, total_tiles);   // in flight during this tile
-                const TileInfo ti = decode_tile<NV>(p, t, cur);
+                const TileInfo ti = decode_tile<NV, BIG>(p, t, cur);
                 if (!ti.valid) continue;
                 const uint32_t buf = p.nbuf == 2 ? tcount & 1u : 0u, use = p.nbuf == 2 ? tcount >> 1 : tcount;
                 if (!ptx::mbar_wait(ptx::smem_addr(&acc_empty[buf]), (use & 1u) ^ 1u, p.err, ptx::kErrWaitAccum,
@@ -526,12 +571,14 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                         continue;
                     }
                     const uint32_t sfa = tmem + kSfCol0 + s * kSfStage, sfb = sfa + 16;
+                    constexpr uint32_t bws = BIG ? 8 : 4;                  // activation word stride
                     auto step = [&](int j) {
                         const uint32_t id = (j & 1) ? id2 : id0;
                         const uint32_t sw = 4 * (j >> 1);                  // scale word j / 2
-                        if (gu) {
-                            mma_mx4(d0, a0 + 2 * j, b + 2 * j, id, sfa + sw, sfb + sw, acc);
-                            mma_mx4(d1, a1 + 2 * j, b + 2 * j, id, sfa + 8 + sw, sfb + sw, acc);
+                        if (n_a == 2) {
+                            const uint32_t bw = bws * (j >> 1);
+                            mma_mx4(d0, a0 + 2 * j, b + 2 * j, id, sfa + sw, sfb + bw, acc);
+                            mma_mx4(d1, a1 + 2 * j, b + 2 * j, id, sfa + 8 + sw, sfb + bw, acc);
                         } else if (j < 4) {
                             mma_mx4(d0, a0 + 2 * j, b + 2 * j, id, sfa + sw, sfb + sw, acc);
                         } else {                                           // second chunk of a wide stage
@@ -573,7 +620,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         SfCursor cur;
         cur.t = blockIdx.x;
         cur.tA = cur.tB = -1;
-        bool live = sf_tile<NV>(p, cur, total_tiles, quad, lane);   // tile records: readable before the wait
+        bool live = sf_tile<NV, BIG>(p, cur, total_tiles, quad, lane);   // tile records: readable before the wait
         if (live) {   // this lane's weight-scale rows of the first tile into L2 meanwhile
             for (int o = 0; o < cur.K / 32; o += 128) {
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(cur.wp0 + o));
@@ -581,14 +628,14 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             }
         }
         pdl_wait();
-        constexpr int kAhead = NV ? 2 : kSfAhead;
-        SfStageT<NV> ring[kAhead];
+        constexpr int kAhead = NV ? 2 : BIG ? 3 : kSfAhead;
+        SfStageT<NV, BIG> ring[kAhead];
 #pragma unroll
         for (int d = 0; d < kAhead; ++d) {
             ring[d].nbc = 0;
             if (live) {
                 sf_fetch(cur, ring[d], n_a);
-                live = sf_next<NV>(p, cur, total_tiles, quad, lane);
+                live = sf_next<NV, BIG>(p, cur, total_tiles, quad, lane);
             }
         }
         uint32_t it = 0;
@@ -628,13 +675,19 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     // written to its whole 4-column group (lane 32q + i reads column 4w + q); the
                     // activation words of column group c at +16 + 4w + c (a wide stage's words 2-3
                     // at +24 + 4w + c). Columns a stage does not use take any value.
+                    // Big tiles: activation word w of column group c at +16 + 8w + c (c < 6).
                     uint32_t r[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) r[j] = j < 8 ? ring[d].a0[(j >> 2) & 1] : ring[d].a1[(j >> 2) & 1];
                     tmem_st_x16(col, r);
+                    if constexpr (BIG) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        r[j] = j < 8 ? ring[d].b[j & 3][(j >> 2) & 1] : ring[d].b[((j & 3) + 2) & 3][(j >> 2) & 1];
+                        for (int j = 0; j < 16; ++j) r[j] = (j & 7) < 6 ? ring[d].b[j & 7][j >> 3] : 0x7F7F7F7Fu;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            r[j] = j < 8 ? ring[d].b[j & 3][(j >> 2) & 1] : ring[d].b[((j & 3) + 2) & 3][(j >> 2) & 1];
+                    }
                     tmem_st_x16(col + 16, r);
                 }
                 tmem_st_wait();
@@ -644,7 +697,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 ring[d].nbc = 0;
                 if (live) {
                     sf_fetch(cur, ring[d], n_a);
-                    live = sf_next<NV>(p, cur, total_tiles, quad, lane);
+                    live = sf_next<NV, BIG>(p, cur, total_tiles, quad, lane);
                 }
             }
         }
@@ -660,7 +713,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
         for (int t = blockIdx.x; t < total_tiles && !*abort_flag; t += gridDim.x) {
             const int2 cur = rec;
             rec = tile_rec(p, t + gridDim.x, total_tiles);
-            const TileInfo ti = decode_tile<NV>(p, t, cur);
+            const TileInfo ti = decode_tile<NV, BIG>(p, t, cur);
             if (!ti.valid) continue;
             const uint32_t buf = p.nbuf == 2 ? tcount & 1u : 0u, use = p.nbuf == 2 ? tcount >> 1 : tcount;
             if (!ptx::mbar_wait(ptx::smem_addr(&acc_full[buf]), use & 1u, p.err, ptx::kErrWaitAccum, abort_flag,
@@ -668,9 +721,53 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 break;
             ++tcount;
             ptx::tc_fence_after();
-            const int mrow = ti.mt * BM + m;
+            const int mrow = ti.mt * mrows + m;
             const uint32_t acc = lane_base + buf * kAccCols;
             const int ncols = kTerms * ti.bh;
+            if constexpr (BIG) {
+                // Big tile: this warp's token groups c0 = 8 * half + 16 * gi (gi < 3). First the
+                // sums of the term columns of both matrices into registers; then the buffer is
+                // released and the next tile's MMAs run while the values are finished and stored.
+                float s0[3][8], s1[3][8];
+#pragma unroll
+                for (int gi = 0; gi < 3; ++gi) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) s0[gi][j] = s1[gi][j] = 0.f;
+                    const int c0 = 8 * half + 16 * gi;
+                    if (c0 >= ti.n_valid) continue;
+#pragma unroll
+                    for (int tt = 0; tt < kTerms; ++tt) {
+                        uint32_t r[8], r1[8];
+                        ptx::tmem_ld8(acc + tt * ti.bh + c0, r);
+                        ptx::tmem_ld8(acc + ncols + tt * ti.bh + c0, r1);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            s0[gi][j] += __uint_as_float(r[j]);
+                            s1[gi][j] += __uint_as_float(r1[j]);
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&acc_empty[buf]));
+#pragma unroll
+                for (int gi = 0; gi < 3; ++gi) {
+                    const int c0 = 8 * half + 16 * gi;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (c0 + j >= ti.n_valid) break;
+                        const size_t row = (size_t)ti.row0 + c0 + j;
+                        if (!gu) {            // two 128-row blocks of the down output
+                            p.y[row * p.H + mrow] = s0[gi][j];
+                            p.y[row * p.H + mrow + BM] = s1[gi][j];
+                        } else {
+                            finish_h(s0[gi][j], s1[gi][j], row, mrow, lane, p.hq, p.hs, p.rows, p.I_max);
+                        }
+                    }
+                }
+                continue;
+            }
             float wg = 1.f;   // NVFP4: the matrix scale of this tile's expert
             if constexpr (NV) wg = __ldg(ti.shared ? q.w_global_shared : q.w_global_routed + ti.ge);
             for (int c0 = 8 * half; c0 < ti.n_valid; c0 += 16) {
@@ -921,18 +1018,39 @@ bool map_packed(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool map_terms(BMaps4 &b, const uint8_t *base, uint64_t K, uint64_t rows) {
+template <bool BIG>
+bool map_terms(BMaps4<BIG> &b, const uint8_t *base, uint64_t K, uint64_t rows) {
     for (int t = 0; t < kTerms; ++t)
-        for (int h = 0; h < 2; ++h)
-            if (!map_packed(&b.m[t][h], base + (size_t)t * rows * (K / 2), K, rows, 16u << h)) return false;
+        for (int h = 0; h < (BIG ? 3 : 2); ++h)
+            if (!map_packed(&b.m[t][h], base + (size_t)t * rows * (K / 2), K, rows, 16u * (h + 1))) return false;
     return true;
 }
 
 }  // namespace
 
+bool tensor_map_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
+    auto enc = encoder();
+    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || (row_bytes & 15)) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool mx4_available() { return encoder() != nullptr; }
 
 bool mx4_supported(const FfnArgs &a) { return encoder() != nullptr && a.H % 128 == 0; }
+
+namespace {
+// Big tiles pay when experts average 48 rows or more; the down launch's row blocks of 256 need H a
+// multiple of 256.
+bool big_tiles(int T, int top_k, int E, int H) { return (long)T * top_k >= (long)kBnBig * E && H % (2 * BM) == 0; }
+}  // namespace
+
+int mx4_ntile(int T, int top_k, int E, int H) { return big_tiles(T, top_k, E, H) ? kBnBig / 2 : kNtileMx4; }
 
 int launch_quant_x4(const FfnArgs &a, cudaStream_t st) {
     const long threads = (long)a.rows * (a.H / 32);
@@ -943,19 +1061,18 @@ int launch_quant_x4(const FfnArgs &a, cudaStream_t st) {
 
 namespace {
 
-template <bool NV>
+template <bool NV, bool BIG>
 int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
-    if (!mx4_supported(a)) return -2;
     const NtileLayout nl = a.tiles ? *a.tiles : ntile_layout(sched, a.E, a.rows);
     const uint64_t slots = a.w_slots ? a.w_slots : a.E;   // weight sets the routed arrays hold
     const dim3 grid(a.grid ? a.grid : num_sms);
-    const size_t smem = NS * kStageBytes + 1024 + 256;
+    constexpr size_t smem = smem_bytes<BIG>();
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(gemm_mx4<kGateUp, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(gemm_mx4<kDown, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-                cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_mx4<kGateUp, NV, BIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_mx4<kDown, NV, BIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
             return -1;
         attr = true;
     }
@@ -974,13 +1091,14 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     NvParams q{};
     q.hf = a.hf;
     CUtensorMap tar, tas;
-    BMaps4 tb;
+    BMaps4<BIG> tb;
     // gate/up
     // Many tokens per expert: gate/up tiles of 32 tokens (N = 128 per matrix, half the MMAs per
-    // token) with one accumulator buffer (gate + up fill 256 TMEM columns).
-    const bool gu32 = (long)a.T * a.top_k >= 16L * a.E;
+    // token) with one accumulator buffer (gate + up fill 256 TMEM columns); more still: big tiles
+    // of 48 tokens for both launches (the permutation then lays out 48-row tiles as its large ones).
+    const bool gu32 = BIG || (long)a.T * a.top_k >= 16L * a.E;
     p.mode = kGateUp;
-    p.bn = gu32 ? kBnDown : kBnGateUp;
+    p.bn = BIG ? kBnBig : gu32 ? kBnDown : kBnGateUp;
     p.nbuf = gu32 ? 1 : 2;
     p.ntile_rec = gu32 ? nl.rec_large : nl.rec_small;
     p.ntile_count = gu32 ? nl.count + 1 : nl.count;
@@ -997,7 +1115,7 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     if (a.shared.gu_codes) ok = ok && map_packed(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q);
+    launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV, BIG>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q);
     int n = 1;
     if (mid) cudaEventRecord(mid, st);
     if constexpr (NV) {   // h (fp32) -> four terms with E4M3 scales per 16 under a scale per (term, row)
@@ -1008,11 +1126,11 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     }
     // down
     p.mode = kDown;
-    p.bn = kBnDown;
-    p.nbuf = 2;
+    p.bn = BIG ? kBnBig : kBnDown;
+    p.nbuf = BIG ? 1 : 2;
     p.ntile_rec = nl.rec_large;
     p.ntile_count = nl.count + 1;
-    p.m_tiles = a.H / BM;
+    p.m_tiles = BIG ? a.H / (2 * BM) : a.H / BM;
     p.w_scales_routed = a.routed.d_scales;
     p.w_scales_shared = a.shared.d_scales;
     q.w_global_routed = a.routed.d_global;
@@ -1024,7 +1142,7 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_pdl(gemm_mx4<kDown, NV>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q);
+    launch_pdl(gemm_mx4<kDown, NV, BIG>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }
@@ -1032,7 +1150,10 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
 }  // namespace
 
 int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
-    return launch_ffn_impl<false>(a, num_sms, sched, mid, st);
+    if (!mx4_supported(a)) return -2;
+    // An expert bank's rounds bring their own 16/32-row records, so banked forwards stay small.
+    if (!a.tiles && big_tiles(a.T, a.top_k, a.E, a.H)) return launch_ffn_impl<false, true>(a, num_sms, sched, mid, st);
+    return launch_ffn_impl<false, false>(a, num_sms, sched, mid, st);
 }
 
 bool nv4_supported(const FfnArgs &a) {
@@ -1047,7 +1168,7 @@ int launch_quant_x_nv(const FfnArgs &a, cudaStream_t st) {
 
 int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st) {
     if (!nv4_supported(a)) return -2;
-    return launch_ffn_impl<true>(a, num_sms, sched, mid, st);
+    return launch_ffn_impl<true, false>(a, num_sms, sched, mid, st);
 }
 
 }  // namespace colimoe

@@ -12,7 +12,10 @@
 // take a stage when its mbarrier completes, compute, and release it. Every wait is bounded.
 //
 // Arithmetic: activation rows are pre-scaled by a power of two that puts their largest magnitude
-// in [2^8, 2^9) and stored as fp16 (exact for bf16 inputs; undone at the end). E2M1 codes become
+// in [2^8, 2^9) and stored as fp16 (undone at the end). A bf16 element keeps its value exactly
+// unless it lies more than about 2^22 below the row's largest magnitude, where fp16 holds it as a
+// subnormal with fewer significant bits or flushes it to zero; such elements contribute below
+// 2^-22 of the row's scale to any sum, which the error bar of the layer absorbs. E2M1 codes become
 // exact fp16 pairs (cvt.rn.f16x2.e2m1x2); the products of one 32-element group are summed with
 // HFMA2 in two chains (8 terms per half each, |sum| < 6 * 2^9 * 8 < 65504), converted to fp32,
 // scaled by the group's UE8M0 factor (fp32 bits s << 23) and summed in fp32. Blocks split the

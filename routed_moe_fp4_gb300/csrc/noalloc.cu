@@ -15,8 +15,10 @@ namespace colimoe {
 namespace {
 
 // Largest T * E this entry point accepts, and the scratch it needs for that size.
+// The partial logits take the router's fixed cap, the same the forward's workspace holds, so both
+// calls choose the same split count and add the partials in the same order.
 constexpr size_t kMaxScores = 262144;              // T * E <= 262144, e.g. 1024 tokens x 256 experts
-constexpr size_t kMaxPartials = 4 * kMaxScores;    // split-K partial logits
+constexpr size_t kMaxPartials = kRouterPartialFloats;          // split-K partial logits
 constexpr size_t kScratchFloats = kMaxScores + kMaxPartials;   // 5 MiB
 
 // One copy per device that loads the library, resident until the process exits.
@@ -95,8 +97,8 @@ extern "C" int coli_moe_route_static(const void *x_bf16, int32_t T, int32_t H, c
     if (rc != COLI_OK) return rc;
     cudaGetLastError();
     const int n = launch_router(static_cast<const __nv_bfloat16 *>(x_bf16), T, H, router_w, router_bias, E, top_k,
-                                d->scratch, idx_out, weights_out, d->scratch + kMaxScores, kMaxPartials, d->num_sms,
-                                nullptr, 0, static_cast<cudaStream_t>(cuda_stream));
+                                d->scratch, idx_out, weights_out, d->scratch + kMaxScores, d->num_sms,
+                                nullptr, 0, nullptr, static_cast<cudaStream_t>(cuda_stream));
     if (n < 0) {
         set_create_error("route_static: kernel launch failed: %s", cudaGetErrorString(cudaGetLastError()));
         return COLI_ERR_CUDA;

@@ -4,8 +4,7 @@
 //
 // The row of (token t, slot j) with e = idx[t][j] is off[e] + #{t' < t : e in idx[t']}: a stable
 // grouping by (expert, token), computed without atomics on positions, so it is the same on every
-// run. Group E is the shared expert with rows off[E] + t for every token t. The activation rows
-// are gathered into that order (xp) for the expert FFN.
+// run. Group E is the shared expert with rows off[E] + t for every token t.
 #include "colimoe_internal.cuh"
 #include "block_scan.cuh"
 #include "topk.cuh"
@@ -260,21 +259,6 @@ permute_scatter(const int32_t *__restrict__ idx, int T, int E, int top_k, const 
     }
 }
 
-// xp[row] = x[src_token[row]] for every row, 16 bytes per thread step.
-__global__ void __launch_bounds__(256)
-permute_gather(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
-               __nv_bfloat16 *__restrict__ xp) {
-    pdl_begin();
-    const int vec_per_row = H / 8;
-    const size_t total = (size_t)rows * vec_per_row;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-        const int row = (int)(i / vec_per_row), v = (int)(i % vec_per_row);
-        const int t = src_token[row];
-        reinterpret_cast<uint4 *>(xp + (size_t)row * H)[v] =
-            __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * H) + v);
-    }
-}
-
 }  // namespace
 
 int launch_route_permute_small(const float *router_b, int T, int E, int top_k, bool with_shared, int cost_tokens,
@@ -290,15 +274,8 @@ int launch_route_permute_small(const float *router_b, int T, int E, int top_k, b
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
-int launch_gather(const __nv_bfloat16 *x, int H, int rows, Workspace &ws, cudaStream_t st) {
-    const size_t vecs = (size_t)rows * (H / 8);
-    const int blocks = (int)((vecs + 255) / 256 < 65536 ? (vecs + 255) / 256 : 65536);
-    launch_pdl(permute_gather, dim3(blocks), dim3(256), 0, st, x, H, (const int32_t *)ws.src_token, rows, ws.xp);
-    return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
-}
-
-int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, const __nv_bfloat16 *x,
-                   int H, bool gather, int cost_tokens, int ntile, Workspace &ws, cudaStream_t st) {
+int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared, int cost_tokens, int ntile,
+                   Workspace &ws, cudaStream_t st) {
     const int n = T * top_k;
     const int rows = n + (with_shared ? T : 0);
     // ws.cnt was cleared by the router's last kernel
@@ -307,9 +284,7 @@ int launch_permute(const int32_t *idx, int T, int E, int top_k, bool with_shared
                with_shared ? T : 0, cost_tokens, ntile_layout(ws.tile_sched, E, rows), ntile);
     launch_pdl(permute_scatter, dim3(E + 1), dim3(256), 0, st, idx, T, E, top_k, (const int32_t *)ws.cnt,
                (const int32_t *)ws.off, ws.src_token, ws.inv_row);
-    if (!gather) return cudaPeekAtLastError() == cudaSuccess ? 3 : -1;
-    const int g = launch_gather(x, H, rows, ws, st);
-    return g < 0 ? -1 : 3 + g;
+    return cudaPeekAtLastError() == cudaSuccess ? 3 : -1;
 }
 
 }  // namespace colimoe

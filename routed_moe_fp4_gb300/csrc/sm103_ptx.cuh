@@ -18,6 +18,7 @@ enum : int {
     kErrWaitEmpty = 2,     // producer waited too long for a free stage
     kErrWaitMma = 3,       // waited too long for an MMA commit
     kErrWaitAccum = 4,     // epilogue waited too long for an accumulator
+    kErrWaitRouter = 5,    // the tensor-core router logits kernel waited too long (any of its waits)
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s

@@ -129,6 +129,10 @@ WORKLOADS: Dict[str, Workload] = {
     # the larger V4 shape of the pages (hidden 7168, 384 experts, same MXFP4 layout); top-8 and
     # I = I_s = 2048 as in the other workloads (the pages give neither for it)
     "v4pro_decode": Workload("v4pro_decode", 8, 7168, 384, 8, 2048, 2048, "normal"),
+    # a reduced stand-in for the skewed prefill's heavy experts, small enough for a counter capture
+    # (33 experts, 0.77 GB): hidden 7168 with about 256 rows per expert, so the expert GEMMs run in
+    # the compute-heavy regime of the large groups
+    "skewed_e32": Workload("skewed_e32", 1024, 7168, 32, 8, 2048, 2048, "normal"),
 }
 SWEEP_T = (1, 2, 4, 16, 64, 128)
 for _t in SWEEP_T:

@@ -78,9 +78,6 @@ def test_gate_up_and_down_bytes_split_the_weights():
     assert b["ffn_gate_up"] == gu_w + x_terms + h_terms
     assert b["ffn_down"] == dn_w + h_terms + rows * wl.H * 4
     assert gu_w + dn_w == 63 * 13_369_344
-    # the E2M1 x E4M3 path moves two and three one-byte terms instead
-    b2 = bench.algorithmic_bytes(wl, _routing(wl, 62), path="mx")
-    assert b2["ffn_gate_up"] == gu_w + 2 * rows * (wl.H + wl.H // 32) + 3 * rows * (wl.I + wl.I // 32)
     # NVFP4: scale bytes per 16 elements
     b3 = bench.algorithmic_bytes(wl, _routing(wl, 62), path="nvf4", group=16)
     assert b3["layer"] - b["layer"] == 63 * 3 * wl.H * wl.I // 32
@@ -143,7 +140,7 @@ def test_clock_record_without_nvidia_smi():
 def test_ffn_path_names_are_unique_per_abi_value():
     abi = [v[0] for v in bench.FFN_PATHS.values() if v[0] is not None]
     assert len(abi) == len(set(abi))
-    assert bench.PATH_BY_ABI[4] == "mxf4" and "nvf4" not in bench.PATH_BY_ABI.values()
+    assert bench.PATH_BY_ABI[2] == "mxf4" and "nvf4" not in bench.PATH_BY_ABI.values()
 
 
 
@@ -245,3 +242,35 @@ def test_layer_roofline_takes_the_binding_bound():
     assert r["binding"] == "tensor"
     assert abs(r["frac_combined"] - 3.26e12 / (1879.7 * 6e12) / 1e-3) < 1e-12
     assert abs(r["tensor_frac"] - r["frac_combined"]) < 1e-12
+
+
+def test_cpu_model_on_an_arm_host_without_a_model_name(tmp_path, monkeypatch):
+    """Grace's /proc/cpuinfo has no "model name": the model comes from lscpu, else from the Arm part."""
+    import subprocess
+    info = tmp_path / "cpuinfo"
+    info.write_text("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU architecture: 8\n"
+                    "CPU part\t: 0xd4f\n")
+
+    def no_lscpu(*a, **k):
+        raise OSError("no lscpu")
+    monkeypatch.setattr(subprocess, "run", no_lscpu)
+    assert bench.cpu_model(str(info)) == "Arm Neoverse-V2"
+
+    class Out:
+        stdout = "Architecture: aarch64\nModel name:   Neoverse-V2\n"
+    monkeypatch.setattr(subprocess, "run", lambda *a, **k: Out())
+    assert bench.cpu_model(str(info)) == "Neoverse-V2"
+    x86 = tmp_path / "cpuinfo_x86"
+    x86.write_text("processor\t: 0\nmodel name\t: Example CPU @ 3.0GHz\n")
+    assert bench.cpu_model(str(x86)) == "Example CPU @ 3.0GHz"
+
+
+def test_config_targets_follow_the_scope_table():
+    """Decode shapes are judged against HBM at 0.70, the prefill shapes against the combined
+    roofline at 0.50; the pass covers every configuration beside the headline decode."""
+    assert bench.config_target("prefill") == ("frac_combined", 0.50)
+    assert bench.config_target("skewed") == ("frac_combined", 0.50)
+    for t in S.SWEEP_T:
+        assert bench.config_target(f"sweep_T{t}") == ("frac", 0.70)
+    assert bench.config_target("v4pro_decode") == ("frac", 0.70)
+    assert set(bench.CONFIG_PASS) == {"prefill", "skewed", "v4pro_decode"} | {f"sweep_T{t}" for t in S.SWEEP_T}

@@ -9,7 +9,7 @@ from tests import parity as P
 
 pytestmark = pytest.mark.gpu
 
-GEMV, GEMM, AUTO, BF16, MXF4 = 1, 2, 0, 3, 4
+GEMV, AUTO, MXF4 = 1, 0, 2
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -22,13 +22,19 @@ def _lib():
     colimoe.load()
 
 
-def _assert_ok(rep):
+def _assert_ok(rep, literal=True):
+    """The parity bar; `literal` also holds the output to max|out - ref64| <= 2e-2 RMS with the bf16
+    rounding included (the default FP4 path; the GEMV keeps h in bf16 and is held to the bar beyond
+    the half ulp only)."""
     print(f"\nPARITY T={rep.T} tokens={rep.tokens_checked} score_err={rep.max_score_err:.2e} "
           f"routing_exact={rep.routing_bit_exact} own_diffs={rep.own_routing_diffs} "
-          f"rel_err={rep.rel_err:.3e} rel_err_bf16={rep.rel_err_bf16:.3e} launches={rep.launches}")
+          f"beyond_half_ulp={rep.rel_err:.3e} literal={rep.rel_err_literal:.3e} "
+          f"vs_rounded_ref={rep.rel_err_bf16:.3e} launches={rep.launches}")
     assert rep.routing_bit_exact, "routing/permutation differ from the oracle on identical scores"
     assert rep.max_score_err <= P.SCORE_TOL, rep
     assert rep.rel_err <= P.OUT_TOL, rep
+    if literal:
+        assert rep.rel_err_literal <= P.OUT_TOL, rep
 
 
 def _run(oracle, inputs, path, n_tokens=None, repeats=1):
@@ -43,7 +49,7 @@ def _run(oracle, inputs, path, n_tokens=None, repeats=1):
 def test_tiny_all_tokens(oracle, path):
     inputs = S.make_inputs("tiny")
     rep, outs, _ = _run(oracle, inputs, path)
-    _assert_ok(rep)
+    _assert_ok(rep, literal=path != GEMV)
     assert rep.launches > 0
 
 
@@ -72,10 +78,12 @@ def test_sweep(oracle, T):
     _assert_ok(rep)
 
 
-def test_prefill_sampled(oracle):
+def test_prefill_all_tokens(oracle):
+    """All 512 tokens of the prefill chunk against the oracle."""
     inputs = S.make_inputs("prefill")
-    rep, _, _ = _run(oracle, inputs, AUTO, n_tokens=12)
+    rep, _, _ = _run(oracle, inputs, AUTO)
     _assert_ok(rep)
+    assert rep.tokens_checked == 512
 
 
 def test_v4pro_decode_all_tokens(oracle):
@@ -86,10 +94,26 @@ def test_v4pro_decode_all_tokens(oracle):
 
 
 def test_skewed_sampled(oracle):
+    """256 of the 4096 tokens: the first and last rows of the Zipf head expert, the lightest
+    expert, last rows of partial tiles of each box height, and a seeded sample; routing and the
+    permutation are compared on every token."""
     inputs = S.make_inputs("skewed")
-    rep, _, routing = _run(oracle, inputs, AUTO, n_tokens=8)
+    outs, routing, launches = P.run_gpu(inputs)
+    named = P.structured_tokens(routing, inputs.workload.T, 256)
+    print("\nskewed tokens: " + ", ".join(f"{k}={v}" for k, v in named.items() if not k.startswith("sample")))
+    assert {"heavy_first_row", "heavy_last_row", "lightest_expert", "partial_tile_1_16",
+            "partial_tile_17_32", "partial_tile_33_47"} <= set(named)
+    rep = P.check(oracle, inputs, outs[0], routing, list(named.values()), launches)
     _assert_ok(rep)
+    assert rep.tokens_checked >= 256
     assert routing["cnt"][:-1].max() > 3000      # the Zipf head expert
+
+
+def test_skewed_e32_sampled(oracle):
+    """About 256 rows per expert at hidden 7168: the big-tile launches on a production shape."""
+    inputs = S.make_inputs("skewed_e32")
+    rep, _, _ = _run(oracle, inputs, AUTO, n_tokens=12)
+    _assert_ok(rep)
 
 
 def test_repeatable_bitwise(oracle):
@@ -122,13 +146,13 @@ def test_edge_cases(oracle, wl):
     _assert_ok(rep)
 
 
-@pytest.mark.parametrize("path", [MXF4, GEMM, BF16, GEMV], ids=["mxf4", "mx", "bf16", "gemv"])
+@pytest.mark.parametrize("path", [MXF4, GEMV], ids=["mxf4", "gemv"])
 @pytest.mark.parametrize("name", ["tiny", "decode", "sweep_T16", "sweep_T128"])
 def test_ffn_paths(oracle, name, path):
     """Each FFN path, forced, against the oracle."""
     inputs = S.make_inputs(name)
     rep, _, _ = _run(oracle, inputs, path, n_tokens=8)
-    _assert_ok(rep)
+    _assert_ok(rep, literal=path != GEMV)
 
 
 @pytest.mark.parametrize("wl", [
@@ -137,17 +161,21 @@ def test_ffn_paths(oracle, name, path):
     _custom("gemm_noshared", I_s=0),
     _custom("gemm_many_rows", T=300, E=4, top_k=2),
     _custom("gemm_half_stages", T=21, H=640, I=384, I_s=256, E=12, top_k=3),
+    # 48 or more rows per expert on average with H a multiple of 256: both launches take 48-token
+    # tiles with two weight matrices each (ragged last tiles, a wider shared expert, K = 3 x 256)
+    _custom("big_ragged", T=200, H=512, E=8, top_k=2, I=256, I_s=384),
+    _custom("big_many_rows", T=400, H=768, E=6, top_k=3, I=384, I_s=128),
 ], ids=lambda w: w.name)
-@pytest.mark.parametrize("path", [MXF4, GEMM, BF16], ids=["mxf4", "mx", "bf16"])
+@pytest.mark.parametrize("path", [MXF4, GEMV], ids=["mxf4", "gemv"])
 def test_gemm_edge_cases(oracle, wl, path):
     inputs = S.make_inputs(wl)
     rep, _, _ = _run(oracle, inputs, path)
-    _assert_ok(rep)
+    _assert_ok(rep, literal=path != GEMV)
 
 
-@pytest.mark.parametrize("path", [MXF4, GEMM, BF16], ids=["mxf4", "mx", "bf16"])
+@pytest.mark.parametrize("path", [MXF4], ids=["mxf4"])
 def test_gemm_matches_gemv(oracle, path):
-    """The FFN paths agree with each other within the parity bar on the same routing."""
+    """The two FFN paths agree with each other within the parity bar on the same routing."""
     inputs = S.make_inputs("sweep_T64")
     o1, r1, _ = P.run_gpu(inputs, path=GEMV)
     o2, r2, _ = P.run_gpu(inputs, path=path)

@@ -24,13 +24,25 @@ def lib():
     return colimoe
 
 
-@pytest.mark.parametrize("name", ["decode", "sweep_T64", "prefill"])
+# Shapes where a split count chosen from the size of the partial-logit buffer would differ
+# between the two calls: few experts with many tokens, a layer created for more tokens than it
+# routes, and T * E exactly at the fixed limit (1024 x 256 and 2048 x 128). Small experts (I = 128)
+# keep the weights cheap; routing does not read them.
+_EXTRA = {
+    "na_e64_t1024": (S.Workload("na_e64_t1024", 1024, 4096, 64, 8, 128, 128, "normal"), None),
+    "na_e256_t1024_max4096": (S.Workload("na_e256_t1024", 1024, 4096, 256, 8, 128, 128, "normal"), 4096),
+    "na_e128_t2048": (S.Workload("na_e128_t2048", 2048, 2048, 128, 6, 128, 0, "normal"), None),
+}
+
+
+@pytest.mark.parametrize("name", ["decode", "sweep_T64", "prefill", *_EXTRA])
 def test_route_static_matches_forward(lib, name):
     import torch
     cm = lib
-    inputs = S.make_inputs(name)
+    wl, max_tokens = _EXTRA.get(name, (name, None))
+    inputs = S.make_inputs(wl)
     wl = inputs.workload
-    layer = cm.MoELayer(inputs)
+    layer = cm.MoELayer(inputs, max_tokens=max_tokens)
     x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
     out = torch.empty_like(x)
     layer.forward(x, out)
