@@ -159,7 +159,7 @@ constexpr size_t kRouterPartialFloats = size_t(1) << 20;   // 4 MiB
 int launch_router(const __nv_bfloat16 *x, int T, int H, const float *router_w, const float *router_b,
                   int E, int top_k, float *scores, int32_t *idx, float *w, float *partial,
                   int num_sms, int32_t *zero, int n_zero, int *err, cudaStream_t st, bool with_topk = true);
-// Small T: the top-k of A1 and all of A2 (launch_permute with gather = false) in one launch.
+// Small T: the top-k of A1 and all of A2 (launch_permute) in one launch.
 // Returns -2 outside T < kSmallRouteTokens, top_k <= 32, E <= 1024.
 constexpr int kSmallRouteTokens = 64;
 int launch_route_permute_small(const float *router_b, int T, int E, int top_k, bool with_shared, int cost_tokens,
@@ -270,13 +270,13 @@ bool mx4_supported(const FfnArgs &a);
 int mx4_ntile(int T, int top_k, int E, int H);
 int launch_ffn_mx4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
 // Expert-grouped activation rows -> four packed E2M1 terms + UE8M0 scales (ws.xq / ws.xqs).
-int launch_quant_x4(const FfnArgs &a, cudaStream_t st);
+int launch_quant_x4(const FfnArgs &a, int num_sms, cudaStream_t st);
 // NVFP4 variant (routed and shared sets carry E4M3 scales per 16 and fp32 globals): the x terms
 // (E4M3 scales per 16 under a power-of-two scale per (term, row)); then both GEMMs with the h
 // terms between them (`mid`, may be null, is recorded after the gate/up launch). Each returns the
 // kernels enqueued, -1 on a launch error; launch_ffn_nv4 -2 when the shapes are unsupported.
 bool nv4_supported(const FfnArgs &a);
-int launch_quant_x_nv(const FfnArgs &a, cudaStream_t st);
+int launch_quant_x_nv(const FfnArgs &a, int num_sms, cudaStream_t st);
 int launch_ffn_nv4(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid, cudaStream_t st);
 
 }  // namespace colimoe

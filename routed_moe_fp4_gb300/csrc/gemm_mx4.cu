@@ -39,6 +39,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "colimoe_internal.cuh"
 #include "sm103_ptx.cuh"
 
@@ -843,19 +845,11 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
     }
 }
 
-// Expert-grouped x rows -> four E2M1 terms (packed, two codes per byte) with UE8M0 scales per 32
-// elements. One thread per (row, 32-element block).
-__global__ void __launch_bounds__(256)
-quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
-              uint8_t *__restrict__ xq, uint8_t *__restrict__ xs) {
-    // signals the next kernel (the gate/up GEMM) only after the wait: that kernel reads the
-    // permutation's tile records before its own wait
-    pdl_wait();
-    pdl_trigger();
+// The four E2M1 terms of one 32-element block of one expert-grouped x row.
+__device__ __forceinline__ void quant_x4_block(const __nv_bfloat16 *__restrict__ x, int H,
+                                               const int32_t *__restrict__ src_token, int rows,
+                                               uint8_t *__restrict__ xq, uint8_t *__restrict__ xs, int row, int b) {
     const int nb = H / 32;
-    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (long)rows * nb) return;
-    const int row = (int)(i / nb), b = (int)(i % nb);
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)src_token[row] * H + b * 32);
     float v[32];
 #pragma unroll
@@ -890,6 +884,23 @@ quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restr
     }
 }
 
+// Expert-grouped x rows -> four E2M1 terms (packed, two codes per byte) with UE8M0 scales per 32
+// elements. One thread per (row, 32-element block), grid-stride over a grid that is resident at
+// once: the gate/up GEMM launched after it (programmatically) takes SMs as soon as every block of
+// this kernel has started, so blocks still queued behind a larger grid would be left to fewer and
+// fewer SMs (measured: 1.1 ms lost on the 4096-token layer).
+__global__ void __launch_bounds__(256)
+quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restrict__ src_token, int rows,
+              uint8_t *__restrict__ xq, uint8_t *__restrict__ xs) {
+    // signals the next kernel (the gate/up GEMM) only after the wait: that kernel reads the
+    // permutation's tile records before its own wait
+    pdl_wait();
+    pdl_trigger();
+    const int nb = H / 32;
+    const long n = (long)rows * nb;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
+        quant_x4_block(x, H, src_token, rows, xq, xs, (int)(i / nb), (int)(i % nb));
+}
 // NVFP4 activation terms: rows -> four E2M1 terms, each with an E4M3 scale per 16 elements under
 // a power-of-two scale per (term, row): G = 2^ceil(log2(max|v| / (6 * 448))) keeps every group's
 // scale max|v_group| / (6 G), rounded up to an E4M3 value, within E4M3's range, and |v| / (scale
@@ -898,13 +909,12 @@ quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restr
 // for the shared expert's rows (from off[E] on). One block of 128 threads per row; a thread owns
 // whole groups, up to four (K <= 8192).
 template <bool FROM_X>
-__global__ void __launch_bounds__(128)
-quant_rows_nv(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ hf, const int32_t *__restrict__ src_token,
-              const int32_t *__restrict__ off_shared, int K_routed, int K_shared, int ld_in, int rows, int ld_out,
-              uint8_t *__restrict__ q, uint8_t *__restrict__ qs, float *__restrict__ gs) {
-    pdl_wait();
-    pdl_trigger();
-    const int row = blockIdx.x, tid = threadIdx.x;
+__device__ __forceinline__ void quant_row_nv(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ hf,
+                                             const int32_t *__restrict__ src_token, const int32_t *__restrict__ off_shared,
+                                             int K_routed, int K_shared, int ld_in, int rows, int ld_out,
+                                             uint8_t *__restrict__ q, uint8_t *__restrict__ qs, float *__restrict__ gs,
+                                             int row) {
+    const int tid = threadIdx.x;
     const int K = FROM_X ? K_routed : (row >= *off_shared ? K_shared : K_routed);
     const int ng = K / 16;
     float v[4][16];
@@ -993,6 +1003,18 @@ quant_rows_nv(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ hf,
     }
 }
 
+template <bool FROM_X>
+__global__ void __launch_bounds__(128)
+quant_rows_nv(const __nv_bfloat16 *__restrict__ x, const float *__restrict__ hf, const int32_t *__restrict__ src_token,
+              const int32_t *__restrict__ off_shared, int K_routed, int K_shared, int ld_in, int rows, int ld_out,
+              uint8_t *__restrict__ q, uint8_t *__restrict__ qs, float *__restrict__ gs) {
+    pdl_wait();
+    pdl_trigger();
+    // grid-stride over rows on a grid resident at once (see quant_x4_rows)
+    for (int row = blockIdx.x; row < rows; row += gridDim.x)
+        quant_row_nv<FROM_X>(x, hf, src_token, off_shared, K_routed, K_shared, ld_in, rows, ld_out, q, qs, gs, row);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -1052,10 +1074,10 @@ bool big_tiles(int T, int top_k, int E, int H) { return (long)T * top_k >= (long
 
 int mx4_ntile(int T, int top_k, int E, int H) { return big_tiles(T, top_k, E, H) ? kBnBig / 2 : kNtileMx4; }
 
-int launch_quant_x4(const FfnArgs &a, cudaStream_t st) {
+int launch_quant_x4(const FfnArgs &a, int num_sms, cudaStream_t st) {
     const long threads = (long)a.rows * (a.H / 32);
-    launch_pdl(quant_x4_rows, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, a.x, a.H, a.src_token, a.rows,
-               a.xq, a.xqs);
+    const long blocks = std::min<long>((threads + 255) / 256, 4L * num_sms);   // 4 blocks of 256 fit an SM
+    launch_pdl(quant_x4_rows, dim3((unsigned)blocks), dim3(256), 0, st, a.x, a.H, a.src_token, a.rows, a.xq, a.xqs);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -1119,7 +1141,8 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     int n = 1;
     if (mid) cudaEventRecord(mid, st);
     if constexpr (NV) {   // h (fp32) -> four terms with E4M3 scales per 16 under a scale per (term, row)
-        launch_pdl(quant_rows_nv<false>, dim3((unsigned)a.rows), dim3(128), 0, st, (const __nv_bfloat16 *)nullptr,
+        launch_pdl(quant_rows_nv<false>, dim3((unsigned)std::min(a.rows, 4 * num_sms)), dim3(128), 0, st,
+                   (const __nv_bfloat16 *)nullptr,
                    (const float *)a.hf, (const int32_t *)nullptr, a.off + a.E, a.I, a.I_s, a.I_max, a.rows, a.I_max,
                    a.hq, a.hqs, a.hg);
         ++n;
@@ -1160,8 +1183,9 @@ bool nv4_supported(const FfnArgs &a) {
     return mx4_supported(a) && a.H <= 8192 && a.I_max <= 8192 && a.routed.gu_global && a.routed.d_global;
 }
 
-int launch_quant_x_nv(const FfnArgs &a, cudaStream_t st) {
-    launch_pdl(quant_rows_nv<true>, dim3((unsigned)a.rows), dim3(128), 0, st, a.x, (const float *)nullptr,
+int launch_quant_x_nv(const FfnArgs &a, int num_sms, cudaStream_t st) {
+    launch_pdl(quant_rows_nv<true>, dim3((unsigned)std::min(a.rows, 4 * num_sms)), dim3(128), 0, st, a.x,
+               (const float *)nullptr,
                a.src_token, a.off + a.E, a.H, a.H, a.H, a.rows, a.H, a.xq, a.xqs, a.xg);
     return cudaPeekAtLastError() == cudaSuccess ? 1 : -1;
 }

@@ -98,8 +98,9 @@ router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
 // finished chunk into fp32 registers (round to nearest, chunk order fixed).
 //
 // Roles: warp 0 issues TMA (x as bf16 in the 128-byte swizzled layout the MMA reads; the fp32
-// router rows as two plain 128-byte boxes), warp 1 allocates TMEM and issues the MMAs, warps 2-5
-// split the fp32 rows into the three bf16 planes (swizzled stores, then a proxy fence), warps 6-9
+// router rows as two plain 128-byte boxes), warp 1 allocates TMEM and issues the MMAs, warps 2-9
+// split the fp32 rows into the three bf16 planes (swizzled stores, then a proxy fence; two warps per
+// scheduler, so that one's shared-memory latency hides behind the other's arithmetic), warps 10-13
 // drain the accumulator chunks and write the result: warp w covers tokens 32 (w % 4) .. + 31. Four
 // stages; every wait is bounded (a wait that runs out records kErrWaitRouter and the block winds
 // down).
@@ -107,7 +108,8 @@ router_logits_small(const __nv_bfloat16 *__restrict__ x, int T, int H, const flo
 // gridDim.z splits H into slices of `hs` columns: with one split the block writes sigmoid(logit)
 // to `out` ([T][E]); with several it writes its partial logits to out + z * T * E and
 // router_split_reduce sums them in split order (deterministic) and applies the sigmoid.
-constexpr int kRtM = 128, kRtN = 64, kRtK = 64, kRtNS = 4, kRtThreads = 320, kRtChunk = 2;
+constexpr int kRtM = 128, kRtN = 64, kRtK = 64, kRtNS = 4, kRtThreads = 448, kRtChunk = 2;
+constexpr int kRtConv = 256;                    // plane-splitting threads (warps 2-9)
 constexpr uint32_t kRtX = kRtM * 128;          // 16 KB: 128 tokens x 64 bf16, swizzled
 constexpr uint32_t kRtW = kRtN * 256;          // 16 KB: 64 experts x 64 fp32, two boxes of 32
 constexpr uint32_t kRtP = kRtN * 128;          // 8 KB: one bf16 plane, 64 experts x 64, swizzled
@@ -144,7 +146,7 @@ router_logits_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRtNS; ++s) {
             ptx::mbar_init(ptx::smem_addr(&tma_full[s]), 1);
-            ptx::mbar_init(ptx::smem_addr(&conv_full[s]), 128);
+            ptx::mbar_init(ptx::smem_addr(&conv_full[s]), kRtConv);
             ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -223,17 +225,17 @@ router_logits_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             ptx::mma_commit(ptx::smem_addr(drain));
             ptx::mbar_wait(ptx::smem_addr(drain), 0, nullptr, 0, nullptr);
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + kRtConv / 32) {
         // ---------------------------------------------------------------- plane split
-        const int ct = threadIdx.x - 64;   // 0..127
+        const int ct = threadIdx.x - 64;   // 0..kRtConv-1
         for (int k = 0; k < nk && !*abort_flag; ++k) {
             const int s = k % kRtNS;
             if (!ptx::mbar_wait(ptx::smem_addr(&tma_full[s]), (k / kRtNS) & 1u, err, ptx::kErrWaitRouter, abort_flag))
                 break;
             uint8_t *st = smem + s * kRtStage;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int ci = ct + 128 * i, r = ci >> 3, c = ci & 7;   // expert row r, 8-element chunk c
+            for (int i = 0; i < kRtN * 8 / kRtConv; ++i) {
+                const int ci = ct + kRtConv * i, r = ci >> 3, c = ci & 7;   // expert row r, 8-element chunk c
                 const float4 *src = reinterpret_cast<const float4 *>(st + kRtOffW + (c >> 2) * (kRtW / 2) + r * 128 +
                                                                      (c & 3) * 32);
                 const float4 u = src[0], v = src[1];
