@@ -199,6 +199,16 @@ COLI_API int coli_moe_set_wait_limit(coli_moe_t *h, int64_t ns);
 COLI_API int coli_moe_set_profiling(coli_moe_t *h, int32_t enable);
 COLI_API int coli_moe_stage_times(coli_moe_t *h, float *ms);
 
+/* Test hook for the failure path of coli_moe_create, host only (touches no device). Runs create's
+ * workspace allocation sequence for cfg with a host allocator that fails at allocation number
+ * fail_at (0-based; negative: never), and frees what was allocated the way create does when an
+ * allocation fails (or, when none failed, the way destroy does). Writes the number of allocations
+ * attempted to *allocations and the number of blocks still allocated afterwards to *still_live
+ * (0: nothing leaked). Returns COLI_ERR_OUT_OF_MEMORY when the sequence failed, COLI_OK when it
+ * completed, COLI_ERR_INVALID_ARG for a NULL pointer or a config create would reject outright. */
+COLI_API int coli_moe_test_alloc_failure(const coli_moe_config *cfg, int32_t fail_at, int32_t *allocations,
+                                         int32_t *still_live);
+
 /* Routing with no device allocation. Runs the router of coli_moe_forward (A1: scores, bias-
  * adjusted top-k, renormalised weights) on the given stream and writes idx_out [T][top_k] (int32)
  * and weights_out [T][top_k] (fp32), device pointers owned by the caller, identical to the idx and

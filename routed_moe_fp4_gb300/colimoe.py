@@ -26,7 +26,8 @@ EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "col
             "coli_moe_device_error", "coli_moe_set_wait_limit", "coli_moe_route_static",
             "coli_bank_create", "coli_bank_destroy", "coli_moe_forward_banked", "coli_bank_set_copy_blocks",
             "coli_bank_state", "coli_dense_create", "coli_dense_forward", "coli_dense_destroy",
-            "coli_dense_last_error", "coli_dense_device_error", "coli_moe_forward_nvfp4")
+            "coli_dense_last_error", "coli_dense_device_error", "coli_moe_forward_nvfp4",
+            "coli_moe_test_alloc_failure")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
 
@@ -124,6 +125,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_dense_last_error.restype = C.c_char_p
     lib.coli_dense_device_error.argtypes = [vp, C.POINTER(C.c_int32)]
     lib.coli_dense_device_error.restype = C.c_int
+    lib.coli_moe_test_alloc_failure.argtypes = [C.POINTER(coli_moe_config), C.c_int32, C.POINTER(C.c_int32),
+                                                C.POINTER(C.c_int32)]
+    lib.coli_moe_test_alloc_failure.restype = C.c_int
     _lib = lib
     return lib
 
@@ -225,6 +229,14 @@ def coli_moe_stage_times(h) -> dict:
     buf = (C.c_float * COLI_STAGES)()
     _check(h, load().coli_moe_stage_times(h, buf))
     return dict(zip(STAGE_NAMES, [float(v) for v in buf]))
+
+
+def coli_moe_test_alloc_failure(cfg: coli_moe_config, fail_at: int):
+    """Runs create's workspace allocation on a host allocator failing at allocation `fail_at`;
+    returns (return code, allocations attempted, blocks still allocated after the cleanup)."""
+    n, live = C.c_int32(0), C.c_int32(0)
+    rc = load().coli_moe_test_alloc_failure(C.byref(cfg), fail_at, C.byref(n), C.byref(live))
+    return rc, n.value, live.value
 
 
 def coli_moe_route_static(x_bf16, T: int, H: int, router_w, router_bias, E: int, top_k: int, idx_out,

@@ -2,11 +2,13 @@
 // workspace, and the stream-ordered launch sequence A1 router -> A2 permute -> A3/A4 expert
 // FFN -> A5 combine. No host synchronisation and no allocation inside a forward.
 #include <stdarg.h>
+#include <stdlib.h>
 #include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
 #include <new>
+#include <type_traits>
 
 #include "colimoe_internal.cuh"
 
@@ -46,18 +48,59 @@ void set_err(coli_moe_t *h, const char *fmt, ...) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-void free_ws(Workspace &ws) {
+// Workspace memory goes through this interface, so that the failure path of create (every block
+// allocated so far freed, nothing leaked) can be exercised without a device: the default is
+// cudaMalloc / cudaFree / cudaMemset; coli_moe_test_alloc_failure substitutes a host allocator
+// that fails at a chosen allocation.
+struct WsAllocator {
+    bool (*alloc)(void **p, size_t bytes, void *ctx);
+    void (*release)(void *p, void *ctx);
+    bool (*zero)(void *p, size_t bytes, void *ctx);
+    void *ctx;
+};
+
+bool dev_alloc(void **p, size_t bytes, void *) { return cudaMalloc(p, bytes) == cudaSuccess; }
+void dev_release(void *p, void *) { cudaFree(p); }
+bool dev_zero(void *p, size_t bytes, void *) { return cudaMemset(p, 0, bytes) == cudaSuccess; }
+constexpr WsAllocator kDeviceAllocator{dev_alloc, dev_release, dev_zero, nullptr};
+
+void free_ws(Workspace &ws, const WsAllocator &A = kDeviceAllocator) {
     void *ptrs[] = {ws.xq, ws.xqs, ws.hq, ws.hqs, ws.xg, ws.hg, ws.hf, ws.scores, ws.logit_part, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
                     ws.n_touched, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
                     ws.out_stage, ws.tile_sched};
     for (void *p : ptrs)
-        if (p) cudaFree(p);
+        if (p) A.release(p, A.ctx);
     ws = Workspace();
 }
 
-template <typename T>
-bool alloc(T **p, size_t count) {
-    return cudaMalloc(reinterpret_cast<void **>(p), count * sizeof(T) + 256) == cudaSuccess;
+// Allocates the whole workspace for (max_tokens, max_top_k); on any failure frees what it had
+// allocated and returns false.
+bool alloc_workspace(Workspace &ws, const coli_moe_config &c, int I_max, const WsAllocator &A) {
+    auto alloc = [&](auto **p, size_t count) {
+        void *q = nullptr;
+        if (!A.alloc(&q, count * sizeof(**p) + 256, A.ctx)) return false;
+        *p = static_cast<std::remove_reference_t<decltype(*p)>>(q);
+        return true;
+    };
+    const size_t Tm = c.max_tokens, km = c.max_top_k, E = c.num_experts, H = c.hidden;
+    const size_t rows = Tm * km + Tm;
+    bool ok = alloc(&ws.scores, Tm * E) && alloc(&ws.logit_part, kRouterPartialFloats) && alloc(&ws.idx, Tm * km) &&
+              alloc(&ws.w, Tm * km) && alloc(&ws.inv_row, Tm * km) && alloc(&ws.src_token, rows) &&
+              alloc(&ws.cnt, E + 1) && alloc(&ws.off, E + 2) && alloc(&ws.touched, E + 1) &&
+              alloc(&ws.touched_cost, E + 2) && alloc(&ws.n_touched, 4) && alloc(&ws.h, rows * (size_t)I_max) &&
+              alloc(&ws.y, rows * H) && alloc(&ws.xh, Tm * H) && alloc(&ws.xinv, Tm) &&
+              alloc(&ws.hh, rows * (size_t)I_max) && alloc(&ws.hinv, rows) && alloc(&ws.err, 4) &&
+              alloc(&ws.x_stage, Tm * H) && alloc(&ws.out_stage, Tm * H) && alloc(&ws.xq, 2 * rows * H) &&
+              alloc(&ws.xqs, 4 * rows * (H / 16)) && alloc(&ws.hq, 2 * rows * (size_t)I_max) &&
+              alloc(&ws.hqs, 4 * rows * (size_t)(I_max / 16)) && alloc(&ws.xg, 4 * rows) && alloc(&ws.hg, 4 * rows) &&
+              alloc(&ws.hf, rows * (size_t)I_max);
+    if (ok) ok = A.zero(ws.err, sizeof(int), A.ctx);
+    if (ok) {
+        ws.tile_sched_bytes = ntile_layout_ints((int)E, (int)rows) * sizeof(int32_t);
+        ok = A.alloc(&ws.tile_sched, ws.tile_sched_bytes + 256, A.ctx);
+    }
+    if (!ok) free_ws(ws, A);
+    return ok;
 }
 
 bool valid_experts(const coli_mxfp4_experts *e) {
@@ -326,28 +369,9 @@ int coli_moe_create(const coli_moe_config *cfg, void *cuda_stream, coli_moe_t **
     h->device = dev;
     h->num_sms = prop.multiProcessorCount;
     h->I_max = c.inter > c.shared_inter ? c.inter : c.shared_inter;
-    const size_t Tm = c.max_tokens, km = c.max_top_k, E = c.num_experts, H = c.hidden;
-    const size_t rows = Tm * km + Tm;
-    Workspace &ws = h->ws;
-    bool ok = alloc(&ws.scores, Tm * E) && alloc(&ws.logit_part, kRouterPartialFloats) && alloc(&ws.idx, Tm * km) && alloc(&ws.w, Tm * km) &&
-              alloc(&ws.inv_row, Tm * km) && alloc(&ws.src_token, rows) && alloc(&ws.cnt, E + 1) &&
-              alloc(&ws.off, E + 2) && alloc(&ws.touched, E + 1) && alloc(&ws.touched_cost, E + 2) && alloc(&ws.n_touched, 4) &&
-              alloc(&ws.h, rows * (size_t)h->I_max) && alloc(&ws.y, rows * H) &&
-              alloc(&ws.xh, Tm * H) && alloc(&ws.xinv, Tm) && alloc(&ws.hh, rows * (size_t)h->I_max) &&
-              alloc(&ws.hinv, rows) && alloc(&ws.err, 4) && alloc(&ws.x_stage, Tm * H) &&
-              alloc(&ws.out_stage, Tm * H);
-    if (ok)
-        ok = alloc(&ws.xq, 2 * rows * H) && alloc(&ws.xqs, 4 * rows * (H / 16)) &&
-             alloc(&ws.hq, 2 * rows * (size_t)h->I_max) && alloc(&ws.hqs, 4 * rows * (size_t)(h->I_max / 16)) &&
-             alloc(&ws.xg, 4 * rows) && alloc(&ws.hg, 4 * rows) && alloc(&ws.hf, rows * (size_t)h->I_max);
-    if (ok) ok = cudaMemset(ws.err, 0, sizeof(int)) == cudaSuccess;
-    if (ok) {
-        ws.tile_sched_bytes = ntile_layout_ints((int)E, (int)rows) * sizeof(int32_t);
-        ok = cudaMalloc(&ws.tile_sched, ws.tile_sched_bytes + 256) == cudaSuccess;
-    }
+    const bool ok = alloc_workspace(h->ws, c, h->I_max, kDeviceAllocator);
     if (!ok) {
         cudaGetLastError();
-        free_ws(ws);
         delete h;
         set_err(nullptr, "workspace allocation failed (max_tokens=%d, max_top_k=%d)", c.max_tokens, c.max_top_k);
         return COLI_ERR_OUT_OF_MEMORY;
@@ -509,6 +533,41 @@ int coli_moe_stage_times(coli_moe_t *h, float *ms) {
         }
     }
     return COLI_OK;
+}
+
+namespace {
+// Host stand-in for the device allocator: malloc / free, failing at allocation number fail_at.
+struct FakeAllocs {
+    int fail_at, count = 0, live = 0, peak = 0;
+};
+bool fake_alloc(void **p, size_t bytes, void *ctx) {
+    FakeAllocs &f = *static_cast<FakeAllocs *>(ctx);
+    if (f.count++ == f.fail_at) return false;
+    *p = malloc(16);   // only the bookkeeping matters: no workspace byte is touched
+    if (!*p) return false;
+    f.peak = ++f.live > f.peak ? f.live : f.peak;
+    return true;
+}
+void fake_release(void *p, void *ctx) {
+    --static_cast<FakeAllocs *>(ctx)->live;
+    free(p);
+}
+bool fake_zero(void *, size_t, void *) { return true; }
+}  // namespace
+
+int coli_moe_test_alloc_failure(const coli_moe_config *cfg, int32_t fail_at, int32_t *allocations,
+                                int32_t *still_live) {
+    if (!cfg || !allocations || !still_live || cfg->num_experts < 1 || cfg->max_tokens < 1 || cfg->max_top_k < 1 ||
+        cfg->hidden < 128 || cfg->inter < 128)
+        return COLI_ERR_INVALID_ARG;
+    FakeAllocs f{fail_at};
+    Workspace ws;
+    const int I_max = cfg->inter > cfg->shared_inter ? cfg->inter : cfg->shared_inter;
+    const bool ok = alloc_workspace(ws, *cfg, I_max, WsAllocator{fake_alloc, fake_release, fake_zero, &f});
+    *allocations = f.count;
+    if (ok) free_ws(ws, WsAllocator{fake_alloc, fake_release, fake_zero, &f});
+    *still_live = f.live;
+    return ok ? COLI_OK : COLI_ERR_OUT_OF_MEMORY;
 }
 
 }  // extern "C"

@@ -130,6 +130,22 @@ __device__ __forceinline__ TileInfo decode_tile(const Mx4Params &p, int t, int2 
     ti.wide = !NV && p.mode == kDown && ti.box == 0 && !BIG;
     ti.kst = ti.wide ? 2 * BK : BK;
     ti.nk = (ti.K + ti.kst - 1) / ti.kst;
+#ifdef COLI_BOUNDS_CHECK
+    // Debug build: a tile whose records would reach outside the buffers is recorded (kErrBounds)
+    // and skipped by every role alike (all of them decode the same records), never trapped. The
+    // weight rows of an m-tile must lie inside its expert's matrix; the activation rows inside
+    // the rows the permutation laid out; the group inside the experts plus the shared one.
+    if (ti.valid && ti.n_valid > 0) {   // n_valid 0: the zero record of an index past the last tile
+        const bool gu = p.mode == kGateUp;
+        const int mrows = BIG && !gu ? 2 * BM : BM;
+        const bool bad = ti.g > p.E || ti.n_valid < 1 || ti.n_valid > ti.bh || ti.row0 < 0 ||
+                         ti.row0 + ti.n_valid > p.rows || (gu ? ti.mt * BM + BM > ti.Ig : ti.mt * mrows + mrows > p.H);
+        if (bad) {
+            ptx::record_error(p.err, ptx::kErrBounds);
+            ti.valid = false;
+        }
+    }
+#endif
     return ti;
 }
 

@@ -19,6 +19,7 @@ enum : int {
     kErrWaitMma = 3,       // waited too long for an MMA commit
     kErrWaitAccum = 4,     // epilogue waited too long for an accumulator
     kErrWaitRouter = 5,    // the tensor-core router logits kernel waited too long (any of its waits)
+    kErrBounds = 7,        // bounds-checked build only: a tile record pointed outside the buffers
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s

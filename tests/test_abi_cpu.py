@@ -171,3 +171,23 @@ def test_route_static_checks_arguments_before_the_device(lib):
     import torch
     if not torch.cuda.is_available():
         assert call() in (cm.COLI_ERR_CUDA, cm.COLI_ERR_UNSUPPORTED_ARCH)
+
+
+def test_create_frees_everything_when_any_allocation_fails():
+    """The workspace allocation of coli_moe_create, run on a host allocator that fails at each
+    allocation in turn: every failure returns COLI_ERR_OUT_OF_MEMORY with nothing left allocated,
+    and the sequence without a failure completes and frees every block."""
+    from routed_moe_fp4_gb300 import build, colimoe as cm
+    build.build()
+    for cfg in (cm.coli_moe_config(256, 4096, 2048, 2048, 8, 8), cm.coli_moe_config(8, 256, 128, 0, 1, 2)):
+        rc, n, live = cm.coli_moe_test_alloc_failure(cfg, -1)
+        assert rc == cm.COLI_OK and live == 0 and n > 20
+        for k in range(n):
+            rc_k, n_k, live_k = cm.coli_moe_test_alloc_failure(cfg, k)
+            assert rc_k == cm.COLI_ERR_OUT_OF_MEMORY, k
+            assert n_k == k + 1, (k, n_k)        # nothing is allocated after the failing call
+            assert live_k == 0, (k, live_k)       # everything allocated before it was freed
+        rc, n2, live = cm.coli_moe_test_alloc_failure(cfg, n)
+        assert rc == cm.COLI_OK and n2 == n and live == 0
+    bad = cm.coli_moe_config(0, 4096, 2048, 2048, 8, 8)
+    assert cm.coli_moe_test_alloc_failure(bad, 0)[0] == cm.COLI_ERR_INVALID_ARG
