@@ -62,6 +62,19 @@ template <bool BIG> constexpr uint32_t stage_bytes() { return 2 * kASmem + kTerm
 // too small to hold the scale loaders' sectors between stages.
 template <bool BIG> constexpr int num_stages() { return BIG ? 3 : 4; }
 template <bool BIG> constexpr size_t smem_bytes() { return num_stages<BIG>() * (size_t)stage_bytes<BIG>() + 1024 + 256; }
+// Scales by TMA (SFT): each stage also holds the 16-byte chunk of every scale row it reads (the
+// stage's 8 scale bytes lie in it; a 512-K stage reads all 16): two weight matrices x 128 rows,
+// then the activation rows as [term][row], after the terms.
+constexpr uint32_t kScW = 2 * BM * 16;   // weight-scale chunks of a stage
+template <bool BIG> constexpr uint32_t sc_off() { return stage_bytes<BIG>(); }
+template <bool BIG> constexpr uint32_t stage_bytes_sft() {
+    return stage_bytes<BIG>() + kScW + kTerms * (BIG ? kBnBig : 32) * 16;
+}
+template <bool BIG> constexpr size_t smem_bytes_sft() {
+    return num_stages<BIG>() * (size_t)stage_bytes_sft<BIG>() + 1024 + 256;
+}
+static_assert(stage_bytes_sft<false>() % 1024 == 0 && stage_bytes_sft<true>() % 1024 == 0, "1 KB-aligned stages");
+static_assert(smem_bytes_sft<false>() <= 232448 && smem_bytes_sft<true>() <= 232448, "shared memory per block");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = 128;             // per accumulator buffer (two buffers; big tiles: one)
 // Scale-factor columns, 32 per stage (64 for NVFP4): after the two 128-column accumulator buffers,
@@ -368,6 +381,44 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Writes one stage's scale words of this loader lane to TMEM at column `col` of its lane quarter.
+// NVFP4: A0 words at +4w, A1 at +16 + 4w, activation words at +32 + 4w. Lane 32q + i reads only
+// column 4w + q of a weight group, so each word is written to all four columns of its group: one
+// 16-column store per operand. MXFP4: weight words 0-3 (a0 then a1; in a wide stage a1 holds
+// words 2-3) at +4w, each written to its whole 4-column group; the activation words of column
+// group c at +16 + 4w + c (a wide stage's words 2-3 at +24 + 4w + c); big tiles: activation word
+// w of column group c at +16 + 8w + c (c < 6). Columns a stage does not use take any value.
+template <bool NV, bool BIG>
+__device__ __forceinline__ void store_sf_stage(uint32_t col, const SfStageT<NV, BIG> &w, int n_a) {
+    uint32_t r[16];
+    if constexpr (NV) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = w.a0[j >> 2];
+        tmem_st_x16(col, r);
+        if (n_a > 1) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = w.a1[j >> 2];
+            tmem_st_x16(col + 16, r);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = w.b[j & 3][j >> 2];
+        tmem_st_x16(col + 32, r);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = j < 8 ? w.a0[(j >> 2) & 1] : w.a1[(j >> 2) & 1];
+        tmem_st_x16(col, r);
+        if constexpr (BIG) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = (j & 7) < 6 ? w.b[j & 7][j >> 3] : 0x7F7F7F7Fu;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                r[j] = j < 8 ? w.b[j & 3][(j >> 2) & 1] : w.b[((j & 3) + 2) & 3][(j >> 2) & 1];
+        }
+        tmem_st_x16(col + 16, r);
+    }
+}
+
 // Largest of 32 non-negative floats across the warp: their bit patterns order like unsigned
 // integers, so one integer warp reduction serves.
 __device__ __forceinline__ float warp_max_abs(float a) {
@@ -418,11 +469,22 @@ template <bool BIG> struct BMaps4 {
     CUtensorMap m[kTerms][BIG ? 3 : 2];   // [term][box height 16 / 32 / 48]
 };
 
-template <int MODE, bool NV, bool BIG>
+// SFT launches: the weight scales (routed, shared: [rows][K/32] bytes, 16 x 128 boxes) and the
+// activation scales ([kTerms][rows][K/32] bytes, 16 x box height x kTerms boxes, by box height).
+template <bool BIG> struct ScMaps {
+    CUtensorMap w_routed, w_shared, act[BIG ? 3 : 2];
+};
+
+// SFT: the scale bytes come by TMA with each stage (ScMaps), and the scale loaders read them from
+// shared memory; otherwise the loaders fetch them from global memory, stages ahead.
+template <int MODE, bool NV, bool BIG, bool SFT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
-         const __grid_constant__ BMaps4<BIG> tm_b, const Mx4Params p, const __grid_constant__ NvParams q) {
-    constexpr uint32_t kStageBytes = stage_bytes<BIG>(), kSfCol0 = sf_col0<BIG>();
+         const __grid_constant__ BMaps4<BIG> tm_b, const Mx4Params p, const __grid_constant__ NvParams q,
+         const __grid_constant__ ScMaps<BIG> tm_sc) {
+    static_assert(!SFT || !NV, "scales by TMA: MXFP4 launches");
+    constexpr uint32_t kStageBytes = SFT ? stage_bytes_sft<BIG>() : stage_bytes<BIG>(), kSfCol0 = sf_col0<BIG>();
+    constexpr uint32_t kOffSc = sc_off<BIG>();
     constexpr int NS = num_stages<BIG>();
     // The kernel before this one in the stream (quant_x4_rows, or the gate/up launch before the
     // down launch) signals its dependents only after its own dependency wait, so every kernel up
@@ -482,10 +544,21 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
                 const int x0 = k * (ti.kst / 2);                      // byte offset along K
                 const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;   // second K chunk
-                ptx::mbar_arrive_expect_tx(fb, (n_a == 2 || two ? 2 : 1) * kASmem + (two ? 2 : 1) * bbytes);
+                // SFT: the scale chunks of the weight rows (one per matrix) and of the activation
+                // rows (one box of kTerms x bh rows), 16 bytes each
+                // SFT: the scale chunks of the weight rows (one per matrix) and of the activation
+                // rows (one box of kTerms x bh rows), 16 bytes each, on the same barrier
+                const uint32_t scbytes = SFT ? n_a * BM * 16 + kTerms * ti.bh * 16 : 0;
+                ptx::mbar_arrive_expect_tx(fb, (n_a == 2 || two ? 2 : 1) * kASmem + (two ? 2 : 1) * bbytes + scbytes);
                 ptx::tma_load_2d_hint(st + kOffA0, ta, x0, arow, fb, pol);
                 if (n_a == 2) ptx::tma_load_2d_hint(st + kOffA1, ta, x0, arow + (gu ? ti.Ig : BM), fb, pol);
                 if (two) ptx::tma_load_2d_hint(st + kOffA1, ta, x0 + BK / 2, arow, fb, pol);
+                if constexpr (SFT) {   // byte offset of the stage's chunk along a scale row
+                    const CUtensorMap *tw = ti.shared ? &tm_sc.w_shared : &tm_sc.w_routed;
+                    const int xs = ti.wide ? k * 16 : (k * 8) & ~15;
+                    ptx::tma_load_2d(st + kOffSc, tw, xs, arow, fb);
+                    if (n_a == 2) ptx::tma_load_2d(st + kOffSc + BM * 16, tw, xs, arow + (gu ? ti.Ig : BM), fb);
+                }
             };
             auto issue_b = [&](const TileInfo &ti, int k, int s) {
                 const uint32_t bbytes = kTerms * ti.bh * (BK / 2);
@@ -493,6 +566,9 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 const uint32_t st = ptx::smem_addr(smem + s * kStageBytes);
                 const int x0 = k * (ti.kst / 2);
                 const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;
+                if constexpr (SFT)   // the activation rows' scale chunks, [term][row]
+                    ptx::tma_load_3d(st + kOffSc + kScW, &tm_sc.act[ti.box], ti.wide ? k * 16 : (k * 8) & ~15,
+                                     ti.row0, 0, fb);
 #pragma unroll
                 for (int tt = 0; tt < kTerms; ++tt) {
                     ptx::tma_load_2d(st + kOffB + tt * ti.bh * (BK / 2), &tm_b.m[tt][ti.box], x0, ti.row0, fb);
@@ -627,6 +703,75 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
             ptx::mma_commit(ptx::smem_addr(drain));
             ptx::mbar_wait(ptx::smem_addr(drain), 0, nullptr, 0, nullptr);
         }
+    } else if (warp < 6 && SFT) {
+        // ------------------------------------------------------------------ scale loaders (SFT)
+        // Each stage's scale chunks arrive by TMA with its weights: once the stage has landed,
+        // this lane takes its weight row's words (row quad * 32 + lane of each matrix) and those
+        // of activation columns lane + 32c from shared memory, and writes them to the stage's TMEM
+        // scale columns. (The TMA into a slot is issued only after the MMAs that read the slot's
+        // previous scale columns have completed.)
+        const int quad = warp & 3, m = quad * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+        uint32_t it = 0;
+        bool run = true;
+        int2 rec = tile_rec(p, blockIdx.x, total_tiles);
+        for (int t = blockIdx.x; t < total_tiles && run; t += gridDim.x) {
+            const int2 cur = rec;
+            rec = tile_rec(p, t + gridDim.x, total_tiles);
+            const TileInfo ti = decode_tile<NV, BIG>(p, t, cur);
+            if (!ti.valid) continue;
+            for (int k = 0; k < ti.nk; ++k, ++it) {
+                const int s = it % NS;
+                // warp-uniform: the TMEM stores below are warp-wide
+                if (__any_sync(0xffffffffu, *abort_flag != 0) ||
+                    !__all_sync(0xffffffffu, ptx::mbar_wait(ptx::smem_addr(&tma_full[s]), (it / NS) & 1u, p.err,
+                                                             ptx::kErrWaitFull, abort_flag, p.wait_ns))) {
+                    run = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint8_t *sc = smem + s * kStageBytes + kOffSc;
+                const uint8_t *sa = sc + kScW;
+                SfStageT<NV, BIG> w;
+                if (ti.wide) {   // 16 bytes per row: words 0-1 and 2-3
+                    const uint4 a = *reinterpret_cast<const uint4 *>(sc + m * 16);
+                    w.a0[0] = a.x;
+                    w.a0[1] = a.y;
+                    w.a1[0] = a.z;
+                    w.a1[1] = a.w;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(sa + (lane + 32 * c) * 16);
+                        w.b[c][0] = v.x;
+                        w.b[c][1] = v.y;
+                        w.b[c + 2][0] = v.z;
+                        w.b[c + 2][1] = v.w;
+                    }
+                } else {         // the stage's 8 bytes: the chunk's half k & 1
+                    const int h = (k & 1) * 8;
+                    const uint2 a0 = *reinterpret_cast<const uint2 *>(sc + m * 16 + h);
+                    w.a0[0] = a0.x;
+                    w.a0[1] = a0.y;
+                    if (n_a > 1) {
+                        const uint2 a1 = *reinterpret_cast<const uint2 *>(sc + BM * 16 + m * 16 + h);
+                        w.a1[0] = a1.x;
+                        w.a1[1] = a1.y;
+                    } else {
+                        w.a1[0] = w.a1[1] = 0x7F7F7F7Fu;
+                    }
+#pragma unroll
+                    for (int c = 0; c < SfStageT<NV, BIG>::C; ++c) {
+                        const uint2 v = *reinterpret_cast<const uint2 *>(sa + (lane + 32 * c) * 16 + h);
+                        w.b[c][0] = v.x;
+                        w.b[c][1] = v.y;
+                    }
+                }
+                store_sf_stage<NV, BIG>(lane_base + kSfCol0 + s * kSfStage, w, n_a);
+                tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
+            }
+        }
     } else if (warp < 6) {
         // ------------------------------------------------------------------ scale loaders
         // The scale words of stage it + kSfAhead are fetched while stage it is stored, so the
@@ -672,42 +817,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                     continue;
                 }
                 ptx::tc_fence_after();
-                const uint32_t col = lane_base + kSfCol0 + s * (NV ? kSfStageNv : kSfStage);
-                if constexpr (NV) {   // A0 words at +4w, A1 at +16 + 4w, activation words at +32 + 4w
-                    // Lane 32q + i reads only column 4w + q of a weight group, so each word is
-                    // written to all four columns of its group: one 16-column store per operand.
-                    uint32_t r[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = ring[d].a0[j >> 2];
-                    tmem_st_x16(col, r);
-                    if (n_a > 1) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) r[j] = ring[d].a1[j >> 2];
-                        tmem_st_x16(col + 16, r);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = ring[d].b[j & 3][j >> 2];
-                    tmem_st_x16(col + 32, r);
-                } else {
-                    // Weight words 0-3 (a0 then a1; in a wide stage a1 holds words 2-3) at +4w, each
-                    // written to its whole 4-column group (lane 32q + i reads column 4w + q); the
-                    // activation words of column group c at +16 + 4w + c (a wide stage's words 2-3
-                    // at +24 + 4w + c). Columns a stage does not use take any value.
-                    // Big tiles: activation word w of column group c at +16 + 8w + c (c < 6).
-                    uint32_t r[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) r[j] = j < 8 ? ring[d].a0[(j >> 2) & 1] : ring[d].a1[(j >> 2) & 1];
-                    tmem_st_x16(col, r);
-                    if constexpr (BIG) {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) r[j] = (j & 7) < 6 ? ring[d].b[j & 7][j >> 3] : 0x7F7F7F7Fu;
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            r[j] = j < 8 ? ring[d].b[j & 3][(j >> 2) & 1] : ring[d].b[((j & 3) + 2) & 3][(j >> 2) & 1];
-                    }
-                    tmem_st_x16(col + 16, r);
-                }
+                store_sf_stage<NV, BIG>(lane_base + kSfCol0 + s * (NV ? kSfStageNv : kSfStage), ring[d], n_a);
                 tmem_st_wait();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
@@ -1056,6 +1166,47 @@ bool map_packed(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale bytes [rows][K/32] (weights) in 16-byte x 128-row boxes: one chunk per row and stage.
+bool map_w_scales(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows) {
+    auto enc = encoder();
+    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || (K / 32) % 16) return false;
+    const cuuint64_t dims[2] = {K / 32, rows};
+    const cuuint64_t strides[1] = {K / 32};
+    const cuuint32_t box[2] = {16, BM};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Activation scale bytes [kTerms][rows][K/32] in boxes of 16 bytes x box_rows x kTerms: one chunk
+// per column of a stage's B operand, term by term. Rows past the last read as zero.
+bool map_act_scales(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+    auto enc = encoder();
+    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || (K / 32) % 16) return false;
+    const cuuint64_t dims[3] = {K / 32, rows, kTerms};
+    const cuuint64_t strides[2] = {K / 32, rows * (K / 32)};
+    const cuuint32_t box[3] = {16, box_rows, kTerms};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool BIG>
+bool map_sc(ScMaps<BIG> &m, const void *w_routed, uint64_t K_routed, uint64_t rows_routed, const void *w_shared,
+            uint64_t K_shared, uint64_t rows_shared, const void *act, uint64_t K_act, uint64_t rows_act) {
+    if (!map_w_scales(&m.w_routed, w_routed, K_routed, rows_routed)) return false;
+    if (w_shared) {
+        if (!map_w_scales(&m.w_shared, w_shared, K_shared, rows_shared)) return false;
+    } else {
+        m.w_shared = m.w_routed;
+    }
+    for (int h = 0; h < (BIG ? 3 : 2); ++h)
+        if (!map_act_scales(&m.act[h], act, K_act, rows_act, 16u * (h + 1))) return false;
+    return true;
+}
+
 template <bool BIG>
 bool map_terms(BMaps4<BIG> &b, const uint8_t *base, uint64_t K, uint64_t rows) {
     for (int t = 0; t < kTerms; ++t)
@@ -1107,11 +1258,17 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     constexpr size_t smem = smem_bytes<BIG>();
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(gemm_mx4<kGateUp, NV, BIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm_mx4<kGateUp, NV, BIG, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess ||
-            cudaFuncSetAttribute(gemm_mx4<kDown, NV, BIG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(gemm_mx4<kDown, NV, BIG, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return -1;
+        if constexpr (!NV)
+            if (cudaFuncSetAttribute(gemm_mx4<kGateUp, false, BIG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes_sft<BIG>()) != cudaSuccess ||
+                cudaFuncSetAttribute(gemm_mx4<kDown, false, BIG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes_sft<BIG>()) != cudaSuccess)
+                return -1;
         attr = true;
     }
     Mx4Params p{};
@@ -1153,7 +1310,25 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     if (a.shared.gu_codes) ok = ok && map_packed(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV, BIG>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q);
+    // Scales by TMA whenever every scale row is a whole number of 16-byte chunks (MXFP4; H, I,
+    // I_s and I_max multiples of 512), else loaded by the scale warps themselves; and for the
+    // 32-token gate/up tiles the warps' own loads too, which measured faster there (512 tokens:
+    // 440 against 463 us), while TMA-fed scales were faster for every other tile shape.
+    ScMaps<BIG> sc{};
+    bool sft = false, sft_gu = false;
+    if constexpr (!NV) {
+        sft = a.H % 512 == 0 && a.I % 512 == 0 && a.I_max % 512 == 0 && (!a.shared.gu_codes || a.I_s % 512 == 0);
+        sft_gu = sft && (BIG || !gu32);
+        if (sft_gu && !map_sc(sc, a.routed.gu_scales, a.H, slots * 2 * a.I, a.shared.gu_codes ? a.shared.gu_scales : nullptr,
+                           a.H, 2 * (uint64_t)a.I_s, a.xqs, a.H, a.rows))
+            return -2;
+        if (sft_gu)
+            launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, false, BIG, true>, grid, dim3(kThreads), smem_bytes_sft<BIG>(),
+                     st, tar, tas, tb, p, q, sc);
+    }
+    if (!sft_gu)
+        launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV, BIG, false>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q,
+                 sc);
     int n = 1;
     if (mid) cudaEventRecord(mid, st);
     if constexpr (NV) {   // h (fp32) -> four terms with E4M3 scales per 16 under a scale per (term, row)
@@ -1181,7 +1356,16 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
     else tas = tar;
     if (!ok) return -2;
-    launch_pdl(gemm_mx4<kDown, NV, BIG>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q);
+    if constexpr (!NV) {
+        if (sft) {
+            if (!map_sc(sc, a.routed.d_scales, a.I, slots * a.H, a.shared.d_codes ? a.shared.d_scales : nullptr, a.I_s,
+                        (uint64_t)a.H, a.hqs, a.I_max, a.rows))
+                return -2;
+            launch_pdl(gemm_mx4<kDown, false, BIG, true>, grid, dim3(kThreads), smem_bytes_sft<BIG>(), st, tar, tas, tb,
+                       p, q, sc);
+        }
+    }
+    if (!sft) launch_pdl(gemm_mx4<kDown, NV, BIG, false>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q, sc);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }

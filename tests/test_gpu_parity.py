@@ -161,10 +161,17 @@ def test_ffn_paths(oracle, name, path):
     _custom("gemm_noshared", I_s=0),
     _custom("gemm_many_rows", T=300, E=4, top_k=2),
     _custom("gemm_half_stages", T=21, H=640, I=384, I_s=256, E=12, top_k=3),
+    # a small batch (x terms per token) with 32-token gate/up tiles: the shared expert's 40 rows
+    # take one 32-row and one 16-row box
+    _custom("gemm_small_gu32", T=40, H=512, E=8, top_k=8, I=256, I_s=256),
     # 48 or more rows per expert on average with H a multiple of 256: both launches take 48-token
     # tiles with two weight matrices each (ragged last tiles, a wider shared expert, K = 3 x 256)
     _custom("big_ragged", T=200, H=512, E=8, top_k=2, I=256, I_s=384),
     _custom("big_many_rows", T=400, H=768, E=6, top_k=3, I=384, I_s=128),
+    # H, I and I_s multiples of 512: the scale bytes come by TMA with each stage, for big tiles
+    # and for small ones with a shared expert twice as wide as the routed ones
+    _custom("sft_big", T=200, H=512, E=8, top_k=2, I=512, I_s=512),
+    _custom("sft_shared_wider", T=21, H=512, E=12, top_k=3, I=512, I_s=1024),
 ], ids=lambda w: w.name)
 @pytest.mark.parametrize("path", [MXF4, GEMV], ids=["mxf4", "gemv"])
 def test_gemm_edge_cases(oracle, wl, path):
