@@ -889,6 +889,9 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                         if (!gu) {            // two 128-row blocks of the down output
                             p.y[row * p.H + mrow] = s0[gi][j];
                             p.y[row * p.H + mrow + BM] = s1[gi][j];
+                        } else if (q.hf) {    // h in fp32; quant_h_rows makes its terms
+                            const float g = s0[gi][j];
+                            q.hf[row * p.I_max + mrow] = __fdiv_rn(g, 1.0f + expf(-g)) * s1[gi][j];
                         } else {
                             finish_h(s0[gi][j], s1[gi][j], row, mrow, lane, p.hq, p.hs, p.rows, p.I_max);
                         }
@@ -937,7 +940,9 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                         else p.y[row * p.H + mrow] = v0[j];
                         continue;
                     }
-                    if constexpr (NV) {   // h in fp32; the next kernel splits it into terms
+                    // h in fp32, and the next kernel splits it into terms: NVFP4, and MXFP4 launches
+                    // with 32-token tiles (the MXFP4 instantiation that takes them holds the code)
+                    if (NV || (!SFT && q.hf)) {
                         const float g = v0[j] * wg, u = v1[j] * wg;
                         q.hf[row * p.I_max + mrow] = __fdiv_rn(g, 1.0f + expf(-g)) * u;
                         continue;
@@ -1027,6 +1032,57 @@ quant_x4_rows(const __nv_bfloat16 *__restrict__ x, int H, const int32_t *__restr
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x)
         quant_x4_block(x, H, src_token, rows, xq, xs, (int)(i / nb), (int)(i % nb));
 }
+// h rows (fp32, [rows][I_max], from a gate/up launch with 32-token or big tiles) -> four E2M1
+// terms with UE8M0 scales per 32 elements, the values the fused epilogue makes for the other
+// launches (the same scale bytes and codes from the same fp32 h). One thread per (row, 32-element
+// block) of a resident grid; routed rows hold I values, the shared expert's rows (from off[E]
+// on) I_s, and blocks past a row's width are never read. Moving this work out of the gate/up
+// epilogue measured 28 % off that launch with big tiles (the epilogue warps had become its
+// bound) and 10 % with 32-token tiles.
+__global__ void __launch_bounds__(256)
+quant_h_rows(const float *__restrict__ hf, const int32_t *__restrict__ off_shared, int I, int I_s, int I_max,
+             int rows, uint8_t *__restrict__ hq, uint8_t *__restrict__ hs) {
+    // signals the down GEMM only after the wait: it reads tile records before its own wait
+    pdl_wait();
+    pdl_trigger();
+    const int nb = I_max / 32, shared0 = *off_shared;
+    const long n = (long)rows * nb;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+        const int row = (int)(i / nb), b = (int)(i % nb);
+        if (b * 32 >= (row >= shared0 ? I_s : I)) continue;
+        const float4 *src = reinterpret_cast<const float4 *>(hf + (size_t)row * I_max + b * 32);
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 f = src[q];
+            v[4 * q] = f.x;
+            v[4 * q + 1] = f.y;
+            v[4 * q + 2] = f.z;
+            v[4 * q + 3] = f.w;
+        }
+#pragma unroll
+        for (int tt = 0; tt < kTerms; ++tt) {
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) amax = fmaxf(amax, fabsf(v[e]));
+            const uint32_t sb = e2m1_scale_byte(amax);
+            const float scale = __uint_as_float(sb << 23), inv = __uint_as_float((254u - sb) << 23);
+            uint32_t packed[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float blo, bhi;
+                const uint32_t byte = e2m1_pair(v[e] * inv, v[e + 1] * inv, blo, bhi);
+                v[e] -= blo * scale;
+                v[e + 1] -= bhi * scale;
+                packed[e / 8] |= byte << (8 * ((e / 2) % 4));
+            }
+            *reinterpret_cast<uint4 *>(hq + ((size_t)tt * rows + row) * (I_max / 2) + b * 16) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            hs[((size_t)tt * rows + row) * nb + b] = (uint8_t)sb;
+        }
+    }
+}
+
 // NVFP4 activation terms: rows -> four E2M1 terms, each with an E4M3 scale per 16 elements under
 // a power-of-two scale per (term, row): G = 2^ceil(log2(max|v| / (6 * 448))) keeps every group's
 // scale max|v_group| / (6 G), rounded up to an E4M3 value, within E4M3's range, and |v| / (scale
@@ -1284,14 +1340,17 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     p.y = a.y;
     p.err = a.err;
     NvParams q{};
-    q.hf = a.hf;
+    // gate/up with 32-token or big tiles writes fp32 h, and quant_h_rows makes its terms (not in
+    // an expert bank's rounds, each of which computes only its own rows)
+    const bool gu32 = BIG || (long)a.T * a.top_k >= 16L * a.E;
+    const bool split_h = !NV && gu32 && !a.tiles;
+    q.hf = NV || split_h ? a.hf : nullptr;
     CUtensorMap tar, tas;
     BMaps4<BIG> tb;
     // gate/up
     // Many tokens per expert: gate/up tiles of 32 tokens (N = 128 per matrix, half the MMAs per
     // token) with one accumulator buffer (gate + up fill 256 TMEM columns); more still: big tiles
     // of 48 tokens for both launches (the permutation then lays out 48-row tiles as its large ones).
-    const bool gu32 = BIG || (long)a.T * a.top_k >= 16L * a.E;
     p.mode = kGateUp;
     p.bn = BIG ? kBnBig : gu32 ? kBnDown : kBnGateUp;
     p.nbuf = gu32 ? 1 : 2;
@@ -1331,6 +1390,12 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
                  sc);
     int n = 1;
     if (mid) cudaEventRecord(mid, st);
+    if (split_h) {
+        const long items = (long)a.rows * (a.I_max / 32);
+        launch_pdl(quant_h_rows, dim3((unsigned)std::max(1L, std::min((items + 255) / 256, 4L * num_sms))), dim3(256), 0,
+                   st, (const float *)a.hf, a.off + a.E, a.I, a.I_s, a.I_max, a.rows, a.hq, a.hqs);
+        ++n;
+    }
     if constexpr (NV) {   // h (fp32) -> four terms with E4M3 scales per 16 under a scale per (term, row)
         launch_pdl(quant_rows_nv<false>, dim3((unsigned)std::min(a.rows, 4 * num_sms)), dim3(128), 0, st,
                    (const __nv_bfloat16 *)nullptr,
