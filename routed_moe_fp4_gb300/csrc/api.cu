@@ -218,6 +218,7 @@ FfnArgs ffn_args(coli_moe_t *h, const void *x_bf16, int32_t T, int32_t top_k, in
     a.n_touched = ws.n_touched;
     a.touched_cost = ws.touched_cost;
     a.src_token = ws.src_token;
+    a.inv_row = ws.inv_row;
     a.x = static_cast<const __nv_bfloat16 *>(x_bf16);
     a.xh = ws.xh;
     a.xinv = ws.xinv;

@@ -76,6 +76,7 @@ struct FfnArgs {
     const int32_t *n_touched;
     const int32_t *touched_cost;    // [n_touched + 1] exclusive prefix of per-group cost
     const int32_t *src_token;
+    const int32_t *inv_row;         // [T][k] grouped row of each (token, slot)
     const __nv_bfloat16 *x;         // [T][H] input tokens
     __half *xh;                     // GEMV path: scaled fp16 tokens and inverse scales
     float *xinv;
@@ -103,7 +104,7 @@ struct FfnArgs {
 // pdl_trigger lets the next kernel be scheduled once every block of this one has started;
 // pdl_wait returns when the kernel before this one has completed and its writes are visible.
 // Since every kernel waits, completion of one kernel implies completion of all earlier ones. A
-// kernel that signals only after its own wait (quant_x4_rows, gemm_mx4) starts its dependent only
+// kernel that signals only after its own wait (quant_x4_rows, quant_x4_tokens, gemm_mx4) starts its dependent only
 // once everything before itself has completed; gemm_mx4 relies on that to read the permutation's
 // outputs, and issue weight loads, before its wait.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
