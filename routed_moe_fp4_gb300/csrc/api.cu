@@ -624,6 +624,7 @@ extern "C" int coli_moe_forward_nvfp4(coli_moe_t *h, const void *x_bf16, int32_t
     FfnArgs a = ffn_args(h, x_bf16, T, top_k, rows, nullptr, nullptr);
     a.routed = nv_set(packed);
     a.shared = nv_set(shared);
+    a.pdl_gate_up = T < kSmallRouteTokens;   // as in coli_moe_forward: a plain launch from 64 tokens on
     if (!nv4_supported(a)) {
         set_err(h, "NVFP4 path unavailable (needs a tensor-map encoder, H and I up to 8192)");
         return COLI_ERR_INVALID_ARG;

@@ -482,7 +482,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant__ CUtensorMap tm_a_shared,
          const __grid_constant__ BMaps4<BIG> tm_b, const Mx4Params p, const __grid_constant__ NvParams q,
          const __grid_constant__ ScMaps<BIG> tm_sc) {
-    static_assert(!SFT || !NV, "scales by TMA: MXFP4 launches");
     constexpr uint32_t kStageBytes = SFT ? stage_bytes_sft<BIG>() : stage_bytes<BIG>(), kSfCol0 = sf_col0<BIG>();
     constexpr uint32_t kOffSc = sc_off<BIG>();
     constexpr int NS = num_stages<BIG>();
@@ -555,7 +554,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 if (two) ptx::tma_load_2d_hint(st + kOffA1, ta, x0 + BK / 2, arow, fb, pol);
                 if constexpr (SFT) {   // byte offset of the stage's chunk along a scale row
                     const CUtensorMap *tw = ti.shared ? &tm_sc.w_shared : &tm_sc.w_routed;
-                    const int xs = ti.wide ? k * 16 : (k * 8) & ~15;
+                    const int xs = NV || ti.wide ? k * 16 : (k * 8) & ~15;   // NVFP4: 16 bytes a stage
                     ptx::tma_load_2d(st + kOffSc, tw, xs, arow, fb);
                     if (n_a == 2) ptx::tma_load_2d(st + kOffSc + BM * 16, tw, xs, arow + (gu ? ti.Ig : BM), fb);
                 }
@@ -567,7 +566,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 const int x0 = k * (ti.kst / 2);
                 const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;
                 if constexpr (SFT)   // the activation rows' scale chunks, [term][row]
-                    ptx::tma_load_3d(st + kOffSc + kScW, &tm_sc.act[ti.box], ti.wide ? k * 16 : (k * 8) & ~15,
+                    ptx::tma_load_3d(st + kOffSc + kScW, &tm_sc.act[ti.box], NV || ti.wide ? k * 16 : (k * 8) & ~15,
                                      ti.row0, 0, fb);
 #pragma unroll
                 for (int tt = 0; tt < kTerms; ++tt) {
@@ -733,7 +732,27 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 const uint8_t *sc = smem + s * kStageBytes + kOffSc;
                 const uint8_t *sa = sc + kScW;
                 SfStageT<NV, BIG> w;
-                if (ti.wide) {   // 16 bytes per row: words 0-1 and 2-3
+                if constexpr (NV) {   // four words per row, one per 64-K MMA
+                    const uint4 a0 = *reinterpret_cast<const uint4 *>(sc + m * 16);
+                    const uint4 a1 = n_a > 1 ? *reinterpret_cast<const uint4 *>(sc + BM * 16 + m * 16)
+                                             : make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+                    w.a0[0] = a0.x;
+                    w.a0[1] = a0.y;
+                    w.a0[2] = a0.z;
+                    w.a0[3] = a0.w;
+                    w.a1[0] = a1.x;
+                    w.a1[1] = a1.y;
+                    w.a1[2] = a1.z;
+                    w.a1[3] = a1.w;
+#pragma unroll
+                    for (int c = 0; c < SfStageT<NV, BIG>::C; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(sa + (lane + 32 * c) * 16);
+                        w.b[c][0] = v.x;
+                        w.b[c][1] = v.y;
+                        w.b[c][2] = v.z;
+                        w.b[c][3] = v.w;
+                    }
+                } else if (ti.wide) {   // 16 bytes per row: words 0-1 and 2-3
                     const uint4 a = *reinterpret_cast<const uint4 *>(sc + m * 16);
                     w.a0[0] = a.x;
                     w.a0[1] = a.y;
@@ -766,7 +785,7 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                         w.b[c][1] = v.y;
                     }
                 }
-                store_sf_stage<NV, BIG>(lane_base + kSfCol0 + s * kSfStage, w, n_a);
+                store_sf_stage<NV, BIG>(lane_base + kSfCol0 + s * (NV ? kSfStageNv : kSfStage), w, n_a);
                 tmem_st_wait();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ptx::smem_addr(&sf_full[s]));
@@ -1279,12 +1298,13 @@ bool map_packed(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uin
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Scale bytes [rows][K/32] (weights) in 16-byte x 128-row boxes: one chunk per row and stage.
-bool map_w_scales(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows) {
+// Scale bytes [rows][K/sdiv] (weights; sdiv elements per scale byte, 32 or 16) in 16-byte x
+// 128-row boxes: one chunk per row and stage.
+bool map_w_scales(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, int sdiv) {
     auto enc = encoder();
-    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || (K / 32) % 16) return false;
-    const cuuint64_t dims[2] = {K / 32, rows};
-    const cuuint64_t strides[1] = {K / 32};
+    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || (K / sdiv) % 16) return false;
+    const cuuint64_t dims[2] = {K / sdiv, rows};
+    const cuuint64_t strides[1] = {K / sdiv};
     const cuuint32_t box[2] = {16, BM};
     const cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
@@ -1292,13 +1312,13 @@ bool map_w_scales(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Activation scale bytes [kTerms][rows][K/32] in boxes of 16 bytes x box_rows x kTerms: one chunk
-// per column of a stage's B operand, term by term. Rows past the last read as zero.
-bool map_act_scales(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+// Activation scale bytes [kTerms][rows][K/sdiv] in boxes of 16 bytes x box_rows x kTerms: one
+// chunk per column of a stage's B operand, term by term. Rows past the last read as zero.
+bool map_act_scales(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint32_t box_rows, int sdiv) {
     auto enc = encoder();
-    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || (K / 32) % 16) return false;
-    const cuuint64_t dims[3] = {K / 32, rows, kTerms};
-    const cuuint64_t strides[2] = {K / 32, rows * (K / 32)};
+    if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || (K / sdiv) % 16) return false;
+    const cuuint64_t dims[3] = {K / sdiv, rows, kTerms};
+    const cuuint64_t strides[2] = {K / sdiv, rows * (K / sdiv)};
     const cuuint32_t box[3] = {16, box_rows, kTerms};
     const cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
@@ -1307,16 +1327,17 @@ bool map_act_scales(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows,
 }
 
 template <bool BIG>
-bool map_sc(ScMaps<BIG> &m, const void *w_routed, uint64_t K_routed, uint64_t rows_routed, const void *w_shared,
-            uint64_t K_shared, uint64_t rows_shared, const void *act, uint64_t K_act, uint64_t rows_act) {
-    if (!map_w_scales(&m.w_routed, w_routed, K_routed, rows_routed)) return false;
+bool map_sc(ScMaps<BIG> &m, int sdiv, const void *w_routed, uint64_t K_routed, uint64_t rows_routed,
+            const void *w_shared, uint64_t K_shared, uint64_t rows_shared, const void *act, uint64_t K_act,
+            uint64_t rows_act) {
+    if (!map_w_scales(&m.w_routed, w_routed, K_routed, rows_routed, sdiv)) return false;
     if (w_shared) {
-        if (!map_w_scales(&m.w_shared, w_shared, K_shared, rows_shared)) return false;
+        if (!map_w_scales(&m.w_shared, w_shared, K_shared, rows_shared, sdiv)) return false;
     } else {
         m.w_shared = m.w_routed;
     }
     for (int h = 0; h < (BIG ? 3 : 2); ++h)
-        if (!map_act_scales(&m.act[h], act, K_act, rows_act, 16u * (h + 1))) return false;
+        if (!map_act_scales(&m.act[h], act, K_act, rows_act, 16u * (h + 1), sdiv)) return false;
     return true;
 }
 
@@ -1384,12 +1405,11 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
             cudaFuncSetAttribute(gemm_mx4<kDown, NV, BIG, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return -1;
-        if constexpr (!NV)
-            if (cudaFuncSetAttribute(gemm_mx4<kGateUp, false, BIG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem_bytes_sft<BIG>()) != cudaSuccess ||
-                cudaFuncSetAttribute(gemm_mx4<kDown, false, BIG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)smem_bytes_sft<BIG>()) != cudaSuccess)
-                return -1;
+        if (cudaFuncSetAttribute(gemm_mx4<kGateUp, NV, BIG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes_sft<BIG>()) != cudaSuccess ||
+            cudaFuncSetAttribute(gemm_mx4<kDown, NV, BIG, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes_sft<BIG>()) != cudaSuccess)
+            return -1;
         attr = true;
     }
     Mx4Params p{};
@@ -1434,23 +1454,22 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     if (a.shared.gu_codes) ok = ok && map_packed(&tas, a.shared.gu_codes, a.H, 2 * (uint64_t)a.I_s, BM);
     else tas = tar;
     if (!ok) return -2;
-    // Scales by TMA whenever every scale row is a whole number of 16-byte chunks (MXFP4; H, I,
-    // I_s and I_max multiples of 512), else loaded by the scale warps themselves; and for the
-    // 32-token gate/up tiles the warps' own loads too, which measured faster there (512 tokens:
-    // 440 against 463 us), while TMA-fed scales were faster for every other tile shape.
+    // Scales by TMA whenever every scale row is a whole number of 16-byte chunks (H, I, I_s and
+    // I_max multiples of 512 for MXFP4, of 256 for NVFP4), else loaded by the scale warps
+    // themselves; and for the 32-token gate/up tiles the warps' own loads too, which measured
+    // faster there (512 tokens: 440 against 463 us), while TMA-fed scales were faster for every
+    // other tile shape.
     ScMaps<BIG> sc{};
-    bool sft = false, sft_gu = false;
-    if constexpr (!NV) {
-        sft = a.H % 512 == 0 && a.I % 512 == 0 && a.I_max % 512 == 0 && (!a.shared.gu_codes || a.I_s % 512 == 0);
-        sft_gu = sft && (BIG || !gu32);
-        if (sft_gu && !map_sc(sc, a.routed.gu_scales, a.H, slots * 2 * a.I, a.shared.gu_codes ? a.shared.gu_scales : nullptr,
-                           a.H, 2 * (uint64_t)a.I_s, a.xqs, a.H, a.rows))
-            return -2;
-        if (sft_gu)
-            launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, false, BIG, true>, grid, dim3(kThreads), smem_bytes_sft<BIG>(),
-                     st, tar, tas, tb, p, q, sc);
-    }
-    if (!sft_gu)
+    const int sdiv = NV ? 16 : 32, kq = 16 * sdiv;
+    const bool sft = a.H % kq == 0 && a.I % kq == 0 && a.I_max % kq == 0 && (!a.shared.gu_codes || a.I_s % kq == 0);
+    const bool sft_gu = sft && (BIG || !gu32);
+    if (sft_gu && !map_sc(sc, sdiv, a.routed.gu_scales, a.H, slots * 2 * a.I,
+                          a.shared.gu_codes ? a.shared.gu_scales : nullptr, a.H, 2 * (uint64_t)a.I_s, a.xqs, a.H, a.rows))
+        return -2;
+    if (sft_gu)
+        launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV, BIG, true>, grid, dim3(kThreads), smem_bytes_sft<BIG>(), st, tar,
+                 tas, tb, p, q, sc);
+    else
         launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV, BIG, false>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q,
                  sc);
     int n = 1;
@@ -1486,16 +1505,15 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
     else tas = tar;
     if (!ok) return -2;
-    if constexpr (!NV) {
-        if (sft) {
-            if (!map_sc(sc, a.routed.d_scales, a.I, slots * a.H, a.shared.d_codes ? a.shared.d_scales : nullptr, a.I_s,
-                        (uint64_t)a.H, a.hqs, a.I_max, a.rows))
-                return -2;
-            launch_pdl(gemm_mx4<kDown, false, BIG, true>, grid, dim3(kThreads), smem_bytes_sft<BIG>(), st, tar, tas, tb,
-                       p, q, sc);
-        }
+    if (sft) {
+        if (!map_sc(sc, sdiv, a.routed.d_scales, a.I, slots * a.H, a.shared.d_codes ? a.shared.d_scales : nullptr, a.I_s,
+                    (uint64_t)a.H, a.hqs, a.I_max, a.rows))
+            return -2;
+        launch_pdl(gemm_mx4<kDown, NV, BIG, true>, grid, dim3(kThreads), smem_bytes_sft<BIG>(), st, tar, tas, tb, p, q,
+                   sc);
+    } else {
+        launch_pdl(gemm_mx4<kDown, NV, BIG, false>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q, sc);
     }
-    if (!sft) launch_pdl(gemm_mx4<kDown, NV, BIG, false>, grid, dim3(kThreads), smem, st, tar, tas, tb, p, q, sc);
     ++n;
     return cudaPeekAtLastError() == cudaSuccess ? n : -1;
 }
