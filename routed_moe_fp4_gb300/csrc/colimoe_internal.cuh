@@ -104,8 +104,9 @@ struct FfnArgs {
 // pdl_trigger lets the next kernel be scheduled once every block of this one has started;
 // pdl_wait returns when the kernel before this one has completed and its writes are visible.
 // Since every kernel waits, completion of one kernel implies completion of all earlier ones. A
-// kernel that signals only after its own wait (quant_x4_rows, quant_x4_tokens, gemm_mx4) starts its dependent only
-// once everything before itself has completed; gemm_mx4 relies on that to read the permutation's
+// kernel that signals only after its own wait (the x- and h-term kernels quant_x4_rows,
+// quant_x4_tokens, quant_h_rows and quant_rows_nv, and gemm_mx4) starts its dependent only once
+// everything before itself has completed; gemm_mx4 relies on that to read the permutation's
 // outputs, and issue weight loads, before its wait.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

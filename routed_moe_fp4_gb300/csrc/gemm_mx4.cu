@@ -13,16 +13,20 @@
 //
 // Activations become four E2M1 terms, each with its own UE8M0 scale per 32 elements (the residual
 // of one term is the input of the next): about 2e-4 relative error for Gaussian data, and exact
-// for values with few significant bits. x terms come from quant_x4_tokens; h terms are made in the
-// gate/up epilogue, where a warp holds the 32 consecutive i-values of one scale block. The terms
-// are stacked along N (term t at activation rows [t * bh, (t + 1) * bh)); the epilogue adds them.
+// for values with few significant bits. x terms come from quant_x4_rows (T < 64) or
+// quant_x4_tokens; h terms are made in the gate/up epilogue, where a warp holds the 32 consecutive
+// i-values of one scale block (with 32- and 48-token tiles the epilogue writes fp32 h and
+// quant_h_rows makes them). The terms are stacked along N (term t at activation rows
+// [t * bh, (t + 1) * bh)); the epilogue adds them.
 //
 // Tiles: 128 weight rows (M) x 16 (gate/up) or up to 32 (down) tokens of one group. One persistent
 // block per SM; warp roles: TMA producer (warp 0), TMEM owner and MMA issuer (warp 1), scale
 // loaders (warps 2-5; weight row 32q + i reads its scales from lane 32q + i, column (word) * 4 + q;
 // activation row n from lane 32q + n % 32, column n / 32 of its word, in every lane quarter q; the
-// words of one stage sit 4 columns apart; their loads run four stages ahead), epilogue (warps
-// 6-13: two per lane quarter, taking alternate 8-column groups of the tile's tokens). Four stages,
+// words of one stage sit 4 columns apart; the scale bytes arrive by TMA with each stage when every
+// scale row is a whole number of 16-byte chunks, else the loaders fetch them four stages ahead),
+// epilogue (warps 6-13: two per lane quarter, taking alternate 8-column groups of the tile's
+// tokens). Four stages,
 // double-buffered accumulators, bounded waits. A stage covers 256 K (512 K for down tiles of up to
 // 16 rows, which leave half of the slot free otherwise); the last stage of a K that is not a
 // multiple of it is partial.
@@ -485,8 +489,8 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
     constexpr uint32_t kStageBytes = SFT ? stage_bytes_sft<BIG>() : stage_bytes<BIG>(), kSfCol0 = sf_col0<BIG>();
     constexpr uint32_t kOffSc = sc_off<BIG>();
     constexpr int NS = num_stages<BIG>();
-    // The kernel before this one in the stream (quant_x4_tokens, or the gate/up launch before the
-    // down launch) signals its dependents only after its own dependency wait, so every kernel up
+    // The kernel before this one in the stream (an x- or h-term kernel, or the gate/up launch
+    // before the down launch) signals its dependents only after its own dependency wait, so every kernel up
     // to the permutation has completed when this one starts: its tile records can be read, and the
     // first weight stages issued, before the wait. Activation terms and scales, and all writes,
     // come after it.
