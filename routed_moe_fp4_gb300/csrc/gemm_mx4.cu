@@ -1468,7 +1468,8 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     const bool sft = a.H % kq == 0 && a.I % kq == 0 && a.I_max % kq == 0 && (!a.shared.gu_codes || a.I_s % kq == 0);
     const bool sft_gu = sft && (BIG || !gu32);
     if (sft_gu && !map_sc(sc, sdiv, a.routed.gu_scales, a.H, slots * 2 * a.I,
-                          a.shared.gu_codes ? a.shared.gu_scales : nullptr, a.H, 2 * (uint64_t)a.I_s, a.xqs, a.H, a.rows))
+                          a.shared.gu_codes ? a.shared.gu_scales : nullptr, a.H, 2 * (uint64_t)a.I_s, a.xqs, a.H,
+                          a.rows))
         return -2;
     if (sft_gu)
         launch_k(a.pdl_gate_up, gemm_mx4<kGateUp, NV, BIG, true>, grid, dim3(kThreads), smem_bytes_sft<BIG>(), st, tar,
@@ -1480,8 +1481,9 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     if (mid) cudaEventRecord(mid, st);
     if (split_h) {
         const long items = (long)a.rows * (a.I_max / 32);
-        launch_pdl(quant_h_rows, dim3((unsigned)std::max(1L, std::min((items + 255) / 256, 4L * num_sms))), dim3(256), 0,
-                   st, (const float *)a.hf, a.off + a.E, a.I, a.I_s, a.I_max, a.rows, a.hq, a.hqs);
+        const long blocks = std::max(1L, std::min((items + 255) / 256, 4L * num_sms));   // a resident grid
+        launch_pdl(quant_h_rows, dim3((unsigned)blocks), dim3(256), 0, st, (const float *)a.hf, a.off + a.E, a.I, a.I_s,
+                   a.I_max, a.rows, a.hq, a.hqs);
         ++n;
     }
     if constexpr (NV) {   // h (fp32) -> four terms with E4M3 scales per 16 under a scale per (term, row)
@@ -1510,8 +1512,8 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     else tas = tar;
     if (!ok) return -2;
     if (sft) {
-        if (!map_sc(sc, sdiv, a.routed.d_scales, a.I, slots * a.H, a.shared.d_codes ? a.shared.d_scales : nullptr, a.I_s,
-                    (uint64_t)a.H, a.hqs, a.I_max, a.rows))
+        if (!map_sc(sc, sdiv, a.routed.d_scales, a.I, slots * a.H, a.shared.d_codes ? a.shared.d_scales : nullptr,
+                    a.I_s, (uint64_t)a.H, a.hqs, a.I_max, a.rows))
             return -2;
         launch_pdl(gemm_mx4<kDown, NV, BIG, true>, grid, dim3(kThreads), smem_bytes_sft<BIG>(), st, tar, tas, tb, p, q,
                    sc);
