@@ -1511,6 +1511,39 @@ int launch_ffn_impl(const FfnArgs &a, int num_sms, void *sched, cudaEvent_t mid,
     if (a.shared.d_codes) ok = ok && map_packed(&tas, a.shared.d_codes, a.I_s, (uint64_t)a.H, BM);
     else tas = tar;
     if (!ok) return -2;
+    if constexpr (!NV && !BIG) {
+        // 32-token down tiles: two 128-row blocks of the down matrix share each tile's terms (the
+        // big-tile kernel, its tiles up to 32 rows here), so the terms are read into shared memory
+        // half as often per weight byte
+        if (gu32 && !a.tiles && a.H % (2 * BM) == 0) {
+            static bool attr2 = false;
+            if (!attr2) {
+                if (cudaFuncSetAttribute(gemm_mx4<kDown, false, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_bytes<true>()) != cudaSuccess ||
+                    cudaFuncSetAttribute(gemm_mx4<kDown, false, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_bytes_sft<true>()) != cudaSuccess)
+                    return -1;
+                attr2 = true;
+            }
+            p.nbuf = 1;
+            p.m_tiles = a.H / (2 * BM);
+            BMaps4<true> tb2;
+            ScMaps<true> sc2{};
+            if (!map_terms(tb2, a.hq, a.I_max, a.rows)) return -2;
+            if (sft) {
+                if (!map_sc(sc2, sdiv, a.routed.d_scales, a.I, slots * a.H, a.shared.d_codes ? a.shared.d_scales : nullptr,
+                            a.I_s, (uint64_t)a.H, a.hqs, a.I_max, a.rows))
+                    return -2;
+                launch_pdl(gemm_mx4<kDown, false, true, true>, grid, dim3(kThreads), smem_bytes_sft<true>(), st, tar, tas,
+                           tb2, p, q, sc2);
+            } else {
+                launch_pdl(gemm_mx4<kDown, false, true, false>, grid, dim3(kThreads), smem_bytes<true>(), st, tar, tas,
+                           tb2, p, q, sc2);
+            }
+            ++n;
+            return cudaPeekAtLastError() == cudaSuccess ? n : -1;
+        }
+    }
     if (sft) {
         if (!map_sc(sc, sdiv, a.routed.d_scales, a.I, slots * a.H, a.shared.d_codes ? a.shared.d_scales : nullptr,
                     a.I_s, (uint64_t)a.H, a.hqs, a.I_max, a.rows))
