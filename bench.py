@@ -42,6 +42,25 @@ from routed_moe_fp4_gb300 import synthetic as S  # noqa: E402
 DEFAULT_WORKLOAD = "decode"
 METRIC = "MoE-layer tokens/s at 1 GB300"
 L2_FLUSH_BYTES = 512 << 20
+L2_FLUSH_NOTE = ("flushed before every timed step: a 512 MiB write, then a read of its first 256 MiB, so the "
+                 "flush's own dirty lines are written back before the timed region")
+
+
+def l2_flusher(buf, stream, read: bool = True):
+    """A function that evicts the L2 on `stream`: a write of `buf` (larger than the L2) and, with
+    `read`, a read of its first half. The write alone leaves the L2 full of dirty lines whose
+    write-back then lands inside the next timed region: measured on the decode layer, 173.7 against
+    161.4 us per step, the difference being that write-back, not the layer's work."""
+    import torch
+    half = buf[: buf.numel() // 2]
+    sink = torch.empty(1, dtype=buf.dtype, device=buf.device)
+
+    def flush():
+        with torch.cuda.stream(stream):
+            buf.fill_(1.0)
+            if read:
+                torch.sum(half, dim=0, keepdim=True, out=sink)
+    return flush
 
 
 def _peaks():
@@ -401,9 +420,7 @@ def config_entry(name: str, steps: int, warmup: int, local: int, flush_buf, gemv
     x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
     out = torch.empty_like(x)
 
-    def flush():
-        with torch.cuda.stream(stream):
-            flush_buf.fill_(1.0)
+    flush = l2_flusher(flush_buf, stream)
     hbm_gbs, bf16_tf, kind = _peaks()
     ms, ci = time_steps(layer, x, out, stream, flush, steps, warmup, local)
     routing = layer.routing(wl.T)
@@ -462,10 +479,7 @@ def run_ours(args, wl_name: str) -> dict:
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     x_host = torch.from_numpy(inputs.x.view(np.int16).copy()).pin_memory()
     out_host = torch.empty_like(x_host).pin_memory()
-
-    def l2_flush():
-        with torch.cuda.stream(stream):
-            flush.fill_(1.0)
+    l2_flush = l2_flusher(flush, stream)
 
     # warm-up: the timed steps' sequence, so the flush kernel is loaded before the timed region
     for _ in range(args.warmup):
@@ -496,6 +510,19 @@ def run_ours(args, wl_name: str) -> dict:
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = max_over_ranks(sum(step_ms), device="cuda")
     ms_per_step = total_ms / args.steps
+
+    # the same steps after a write-only flush, outside the timed region: its dirty lines are
+    # written back inside each step (reported beside the timed number, not instead of it)
+    wo_flush = l2_flusher(flush, stream, read=False)
+    wo_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(min(args.steps, 20))]
+    for a, b in wo_ev:
+        wo_flush()
+        a.record(stream)
+        layer.forward(x, out)
+        b.record(stream)
+    torch.cuda.synchronize()
+    wo_ms = sum(a.elapsed_time(b) for a, b in wo_ev) / len(wo_ev)
 
     # stage breakdown (profiled forwards, outside the timed region)
     layer.set_profiling(True)
@@ -571,7 +598,7 @@ def run_ours(args, wl_name: str) -> dict:
                                f"I_s={wl.I_s}, " + ("NVFP4 E2M1 + E4M3/16 + fp32 per matrix" if nv
                                                     else "MXFP4 E2M1 + UE8M0/32"), "tokens_per_gpu": wl.T,
                    "ffn_path": path, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": "flushed (512 MiB write) before every timed step"},
+                   "l2": L2_FLUSH_NOTE},
         "roofline": {"kernel": f"{kernel} (gate/up launch)", "bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
                      "unit": "GB/s", "frac": achieved / hbm_gbs, "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": ab[dom],
@@ -581,6 +608,7 @@ def run_ours(args, wl_name: str) -> dict:
         "stages_ms": stages, "touched_experts": ab["touched_experts"],
         # per-step spread of the timed region on this rank (value and ms_per_step use the mean)
         "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
+        "write_only_flush_ms_per_step": wo_ms,
         "e2e": {"value": tokens / (e2e_step * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_step,
                 "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
         "graph": graph_info,
@@ -639,10 +667,7 @@ def run_bank(args, wl_name: str) -> dict:
           for i in range(n)]
     out = torch.empty_like(xs[0])
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-
-    def l2_flush():
-        with torch.cuda.stream(stream):
-            flush.fill_(1.0)
+    l2_flush = l2_flusher(flush, stream)
 
     for i in range(args.warmup):
         l2_flush()
@@ -703,7 +728,7 @@ def run_bank(args, wl_name: str) -> dict:
                                f"memory, expert bank of {args.bank} device slots",
                    "tokens_per_gpu": wl.T, "ffn_path": "mxf4", "bank_slots": args.bank,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": "flushed (512 MiB write) before every timed step"},
+                   "l2": L2_FLUSH_NOTE},
         "roofline": {"kernel": "bank_refill (experts over the host link)", "bound": "host link",
                      "achieved": copied_per_step / (ms_per_step * 1e-3) / 1e9, "peak": link, "unit": "GB/s",
                      "frac": copied_per_step / (ms_per_step * 1e-3) / 1e9 / link, "traffic": None,
@@ -742,10 +767,7 @@ def run_dense(args, name: str) -> dict:
     x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
     out = torch.empty((wl.T, wl.N), dtype=torch.int16, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-
-    def l2_flush():
-        with torch.cuda.stream(stream):
-            flush.fill_(1.0)
+    l2_flush = l2_flusher(flush, stream)
 
     for _ in range(args.warmup):
         l2_flush()
@@ -768,6 +790,29 @@ def run_dense(args, name: str) -> dict:
     if ws > 1:
         dist.barrier()
     ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), device="cuda") / args.steps
+    assert layer.device_error() == 0
+    ran = layer.last_path()
+
+    # both kernel paths forced, outside the timed region (a path that cannot take the shape: null)
+    def time_path(path):
+        layer.set_path(path)
+        try:
+            for _ in range(3):
+                l2_flush()
+                layer.forward(x, out)
+        except cm.ColiError:
+            return None
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            l2_flush()
+            a.record(stream)
+            layer.forward(x, out)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    paths_ms = {"cuda_cores": time_path(cm.COLI_DENSE_CUDA_CORES), "tensor": time_path(cm.COLI_DENSE_TENSOR)}
+    layer.set_path(cm.COLI_DENSE_AUTO)
     assert layer.device_error() == 0
 
     x_host = torch.from_numpy(inputs.x.view(np.int16).copy()).pin_memory()
@@ -797,23 +842,26 @@ def run_dense(args, name: str) -> dict:
     else:
         roof = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": fp8_tf, "unit": "TFLOP/s",
                 "peak_source": f"{peak_kind} bf16_tflops x 2 (nominal FP8/bf16 ratio)", "algorithmic_flops": flops}
-    roof.update({"kernel": "gemm_fp8 (with its activation split)", "frac": roof["achieved"] / roof["peak"],
-                 "traffic": None, "kernel_ms": ms})
+    cores = ran == cm.COLI_DENSE_CUDA_CORES
+    roof.update({"kernel": "gemv_fp8 (one launch)" if cores else "gemm_fp8 (with its activation split)",
+                 "frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel_ms": ms})
     tokens = wl.T * ws
     res = {
         "metric": "FP8 dense projection tokens/s at 1 GB300", "value": tokens / (ms * 1e-3), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 weights x two e4m3 activation terms, fp32 accumulate, fp32 block-scale folding",
+        "dtype": ("e4m3 weights x bf16 activations on the CUDA cores, exact fp32 products, fp32 accumulate"
+                  if cores else "e4m3 weights x two e4m3 activation terms, fp32 accumulate, fp32 block-scale folding"),
         "data": "synthetic (seeded SplitMix64; E4M3 weights with fp32 128x128 block scales, bf16 activations)",
         "config": {"workload": f"{wl.name}: T={wl.T}, K={wl.K}, N={wl.N}, E4M3 + fp32 scale per 128x128",
                    "tokens_per_gpu": wl.T, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": "flushed (512 MiB write) before every timed step"},
+                   "l2": L2_FLUSH_NOTE},
         "roofline": roof,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if cores else 2) * args.steps,
         "clocks": clock_info,
+        "paths_ms": paths_ms,
     }
     if not args.skip_cpu and rank == 0:
         from oracle.oracle import Oracle

@@ -325,13 +325,15 @@ COLI_API int coli_moe_forward_nvfp4(coli_moe_t *h, const void *x_bf16, int32_t T
  * support -- CUDA/VRAM expert tiering", dense-on-GPU tier comment). E4M3 is the OCP 8-bit float
  * (bias 7, subnormals, max 448, S.1111.111 NaN); the output is the exact sum rounded once, up to the
  * activation split (x enters as two E4M3 terms under a per-token power-of-two scale, about 2^-9
- * relative per element) and fp32 accumulation.
+ * relative per element) and fp32 accumulation; on the CUDA-core path (below) the products are
+ * exact and only the fp32 sums round.
  *
  * A dense handle holds the workspace for up to max_tokens rows of up to max_k features and is
  * bound to one stream. Layout: x bf16 [T][K], w E4M3 codes [N][K] (K-major rows), w_scale fp32
  * [N/128][K/128], out bf16 [T][N]; all device pointers owned by the caller; K and N multiples of 128.
- * coli_dense_forward enqueues two kernels on the stream, returns without synchronising and
- * allocates nothing; forwards on one handle must not overlap on the device. */
+ * coli_dense_forward enqueues one kernel (CUDA-core path) or two (tensor-core path) on the stream,
+ * returns without synchronising and allocates nothing; forwards on one handle must not overlap on
+ * the device. */
 typedef struct coli_dense coli_dense_t;
 COLI_API int coli_dense_create(int32_t max_tokens, int32_t max_k, void *cuda_stream, coli_dense_t **out);
 COLI_API int coli_dense_forward(coli_dense_t *d, const void *x_bf16, int32_t T, int32_t K, const uint8_t *w_e4m3,
@@ -342,6 +344,22 @@ COLI_API const char *coli_dense_last_error(const coli_dense_t *d);
 /* Synchronises d's stream, returns the device error word (0: none; a bounded wait that ran out
  * records its code, as for coli_moe_device_error) and clears it. */
 COLI_API int coli_dense_device_error(coli_dense_t *d, int32_t *code);
+/* Kernel path of coli_dense_forward. */
+enum {
+    COLI_DENSE_AUTO = 0,        /* COLI_DENSE_CUDA_CORES where it measured faster: up to 8 tokens for
+                                   N x K <= 4 MiB, 4 for <= 7 MiB, 2 for <= 14 MiB; else
+                                   COLI_DENSE_TENSOR */
+    COLI_DENSE_CUDA_CORES = 1,  /* one kernel: each block copies its weight rows into shared memory and
+                                   multiplies them by the tokens in fp32 (exact products); needs
+                                   K <= 8192 and ceil(N / SMs) x K bytes within shared memory */
+    COLI_DENSE_TENSOR = 2       /* two E4M3 terms of x, then the tcgen05 E4M3 GEMM (kind::f8f6f4) */
+};
+/* Forces the path (COLI_DENSE_AUTO restores the automatic choice). COLI_ERR_INVALID_ARG for an
+ * unknown path; a forward on a forced CUDA-core path whose shape it does not support returns
+ * COLI_ERR_INVALID_ARG. */
+COLI_API int coli_dense_set_path(coli_dense_t *d, int32_t path);
+/* Path the last forward on d ran (COLI_DENSE_AUTO before the first). */
+COLI_API int coli_dense_last_path(const coli_dense_t *d);
 
 #ifdef __cplusplus
 }

@@ -19,6 +19,7 @@ COLI_ERR_UNSUPPORTED_ARCH = -2
 COLI_ERR_OUT_OF_MEMORY = -3
 COLI_ERR_CUDA = -4
 COLI_FFN_AUTO, COLI_FFN_GEMV, COLI_FFN_GEMM_MXF4 = 0, 1, 2
+COLI_DENSE_AUTO, COLI_DENSE_CUDA_CORES, COLI_DENSE_TENSOR = 0, 1, 2
 
 EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "coli_moe_destroy",
             "coli_moe_last_error", "coli_moe_set_ffn_path", "coli_moe_debug_routing",
@@ -26,8 +27,8 @@ EXPORTED = ("coli_moe_create", "coli_moe_forward", "coli_moe_forward_host", "col
             "coli_moe_device_error", "coli_moe_set_wait_limit", "coli_moe_route_static",
             "coli_bank_create", "coli_bank_destroy", "coli_moe_forward_banked", "coli_bank_set_copy_blocks",
             "coli_bank_state", "coli_dense_create", "coli_dense_forward", "coli_dense_destroy",
-            "coli_dense_last_error", "coli_dense_device_error", "coli_moe_forward_nvfp4",
-            "coli_moe_test_alloc_failure")
+            "coli_dense_last_error", "coli_dense_device_error", "coli_dense_set_path", "coli_dense_last_path",
+            "coli_moe_forward_nvfp4", "coli_moe_test_alloc_failure")
 COLI_STAGES = 5
 STAGE_NAMES = ("router", "permute", "ffn_gate_up", "ffn_down", "combine")
 
@@ -125,6 +126,10 @@ def load(path: str = LIB_PATH) -> C.CDLL:
     lib.coli_dense_last_error.restype = C.c_char_p
     lib.coli_dense_device_error.argtypes = [vp, C.POINTER(C.c_int32)]
     lib.coli_dense_device_error.restype = C.c_int
+    lib.coli_dense_set_path.argtypes = [vp, C.c_int32]
+    lib.coli_dense_set_path.restype = C.c_int
+    lib.coli_dense_last_path.argtypes = [vp]
+    lib.coli_dense_last_path.restype = C.c_int
     lib.coli_moe_test_alloc_failure.argtypes = [C.POINTER(coli_moe_config), C.c_int32, C.POINTER(C.c_int32),
                                                 C.POINTER(C.c_int32)]
     lib.coli_moe_test_alloc_failure.restype = C.c_int
@@ -488,6 +493,14 @@ def coli_dense_device_error(d) -> int:
     return code.value
 
 
+def coli_dense_set_path(d, path: int) -> int:
+    return _dcheck(d, load().coli_dense_set_path(d, path))
+
+
+def coli_dense_last_path(d) -> int:
+    return load().coli_dense_last_path(d)
+
+
 class DenseLayer:
     """A dense handle plus device copies of one FP8 projection's weights (E4M3 codes, block scales)."""
 
@@ -503,6 +516,12 @@ class DenseLayer:
     def forward(self, x, out, T: Optional[int] = None) -> None:
         T = x.shape[0] if T is None else T
         coli_dense_forward(self.d, x, T, self.wl.K, self.w, self.w_scale, self.wl.N, out)
+
+    def set_path(self, path: int) -> None:
+        coli_dense_set_path(self.d, path)
+
+    def last_path(self) -> int:
+        return coli_dense_last_path(self.d)
 
     def device_error(self) -> int:
         return coli_dense_device_error(self.d)

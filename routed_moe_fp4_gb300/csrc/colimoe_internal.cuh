@@ -263,6 +263,12 @@ struct DenseArgs {
 constexpr int kSplitMaxTokens = 64;   // the FP8 GEMM splits K only up to this many tokens
 bool fp8_available();
 int launch_dense_fp8(const DenseArgs &a, int num_sms, cudaStream_t st);
+// The CUDA-core projection for few tokens (gemv_fp8.cu): one kernel, no workspace. Supported when
+// K <= 8192 and one block's weight rows fit in shared memory; launch returns -2 otherwise. The
+// automatic choice takes it for up to dense_gemv_max_tokens(K, N) tokens (0 for large matrices).
+bool dense_gemv_supported(int T, int K, int N, int num_sms);
+int dense_gemv_max_tokens(int K, int N);
+int launch_dense_gemv(const DenseArgs &a, int num_sms, cudaStream_t st);
 
 // Block-scaled tcgen05 GEMM path with FP4 on both sides (gemm_mx4.cu): E2M1 weights x four E2M1
 // activation terms.

@@ -1,6 +1,6 @@
 // C ABI of the FP8 dense projection (coli_dense_* in colimoe.h): argument checks, the workspace
-// for the activation terms, and the two launches of gemm_fp8.cu. No host synchronisation and no
-// allocation inside a forward.
+// for the activation terms, the choice between the CUDA-core kernel of gemv_fp8.cu (a few tokens)
+// and the two launches of gemm_fp8.cu. No host synchronisation and no allocation inside a forward.
 #include <stdarg.h>
 #include <stdio.h>
 
@@ -20,6 +20,8 @@ struct coli_dense {
     int *cnt = nullptr;        // split-K arrival counters [SMs]
     int *err = nullptr;        // device error word
     uint64_t wait_ns = 0;
+    int32_t path = COLI_DENSE_AUTO;   // forced kernel path, or the automatic choice
+    int32_t last_path = COLI_DENSE_AUTO;
     char msg[256] = {0};
 };
 
@@ -126,7 +128,17 @@ int coli_dense_forward(coli_dense_t *d, const void *x_bf16, int32_t T, int32_t K
     a.cnt = d->cnt;
     a.err = d->err;
     a.wait_ns = d->wait_ns;
-    const int n = launch_dense_fp8(a, d->num_sms, d->stream);
+    // A few tokens on a small matrix: the CUDA-core kernel (one launch, latency-bound work); else
+    // the tensor-core GEMM
+    const bool gemv_ok = dense_gemv_supported(T, K, N, d->num_sms);
+    if (d->path == COLI_DENSE_CUDA_CORES && !gemv_ok) {
+        dense_err(d, "the CUDA-core path needs K <= 8192 and one block's weight rows within shared memory");
+        return COLI_ERR_INVALID_ARG;
+    }
+    const bool gemv = d->path == COLI_DENSE_CUDA_CORES || (d->path == COLI_DENSE_AUTO && gemv_ok &&
+                                                           T <= dense_gemv_max_tokens(K, N));
+    const int n = gemv ? launch_dense_gemv(a, d->num_sms, d->stream) : launch_dense_fp8(a, d->num_sms, d->stream);
+    d->last_path = gemv ? COLI_DENSE_CUDA_CORES : COLI_DENSE_TENSOR;
     if (n == -2) {
         dense_err(d, "tensor maps for the FP8 GEMM could not be encoded");
         return COLI_ERR_INVALID_ARG;
@@ -145,6 +157,18 @@ void coli_dense_destroy(coli_dense_t *d) {
 }
 
 const char *coli_dense_last_error(const coli_dense_t *d) { return d ? d->msg : g_dense_err; }
+
+int coli_dense_set_path(coli_dense_t *d, int32_t path) {
+    if (!d) return COLI_ERR_INVALID_ARG;
+    if (path < COLI_DENSE_AUTO || path > COLI_DENSE_TENSOR) {
+        dense_err(d, "unknown dense path %d", path);
+        return COLI_ERR_INVALID_ARG;
+    }
+    d->path = path;
+    return COLI_OK;
+}
+
+int coli_dense_last_path(const coli_dense_t *d) { return d ? d->last_path : COLI_DENSE_AUTO; }
 
 int coli_dense_device_error(coli_dense_t *d, int32_t *code) {
     if (!d || !code) return COLI_ERR_INVALID_ARG;
