@@ -288,6 +288,9 @@ DENSE_WORKLOADS: Dict[str, DenseWorkload] = {
     "dense_tiny": DenseWorkload("dense_tiny", 5, 384, 256),
     "dense_decode": DenseWorkload("dense_decode", 8, 4096, 4096),
     "dense_prefill": DenseWorkload("dense_prefill", 512, 4096, 4096),
+    # a narrow projection out of the larger hidden size: 3.5 MiB of weights, the size class where
+    # the CUDA-core kernel is the automatic choice for up to 8 tokens
+    "dense_narrow": DenseWorkload("dense_narrow", 8, 7168, 512),
 }
 
 
