@@ -344,10 +344,10 @@ def layer_roofline(layer_bytes: int, flops: float, ms: float, hbm_gbs: float, bf
             "peak_source": f"{peak_kind} hbm_gbs; {peak_kind} bf16_tflops x {FP4_OVER_BF16:g} (nominal FP4/bf16)"}
 
 
-def profiled_traffic(kernel: str, workload: str, profile: str = ""):
-    """DRAM bytes per gate/up launch from a committed ncu summary (profiles/<profile>_<workload>.json,
-    profile defaulting to the kernel's source stem), or None when the kernel's source has changed
-    since the counters were taken."""
+def profiled_traffic(kernel: str, workload: str, profile: str = "", part: str = "gate_up"):
+    """DRAM bytes per launch of `part` (the gate/up launch by default) from a committed ncu summary
+    (profiles/<profile>_<workload>.json, profile defaulting to the kernel's source stem), or None
+    when the kernel's source has changed since the counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", f"{profile or kernel}_{workload}.json")
     if not os.path.exists(path):
@@ -358,7 +358,7 @@ def profiled_traffic(kernel: str, workload: str, profile: str = ""):
         sha = hashlib.sha256(f.read()).hexdigest()
     if prof.get("source_sha256") != sha:
         return None
-    return prof["gate_up"]["dram_read_bytes"] + prof["gate_up"]["dram_write_bytes"]
+    return prof[part]["dram_read_bytes"] + prof[part]["dram_write_bytes"]
 
 
 def max_over_ranks(value: float, device=None) -> float:
@@ -844,7 +844,8 @@ def run_dense(args, name: str) -> dict:
                 "peak_source": f"{peak_kind} bf16_tflops x 2 (nominal FP8/bf16 ratio)", "algorithmic_flops": flops}
     cores = ran == cm.COLI_DENSE_CUDA_CORES
     roof.update({"kernel": "gemv_fp8 (one launch)" if cores else "gemm_fp8 (with its activation split)",
-                 "frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel_ms": ms})
+                 "frac": roof["achieved"] / roof["peak"],
+                 "traffic": profiled_traffic("gemv_fp8", name, part="launch") if cores else None, "kernel_ms": ms})
     tokens = wl.T * ws
     res = {
         "metric": "FP8 dense projection tokens/s at 1 GB300", "value": tokens / (ms * 1e-3), "unit": "tokens/s",
