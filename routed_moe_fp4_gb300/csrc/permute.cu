@@ -118,7 +118,7 @@ route_permute_small(const float *__restrict__ scores, const float *__restrict__ 
     pdl_begin();
     __shared__ int idx_s[(kSmallRouteTokens - 1) * 32];
     __shared__ int cnt_s[1025], off_s[1026], touched_s[1025];
-    __shared__ int smem[33];
+    __shared__ unsigned long long smem[33];
     __shared__ int s_nt;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = E + 1;
@@ -127,16 +127,19 @@ route_permute_small(const float *__restrict__ scores, const float *__restrict__ 
     __syncthreads();
     for (int i = threadIdx.x; i < T * top_k; i += blockDim.x) atomicAdd(&cnt_s[idx_s[i]], 1);
     __syncthreads();
-    // groups: offsets, touched list and GEMV costs
+    // groups: offsets, touched list and GEMV costs, in one scan of three 21-bit fields (row count,
+    // touched flag, cost: their sums stay below 2^21 with T < 64 tokens and k <= 32)
+    constexpr unsigned long long kF = (1ull << 21) - 1;
     int base = 0, tbase = 0, cbase = 0;
     for (int g0 = 0; g0 < G; g0 += 1024) {
         const int g = g0 + threadIdx.x;
         const int c = g < G ? cnt_s[g] : 0;
         const int cost = c > 0 ? 1 + (c + cost_tokens - 1) / cost_tokens : 0;
-        int tot, ttot, ctot;
-        const int ex = block_exclusive_scan(c, smem, &tot);
-        const int tex = block_exclusive_scan(c > 0 ? 1 : 0, smem, &ttot);
-        const int cex = block_exclusive_scan(cost, smem, &ctot);
+        unsigned long long tot3;
+        const unsigned long long ex3 = block_exclusive_scan64(
+            (unsigned long long)c | ((unsigned long long)(c > 0) << 21) | ((unsigned long long)cost << 42), smem, &tot3);
+        const int ex = (int)(ex3 & kF), tex = (int)((ex3 >> 21) & kF), cex = (int)(ex3 >> 42);
+        const int tot = (int)(tot3 & kF), ttot = (int)((tot3 >> 21) & kF), ctot = (int)(tot3 >> 42);
         if (g < G) {
             cnt[g] = c;
             off[g] = off_s[g] = base + ex;
@@ -164,9 +167,11 @@ route_permute_small(const float *__restrict__ scores, const float *__restrict__ 
             const int g = u < nt ? touched_s[u] : 0;
             const int c = u < nt ? cnt_s[g] : 0;
             const int ns = (c + ntile - 1) / ntile, nlg = (c + 2 * ntile - 1) / (2 * ntile);
-            int tot_s, tot_l;
-            const int ex_s = block_exclusive_scan(ns, smem, &tot_s);
-            const int ex_l = block_exclusive_scan(nlg, smem, &tot_l);
+            unsigned long long tot2;
+            const unsigned long long ex2 =
+                block_exclusive_scan64((unsigned long long)ns | ((unsigned long long)nlg << 32), smem, &tot2);
+            const int ex_s = (int)(ex2 & 0xFFFFFFFFull), ex_l = (int)(ex2 >> 32);
+            const int tot_s = (int)(tot2 & 0xFFFFFFFFull), tot_l = (int)(tot2 >> 32);
             if (u < nt) {
                 const int o = off_s[g];
                 nl.prefix_small[u] = c_small + ex_s;

@@ -14,7 +14,7 @@
 
 namespace colimoe {
 
-// Lane 0 writes idx[t][0..k) and w[t][0..k) (and idx_sm[t * k + j] when idx_sm is non-null).
+// Lane j writes idx[t][j] and w[t][j] (and idx_sm[t * k + j] when idx_sm is non-null).
 template <int NPL>
 __device__ __forceinline__ void topk_token(const float *__restrict__ scores, const float *__restrict__ bias, int E,
                                            int top_k, int t, int lane, int32_t *__restrict__ idx,
@@ -33,8 +33,8 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ scores, con
             taken |= 1u << i;          // padding slots are never chosen
         }
     }
-    float s_sel[32];
-    int e_sel[32];
+    float my_s = 0.f;              // lane j keeps slot j's score and expert (top_k <= 32)
+    int my_e = 0;
     for (int j = 0; j < top_k; ++j) {
         float bk = -INFINITY, bs = 0.f;
         int be = INT_MAX;
@@ -75,17 +75,18 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ scores, con
             bs = cs;
         }
         if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        s_sel[j] = bs;
-        e_sel[j] = be;
-    }
-    if (lane == 0) {
-        float S = 0.0f;
-        for (int j = 0; j < top_k; ++j) S = __fadd_rn(S, s_sel[j]);
-        for (int j = 0; j < top_k; ++j) {
-            idx[(size_t)t * top_k + j] = e_sel[j];
-            w[(size_t)t * top_k + j] = __fdiv_rn(s_sel[j], S);
-            if (idx_sm) idx_sm[t * top_k + j] = e_sel[j];
+        if (lane == j) {
+            my_s = bs;
+            my_e = be;
         }
+    }
+    // S in slot order, the same chain on every lane; then lane j writes slot j
+    float S = 0.0f;
+    for (int j = 0; j < top_k; ++j) S = __fadd_rn(S, __shfl_sync(0xffffffffu, my_s, j));
+    if (lane < top_k) {
+        idx[(size_t)t * top_k + lane] = my_e;
+        w[(size_t)t * top_k + lane] = __fdiv_rn(my_s, S);
+        if (idx_sm) idx_sm[t * top_k + lane] = my_e;
     }
 }
 
