@@ -764,6 +764,9 @@ def run_dense(args, name: str) -> dict:
     wl = inputs.workload
     stream = torch.cuda.Stream()
     layer = cm.DenseLayer(inputs, stream=stream)
+    forced = {"auto": cm.COLI_DENSE_AUTO, "cores": cm.COLI_DENSE_CUDA_CORES, "tensor": cm.COLI_DENSE_TENSOR}[
+        args.dense_path]
+    layer.set_path(forced)
     x = torch.from_numpy(inputs.x.view(np.int16)).cuda()
     out = torch.empty((wl.T, wl.N), dtype=torch.int16, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -812,7 +815,7 @@ def run_dense(args, name: str) -> dict:
         torch.cuda.synchronize()
         return sum(a.elapsed_time(b) for a, b in ev) / args.steps
     paths_ms = {"cuda_cores": time_path(cm.COLI_DENSE_CUDA_CORES), "tensor": time_path(cm.COLI_DENSE_TENSOR)}
-    layer.set_path(cm.COLI_DENSE_AUTO)
+    layer.set_path(forced)
     assert layer.device_error() == 0
 
     x_host = torch.from_numpy(inputs.x.view(np.int16).copy()).pin_memory()
@@ -856,7 +859,8 @@ def run_dense(args, name: str) -> dict:
         "data": "synthetic (seeded SplitMix64; E4M3 weights with fp32 128x128 block scales, bf16 activations)",
         "config": {"workload": f"{wl.name}: T={wl.T}, K={wl.K}, N={wl.N}, E4M3 + fp32 scale per 128x128",
                    "tokens_per_gpu": wl.T, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": L2_FLUSH_NOTE},
+                   "l2": L2_FLUSH_NOTE, "path": "cuda cores" if cores else "tensor cores",
+                   "path_choice": "forced" if args.dense_path != "auto" else "automatic"},
         "roofline": roof,
         "e2e": {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": int(x_host.numel() * 2), "d2h_bytes_per_step": int(out_host.numel() * 2)},
@@ -1001,6 +1005,8 @@ def main():
     ap.add_argument("--copy-blocks", type=int, default=0, help="bank: blocks that copy while a round computes")
     ap.add_argument("--dense", default="", choices=[""] + sorted(S.DENSE_WORKLOADS),
                     help="time the FP8 dense projection on this workload instead of the MoE layer")
+    ap.add_argument("--dense-path", default="auto", choices=["auto", "cores", "tensor"],
+                    help="FP8 projection: force the CUDA-core or the tensor-core kernel path")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
