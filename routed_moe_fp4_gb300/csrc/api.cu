@@ -67,7 +67,7 @@ constexpr WsAllocator kDeviceAllocator{dev_alloc, dev_release, dev_zero, nullptr
 void free_ws(Workspace &ws, const WsAllocator &A = kDeviceAllocator) {
     void *ptrs[] = {ws.xq, ws.xqs, ws.hq, ws.hqs, ws.xg, ws.hg, ws.hf, ws.scores, ws.logit_part, ws.idx,  ws.w,  ws.inv_row, ws.src_token, ws.cnt, ws.off, ws.touched, ws.touched_cost,
                     ws.n_touched, ws.h, ws.y, ws.xh, ws.xinv, ws.hh, ws.hinv, ws.err, ws.x_stage,
-                    ws.out_stage, ws.tile_sched};
+                    ws.out_stage, ws.tile_sched, ws.h_ready};
     for (void *p : ptrs)
         if (p) A.release(p, A.ctx);
     ws = Workspace();
@@ -93,7 +93,7 @@ bool alloc_workspace(Workspace &ws, const coli_moe_config &c, int I_max, const W
               alloc(&ws.x_stage, Tm * H) && alloc(&ws.out_stage, Tm * H) && alloc(&ws.xq, 2 * rows * H) &&
               alloc(&ws.xqs, 4 * rows * (H / 16)) && alloc(&ws.hq, 2 * rows * (size_t)I_max) &&
               alloc(&ws.hqs, 4 * rows * (size_t)(I_max / 16)) && alloc(&ws.xg, 4 * rows) && alloc(&ws.hg, 4 * rows) &&
-              alloc(&ws.hf, rows * (size_t)I_max);
+              alloc(&ws.hf, rows * (size_t)I_max) && alloc(&ws.h_ready, E + 1);
     if (ok) ok = A.zero(ws.err, sizeof(int), A.ctx);
     if (ok) {
         ws.tile_sched_bytes = ntile_layout_ints((int)E, (int)rows) * sizeof(int32_t);
@@ -235,6 +235,7 @@ FfnArgs ffn_args(coli_moe_t *h, const void *x_bf16, int32_t T, int32_t top_k, in
     a.hf = ws.hf;
     a.err = ws.err;
     a.wait_ns = h->wait_ns;
+    a.h_ready = ws.h_ready;
     return a;
 }
 

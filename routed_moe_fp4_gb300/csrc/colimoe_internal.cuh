@@ -58,6 +58,8 @@ struct Workspace {
     __nv_bfloat16 *out_stage = nullptr;  // [Tm][H] forward_host output staging
     void *tile_sched = nullptr;     // n-tile layout of the block-scaled GEMM (NtileLayout)
     size_t tile_sched_bytes = 0;
+    int32_t *h_ready = nullptr;     // [E+1] per group: epilogue warps that have stored a gate/up
+                                    // tile's h terms (FP4 path, few tokens: the down launch's start)
 };
 
 struct NtileLayout;
@@ -95,6 +97,7 @@ struct FfnArgs {
     int w_slots = 0;
     int grid = 0;
     bool pdl_gate_up = true;
+    int32_t *h_ready = nullptr;     // [E+1] the workspace's per-group h counters (null: not used)
 };
 
 // Programmatic dependent launch. Every kernel of the library is launched with programmatic

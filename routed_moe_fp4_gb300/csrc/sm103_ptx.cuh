@@ -19,6 +19,7 @@ enum : int {
     kErrWaitMma = 3,       // waited too long for an MMA commit
     kErrWaitAccum = 4,     // epilogue waited too long for an accumulator
     kErrWaitRouter = 5,    // the tensor-core router logits kernel waited too long (any of its waits)
+    kErrWaitH = 6,         // the down launch waited too long for its group's gate/up tiles
     kErrBounds = 7,        // bounds-checked build only: a tile record pointed outside the buffers
 };
 
@@ -132,6 +133,43 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int3
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar)
         : "memory");
+}
+
+// Counters between blocks of different grids: a release add after this thread's (and, through a
+// preceding barrier, its peers') writes, and an acquire load that orders the reads after it.
+__device__ __forceinline__ void red_release_add(int *addr, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int *addr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
+// Orders this thread's generic-proxy view of global memory before its later async-proxy (TMA)
+// accesses: data that another block wrote with ordinary stores, and that an acquire made visible
+// here, may then be loaded by TMA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits until *counter >= target (acquire); false after limit_ns (error recorded, *abort set) or
+// as soon as *abort becomes non-zero.
+__device__ __forceinline__ bool wait_counter(const int *counter, int target, int *err, int code, volatile int *abort,
+                                             uint64_t limit_ns) {
+    if (ld_acquire(counter) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        if (ld_acquire(counter) >= target) return true;
+        if (abort && *abort) return false;
+        if (globaltimer() - t0 > limit_ns) {
+            record_error(err, code);
+            if (abort) *abort = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
 }
 
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
