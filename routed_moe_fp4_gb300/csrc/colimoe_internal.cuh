@@ -110,7 +110,10 @@ struct FfnArgs {
 // kernel that signals only after its own wait (the x- and h-term kernels quant_x4_rows,
 // quant_x4_tokens, quant_h_rows and quant_rows_nv, and gemm_mx4) starts its dependent only once
 // everything before itself has completed; gemm_mx4 relies on that to read the permutation's
-// outputs, and issue weight loads, before its wait.
+// outputs, and issue weight loads, before its wait. One exception: the down launch of a forward
+// of 4 to 63 tokens does not wait for the gate/up launch before it; it waits per expert on
+// counters that the gate/up epilogues release (gemm_mx4.cu), and writes only y, which the combine
+// reads after its own wait.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_begin() {
