@@ -557,8 +557,6 @@ gemm_mx4(const __grid_constant__ CUtensorMap tm_a_routed, const __grid_constant_
                 const int x0 = k * (ti.kst / 2);                      // byte offset along K
                 const bool two = !gu && ti.wide && ti.K - k * ti.kst > BK;   // second K chunk
                 // SFT: the scale chunks of the weight rows (one per matrix) and of the activation
-                // rows (one box of kTerms x bh rows), 16 bytes each
-                // SFT: the scale chunks of the weight rows (one per matrix) and of the activation
                 // rows (one box of kTerms x bh rows), 16 bytes each, on the same barrier
                 const uint32_t scbytes = SFT ? n_a * BM * 16 + kTerms * ti.bh * 16 : 0;
                 ptx::mbar_arrive_expect_tx(fb, (n_a == 2 || two ? 2 : 1) * kASmem + (two ? 2 : 1) * bbytes + scbytes);
