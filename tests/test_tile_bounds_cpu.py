@@ -80,3 +80,56 @@ def test_tiles_stay_in_bounds(E, H, I, I_s, T, k, skew):
     bad[-1] = (row0 + 1, g, n)
     with pytest.raises(AssertionError):
         check_launch(bad, E, rows, H // (2 * BM) if big else H // BM, False, I, I_s, H, big, 48 if big else 32)
+
+
+EPI_WARPS = 8
+BN_GATE_UP = 16
+
+
+def h_counter_increments(recs, E, m_tiles, I, I_s):
+    """Per group: the raises the gate/up launch makes (every epilogue warp, once per valid tile)."""
+    inc = [0] * (E + 1)
+    for t in range(len(recs) * m_tiles):
+        row0, g, n = recs[t // m_tiles]
+        Ig = I_s if g == E else I
+        if (t % m_tiles) * BM < Ig:
+            inc[g] += EPI_WARPS
+    return inc
+
+
+def h_counter_target(c, Ig):
+    """What the down launch's producer waits for: the group's 16-row gate/up tiles x its m-tiles x
+    the epilogue warps."""
+    return EPI_WARPS * (-(-c // BN_GATE_UP)) * (-(-Ig // BM))
+
+
+@pytest.mark.parametrize("E,I,I_s,T,k", [
+    (256, 2048, 2048, 8, 8),      # decode
+    (256, 2048, 2048, 4, 8),      # four tokens
+    (256, 2048, 2048, 63, 8),     # the largest token count of the mode
+    (64, 2048, 1024, 40, 6),      # narrower shared expert
+    (12, 512, 1024, 21, 3),       # wider shared expert
+    (16, 384, 0, 30, 2),          # no shared expert
+])
+def test_h_counter_targets_match_the_gate_up_raises(E, I, I_s, T, k):
+    """The down launch of a few-token forward starts on a group once its counter reaches the target:
+    that target must equal the raises the gate/up launch makes for the group, or the down launch
+    would wait until its limit (too high) or read h early (too low)."""
+    rng = np.random.default_rng(E + 31 * T)
+    cnt = np.zeros(E, np.int64)
+    for _ in range(T):
+        cnt[rng.choice(E, size=min(k, E), replace=False)] += 1
+    cnt = list(cnt) + ([T] if I_s else [])
+    small, _ = records(cnt, BN_GATE_UP)
+    I_max = max(I, I_s)
+    inc = h_counter_increments(small, E, -(-I_max // BM), I, I_s)
+    for g, c in enumerate(cnt):
+        if c == 0:
+            continue
+        Ig = I_s if g == E else I
+        assert inc[g] == h_counter_target(c, Ig), (g, c, inc[g])
+    # a planted mistake is caught: counting m-tiles of the widest intermediate size for every group
+    # (it differs for the group whose intermediate size is the smaller one)
+    if I_s and -(-I // BM) != -(-I_s // BM):
+        narrow = E if I_s < I else next(g for g, c in enumerate(cnt[:E]) if c)
+        assert inc[narrow] != EPI_WARPS * (-(-cnt[narrow] // BN_GATE_UP)) * (-(-I_max // BM))
